@@ -1,0 +1,71 @@
+"""Sparse MLA decode over the selected latent rows.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+[P2] section "GLM-5.3 的草稿层到底长什么样": the MLA latent has
+kv_lora_rank = 512 plus qk_rope_head_dim = 64, i.e. 576 values per token;
+[P2] "验证段的逐层算子" op 7 and [P3] "稀疏 MLA 的前向路径": attention runs
+only over the positions the indexer selected.  With the absorbed query
+(q_nope already multiplied into the latent space, 512, plus q_rope, 64) the
+key of position s is the whole latent row c[s, 0:576] and the value is
+c[s, 0:512].  For query row r and head h:
+
+    logit_j = scale * q[r, h, :] . c[s_j, :]          over the valid s_j
+    o[r, h] = sum_j softmax(logit)_j * c[s_j, 0:512]
+    lse[r, h] = log sum_j exp(logit_j)
+
+Entries equal to -1 are padding and are skipped.  Appended positions (the
+shared-index draft steps, [P1] "阶段 5:Draft 后续步骤(复用 top-k)") are
+base+1 .. base+n_append and are attended in addition to the selected set.
+The softmax scale is not on the pages; the caller passes it (1/sqrt(576) in
+the workloads).  All arithmetic is float64; a row with no valid index has
+o = 0 and lse = -inf.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+D_LATENT = 576
+D_V = 512
+
+
+def row_index_list(idx_r: np.ndarray, n_append: int = 0, base: int | None = None):
+    """The positions attended by one row: the valid selected ones, then the
+    appended base+1..base+n_append."""
+    sel = [int(s) for s in np.asarray(idx_r).tolist() if int(s) >= 0]
+    if n_append:
+        sel += [int(base) + 1 + j for j in range(n_append)]
+    return sel
+
+
+def sparse_mla(q, latent, cache_start, row_req, idx, scale, n_append=0,
+               append_base=None, rows=None, heads=None, d_v=D_V):
+    """q [R, H, 576], latent [T, 576] pool, cache_start [B], row_req [R],
+    idx [R, k] positions within the request (-1 = padding).
+
+    Returns dict row -> (o [H, d_v] float64, lse [H] float64) for the chosen
+    rows (all by default) and heads (all by default)."""
+    R, H = q.shape[0], q.shape[1]
+    rows = range(R) if rows is None else rows
+    heads = range(H) if heads is None else heads
+    out = {}
+    for r in rows:
+        b = int(row_req[r])
+        base = int(cache_start[b])
+        pos = row_index_list(idx[r], n_append,
+                             None if append_base is None else append_base[r])
+        C = np.asarray(latent[[base + s for s in pos]], dtype=np.float64).reshape(len(pos), D_LATENT)
+        o = np.zeros((len(heads), d_v))
+        lse = np.zeros(len(heads))
+        for i, h in enumerate(heads):
+            if len(pos) == 0:
+                o[i], lse[i] = 0.0, -np.inf
+                continue
+            logits = scale * (C @ np.asarray(q[r, h], dtype=np.float64))
+            m = np.max(logits)
+            e = np.exp(logits - m)
+            ssum = np.sum(e)
+            o[i] = (e @ C[:, :d_v]) / ssum
+            lse[i] = m + np.log(ssum)
+        out[r] = (o, lse)
+    return out

@@ -1,0 +1,356 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself:
+a library codec, hand-worked examples, closed forms, brute force and
+textbook dense attention.  CPU only."""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import accept, fp8, indexer, merge, mla, share, topk, writeback
+
+
+# --------------------------------------------------------------------- FP8 codec
+
+def test_fp8_decode_exhaustive_vs_library():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = fp8.decode_e4m3(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan_ours = np.isnan(ours)
+    assert np.array_equal(nan_ours, np.isnan(lib))
+    assert np.array_equal(ours[~nan_ours], lib[~nan_ours])
+    # hand-checked code points of the OCP E4M3 table
+    assert fp8.decode_e4m3(np.uint8(0x7E)) == 448.0
+    assert fp8.decode_e4m3(np.uint8(0x01)) == 2.0 ** -9
+    assert fp8.decode_e4m3(np.uint8(0x08)) == 2.0 ** -6
+    assert fp8.decode_e4m3(np.uint8(0x38)) == 1.0
+    assert fp8.decode_e4m3(np.uint8(0xB8)) == -1.0
+    assert np.isnan(fp8.decode_e4m3(np.uint8(0x7F))) and np.isnan(fp8.decode_e4m3(np.uint8(0xFF)))
+
+
+def test_fp8_encode_matches_library_rounding():
+    rng = np.random.default_rng(0)
+    y = np.concatenate([rng.normal(0, 50, 20000), rng.uniform(-448, 448, 20000),
+                        rng.normal(0, 0.01, 5000)]).astype(np.float32)
+    ours = fp8.encode_e4m3_rne_satfinite(y.astype(np.float64))
+    lib = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    # negative zero: the library keeps the sign of -0 results; compare values
+    assert np.array_equal(fp8.decode_e4m3(ours), fp8.decode_e4m3(lib))
+
+
+def test_fp8_encode_ties_and_saturation():
+    # 1.0625 is halfway between 1.0 (0x38, even) and 1.125 (0x39): ties to even
+    assert fp8.encode_e4m3_rne_satfinite(np.array([1.0625]))[0] == 0x38
+    # 1.1875 is halfway between 1.125 (0x39) and 1.25 (0x3A): ties to even
+    assert fp8.encode_e4m3_rne_satfinite(np.array([1.1875]))[0] == 0x3A
+    assert fp8.encode_e4m3_rne_satfinite(np.array([1000.0]))[0] == 0x7E
+    assert fp8.encode_e4m3_rne_satfinite(np.array([-1000.0]))[0] == 0xFE
+    # every finite code round-trips
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    back = fp8.encode_e4m3_rne_satfinite(fp8.decode_e4m3(codes))
+    dec = fp8.decode_e4m3(back)
+    assert np.array_equal(dec, fp8.decode_e4m3(codes))
+
+
+def test_quantize_block128_definition():
+    rng = np.random.default_rng(1)
+    x = rng.normal(0, 3, (5, 256)).astype(np.float32)
+    x[2, :128] = 0.0                                   # amax = 0 block
+    codes, scale = fp8.quantize_block128(x)
+    assert codes.shape == x.shape and scale.shape == (5, 2)
+    assert scale[2, 0] == 1.0 and np.all(codes[2, :128] == 0)
+    amax = np.abs(x.reshape(5, 2, 128)).max(-1)
+    nz = amax > 0
+    assert np.array_equal(scale[nz], (amax / np.float32(448.0)).astype(np.float32)[nz])
+    # the block maximum maps to +-448 and the library codec agrees per element
+    y = (x.reshape(5, 2, 128) / scale[..., None]).astype(np.float32).reshape(5, 256)
+    lib = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(fp8.decode_e4m3(codes), fp8.decode_e4m3(lib))
+    deq = fp8.decode_e4m3(codes).reshape(5, 2, 128) * scale[..., None]
+    assert np.max(np.abs(deq).max(-1)[nz] - amax[nz]) <= 1e-6 * amax.max()
+
+
+# --------------------------------------------------------------------- merge
+
+def test_merge_hand_worked():
+    # two requests with 2 and 1 prompt tokens, K = 3 drafts each
+    prompt = np.array([10, 11, 20])
+    po = np.array([0, 2, 3], dtype=np.uint32)
+    draft = np.array([[1, 2, 3], [4, 5, 6]])
+    toks, mo = merge.merge_tokens(prompt, po, draft)
+    assert mo.tolist() == [0, 5, 9]
+    assert toks.tolist() == [10, 11, 1, 2, 3, 20, 4, 5, 6]
+    assert merge.host_merged_offsets(po, 3).tolist() == [0, 5, 9]
+
+
+def test_merge_k0_identity_and_empty():
+    prompt = np.array([7, 8, 9, 10])
+    po = np.array([0, 1, 4], dtype=np.uint32)
+    toks, mo = merge.merge_tokens(prompt, po, np.zeros((2, 0), dtype=np.int64))
+    assert toks.tolist() == [7, 8, 9, 10] and mo.tolist() == [0, 1, 4]
+    toks, mo = merge.merge_tokens(np.zeros(0, dtype=np.int64), np.array([0, 0, 0], dtype=np.uint32),
+                                  np.array([[1, 2], [3, 4]]))
+    assert toks.tolist() == [1, 2, 3, 4] and mo.tolist() == [0, 2, 4]
+
+
+# --------------------------------------------------------------------- indexer
+
+def test_indexer_hand_worked():
+    # H = 2 heads, D = 2.  q = [[1, 2], [-1, 1]], key = [3, 1]:
+    # head dots 5 and -2 -> ReLU 5 and 0; w = [0.5, 2] -> 2.5
+    q = np.array([[[1.0, 2.0], [-1.0, 1.0]]])
+    w = np.array([[0.5, 2.0]])
+    k = np.array([[3.0, 1.0], [-1.0, 0.0], [0.0, 0.0]])
+    out = indexer.indexer_scores(q, None, w, k, None, np.array([0]), np.array([0]),
+                                 np.array([2]), fp8=False)
+    # key 1: dots -1 and 1 -> 0 + 2*1 = 2; key 2: all zero -> 0
+    assert out[0].tolist() == [2.5, 2.0, 0.0]
+
+
+def test_indexer_brute_force_loops_and_visibility():
+    rng = np.random.default_rng(2)
+    H, D, T = 3, 8, 40
+    q = rng.normal(size=(4, H, D))
+    w = rng.uniform(-1, 1, size=(4, H))      # negative weights stay outside the ReLU
+    k = rng.normal(size=(T, D))
+    cache_start = np.array([0, 17])
+    row_req = np.array([0, 0, 1, 1])
+    row_pos = np.array([10, 11, 20, 22])
+    out = indexer.indexer_scores(q, None, w, k, None, cache_start, row_req, row_pos, fp8=False)
+    for r in range(4):
+        base = cache_start[row_req[r]]
+        assert len(out[r]) == row_pos[r] + 1
+        for s in range(row_pos[r] + 1):
+            tot = 0.0
+            for h in range(H):
+                d = sum(q[r, h, i] * k[base + s, i] for i in range(D))
+                if d > 0:
+                    tot += w[r, h] * d
+            assert abs(out[r][s] - tot) <= 1e-12 * max(1.0, abs(tot))
+
+
+def test_indexer_fp8_scales_commute_with_relu():
+    rng = np.random.default_rng(3)
+    H, D, T = 4, 128, 50
+    qx = rng.normal(size=(1, H, D)).astype(np.float32)
+    kx = rng.normal(size=(T, D)).astype(np.float32)
+    w = rng.uniform(0, 1, size=(1, H)).astype(np.float32)
+    qc, qs = fp8.quantize_block128(qx)
+    kc, ks = fp8.quantize_block128(kx)
+    ks = ks[:, 0]
+    qs = qs[..., 0]
+    out = indexer.indexer_scores(qc, qs, w, kc, ks, np.array([0]), np.array([0]),
+                                 np.array([T - 1]), fp8=True)[0]
+    # same thing with the scales folded outside the ReLU (positive scales commute)
+    dots = fp8.decode_e4m3(kc) @ fp8.decode_e4m3(qc[0]).T            # [T, H]
+    alt = ks.astype(np.float64) * (np.maximum(dots, 0) @ (w[0].astype(np.float64) * qs[0]))
+    assert np.allclose(out, alt, rtol=1e-12, atol=0)
+    # and it approximates the unquantized score to FP8 accuracy
+    exact = np.maximum(kx.astype(np.float64) @ qx[0].T.astype(np.float64), 0) @ w[0]
+    assert np.max(np.abs(out - exact)) < 0.1 * np.max(np.abs(exact))
+
+
+def test_indexer_single_head_is_plain_dot():
+    rng = np.random.default_rng(4)
+    k = np.abs(rng.normal(size=(9, 5)))
+    q = np.abs(rng.normal(size=(1, 1, 5)))
+    out = indexer.indexer_scores(q, None, np.ones((1, 1)), k, None, np.array([0]),
+                                 np.array([0]), np.array([8]), fp8=False)[0]
+    assert np.allclose(out, np.dot(k, q[0, 0]), rtol=1e-14)
+
+
+# --------------------------------------------------------------------- top-k
+
+def _brute_topk(scores, k):
+    """Best subset by exhaustive search: the k-subset with the largest sorted
+    score vector, ties to the subset with smaller positions."""
+    V = len(scores)
+    best = None
+    for sub in itertools.combinations(range(V), min(k, V)):
+        key = (sorted((scores[i] for i in sub), reverse=True), [-i for i in sorted(sub)])
+        if best is None or key > best[0]:
+            best = (key, sub)
+    return sorted(best[1])
+
+
+def test_topk_brute_force_with_ties():
+    rng = np.random.default_rng(5)
+    for trial in range(40):
+        V = int(rng.integers(1, 10))
+        k = int(rng.integers(1, 8))
+        scores = rng.integers(0, 4, V).astype(np.float64)     # many exact ties
+        got = topk.topk_select(scores, k)
+        want = _brute_topk(scores, k)
+        assert got[:len(want)].tolist() == want
+        assert np.all(got[len(want):] == -1)
+
+
+def test_topk_short_row_takes_all():
+    got = topk.topk_select(np.array([0.5, -1.0, 2.0]), 8)
+    assert got.tolist() == [0, 1, 2, -1, -1, -1, -1, -1]
+
+
+def test_topk_ties_to_lower_index():
+    got = topk.topk_select(np.array([1.0, 3.0, 1.0, 1.0, 0.0]), 3)
+    assert got.tolist() == [0, 1, 2]
+
+
+# --------------------------------------------------------------------- sparse MLA
+
+def _dense_attention(q, C, scale):
+    """Textbook softmax attention with torch in float64: q [H, 576], C [n, 576]."""
+    qt = torch.from_numpy(np.asarray(q, dtype=np.float64))
+    Ct = torch.from_numpy(np.asarray(C, dtype=np.float64))
+    logits = scale * qt @ Ct.T
+    p = torch.softmax(logits, dim=-1)
+    return (p @ Ct[:, :512]).numpy(), torch.logsumexp(logits, dim=-1).numpy()
+
+
+def test_sparse_mla_equals_dense_when_k_covers_context():
+    rng = np.random.default_rng(6)
+    H, T = 4, 60
+    latent = rng.normal(size=(T, 576))
+    q = rng.normal(size=(3, H, 576))
+    cache_start = np.array([0, 25])
+    row_req = np.array([0, 1, 1])
+    row_pos = np.array([20, 30, 34])
+    k = 64
+    idx = np.full((3, k), -1)
+    for r in range(3):
+        idx[r, :row_pos[r] + 1] = rng.permutation(row_pos[r] + 1)   # any order
+    out = mla.sparse_mla(q, latent, cache_start, row_req, idx, 0.07)
+    for r in range(3):
+        base = cache_start[row_req[r]]
+        o_ref, lse_ref = _dense_attention(q[r], latent[base:base + row_pos[r] + 1], 0.07)
+        assert np.allclose(out[r][0], o_ref, rtol=1e-12, atol=1e-13)
+        assert np.allclose(out[r][1], lse_ref, rtol=1e-12)
+
+
+def test_sparse_mla_closed_forms():
+    rng = np.random.default_rng(7)
+    latent = rng.normal(size=(20, 576))
+    q = rng.normal(size=(1, 2, 576))
+    # one selected row: output is that row's first 512 values, lse = its logit
+    idx = np.array([[7, -1, -1]])
+    o, lse = mla.sparse_mla(q, latent, np.array([0]), np.array([0]), idx, 0.1)[0]
+    assert np.allclose(o, latent[7, :512][None].repeat(2, 0), rtol=1e-14)
+    assert np.allclose(lse, 0.1 * latent[7] @ q[0].T, rtol=1e-13)
+    # q = 0: uniform weights, the mean of the selected rows; lse = log n
+    idx = np.array([[3, 9, 11, 4]])
+    o, lse = mla.sparse_mla(np.zeros((1, 1, 576)), latent, np.array([0]), np.array([0]), idx, 1.0)[0]
+    assert np.allclose(o[0], latent[[3, 9, 11, 4], :512].mean(0), rtol=1e-13)
+    assert np.allclose(lse, math.log(4.0))
+    # empty selection
+    o, lse = mla.sparse_mla(q, latent, np.array([0]), np.array([0]), np.full((1, 4), -1), 0.1)[0]
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+def test_sparse_mla_appended_positions():
+    rng = np.random.default_rng(8)
+    latent = rng.normal(size=(30, 576))
+    q = rng.normal(size=(1, 2, 576))
+    idx = np.array([[2, 5, -1]])
+    got = mla.sparse_mla(q, latent, np.array([3]), np.array([0]), idx, 0.05,
+                         n_append=2, append_base=np.array([10]))[0]
+    want = mla.sparse_mla(q, latent, np.array([3]), np.array([0]),
+                          np.array([[2, 5, 11, 12]]), 0.05)[0]
+    assert np.allclose(got[0], want[0], rtol=1e-14) and np.allclose(got[1], want[1], rtol=1e-14)
+
+
+# --------------------------------------------------------------------- acceptance
+
+def test_accept_hand_worked():
+    draft = np.array([[5, 6, 7], [5, 6, 7], [5, 6, 7], [42, 42, 42], [1, 2, 3]])
+    tgt = np.array([[5, 6, 7, 99],      # all match -> 3, bonus 99
+                    [9, 6, 7, 99],      # mismatch at 0 -> 0, next 9
+                    [5, 6, 8, 99],      # mismatch at 2 -> 2, next 8
+                    [42, 42, 42, 77],   # sentinel row -> 0 accepted, next = argmax[0]
+                    [1, 2, 3, 4]])
+    n, nxt = accept.accept_greedy(draft, tgt, magic_draft_id=42)
+    assert n.tolist() == [3, 0, 2, 0, 3]
+    assert nxt.tolist() == [99, 9, 8, 42, 4]
+    n, nxt = accept.accept_greedy(draft, tgt, magic_draft_id=-1)
+    assert n.tolist() == [3, 0, 2, 3, 3]
+
+
+def test_accept_k0():
+    n, nxt = accept.accept_greedy(np.zeros((2, 0), dtype=np.int64), np.array([[3], [4]]))
+    assert n.tolist() == [0, 0] and nxt.tolist() == [3, 4]
+
+
+def test_accept_length_closed_form():
+    # synthetic acceptance with per-position probability p: mean accept length
+    # 1 + sum_{i=1..K} p^i = 2.76 for p = 0.67065, K = 5
+    from mtp_speculative_decode_gb300 import workloads as W
+    p, K = W.ACCEPT_P, 5
+    assert abs(1 + sum(p ** i for i in range(1, K + 1)) - 2.76) < 1e-3
+    import torch as _t
+    B = 200000
+    draft = W.integers(11, "draft_tokens", (B, K), 0, W.GLM_VOCAB)
+    tgt = W.synthetic_argmax(11, draft, W.GLM_VOCAB, p).numpy()
+    d = draft.numpy()
+    match = d == tgt[:, :K]
+    n = np.argmin(np.concatenate([match, np.zeros((B, 1), bool)], 1), axis=1)
+    mean = 1 + n.mean()
+    assert abs(mean - 2.76) < 4 * n.std() / math.sqrt(B) + 1e-3
+    # the oracle agrees with this direct count on a slice
+    n2, _ = accept.accept_greedy(d[:500], tgt[:500])
+    assert np.array_equal(n2, n[:500])
+
+
+# --------------------------------------------------------------------- write-back
+
+def test_writeback_bytes():
+    rng = np.random.default_rng(9)
+    B, W, T = 3, 6, 40
+    src_l = rng.normal(size=(B, W, 576)).astype(np.float32)
+    src_k = rng.integers(0, 256, (B, W, 128), dtype=np.uint8)
+    src_s = rng.uniform(size=(B, W)).astype(np.float32)
+    dst_l = rng.normal(size=(T, 576)).astype(np.float32)
+    dst_k = rng.integers(0, 256, (T, 128), dtype=np.uint8)
+    dst_s = rng.uniform(size=T).astype(np.float32)
+    acc = np.array([1, 6, 3])
+    start = np.array([2, 10, 30])
+    ol, ok, os_ = writeback.kv_writeback(src_l, src_k, src_s, acc, dst_l, dst_k, dst_s, start)
+    written = np.zeros(T, bool)
+    for b in range(B):
+        for i in range(acc[b]):
+            t = start[b] + i
+            written[t] = True
+            assert ol[t].tobytes() == src_l[b, i].tobytes()
+            assert ok[t].tobytes() == src_k[b, i].tobytes()
+            assert os_[t].tobytes() == src_s[b, i].tobytes()
+    assert ol[~written].tobytes() == dst_l[~written].tobytes()
+    assert ok[~written].tobytes() == dst_k[~written].tobytes()
+    assert os_[~written].tobytes() == dst_s[~written].tobytes()
+    assert written.sum() == 1 + 6 + 3
+
+
+# --------------------------------------------------------------------- index sharing
+
+def test_share_gather_rows():
+    s0 = np.arange(12).reshape(6, 2)
+    ro = np.array([0, 2, 6])
+    assert share.topk_share_gather(s0, ro, np.array([1, 3])).tolist() == [[2, 3], [10, 11]]
+    assert share.topk_share_gather(s0, ro, None).tolist() == [[0, 1], [4, 5]]
+
+
+def test_shared_steps_equal_rerun_when_context_below_k():
+    """When P_b + j + 1 <= k the indexer selects everything visible, so the
+    shared set plus the appended positions equals rerunning the indexer."""
+    rng = np.random.default_rng(10)
+    H, D, P = 2, 16, 30
+    k_cache = rng.normal(size=(P + 8, D))
+    k = 64
+    q0 = rng.normal(size=(1, H, D))
+    s0 = topk.topk_select(indexer.indexer_scores(q0, None, np.ones((1, H)), k_cache, None,
+                                                 np.array([0]), np.array([0]), np.array([P]),
+                                                 fp8=False)[0], k)
+    for j in range(1, 4):
+        qj = rng.normal(size=(1, H, D))
+        rerun = topk.topk_select(indexer.indexer_scores(qj, None, np.ones((1, H)), k_cache, None,
+                                                        np.array([0]), np.array([0]),
+                                                        np.array([P + j]), fp8=False)[0], k)
+        shared = share.shared_step_positions(s0, P, j)
+        assert sorted(shared) == sorted(int(x) for x in rerun if x >= 0)
