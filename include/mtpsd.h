@@ -1,0 +1,252 @@
+/*
+ * mtpsd — decode-time DSA sparse attention for MTP speculative decoding on
+ * one NVIDIA GB300 (sm_103a).  C ABI of libmtpsd.so.
+ *
+ * Source pages cited below (title, section):
+ *   [P1] "MAX 中 GLM-5.2 (DeepSeek-V3.2 Sparse) 的统一 MTP 推测解码架构解析"
+ *   [P2] "GLM-5.3 推理全链路(十四):MTP 的三段前向——草稿、验证与 draft_extend 的算子与通信账"
+ *   [P3] "MAX Pipeline 中的 DeepSeek-V3.2 架构实现解析:稀疏注意力、Lightning Indexer 与 MoE 并行推理"
+ *   [P4] "MAX 推测解码配置指南:解读 max.pipelines.speculative 模块"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument is a DEVICE pointer owned by the caller, unless the
+ *   comment says "host".  The library never allocates device memory and never
+ *   frees caller memory; scratch space is a caller-provided workspace whose
+ *   size the matching *_workspace_size() query returns.
+ * - Every call that takes a stream is asynchronous on that stream (a
+ *   cudaStream_t passed as void*; NULL = the legacy default stream), makes no
+ *   host<->device copy and does not synchronize.
+ * - Return value: MTPSD_OK (0) or a negative MTPSD_E* code.  Argument and
+ *   shape checks run on the host before any launch; on failure nothing is
+ *   launched and mtpsd_last_error() describes the problem (thread-local).
+ * - Device-side range violations (an index outside the visible context, a
+ *   write outside the pool) skip the offending element and OR a MTPSD_STATUS_*
+ *   bit into *dev_status (an int32 the caller zeroes; NULL = not reported).
+ *   Kernels never trap.  Every device-side wait is bounded: on expiry the
+ *   kernel ORs MTPSD_STATUS_WAIT_TIMEOUT, releases what it holds and returns.
+ * - Cache layout: a flat pool of tokens; request b owns the contiguous pool
+ *   rows starting at cache_start[b] (int64); position s of request b is pool
+ *   row cache_start[b] + s.
+ * - Query rows are grouped by request: the rows of request b are
+ *   row_offsets[b] .. row_offsets[b+1]-1 (uint32 [B+1], exclusive prefix sum,
+ *   the same convention as merged_offsets of mtpsd_merge_tokens).  Row r sits
+ *   at position row_pos[r] of its request and sees positions 0..row_pos[r]
+ *   (chain causal mask, [P2] "验证输入是怎么拼出来的"; the row's own key is
+ *   already in the cache, [P2] "验证段的逐层算子" op 3).
+ */
+#ifndef MTPSD_H
+#define MTPSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+#define MTPSD_OK 0
+#define MTPSD_EINVAL (-1)        /* bad argument, shape or alignment */
+#define MTPSD_EUNSUPPORTED (-2)  /* valid but not implemented (dtype, head dim) */
+#define MTPSD_ECUDA (-3)         /* a CUDA runtime call or launch failed */
+#define MTPSD_EWORKSPACE (-4)    /* workspace missing or too small */
+
+/* element types */
+#define MTPSD_F32 0
+#define MTPSD_BF16 1
+#define MTPSD_FP8_E4M3 2
+
+/* bits ORed into *dev_status */
+#define MTPSD_STATUS_INDEX_RANGE 1   /* a selected index outside 0..row_pos (skipped) */
+#define MTPSD_STATUS_WRITE_RANGE 2   /* a write-back row outside the pool (skipped) */
+#define MTPSD_STATUS_WAIT_TIMEOUT 4  /* a bounded device wait expired (kernel gave up) */
+#define MTPSD_STATUS_ROW_RANGE 8     /* a row position outside its request's pool rows (skipped) */
+
+/* ------------------------------------------------------------------------
+ * Ragged token merge.  [P4] "Token 合并:RaggedTokenMerger 与 ragged_token_merger"
+ * and [P1] "阶段 1:Token 合并".
+ *   prompt_tokens  [S] int64        prompt_offsets [B+1] uint32 (exclusive prefix sum)
+ *   draft_tokens   [B, K] int64     (row-major; K may be 0)
+ *   merged_tokens  [S + B*K] int64  merged_offsets [B+1] uint32
+ * merged_offsets[i] = prompt_offsets[i] + i*K; request b's merged segment is
+ * its prompt tokens followed by its K drafts.  S is the host-known total
+ * (= prompt_offsets[B]).  B >= 1, K >= 0.
+ */
+int mtpsd_merge_tokens(const int64_t* prompt_tokens, int64_t S, const uint32_t* prompt_offsets,
+                       const int64_t* draft_tokens, int32_t B, int32_t K,
+                       int64_t* merged_tokens, uint32_t* merged_offsets, void* stream);
+
+/* Host mirror of the merged offsets, so a caller building a CUDA graph needs
+ * no device->host copy ([P4], compute_host_merged_offsets).  All host pointers:
+ * prompt_offsets [B+1], out [B+1]. */
+void mtpsd_host_merged_offsets(const uint32_t* prompt_offsets, int32_t B, int32_t K, uint32_t* out);
+
+/* ------------------------------------------------------------------------
+ * Dynamic FP8 E4M3 quantization with one float32 scale per block of 128
+ * contiguous values.  [P3] "Indexer 的结构与计算流程" (q and k quantized to FP8
+ * with block size 128) and "双 KV 缓存" (float32 scale per token).
+ *   x [n_blocks*128] float32 -> codes [n_blocks*128] uint8, scales [n_blocks] float32
+ * scale = amax/448 (1 when amax == 0), code = round-to-nearest-even,
+ * saturating, of x/scale (float32 division).
+ */
+int mtpsd_quantize_fp8_block128(const float* x, int64_t n_blocks, uint8_t* codes, float* scales,
+                                void* stream);
+
+/* ------------------------------------------------------------------------
+ * Lightning-indexer scores and per-row top-k in one call.
+ * [P3] "Indexer 的结构与计算流程" (index heads, weights_proj, FP8 block-128,
+ * the fused mla_fp8_index_top_k output of shape (total_seq_len, index_topk));
+ * [P2] "验证段的逐层算子" ops 5-6 (every verify query scores the history and
+ * picks its own 2048).  Score of row r at position s (0 <= s <= row_pos[r]):
+ *   I[r,s] = sum_h w[r,h] * ReLU( q_scale[r,h] * k_scale[s] * sum_d q[r,h,d]*k[s,d] )
+ * (float32 configuration: the scales are 1).  topk_idx[r, :] holds the
+ * positions of the topk largest I[r, .] (ties to the lower position), in
+ * ascending position order, padded with -1 when row_pos[r]+1 < topk.
+ */
+typedef struct {
+  int32_t B;               /* requests */
+  int32_t R;               /* query rows, = row_offsets[B] */
+  int32_t n_heads;         /* indexer heads H (64 in the FP8 production shape) */
+  int32_t head_dim;        /* D: 128 for MTPSD_FP8_E4M3 (one scale per head vector); any multiple of 4 up to 256 for MTPSD_F32 */
+  int32_t topk;            /* k, 1..4096 */
+  int32_t dtype;           /* MTPSD_FP8_E4M3 or MTPSD_F32 (q, k_cache) */
+  const void* q;           /* [R, H, D] uint8 codes or float32 */
+  const float* q_scale;    /* [R, H] (FP8 only, else NULL) */
+  const float* weights;    /* [R, H] per-head weights (weights_proj output) */
+  const void* k_cache;     /* [pool_tokens, D] uint8 codes or float32 */
+  const float* k_scale;    /* [pool_tokens] (FP8 only, else NULL) */
+  int64_t pool_tokens;
+  const int64_t* cache_start; /* [B] */
+  const uint32_t* row_offsets; /* [B+1] */
+  const int64_t* row_pos;  /* [R] */
+  int64_t max_visible;     /* host-known bound >= row_pos[r]+1 for every r; sizes the score buffer */
+  int32_t* topk_idx;       /* [R, topk] out */
+  float* topk_score;       /* [R, topk] out, nullable (score of each selected position, -inf on padding) */
+  float* scores;           /* [R, ld] out, nullable: the raw scores, ld = mtpsd_scores_ld(max_visible) */
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* dev_status;     /* nullable */
+} mtpsd_indexer_args;
+
+/* Row stride (floats) of the score matrix for a given max_visible. */
+int64_t mtpsd_scores_ld(int64_t max_visible);
+size_t mtpsd_indexer_topk_workspace_size(int32_t B, int32_t R, int64_t max_visible, int32_t topk);
+int mtpsd_indexer_topk(const mtpsd_indexer_args* args, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Standalone per-row top-k over a score matrix (the selection half of the
+ * call above, for callers that produce scores themselves).
+ *   scores [R, ld] float32, row_len [R] int64 (valid prefix of each row)
+ *   -> out_idx [R, topk] (ascending positions, -1 padded), out_score nullable.
+ * NaN scores are not supported.
+ */
+size_t mtpsd_topk_workspace_size(int32_t R, int32_t topk);
+int mtpsd_topk(const float* scores, int64_t ld, int32_t R, const int64_t* row_len, int64_t max_len,
+               int32_t topk, int32_t* out_idx, float* out_score, void* workspace,
+               size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Sparse MLA decode over the selected latent rows.
+ * [P2] "GLM-5.3 的草稿层到底长什么样" (kv_lora_rank 512 + qk_rope 64 = 576),
+ * "验证段的逐层算子" op 7; [P3] "稀疏 MLA 的前向路径".  With the absorbed query
+ * the key of position s is latent[s, 0:576] and its value latent[s, 0:512]:
+ *   o[r,h]   = sum_j softmax_j(scale * q[r,h,:].latent[s_j,:]) * latent[s_j, 0:512]
+ *   lse[r,h] = log sum_j exp(scale * q[r,h,:].latent[s_j,:])     (natural log)
+ * over the valid positions s_j of idx[r, 0:n_idx] (-1 = padding, skipped) and,
+ * when n_append > 0, the appended positions append_base[r]+1 .. append_base[r]+n_append
+ * ([P1] "阶段 5:Draft 后续步骤(复用 top-k)": the MLA cache grows by one per draft
+ * step while the shared indexer selection stays fixed).  Every position must
+ * satisfy 0 <= s <= row_pos[r] + row_pos_add; others are skipped and flagged.
+ * A row with no valid position gets o = 0 and lse = -inf.
+ */
+typedef struct {
+  int32_t B;
+  int32_t R;
+  int32_t n_heads;         /* query heads H: a multiple of 16 for MTPSD_BF16, any for MTPSD_F32 */
+  int32_t d_latent;        /* 576 */
+  int32_t d_v;             /* 512 */
+  int32_t n_idx;           /* selected entries per row (row stride of idx) */
+  int32_t n_append;        /* appended positions per row (0 = none) */
+  int32_t dtype;           /* MTPSD_BF16 or MTPSD_F32: q, latent and out */
+  float softmax_scale;
+  int64_t row_pos_add;     /* added to row_pos[r] (draft step j of a shared loop passes j) */
+  const void* q;           /* [R, H, d_latent] */
+  const void* latent;      /* [pool_tokens, d_latent] */
+  int64_t pool_tokens;
+  const int64_t* cache_start;  /* [B] */
+  const uint32_t* row_offsets; /* [B+1] */
+  const int64_t* row_pos;      /* [R] */
+  const int32_t* idx;          /* [R, n_idx] */
+  const int64_t* append_base;  /* [R] or NULL when n_append == 0 */
+  void* out;                   /* [R, H, d_v] */
+  float* lse;                  /* [R, H] nullable */
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* dev_status;         /* nullable */
+} mtpsd_mla_args;
+
+size_t mtpsd_sparse_mla_workspace_size(int32_t R, int32_t n_heads, int32_t n_idx, int32_t n_append,
+                                       int32_t dtype);
+int mtpsd_sparse_mla_decode(const mtpsd_mla_args* args, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Greedy acceptance.  [P2] "接受判定:greedy 与 rejection sampling" (accept
+ * while draft == target argmax, stop at the first mismatch); [P1] "阶段 3:拒绝
+ * 采样与 Bitmask" (outputs num_accepted and next_tokens); [P4] MAGIC_DRAFT_TOKEN_ID.
+ *   draft [B, K] int64, target_argmax [B, K+1] int64
+ *   -> num_accepted [B] int32 (n_b), next_tokens [B] int64 (= target_argmax[b, n_b])
+ * magic_draft_id >= 0: a draft row made entirely of that id accepts 0
+ * (42 is the pages' sentinel); -1 disables the check.
+ */
+int mtpsd_accept_greedy(const int64_t* draft, const int64_t* target_argmax, int32_t B, int32_t K,
+                        int64_t magic_draft_id, int32_t* num_accepted, int64_t* next_tokens,
+                        void* stream);
+
+/* ------------------------------------------------------------------------
+ * Accepted-segment KV write-back.  [P2] "KV 交账:接受段的搬移与拒绝段的回收"
+ * and "draft_extend:把接受段写回草稿层" / "草稿层 KV 的账": only the accepted
+ * rows (bonus included: num_accepted[b]+1 rows, at least 1, at most W) of the
+ * W-row window are copied, byte for byte, to positions dst_pos[b] + i of
+ * request b (pool rows cache_start[b] + dst_pos[b] + i); rejected rows are not
+ * written.  Both caches of the layer move together.
+ *   src_latent [B, W, 576] (latent_dtype: MTPSD_BF16 or MTPSD_F32)
+ *   src_idxk [B, W, idx_dim] uint8, src_idxs [B, W] float32
+ *   dst_latent [pool_tokens, 576], dst_idxk [pool_tokens, idx_dim], dst_idxs [pool_tokens]
+ *   cache_start [B], dst_pos [B] int64
+ *   next_pos [B] int64 out, nullable: dst_pos[b] + num_accepted[b] + 1, the
+ *   position of the next draft row.
+ * idx_dim is the key size in bytes per token (128 for FP8 keys, a multiple
+ * of 16), or 0 to move the latent only (then src_idxk/dst_idxk may be NULL).
+ * src_idxs/dst_idxs may both be NULL when the keys carry no scale (float32
+ * keys).  A destination row outside the pool is skipped and flagged
+ * MTPSD_STATUS_WRITE_RANGE.
+ */
+int mtpsd_kv_writeback(const void* src_latent, const uint8_t* src_idxk, const float* src_idxs,
+                       int32_t B, int32_t W, int32_t latent_dtype, int32_t idx_dim,
+                       const int32_t* num_accepted, void* dst_latent, uint8_t* dst_idxk,
+                       float* dst_idxs, const int64_t* cache_start, const int64_t* dst_pos,
+                       int64_t pool_tokens, int64_t* next_pos, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * index_share_for_mtp_iteration gather.  [P1] "阶段 5:Draft 后续步骤(复用
+ * top-k)" (gather_accepted_hidden_states over step0_topk at num_accepted);
+ * [P2] "索引器复用的收益与边界" (compact_topk_indices: one row per request).
+ *   step0_topk [R0, k] int32, row_offsets [B+1] uint32 (rows of each request
+ *   in the step-0 output), num_accepted [B] int32 or NULL (row 0 of each
+ *   segment) -> shared_idx[b, :] = step0_topk[row_offsets[b] + num_accepted[b], :].
+ * A local row outside the request's segment is clamped to its last row and
+ * flagged MTPSD_STATUS_INDEX_RANGE.
+ */
+int mtpsd_topk_share_gather(const int32_t* step0_topk, const uint32_t* row_offsets,
+                            const int32_t* num_accepted, int32_t B, int32_t k, int32_t* shared_idx,
+                            int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+const char* mtpsd_last_error(void);
+int32_t mtpsd_version(void); /* 100*major + minor */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MTPSD_H */

@@ -1,0 +1,216 @@
+// C ABI of libmtpsd: host-side argument checks, workspace carving and
+// dispatch to the kernels.  Nothing here allocates device memory.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mtpsd {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+static int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace mtpsd
+
+using namespace mtpsd;
+
+extern "C" {
+
+const char* mtpsd_last_error(void) { return g_err; }
+
+int32_t mtpsd_version(void) { return 100; }
+
+int mtpsd_merge_tokens(const int64_t* prompt_tokens, int64_t S, const uint32_t* prompt_offsets,
+                       const int64_t* draft_tokens, int32_t B, int32_t K, int64_t* merged_tokens,
+                       uint32_t* merged_offsets, void* stream) {
+  g_err[0] = 0;
+  if (B < 1 || K < 0 || S < 0) return fail(MTPSD_EINVAL, "merge_tokens: need B >= 1, K >= 0, S >= 0");
+  if (!prompt_offsets || !merged_offsets || (S > 0 && !prompt_tokens) || (K > 0 && !draft_tokens) ||
+      (S + (int64_t)B * K > 0 && !merged_tokens))
+    return fail(MTPSD_EINVAL, "merge_tokens: null pointer");
+  if (S + (int64_t)B * K > 0xffffffffLL) return fail(MTPSD_EINVAL, "merge_tokens: merged length exceeds uint32 offsets");
+  return launch_merge_tokens(prompt_tokens, S, prompt_offsets, draft_tokens, B, K, merged_tokens, merged_offsets,
+                             (cudaStream_t)stream);
+}
+
+void mtpsd_host_merged_offsets(const uint32_t* prompt_offsets, int32_t B, int32_t K, uint32_t* out) {
+  for (int32_t i = 0; i <= B; ++i) out[i] = prompt_offsets[i] + (uint32_t)((int64_t)i * K);
+}
+
+int mtpsd_quantize_fp8_block128(const float* x, int64_t n_blocks, uint8_t* codes, float* scales, void* stream) {
+  g_err[0] = 0;
+  if (n_blocks < 0) return fail(MTPSD_EINVAL, "quantize: n_blocks < 0");
+  if (n_blocks == 0) return MTPSD_OK;
+  if (!x || !codes || !scales) return fail(MTPSD_EINVAL, "quantize: null pointer");
+  if (!aligned(x, 16) || !aligned(codes, 4))
+    return fail(MTPSD_EINVAL, "quantize: x must be 16-byte and codes 4-byte aligned");
+  return launch_quantize_fp8(x, n_blocks, codes, scales, (cudaStream_t)stream);
+}
+
+int64_t mtpsd_scores_ld(int64_t max_visible) { return (int64_t)align_up((size_t)(max_visible > 0 ? max_visible : 1), 4); }
+
+size_t mtpsd_indexer_topk_workspace_size(int32_t B, int32_t R, int64_t max_visible, int32_t topk) {
+  (void)topk;
+  size_t scores = (size_t)R * (size_t)mtpsd_scores_ld(max_visible) * sizeof(float);
+  size_t tiles = align_up(((size_t)B + 1) * sizeof(int32_t), 256);
+  return align_up(scores, 256) + tiles;
+}
+
+int mtpsd_indexer_topk(const mtpsd_indexer_args* a, void* stream) {
+  g_err[0] = 0;
+  if (!a) return fail(MTPSD_EINVAL, "indexer_topk: null args");
+  if (a->B < 1 || a->R < 0 || a->n_heads < 1 || a->topk < 1 || a->topk > 4096)
+    return fail(MTPSD_EINVAL, "indexer_topk: need B >= 1, R >= 0, n_heads >= 1, 1 <= topk <= 4096");
+  if (a->max_visible < 0 || a->max_visible > 0x7fffffffLL)
+    return fail(MTPSD_EINVAL, "indexer_topk: max_visible out of range");
+  if (a->dtype == MTPSD_FP8_E4M3) {
+    if (a->head_dim != 128) return fail(MTPSD_EUNSUPPORTED, "indexer_topk: FP8 needs head_dim 128 (one block-128 scale per head)");
+    if (!a->q_scale || !a->k_scale) return fail(MTPSD_EINVAL, "indexer_topk: FP8 needs q_scale and k_scale");
+  } else if (a->dtype == MTPSD_F32) {
+    if (a->head_dim < 1 || a->head_dim > 256) return fail(MTPSD_EUNSUPPORTED, "indexer_topk: float32 head_dim 1..256");
+  } else {
+    return fail(MTPSD_EUNSUPPORTED, "indexer_topk: dtype must be MTPSD_FP8_E4M3 or MTPSD_F32");
+  }
+  if ((size_t)a->n_heads * a->head_dim > 16384) return fail(MTPSD_EUNSUPPORTED, "indexer_topk: n_heads*head_dim > 16384");
+  if (a->R == 0) return MTPSD_OK;
+  if (!a->q || !a->weights || !a->k_cache || !a->cache_start || !a->row_offsets || !a->row_pos || !a->topk_idx)
+    return fail(MTPSD_EINVAL, "indexer_topk: null pointer");
+  size_t need = mtpsd_indexer_topk_workspace_size(a->B, a->R, a->max_visible, a->topk);
+  if (!a->workspace || a->workspace_bytes < need)
+    return fail(MTPSD_EWORKSPACE, "indexer_topk: workspace of %zu bytes needed, %zu given", need, a->workspace_bytes);
+  if (!aligned(a->workspace, 256)) return fail(MTPSD_EINVAL, "indexer_topk: workspace must be 256-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t ld = mtpsd_scores_ld(a->max_visible);
+  float* scores = a->scores ? a->scores : (float*)a->workspace;
+  IndexerPlan p;
+  p.B = a->B; p.R = a->R; p.H = a->n_heads; p.D = a->head_dim; p.dtype = a->dtype;
+  p.q = a->q; p.q_scale = a->q_scale; p.w = a->weights; p.k = a->k_cache; p.k_scale = a->k_scale;
+  p.pool = a->pool_tokens; p.cache_start = a->cache_start; p.row_offsets = a->row_offsets; p.row_pos = a->row_pos;
+  p.max_visible = a->max_visible; p.scores = scores; p.ld = ld;
+  p.tile_offsets = (int32_t*)((char*)a->workspace + align_up((size_t)a->R * ld * sizeof(float), 256));
+  p.status = a->dev_status;
+  int rc = indexer_tc_supported(p) ? launch_indexer_scores_tc(p, st) : launch_indexer_scores(p, st);
+  if (rc) return rc;
+  TopkPlan t;
+  t.scores = scores; t.ld = ld; t.R = a->R; t.row_len = a->row_pos; t.len_plus_one = 1;
+  t.max_len = a->max_visible; t.k = a->topk; t.out_idx = a->topk_idx; t.out_score = a->topk_score;
+  t.status = a->dev_status;
+  return launch_topk(t, st);
+}
+
+size_t mtpsd_topk_workspace_size(int32_t R, int32_t topk) {
+  (void)R; (void)topk;
+  return 0;
+}
+
+int mtpsd_topk(const float* scores, int64_t ld, int32_t R, const int64_t* row_len, int64_t max_len, int32_t topk,
+               int32_t* out_idx, float* out_score, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+               void* stream) {
+  g_err[0] = 0;
+  (void)workspace; (void)workspace_bytes;
+  if (R < 0 || topk < 1 || topk > 4096 || max_len < 0 || max_len > 0x7fffffffLL || ld < max_len)
+    return fail(MTPSD_EINVAL, "topk: need R >= 0, 1 <= topk <= 4096, 0 <= max_len <= ld");
+  if (R == 0) return MTPSD_OK;
+  if (!scores || !row_len || !out_idx) return fail(MTPSD_EINVAL, "topk: null pointer");
+  TopkPlan t;
+  t.scores = scores; t.ld = ld; t.R = R; t.row_len = row_len; t.len_plus_one = 0; t.max_len = max_len;
+  t.k = topk; t.out_idx = out_idx; t.out_score = out_score; t.status = dev_status;
+  return launch_topk(t, (cudaStream_t)stream);
+}
+
+size_t mtpsd_sparse_mla_workspace_size(int32_t R, int32_t n_heads, int32_t n_idx, int32_t n_append, int32_t dtype) {
+  if (R <= 0 || n_heads <= 0 || n_idx < 0 || n_append < 0) return 0;
+  return mla_workspace_bytes(R, n_heads, n_idx, n_append, dtype);
+}
+
+int mtpsd_sparse_mla_decode(const mtpsd_mla_args* a, void* stream) {
+  g_err[0] = 0;
+  if (!a) return fail(MTPSD_EINVAL, "sparse_mla_decode: null args");
+  if (a->B < 1 || a->R < 0 || a->n_heads < 1 || a->n_idx < 0 || a->n_append < 0)
+    return fail(MTPSD_EINVAL, "sparse_mla_decode: need B >= 1, R >= 0, n_heads >= 1, n_idx >= 0, n_append >= 0");
+  if (a->d_latent != 576 || a->d_v != 512)
+    return fail(MTPSD_EUNSUPPORTED, "sparse_mla_decode: d_latent must be 576 and d_v 512");
+  if ((int64_t)a->n_idx + a->n_append > 65536) return fail(MTPSD_EUNSUPPORTED, "sparse_mla_decode: more than 65536 positions per row");
+  if (a->dtype == MTPSD_BF16) {
+    if (a->n_heads % 16) return fail(MTPSD_EUNSUPPORTED, "sparse_mla_decode: bf16 needs n_heads % 16 == 0");
+  } else if (a->dtype != MTPSD_F32) {
+    return fail(MTPSD_EUNSUPPORTED, "sparse_mla_decode: dtype must be MTPSD_BF16 or MTPSD_F32");
+  }
+  if (a->n_append > 0 && !a->append_base) return fail(MTPSD_EINVAL, "sparse_mla_decode: n_append > 0 needs append_base");
+  if (a->R == 0) return MTPSD_OK;
+  if (!a->q || !a->latent || !a->cache_start || !a->row_offsets || !a->row_pos || !a->out || (a->n_idx > 0 && !a->idx))
+    return fail(MTPSD_EINVAL, "sparse_mla_decode: null pointer");
+  if (a->dtype == MTPSD_BF16 && (!aligned(a->q, 16) || !aligned(a->latent, 16) || !aligned(a->out, 4)))
+    return fail(MTPSD_EINVAL, "sparse_mla_decode: q and latent must be 16-byte aligned");
+  MlaPlan p;
+  p.B = a->B; p.R = a->R; p.H = a->n_heads; p.d_latent = a->d_latent; p.d_v = a->d_v; p.n_idx = a->n_idx;
+  p.n_append = a->n_append; p.dtype = a->dtype; p.scale = a->softmax_scale; p.row_pos_add = a->row_pos_add;
+  p.q = a->q; p.latent = a->latent; p.pool = a->pool_tokens; p.cache_start = a->cache_start;
+  p.row_offsets = a->row_offsets; p.row_pos = a->row_pos; p.idx = a->idx; p.append_base = a->append_base;
+  p.out = a->out; p.lse = a->lse; p.ws = a->workspace; p.ws_bytes = a->workspace_bytes; p.status = a->dev_status;
+  return launch_sparse_mla(p, (cudaStream_t)stream);
+}
+
+int mtpsd_accept_greedy(const int64_t* draft, const int64_t* target_argmax, int32_t B, int32_t K,
+                        int64_t magic_draft_id, int32_t* num_accepted, int64_t* next_tokens, void* stream) {
+  g_err[0] = 0;
+  if (B < 0 || K < 0) return fail(MTPSD_EINVAL, "accept_greedy: need B >= 0, K >= 0");
+  if (B == 0) return MTPSD_OK;
+  if ((K > 0 && !draft) || !target_argmax || !num_accepted || !next_tokens)
+    return fail(MTPSD_EINVAL, "accept_greedy: null pointer");
+  return launch_accept_greedy(draft, target_argmax, B, K, magic_draft_id, num_accepted, next_tokens,
+                              (cudaStream_t)stream);
+}
+
+int mtpsd_kv_writeback(const void* src_latent, const uint8_t* src_idxk, const float* src_idxs, int32_t B, int32_t W,
+                       int32_t latent_dtype, int32_t idx_dim, const int32_t* num_accepted, void* dst_latent,
+                       uint8_t* dst_idxk, float* dst_idxs, const int64_t* cache_start, const int64_t* dst_pos, int64_t pool_tokens,
+                       int64_t* next_pos, int32_t* dev_status, void* stream) {
+  g_err[0] = 0;
+  if (B < 0 || W < 1 || pool_tokens < 0 || B > 65535) return fail(MTPSD_EINVAL, "kv_writeback: need 0 <= B <= 65535, W >= 1");
+  int lat_bytes;
+  if (latent_dtype == MTPSD_BF16) lat_bytes = 576 * 2;
+  else if (latent_dtype == MTPSD_F32) lat_bytes = 576 * 4;
+  else return fail(MTPSD_EUNSUPPORTED, "kv_writeback: latent dtype must be MTPSD_BF16 or MTPSD_F32");
+  if (idx_dim != 0 && idx_dim % 16) return fail(MTPSD_EUNSUPPORTED, "kv_writeback: idx_dim must be a multiple of 16");
+  if (B == 0) return MTPSD_OK;
+  if (!src_latent || !dst_latent || !num_accepted || !cache_start || !dst_pos) return fail(MTPSD_EINVAL, "kv_writeback: null pointer");
+  if (idx_dim && (!src_idxk || !dst_idxk)) return fail(MTPSD_EINVAL, "kv_writeback: null indexer key pointer");
+  if ((src_idxs == nullptr) != (dst_idxs == nullptr)) return fail(MTPSD_EINVAL, "kv_writeback: give both key scale pointers or neither");
+  if (!aligned(src_latent, 16) || !aligned(dst_latent, 16) || (idx_dim && (!aligned(src_idxk, 16) || !aligned(dst_idxk, 16))))
+    return fail(MTPSD_EINVAL, "kv_writeback: latent and key buffers must be 16-byte aligned");
+  return launch_kv_writeback(src_latent, src_idxk, src_idxs, B, W, lat_bytes, idx_dim, num_accepted, dst_latent,
+                             dst_idxk, dst_idxs, cache_start, dst_pos, pool_tokens, next_pos, dev_status, (cudaStream_t)stream);
+}
+
+int mtpsd_topk_share_gather(const int32_t* step0_topk, const uint32_t* row_offsets, const int32_t* num_accepted,
+                            int32_t B, int32_t k, int32_t* shared_idx, int32_t* dev_status, void* stream) {
+  g_err[0] = 0;
+  if (B < 0 || k < 1) return fail(MTPSD_EINVAL, "topk_share_gather: need B >= 0, k >= 1");
+  if (B == 0) return MTPSD_OK;
+  if (!step0_topk || !row_offsets || !shared_idx) return fail(MTPSD_EINVAL, "topk_share_gather: null pointer");
+  if ((k & 3) == 0 && (!aligned(step0_topk, 16) || !aligned(shared_idx, 16)))
+    return fail(MTPSD_EINVAL, "topk_share_gather: buffers must be 16-byte aligned when k % 4 == 0");
+  return launch_share_gather(step0_topk, row_offsets, num_accepted, B, k, shared_idx, dev_status, (cudaStream_t)stream);
+}
+
+}  // extern "C"

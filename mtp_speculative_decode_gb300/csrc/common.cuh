@@ -1,0 +1,62 @@
+// Shared device/host helpers of libmtpsd (internal header).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mtpsd.h"
+
+#define MTPSD_HD __host__ __device__ __forceinline__
+
+namespace mtpsd {
+
+// Thread-local error message for mtpsd_last_error().
+void set_error(const char* fmt, ...);
+
+inline int check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("%s: %s", what, cudaGetErrorString(e));
+    return MTPSD_ECUDA;
+  }
+  return MTPSD_OK;
+}
+
+__device__ __forceinline__ void flag_status(int32_t* st, int32_t bit) {
+  if (st) atomicOr(st, bit);
+}
+
+// Request owning query row r: the b with row_offsets[b] <= r < row_offsets[b+1].
+__device__ __forceinline__ int request_of_row(const uint32_t* row_offsets, int B, uint32_t r) {
+  int lo = 0, hi = B;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (row_offsets[mid] <= r) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+MTPSD_HD int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline int num_sms() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  return sms;
+}
+
+// Order-preserving map of a float to uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);   // -0 and +0 compare equal
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(u);
+}
+
+}  // namespace mtpsd

@@ -1,0 +1,57 @@
+// Internal launchers of libmtpsd (called by api.cu after argument checks).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mtpsd {
+
+int launch_merge_tokens(const int64_t* prompt, int64_t S, const uint32_t* po, const int64_t* draft,
+                        int B, int K, int64_t* out, uint32_t* mo, cudaStream_t st);
+int launch_quantize_fp8(const float* x, int64_t n_blocks, uint8_t* codes, float* scales, cudaStream_t st);
+int launch_accept_greedy(const int64_t* draft, const int64_t* tgt, int B, int K, int64_t magic,
+                         int32_t* n_acc, int64_t* next, cudaStream_t st);
+int launch_kv_writeback(const void* src_l, const uint8_t* src_k, const float* src_s, int B, int W,
+                        int lat_bytes, int idx_bytes, const int32_t* n_acc, void* dst_l, uint8_t* dst_k,
+                        float* dst_s, const int64_t* cache_start, const int64_t* dst_pos, int64_t pool, int64_t* next_pos,
+                        int32_t* status, cudaStream_t st);
+int launch_share_gather(const int32_t* s0, const uint32_t* ro, const int32_t* n_acc, int B, int k,
+                        int32_t* out, int32_t* status, cudaStream_t st);
+
+// indexer scores into a [R, ld] float matrix (positions > row_pos are not written)
+struct IndexerPlan {
+  int B, R, H, D, dtype;
+  const void* q; const float* q_scale; const float* w;
+  const void* k; const float* k_scale; int64_t pool;
+  const int64_t* cache_start; const uint32_t* row_offsets; const int64_t* row_pos;
+  int64_t max_visible; float* scores; int64_t ld;
+  int32_t* tile_offsets;   // [B+1] workspace
+  int32_t* status;
+};
+int launch_indexer_scores(const IndexerPlan& p, cudaStream_t st);
+bool indexer_tc_supported(const IndexerPlan& p);
+int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st);
+
+// top-k over rows of a score matrix; row length = row_len[r] or row_pos[r]+1
+struct TopkPlan {
+  const float* scores; int64_t ld; int R; const int64_t* row_len; int len_plus_one;
+  int64_t max_len; int k; int32_t* out_idx; float* out_score; int32_t* status;
+};
+int launch_topk(const TopkPlan& p, cudaStream_t st);
+
+// sparse MLA
+struct MlaPlan {
+  int B, R, H, d_latent, d_v, n_idx, n_append, dtype;
+  float scale; int64_t row_pos_add;
+  const void* q; const void* latent; int64_t pool;
+  const int64_t* cache_start; const uint32_t* row_offsets; const int64_t* row_pos;
+  const int32_t* idx; const int64_t* append_base;
+  void* out; float* lse;
+  void* ws; size_t ws_bytes;
+  int32_t* status;
+};
+size_t mla_workspace_bytes(int R, int H, int n_idx, int n_append, int dtype);
+int launch_sparse_mla(const MlaPlan& p, cudaStream_t st);
+
+}  // namespace mtpsd

@@ -1,0 +1,208 @@
+"""One MTP decode step of the DSA layer on the GPU, as a sequence of C-ABI calls.
+
+Order of the step ([P1] "UnifiedMTPGlm5_2 前向传播详解", [P2] "三段前向的分工"):
+
+1. merge_tokens: prompt (bonus) token + K drafts per request -> verify rows
+2. quantize_fp8_block128 of the indexer queries (dynamic FP8, block 128)
+3. indexer_topk over the target caches for every verify row
+4. sparse_mla_decode over the selected latent rows
+5. accept_greedy against the target argmax
+6. kv_writeback of the accepted segment into the draft-layer caches
+7. the draft loop with index_share_for_mtp_iteration: indexer + top-k at draft
+   step 0 only, then sparse MLA at steps 0..n-1 over the shared selection plus
+   the positions appended since step 0.
+
+All device buffers are allocated once in __init__ (torch), so a step issues
+only kernel launches of libmtpsd on one stream: no allocation, no host sync.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+from . import api
+from . import workloads as W
+
+
+def _dev_u32(x, device):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.uint32)).to(device)
+
+
+def _dev(x, device, dtype=None):
+    t = torch.as_tensor(x)
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(device).contiguous()
+
+
+class DecodeStep:
+    def __init__(self, w: W.Workload, device="cuda", draft: Optional[Dict[str, torch.Tensor]] = None):
+        self.w = w
+        spec = w.spec
+        self.spec = spec
+        self.device = device
+        self.fp8 = not spec.latent_f32
+        B, K, R = spec.B, spec.K, w.R
+        self.B, self.K, self.R = B, K, R
+        t = w.tensors
+        # --- resident caches (target layer)
+        self.cache_start = _dev(w.cache_start, device, torch.int64)
+        self.latent = _dev(t["latent"], device)
+        if self.fp8:
+            k_raw = _dev(t["k_idx"], device)
+            self.k_cache, k_scale = api.quantize_fp8_block128(k_raw)
+            self.k_scale = k_scale.reshape(-1).contiguous()
+            del k_raw
+        else:
+            self.k_cache = _dev(t["k_idx"], device)
+            self.k_scale = None
+        # --- verify rows (host-known layout)
+        self.row_pos = _dev(w.row_pos, device, torch.int64)
+        self.max_visible = int(w.L.max()) + w.r
+        # --- per-step inputs
+        self.prompt_tokens = _dev(w.prompt_tokens, device, torch.int64)
+        self.prompt_offsets = _dev_u32(w.prompt_offsets, device)
+        self.draft_tokens = _dev(w.draft_tokens, device, torch.int64)
+        self.target_argmax = _dev(w.target_argmax, device, torch.int64)
+        self.q_idx_raw = _dev(t["q_idx"], device)
+        self.w_idx = _dev(t["w_idx"], device)
+        self.q_mla = _dev(t["q_mla"], device)
+        # --- outputs / intermediates
+        S = w.prompt_tokens.shape[0]
+        self.merged_tokens = torch.empty(S + B * K, dtype=torch.int64, device=device)
+        self.merged_offsets = torch.empty(B + 1, dtype=torch.uint32, device=device)
+        if spec.verify:
+            # verify rows are the merged segments (1 input token + K drafts each)
+            host_mo = api.host_merged_offsets(w.prompt_offsets, K)
+            self.row_offsets = _dev_u32(host_mo, device)
+        else:
+            self.row_offsets = _dev_u32(np.arange(B + 1), device)
+        if self.fp8:
+            self.q_idx = torch.empty(self.q_idx_raw.shape, dtype=torch.uint8, device=device)
+            self.q_scale = torch.empty(self.q_idx_raw.shape[:2], dtype=torch.float32, device=device)
+        else:
+            self.q_idx, self.q_scale = self.q_idx_raw, None
+        self.topk_idx = torch.empty(R, spec.topk, dtype=torch.int32, device=device)
+        self.out = torch.empty(R, spec.H_Q, 512, dtype=self.q_mla.dtype, device=device)
+        self.lse = torch.empty(R, spec.H_Q, dtype=torch.float32, device=device)
+        self.num_accepted = torch.empty(B, dtype=torch.int32, device=device)
+        self.next_tokens = torch.empty(B, dtype=torch.int64, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ws_idx = torch.empty(api.indexer_topk_workspace_size(B, R, self.max_visible, spec.topk),
+                                  dtype=torch.uint8, device=device)
+        n = api.sparse_mla_workspace_size(R, spec.H_Q, spec.topk, 0, 1 if self.fp8 else 0)
+        self.ws_mla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+        # --- draft layer
+        self.has_draft = spec.draft_steps > 0
+        if self.has_draft:
+            d = draft if draft is not None else W.draft_tensors(w)
+            self.d_latent = _dev(d["d_latent"], device)
+            if self.fp8:
+                kr = _dev(d["d_k_idx"], device)
+                self.d_k_cache, ks = api.quantize_fp8_block128(kr)
+                self.d_k_scale = ks.reshape(-1).contiguous()
+                sr = _dev(d["src_k_idx"], device)
+                self.src_idxk, ss = api.quantize_fp8_block128(sr)
+                self.src_idxs = ss.reshape(B, -1).contiguous()
+                del kr, sr
+            else:
+                # float32 keys move as raw bytes, without a scale
+                self.d_k_cache = _dev(d["d_k_idx"], device)
+                self.d_k_scale = None
+                self.src_idxk = _dev(d["src_k_idx"], device).view(torch.uint8)
+                self.src_idxs = None
+            self.src_latent = _dev(d["src_latent"], device)
+            self.dst_pos = _dev(w.L, device, torch.int64)    # accepted segment starts at L_b
+            self.next_pos = torch.empty(B, dtype=torch.int64, device=device)
+            self.d_q_idx_raw = _dev(d["d_q_idx"], device)
+            self.d_w_idx = _dev(d["d_w_idx"], device)
+            if self.fp8:
+                self.d_q_idx = torch.empty(self.d_q_idx_raw.shape, dtype=torch.uint8, device=device)
+                self.d_q_scale = torch.empty(self.d_q_idx_raw.shape[:2], dtype=torch.float32, device=device)
+            else:
+                self.d_q_idx, self.d_q_scale = self.d_q_idx_raw, None
+            self.d_q_mla = [_dev(d[f"d_q_mla{j}"], device) for j in range(spec.draft_steps)]
+            self.d_row_offsets = _dev_u32(np.arange(B + 1), device)
+            self.d_max_visible = int(w.L.max()) + (K + 1) + 1
+            self.d_topk = torch.empty(B, spec.topk, dtype=torch.int32, device=device)
+            self.shared_idx = torch.empty(B, spec.topk, dtype=torch.int32, device=device)
+            self.d_out = [torch.empty(B, spec.H_Q, 512, dtype=self.q_mla.dtype, device=device)
+                          for _ in range(spec.draft_steps)]
+            self.d_lse = [torch.empty(B, spec.H_Q, dtype=torch.float32, device=device)
+                          for _ in range(spec.draft_steps)]
+            self.ws_didx = torch.empty(api.indexer_topk_workspace_size(B, B, self.d_max_visible, spec.topk),
+                                       dtype=torch.uint8, device=device)
+            n = max(api.sparse_mla_workspace_size(B, spec.H_Q, spec.topk, j, 1 if self.fp8 else 0)
+                    for j in range(spec.draft_steps))
+            self.ws_dmla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+    # ------------------------------------------------------------------ phases
+    def merge(self, stream=None):
+        api.merge_tokens(self.prompt_tokens, self.prompt_offsets, self.draft_tokens, self.merged_tokens,
+                         self.merged_offsets, stream=stream)
+
+    def verify_indexer(self, stream=None):
+        if self.fp8:
+            api.quantize_fp8_block128(self.q_idx_raw, self.q_idx, self.q_scale, stream=stream)
+        api.indexer_topk(self.q_idx, self.q_scale, self.w_idx, self.k_cache, self.k_scale, self.cache_start,
+                         self.row_offsets, self.row_pos, self.spec.topk, self.max_visible, topk_idx=self.topk_idx,
+                         workspace=self.ws_idx, dev_status=self.status, stream=stream)
+
+    def verify_mla(self, stream=None):
+        api.sparse_mla_decode(self.q_mla, self.latent, self.cache_start, self.row_offsets, self.row_pos,
+                              self.topk_idx, W.SOFTMAX_SCALE, out=self.out, lse=self.lse, workspace=self.ws_mla,
+                              dev_status=self.status, stream=stream)
+
+    def accept(self, stream=None):
+        api.accept_greedy(self.draft_tokens, self.target_argmax, 42, self.num_accepted, self.next_tokens,
+                          stream=stream)
+
+    def writeback(self, stream=None):
+        api.kv_writeback(self.src_latent, self.src_idxk, self.src_idxs, self.num_accepted, self.d_latent,
+                         self.d_k_cache.view(torch.uint8), self.d_k_scale, self.cache_start, self.dst_pos,
+                         next_pos=self.next_pos, dev_status=self.status, stream=stream)
+
+    def draft_indexer(self, stream=None):
+        if self.fp8:
+            api.quantize_fp8_block128(self.d_q_idx_raw, self.d_q_idx, self.d_q_scale, stream=stream)
+        api.indexer_topk(self.d_q_idx, self.d_q_scale, self.d_w_idx, self.d_k_cache, self.d_k_scale,
+                         self.cache_start, self.d_row_offsets, self.next_pos, self.spec.topk, self.d_max_visible,
+                         topk_idx=self.d_topk, workspace=self.ws_didx, dev_status=self.status, stream=stream)
+        api.topk_share_gather(self.d_topk, self.d_row_offsets, None, self.shared_idx, dev_status=self.status,
+                              stream=stream)
+
+    def draft_mla(self, j: int, stream=None):
+        api.sparse_mla_decode(self.d_q_mla[j], self.d_latent, self.cache_start, self.d_row_offsets, self.next_pos,
+                              self.shared_idx, W.SOFTMAX_SCALE, n_append=j,
+                              append_base=self.next_pos if j else None, row_pos_add=j, out=self.d_out[j],
+                              lse=self.d_lse[j], workspace=self.ws_dmla, dev_status=self.status, stream=stream)
+
+    def step(self, stream=None):
+        """The whole hot path once."""
+        if self.spec.verify:
+            self.merge(stream)
+            self.verify_indexer(stream)
+            self.verify_mla(stream)
+        self.accept(stream)
+        if self.has_draft:
+            self.writeback(stream)
+            self.draft_indexer(stream)
+            for j in range(self.spec.draft_steps):
+                self.draft_mla(j, stream)
+
+    def launches_per_step(self) -> int:
+        """Kernel launches of one step (for the benchmark's launch count)."""
+        n = 0
+        if self.spec.verify:
+            n += 1 + (1 if self.fp8 else 0) + 2 + self._mla_launches(self.spec.topk, 0, self.R)
+        n += 1
+        if self.has_draft:
+            n += 1 + (1 if self.fp8 else 0) + 2 + 1
+            n += sum(self._mla_launches(self.spec.topk, j, self.B) for j in range(self.spec.draft_steps))
+        return n
+
+    def _mla_launches(self, n_idx, n_append, R):
+        return 1 + (1 if api.sparse_mla_workspace_size(R, self.spec.H_Q, n_idx, n_append,
+                                                        1 if self.fp8 else 0) else 0)

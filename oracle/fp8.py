@@ -46,7 +46,8 @@ _POS_VALUES = _TABLE[:0x7F].copy()
 
 def encode_e4m3_rne_satfinite(y: np.ndarray) -> np.ndarray:
     """Round float values to the nearest E4M3 code, ties to the even code,
-    saturating magnitudes above 448 to +-448 (no NaN produced for finite input).
+    saturating magnitudes above 448 to +-448 (no NaN produced for finite input);
+    the sign bit always follows the input's sign.
 
     Done by search over the 127 non-negative representable values: the two
     neighbours of |y| are found, the nearer one taken, and on an exact tie the
@@ -65,7 +66,9 @@ def encode_e4m3_rne_satfinite(y: np.ndarray) -> np.ndarray:
     code = np.where(take_hi, hi, lo).astype(np.uint8)
     # exact hits (including a == 0)
     code = np.where(v_hi == a, hi.astype(np.uint8), code)
-    neg = (np.signbit(y)) & (code != 0)
+    # the sign bit is kept for every result, zero included (a negative value
+    # that rounds to zero gives the negative-zero code 0x80)
+    neg = np.signbit(y)
     return (code | (neg.astype(np.uint8) << 7)).astype(np.uint8)
 
 

@@ -29,6 +29,15 @@ D_LATENT = 576
 D_V = 512
 
 
+def _f64(x, index) -> np.ndarray:
+    """x[index] as float64 numpy (x: numpy array or CPU torch tensor, e.g. bf16)."""
+    if hasattr(x, "detach"):
+        import torch
+        return x[torch.as_tensor(index, dtype=torch.long)].double().numpy() if isinstance(index, list) \
+            else x[index].double().numpy()
+    return np.asarray(x[index], dtype=np.float64)
+
+
 def row_index_list(idx_r: np.ndarray, n_append: int = 0, base: int | None = None):
     """The positions attended by one row: the valid selected ones, then the
     appended base+1..base+n_append."""
@@ -54,18 +63,17 @@ def sparse_mla(q, latent, cache_start, row_req, idx, scale, n_append=0,
         base = int(cache_start[b])
         pos = row_index_list(idx[r], n_append,
                              None if append_base is None else append_base[r])
-        C = np.asarray(latent[[base + s for s in pos]], dtype=np.float64).reshape(len(pos), D_LATENT)
-        o = np.zeros((len(heads), d_v))
-        lse = np.zeros(len(heads))
-        for i, h in enumerate(heads):
-            if len(pos) == 0:
-                o[i], lse[i] = 0.0, -np.inf
-                continue
-            logits = scale * (C @ np.asarray(q[r, h], dtype=np.float64))
-            m = np.max(logits)
-            e = np.exp(logits - m)
-            ssum = np.sum(e)
-            o[i] = (e @ C[:, :d_v]) / ssum
-            lse[i] = m + np.log(ssum)
+        C = _f64(latent, [base + s for s in pos]).reshape(len(pos), D_LATENT)
+        heads_l = list(heads)
+        if len(pos) == 0:
+            out[r] = (np.zeros((len(heads_l), d_v)), np.full(len(heads_l), -np.inf))
+            continue
+        Q = _f64(q, r)[heads_l]                                    # [h, 576]
+        logits = scale * (Q @ C.T)                                 # [h, n]
+        m = np.max(logits, axis=1, keepdims=True)
+        e = np.exp(logits - m)
+        ssum = np.sum(e, axis=1)
+        o = (e @ C[:, :d_v]) / ssum[:, None]
+        lse = m[:, 0] + np.log(ssum)
         out[r] = (o, lse)
     return out

@@ -1,0 +1,103 @@
+"""The C-ABI library loads and exports every symbol include/mtpsd.h declares,
+the ctypes structures match the C layout, and host-side argument checks
+reject bad calls before any launch.  CPU only (no compute call)."""
+import ctypes as C
+import os
+import re
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mtpsd.h")
+
+
+@pytest.fixture(scope="module")
+def native():
+    from mtp_speculative_decode_gb300 import _native
+    if not os.path.exists(_native.LIB_PATH):
+        from mtp_speculative_decode_gb300 import build
+        build.build()
+    _native.lib()
+    return _native
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mtpsd_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(native):
+    names = declared_functions()
+    assert len(names) >= 14
+    lib = native.lib()
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+        assert n in native.SIGNATURES, f"{n} has no ctypes signature"
+    assert set(native.SIGNATURES) == set(names)
+
+
+def _c_offsets(struct, fields):
+    src = "#include <stddef.h>\n#include <stdio.h>\n#include \"mtpsd.h\"\nint main(void){\n"
+    src += f'printf("%zu\\n", sizeof({struct}));\n'
+    for f in fields:
+        src += f'printf("%zu\\n", offsetof({struct}, {f}));\n'
+    src += "return 0;}\n"
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "t.c")
+        exe = os.path.join(d, "t")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-I", os.path.dirname(HEADER), c, "-o", exe], check=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout.split()
+    return [int(x) for x in out]
+
+
+@pytest.mark.parametrize("cname,pyname", [("mtpsd_indexer_args", "IndexerArgs"), ("mtpsd_mla_args", "MlaArgs")])
+def test_struct_layout_matches_header(native, cname, pyname):
+    st = getattr(native, pyname)
+    fields = [f for f, _ in st._fields_]
+    got = _c_offsets(cname, fields)
+    assert got[0] == C.sizeof(st)
+    assert got[1:] == [getattr(st, f).offset for f in fields]
+
+
+def test_host_checks_reject_before_launch(native):
+    lib = native.lib()
+    assert lib.mtpsd_merge_tokens(None, 0, None, None, 0, 0, None, None, None) == native.MTPSD_EINVAL
+    assert b"B >= 1" in lib.mtpsd_last_error()
+    assert lib.mtpsd_accept_greedy(None, None, -1, 0, -1, None, None, None) == native.MTPSD_EINVAL
+    a = native.IndexerArgs(B=1, R=1, n_heads=64, head_dim=64, topk=16, dtype=native.MTPSD_FP8_E4M3)
+    assert lib.mtpsd_indexer_topk(C.byref(a), None) == native.MTPSD_EUNSUPPORTED
+    a = native.IndexerArgs(B=1, R=1, n_heads=64, head_dim=128, topk=16, dtype=native.MTPSD_FP8_E4M3,
+                           q=1, q_scale=1, weights=1, k_cache=1, k_scale=1, cache_start=1, row_offsets=1,
+                           row_pos=1, topk_idx=1, max_visible=100)
+    assert lib.mtpsd_indexer_topk(C.byref(a), None) == native.MTPSD_EWORKSPACE
+    m = native.MlaArgs(B=1, R=1, n_heads=128, d_latent=512, d_v=512, n_idx=16, dtype=native.MTPSD_BF16)
+    assert lib.mtpsd_sparse_mla_decode(C.byref(m), None) == native.MTPSD_EUNSUPPORTED
+    m = native.MlaArgs(B=1, R=1, n_heads=20, d_latent=576, d_v=512, n_idx=16, dtype=native.MTPSD_BF16)
+    assert lib.mtpsd_sparse_mla_decode(C.byref(m), None) == native.MTPSD_EUNSUPPORTED
+    m = native.MlaArgs(B=1, R=1, n_heads=16, d_latent=576, d_v=512, n_idx=16, n_append=2,
+                       dtype=native.MTPSD_BF16)
+    assert lib.mtpsd_sparse_mla_decode(C.byref(m), None) == native.MTPSD_EINVAL
+    assert lib.mtpsd_kv_writeback(None, None, None, 1, 6, 7, 128, None, None, None, None, None, None, 10, None,
+                                  None, None) == native.MTPSD_EUNSUPPORTED
+    assert lib.mtpsd_topk(None, 10, 1, None, 20, 4, None, None, None, 0, None, None) == native.MTPSD_EINVAL
+
+
+def test_host_merged_offsets_mirror(native):
+    from mtp_speculative_decode_gb300 import host_merged_offsets
+    from oracle import merge as omerge
+    rng = np.random.default_rng(0)
+    for K in (0, 1, 5):
+        po = np.concatenate([[0], np.cumsum(rng.integers(0, 4, 30))]).astype(np.uint32)
+        assert np.array_equal(host_merged_offsets(po, K), omerge.host_merged_offsets(po, K))
+
+
+def test_workspace_queries(native):
+    lib = native.lib()
+    assert lib.mtpsd_scores_ld(8198) % 4 == 0 and lib.mtpsd_scores_ld(8198) >= 8198
+    ws = lib.mtpsd_indexer_topk_workspace_size(32, 192, 8198, 2048)
+    assert ws >= 192 * 8198 * 4
