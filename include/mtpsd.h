@@ -135,6 +135,31 @@ size_t mtpsd_indexer_topk_workspace_size(int32_t B, int32_t R, int64_t max_visib
 int mtpsd_indexer_topk(const mtpsd_indexer_args* args, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Allocation-free variant of mtpsd_indexer_topk (the source pages have no
+ * counterpart: this is a deployment convenience of this library).
+ *
+ * For callers that cannot allocate device memory: a plugin or C host whose
+ * allocator owns the device memory and hands out no scratch, a serving loop
+ * that forbids allocation after start-up, or a caller holding only the raw
+ * input/output pointers.  Same arguments and results as mtpsd_indexer_topk,
+ * but args->workspace and args->workspace_bytes are ignored: the score
+ * scratch lives in a static device array of MTPSD_NOALLOC_SCRATCH_BYTES
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  The caller still passes every input and output.
+ * - A call needing more than MTPSD_NOALLOC_SCRATCH_BYTES of scratch
+ *   (mtpsd_indexer_topk_workspace_size(B, R, max_visible, topk), about
+ *   R * max_visible * 4 bytes) returns MTPSD_EWORKSPACE before any launch.
+ * - The first call on a device (the current device) looks up the array's
+ *   device address; make that first call before any stream capture.
+ * - All calls share the one array, which keeps the last call's contents
+ *   (nothing in it needs to start at zero).  Calls that overlap on the GPU
+ *   (on different streams without ordering) race on it.
+ * - Calls no cudaMalloc / cudaFree or other allocating routine.
+ */
+#define MTPSD_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
+int mtpsd_indexer_topk_noalloc(const mtpsd_indexer_args* args, void* stream);
+
+/* ------------------------------------------------------------------------
  * Standalone per-row top-k over a score matrix (the selection half of the
  * call above, for callers that produce scores themselves).
  *   scores [R, ld] float32, row_len [R] int64 (valid prefix of each row)

@@ -21,6 +21,8 @@ MTPSD_F32 = 0
 MTPSD_BF16 = 1
 MTPSD_FP8_E4M3 = 2
 
+NOALLOC_SCRATCH_BYTES = 16 << 20   # MTPSD_NOALLOC_SCRATCH_BYTES
+
 STATUS_INDEX_RANGE = 1
 STATUS_WRITE_RANGE = 2
 STATUS_WAIT_TIMEOUT = 4
@@ -59,6 +61,7 @@ SIGNATURES = {
     "mtpsd_scores_ld": (i64, [i64]),
     "mtpsd_indexer_topk_workspace_size": (C.c_size_t, [i32, i32, i64, i32]),
     "mtpsd_indexer_topk": (C.c_int, [C.POINTER(IndexerArgs), vp]),
+    "mtpsd_indexer_topk_noalloc": (C.c_int, [C.POINTER(IndexerArgs), vp]),
     "mtpsd_topk_workspace_size": (C.c_size_t, [i32, i32]),
     "mtpsd_topk": (C.c_int, [vp, i64, i32, vp, i64, i32, vp, vp, vp, C.c_size_t, vp, vp]),
     "mtpsd_sparse_mla_workspace_size": (C.c_size_t, [i32, i32, i32, i32, i32]),
