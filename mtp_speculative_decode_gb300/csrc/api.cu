@@ -71,8 +71,7 @@ int64_t mtpsd_scores_ld(int64_t max_visible) { return (int64_t)align_up((size_t)
 size_t mtpsd_indexer_topk_workspace_size(int32_t B, int32_t R, int64_t max_visible, int32_t topk) {
   (void)topk;
   size_t scores = (size_t)R * (size_t)mtpsd_scores_ld(max_visible) * sizeof(float);
-  size_t tiles = align_up(((size_t)B + 1) * sizeof(int32_t), 256);
-  return align_up(scores, 256) + tiles;
+  return align_up(scores, 256) + indexer_tc_plan_bytes(B, R);
 }
 
 int mtpsd_indexer_topk(const mtpsd_indexer_args* a, void* stream) {
@@ -106,7 +105,7 @@ int mtpsd_indexer_topk(const mtpsd_indexer_args* a, void* stream) {
   p.q = a->q; p.q_scale = a->q_scale; p.w = a->weights; p.k = a->k_cache; p.k_scale = a->k_scale;
   p.pool = a->pool_tokens; p.cache_start = a->cache_start; p.row_offsets = a->row_offsets; p.row_pos = a->row_pos;
   p.max_visible = a->max_visible; p.scores = scores; p.ld = ld;
-  p.tile_offsets = (int32_t*)((char*)a->workspace + align_up((size_t)a->R * ld * sizeof(float), 256));
+  p.plan_ws = (char*)a->workspace + align_up((size_t)a->R * ld * sizeof(float), 256);
   p.status = a->dev_status;
   int rc = indexer_tc_supported(p) ? launch_indexer_scores_tc(p, st) : launch_indexer_scores(p, st);
   if (rc) return rc;

@@ -26,10 +26,11 @@ struct IndexerPlan {
   const void* k; const float* k_scale; int64_t pool;
   const int64_t* cache_start; const uint32_t* row_offsets; const int64_t* row_pos;
   int64_t max_visible; float* scores; int64_t ld;
-  int32_t* tile_offsets;   // [B+1] workspace
+  void* plan_ws;           // workspace for the tensor-core kernel's work plan (indexer_tc_plan_bytes)
   int32_t* status;
 };
 int launch_indexer_scores(const IndexerPlan& p, cudaStream_t st);
+size_t indexer_tc_plan_bytes(int B, int R);
 bool indexer_tc_supported(const IndexerPlan& p);
 int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st);
 

@@ -1,20 +1,577 @@
 // FP8 lightning-indexer score GEMM on the 5th-generation tensor cores
-// (tcgen05 + TMEM + TMA).  Placeholder until the kernel lands: the generic
-// CUDA-core kernel serves every shape.
+// (tcgen05.mma kind::f8f6f4 + TMEM accumulators + TMA-staged operands).
+//
+// [P3] "Indexer 的结构与计算流程":
+//   I[r,s] = sum_h w[r,h] * ReLU(q_scale[r,h] * k_scale[s] * q[r,h,:].k[s,:])
+// Since the scales are positive they commute with the ReLU:
+//   I[r,s] = k_scale[s] * sum_h (w[r,h] q_scale[r,h]) * ReLU(q8[r,h,:].k8[s,:])
+// so the tensor cores see only FP8 codes and the scales enter the epilogue.
+//
+// Shape of one MMA: M = 128 cached positions (the A operand: a 128 x 128 B
+// key tile, K-major, loaded by TMA with the 128-byte swizzle), N = 128 query
+// columns (2 rows x 64 heads, or 4 rows x 32 heads: the B operand, K-major),
+// K = 128 FP8 values in 4 steps of 32.  Putting the positions on M makes the
+// head sum of the epilogue thread-local: TMEM lane = position, columns =
+// (row, head).  The accumulators rotate through 4 TMEM slots of 128 columns
+// (512 columns) so that the MMAs of the next chunk run while the epilogue
+// drains the previous one.
+//
+// Roles (320 threads, one persistent CTA per SM):
+//   warps 0-7  epilogue: tcgen05.ld of its 32 lanes x 64 columns, ReLU,
+//              weight, head sum, k_scale, coalesced score store
+//   warp 8     TMA producer: query rows of the current request group and a
+//              6-stage ring of key tiles
+//   warp 9     TMEM allocation and the single-thread MMA issue
+// Work: the rows of each request are cut into groups of up to 512/H rows
+// (the query block kept in shared memory); each group scans
+// ceil(max visible / 128) key tiles; the flattened (group, tile) list is split
+// into equal contiguous ranges, one per CTA, so a CTA reloads the query block
+// only when its range crosses a group boundary.
+// Every mbarrier wait is bounded (2 s): on expiry the kernel flags
+// MTPSD_STATUS_WAIT_TIMEOUT, drains its own copies in flight, frees TMEM and
+// returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <stdlib.h>
+#include <string.h>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace mtpsd {
+namespace itc {
+
+constexpr int TILE_M = 128;
+constexpr int KB = 128;                   // bytes per key / query head vector
+constexpr int NSTAGE = 6;
+constexpr int NSLOT = 4;
+constexpr int SLOT_COLS = 128;
+constexpr int Q_ROWS = 512;               // query head vectors held in shared memory
+constexpr int EPI_WARPS = 8;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int THREADS = 320;
+constexpr int MAX_GROUP_ROWS = Q_ROWS / 32;
+
+constexpr int OFF_K = 0;
+constexpr int OFF_Q = OFF_K + NSTAGE * TILE_M * KB;      // 98304
+constexpr int OFF_WQ = OFF_Q + Q_ROWS * KB;              // per epilogue warp: [Q_ROWS] float
+constexpr int OFF_VIS = OFF_WQ + EPI_WARPS * Q_ROWS * 4; // per epilogue warp: [MAX_GROUP_ROWS] int64
+constexpr int OFF_BAR = OFF_VIS + EPI_WARPS * MAX_GROUP_ROWS * 8;
+constexpr int N_BARS = 2 * NSTAGE + 2 + 2 * NSLOT + 1;
+constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;         // + alignment slack
+
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+
+struct Params {
+  const float* q_scale;
+  const float* w;
+  const float* k_scale;
+  const int64_t* cache_start;
+  const int64_t* row_pos;
+  int64_t pool;
+  int64_t max_visible;
+  float* scores;
+  int64_t ld;
+  int H;
+  const int* g_b;
+  const int* g_row0;
+  const int* g_nrows;
+  const int* g_vmax;
+  const int* g_tile0;      // [n_groups + 1]
+  const int* n_groups;
+  int32_t* status;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(saddr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false when it gave up (time limit or another role aborted).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int32_t* status) {
+  if (mbar_try(bar, parity)) return true;
+  uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+        *abort_flag = 1;
+        flag_status(status, MTPSD_STATUS_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(saddr(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms of
+// 1024 bytes (stride byte offset 1024), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_byte_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_byte_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                 // leading byte offset (unused with this swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+  d |= (uint64_t)1 << 46;                 // version
+  d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f8f6f4, A = B = E4M3, D = F32, both K-major,
+// N = 128, M = 128.
+constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void mma_fp8(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(IDESC), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// (group, tile) cursor over the flattened work list
+struct Cursor {
+  int g, tile;
+  __device__ void start(const Params& p, int n_groups, int it) {
+    int lo = 0, hi = n_groups;   // last g with g_tile0[g] <= it
+    while (hi - lo > 1) {
+      int mid = (lo + hi) >> 1;
+      if (p.g_tile0[mid] <= it) lo = mid; else hi = mid;
+    }
+    g = lo;
+    while (g + 1 < n_groups && p.g_tile0[g + 1] <= it) ++g;   // skip groups without tiles
+    tile = it - p.g_tile0[g];
+  }
+  __device__ void next(const Params& p, int n_groups) {
+    ++tile;
+    while (g + 1 <= n_groups - 1 && tile >= p.g_tile0[g + 1] - p.g_tile0[g]) {
+      tile -= p.g_tile0[g + 1] - p.g_tile0[g];
+      ++g;
+    }
+  }
+};
+
+// ------------------------------------------------------------------- kernels
+// Group plan: one block.  For each request, its rows are cut into groups of
+// at most group_rows rows; each group scans ceil(vmax/128) tiles, vmax being
+// the largest visible length of its rows (clamped to max_visible).
+__global__ void __launch_bounds__(1024) plan_kernel(const uint32_t* __restrict__ ro, const int64_t* __restrict__ row_pos,
+                                                    int B, int64_t max_visible, int group_rows, int* g_b,
+                                                    int* g_row0, int* g_nrows, int* g_vmax, int* g_tile0,
+                                                    int* n_groups) {
+  __shared__ int s_groups[1024], s_tiles[1024];
+  __shared__ int carry_g, carry_t;
+  if (threadIdx.x == 0) carry_g = carry_t = 0;
+  __syncthreads();
+  for (int base = 0; base < B; base += 1024) {
+    const int b = base + threadIdx.x;
+    int ng = 0, nt = 0;
+    if (b < B) {
+      int r0 = (int)ro[b], r1 = (int)ro[b + 1];
+      for (int a = r0; a < r1; a += group_rows) {
+        int e = min(r1, a + group_rows);
+        int64_t vm = 0;
+        for (int r = a; r < e; ++r) vm = max(vm, min(row_pos[r] + 1, max_visible));
+        ++ng;
+        nt += (int)((vm + TILE_M - 1) / TILE_M);
+      }
+    }
+    s_groups[threadIdx.x] = ng;
+    s_tiles[threadIdx.x] = nt;
+    __syncthreads();
+    // inclusive scans (Hillis-Steele)
+    for (int o = 1; o < 1024; o <<= 1) {
+      int vg = threadIdx.x >= o ? s_groups[threadIdx.x - o] : 0;
+      int vt = threadIdx.x >= o ? s_tiles[threadIdx.x - o] : 0;
+      __syncthreads();
+      s_groups[threadIdx.x] += vg;
+      s_tiles[threadIdx.x] += vt;
+      __syncthreads();
+    }
+    int gpos = carry_g + s_groups[threadIdx.x] - ng;
+    int tpos = carry_t + s_tiles[threadIdx.x] - nt;
+    if (b < B) {
+      int r0 = (int)ro[b], r1 = (int)ro[b + 1];
+      for (int a = r0; a < r1; a += group_rows) {
+        int e = min(r1, a + group_rows);
+        int64_t vm = 0;
+        for (int r = a; r < e; ++r) vm = max(vm, min(row_pos[r] + 1, max_visible));
+        g_b[gpos] = b;
+        g_row0[gpos] = a;
+        g_nrows[gpos] = e - a;
+        g_vmax[gpos] = (int)vm;
+        g_tile0[gpos] = tpos;
+        ++gpos;
+        tpos += (int)((vm + TILE_M - 1) / TILE_M);
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 1023) {
+      carry_g += s_groups[1023];
+      carry_t += s_tiles[1023];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    g_tile0[carry_g] = carry_t;
+    *n_groups = carry_g;
+  }
+}
+
+template <int H>
+__global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                                                const __grid_constant__ CUtensorMap tmap_q,
+                                                                Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(sm + OFF_BAR);
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = bars + NSTAGE;
+  uint64_t* q_full = bars + 2 * NSTAGE;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* slot_full = q_full + 2;
+  uint64_t* slot_empty = slot_full + NSLOT;
+  uint64_t* drain = slot_empty + NSLOT;
+  uint32_t* tmem_slot = (uint32_t*)(sm + OFF_MISC);
+  volatile int* abort_flag = (volatile int*)(sm + OFF_MISC + 4);
+  // per-warp copies of the group's weights and visible lengths: each epilogue
+  // warp fills and reads its own, so only __syncwarp orders them
+  float* wq = (float*)(sm + OFF_WQ) + (threadIdx.x >> 5) * Q_ROWS;
+  int64_t* vis = (int64_t*)(sm + OFF_VIS) + (threadIdx.x >> 5) * MAX_GROUP_ROWS;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_groups = *p.n_groups;
+  const int total = n_groups > 0 ? p.g_tile0[n_groups] : 0;
+  const int it0 = (int)(((int64_t)blockIdx.x * total) / gridDim.x);
+  const int it1 = (int)(((int64_t)(blockIdx.x + 1) * total) / gridDim.x);
+  if (it0 >= it1) return;   // uniform per CTA, before any barrier or TMEM use
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(&slot_full[i], 1);
+      mbar_init(&slot_empty[i], EPI_WARPS);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == MMA_WARP) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
+                 "r"(NSLOT * SLOT_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == PRODUCER_WARP) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_k) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_q) : "memory");
+      int n_load = 0, gq = 0, cur_g = -1;
+      bool ok = true;
+      Cursor c;
+      c.start(p, n_groups, it0);
+      for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups)) {
+        const int g = c.g;
+        if (g != cur_g) {
+          if (gq > 0) ok = mbar_wait(q_empty, (gq - 1) & 1, abort_flag, p.status);
+          if (!ok) break;
+          const int nrows = p.g_nrows[g], row0 = p.g_row0[g];
+          mbar_expect_tx(q_full, (uint32_t)(nrows * H * KB));
+          for (int i = 0; i < nrows; ++i)
+            tma_load_2d(saddr(sm + OFF_Q + i * H * KB), &tmap_q, 0, (row0 + i) * H, q_full);
+          ++gq;
+          cur_g = g;
+        }
+        const int stage = n_load % NSTAGE, round = n_load / NSTAGE;
+        if (round > 0) ok = mbar_wait(&k_empty[stage], (round - 1) & 1, abort_flag, p.status);
+        if (!ok) break;
+        mbar_expect_tx(&k_full[stage], TILE_M * KB);
+        const int64_t y = p.cache_start[p.g_b[g]] + (int64_t)c.tile * TILE_M;
+        tma_load_2d(saddr(sm + OFF_K + stage * TILE_M * KB), &tmap_k, 0, (int)y, &k_full[stage]);
+        ++n_load;
+      }
+      if (*abort_flag) {   // drain this CTA's copies still in flight (bounded)
+        volatile int dummy = 0;
+        for (int s = 0; s < NSTAGE; ++s) {
+          const int issued = n_load / NSTAGE + (s < n_load % NSTAGE ? 1 : 0);   // loads of stage s
+          if (issued > 0) mbar_wait(&k_full[s], (issued - 1) & 1, &dummy, p.status);
+        }
+        if (gq > 0) mbar_wait(q_full, (gq - 1) & 1, &dummy, p.status);
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      int n_cons = 0, n_chunk = 0, gq = 0, cur_g = -1, nch = 0;
+      bool ok = true;
+      Cursor c;
+      c.start(p, n_groups, it0);
+      for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups)) {
+        const int g = c.g;
+        if (g != cur_g) {
+          if (cur_g >= 0) mma_commit(q_empty);
+          ok = mbar_wait(q_full, gq & 1, abort_flag, p.status);
+          if (!ok) break;
+          ++gq;
+          cur_g = g;
+          nch = (p.g_nrows[g] * H + SLOT_COLS - 1) / SLOT_COLS;
+        }
+        const int stage = n_cons % NSTAGE, round = n_cons / NSTAGE;
+        ok = mbar_wait(&k_full[stage], round & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a_base = saddr(sm + OFF_K + stage * TILE_M * KB);
+        for (int ch = 0; ch < nch && ok; ++ch) {
+          const int slot = n_chunk % NSLOT, sround = n_chunk / NSLOT;
+          if (sround > 0) {
+            ok = mbar_wait(&slot_empty[slot], (sround - 1) & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          const uint32_t b_base = saddr(sm + OFF_Q + ch * SLOT_COLS * KB);
+          const uint32_t d = tmem_base + (uint32_t)(slot * SLOT_COLS);
+#pragma unroll
+          for (int kk = 0; kk < KB / 32; ++kk)
+            mma_fp8(d, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), kk > 0 ? 1u : 0u);
+          mma_commit(&slot_full[slot]);
+          ++n_chunk;
+        }
+        if (!ok) break;
+        mma_commit(&k_empty[stage]);
+        ++n_cons;
+      }
+      // all issued MMAs complete before TMEM is released
+      mma_commit(drain);
+      volatile int dummy = 0;
+      mbar_wait(drain, 0, &dummy, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wg = warp >> 2;              // which 64 of the slot's 128 columns
+    const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+    const int pos_in_tile = quarter * 32 + lane;
+    constexpr int rows_per_wg = 64 / H;    // 1 (H = 64) or 2 (H = 32)
+    int n_chunk = 0, cur_g = -1, nrows = 0, row0 = 0, nch = 0;
+    int64_t vmax = 0, cstart = 0;
+    bool ok = true;
+    Cursor c;
+    c.start(p, n_groups, it0);
+    for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups)) {
+      const int g = c.g;
+      if (g != cur_g) {
+        __syncwarp();   // the warp is done with the previous group's copies
+        nrows = p.g_nrows[g];
+        row0 = p.g_row0[g];
+        vmax = p.g_vmax[g];
+        cstart = p.cache_start[p.g_b[g]];
+        nch = (nrows * H + SLOT_COLS - 1) / SLOT_COLS;
+        for (int e = lane; e < nrows * H; e += 32)
+          wq[e] = p.w[(int64_t)row0 * H + e] * p.q_scale[(int64_t)row0 * H + e];
+        for (int i = lane; i < nrows; i += 32) vis[i] = min(p.row_pos[row0 + i] + 1, p.max_visible);
+        __syncwarp();
+        cur_g = g;
+      }
+      const int64_t s = (int64_t)c.tile * TILE_M + pos_in_tile;
+      const int64_t prow = cstart + s;
+      const float ks = (s < vmax && prow >= 0 && prow < p.pool) ? p.k_scale[prow] : 0.f;
+      for (int ch = 0; ch < nch; ++ch) {
+        const int slot = n_chunk % NSLOT, sround = n_chunk / NSLOT;
+        // warp-uniform outcome: tcgen05.ld below is a warp-collective instruction
+        ok = __all_sync(0xffffffffu, mbar_wait(&slot_full[slot], sround & 1, abort_flag, p.status));
+        if (!ok) break;
+        tc_fence_after();
+        float v[64];
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(slot * SLOT_COLS + wg * 64);
+        tmem_ld32(taddr, v);
+        tmem_ld32(taddr + 32, v + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&slot_empty[slot]);
+        ++n_chunk;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (j >= rows_per_wg) break;
+          const int i = ch * (SLOT_COLS / H) + wg * rows_per_wg + j;   // row within the group
+          if (i >= nrows) break;
+          const float4* wr = (const float4*)(wq + i * H);
+          float acc = 0.f;
+          const int hb = j * H;   // first column of row i within this warp's 64
+#pragma unroll
+          for (int h4 = 0; h4 < H / 4; ++h4) {
+            float4 ww = wr[h4];
+            acc = fmaf(ww.x, fmaxf(v[hb + h4 * 4 + 0], 0.f), acc);
+            acc = fmaf(ww.y, fmaxf(v[hb + h4 * 4 + 1], 0.f), acc);
+            acc = fmaf(ww.z, fmaxf(v[hb + h4 * 4 + 2], 0.f), acc);
+            acc = fmaf(ww.w, fmaxf(v[hb + h4 * 4 + 3], 0.f), acc);
+          }
+          if (s < vis[i]) p.scores[(int64_t)(row0 + i) * p.ld + s] = acc * ks;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(NSLOT * SLOT_COLS));
+  }
+}
+
+}  // namespace itc
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+  }
+  return fn;
+}
+
+static bool make_map_rows128(CUtensorMap* map, const void* base, int64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static bool tc_device_ok() {
+  static int ok = -1;
+  if (ok < 0) {
+    int dev = 0, major = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    ok = (major == 10) ? 1 : 0;
+  }
+  return ok == 1;
+}
+
+size_t indexer_tc_plan_bytes(int B, int R) {
+  size_t n = (size_t)B + (size_t)R + 2;
+  return ((5 * n + 1) * sizeof(int) + 255) / 256 * 256;
+}
 
 bool indexer_tc_supported(const IndexerPlan& p) {
-  (void)p;
-  return false;
+  const char* env = getenv("MTPSD_INDEXER");
+  if (env && strcmp(env, "generic") == 0) return false;
+  if (p.dtype != MTPSD_FP8_E4M3 || p.D != 128) return false;
+  if (p.H != 64 && p.H != 32) return false;
+  if (((uintptr_t)p.k % 16) || ((uintptr_t)p.q % 16)) return false;
+  if (p.pool < 1 || p.pool > 0x7fffffffLL || (int64_t)p.R * p.H > 0x7fffffffLL) return false;
+  if (p.max_visible > 0x7fffffffLL - itc::TILE_M) return false;
+  if (!p.plan_ws) return false;
+  return tc_device_ok() && encode_fn() != nullptr;
 }
 
 int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {
-  (void)p; (void)st;
-  set_error("indexer: tensor-core kernel not built");
-  return MTPSD_EUNSUPPORTED;
+  using namespace itc;
+  CUtensorMap mk, mq;
+  if (!make_map_rows128(&mk, p.k, p.pool, TILE_M) || !make_map_rows128(&mq, p.q, (int64_t)p.R * p.H, (uint32_t)p.H)) {
+    set_error("indexer: cuTensorMapEncodeTiled failed");
+    return MTPSD_ECUDA;
+  }
+  const size_t n = (size_t)p.B + (size_t)p.R + 2;
+  int* w = (int*)p.plan_ws;
+  int* g_b = w;
+  int* g_row0 = g_b + n;
+  int* g_nrows = g_row0 + n;
+  int* g_vmax = g_nrows + n;
+  int* g_tile0 = g_vmax + n;
+  int* n_groups = g_tile0 + n;
+  const int group_rows = Q_ROWS / p.H;
+  plan_kernel<<<1, 1024, 0, st>>>(p.row_offsets, p.row_pos, p.B, p.max_visible, group_rows, g_b, g_row0, g_nrows,
+                                  g_vmax, g_tile0, n_groups);
+  int rc = check_launch("indexer_tc_plan");
+  if (rc) return rc;
+  Params kp;
+  kp.q_scale = p.q_scale; kp.w = p.w; kp.k_scale = p.k_scale; kp.cache_start = p.cache_start;
+  kp.row_pos = p.row_pos; kp.pool = p.pool; kp.max_visible = p.max_visible; kp.scores = p.scores; kp.ld = p.ld;
+  kp.H = p.H; kp.g_b = g_b; kp.g_row0 = g_row0; kp.g_nrows = g_nrows; kp.g_vmax = g_vmax; kp.g_tile0 = g_tile0;
+  kp.n_groups = n_groups; kp.status = p.status;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(indexer_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaFuncSetAttribute(indexer_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr = true;
+  }
+  if (p.H == 64)
+    indexer_tc_kernel<64><<<num_sms(), THREADS, SMEM_BYTES, st>>>(mk, mq, kp);
+  else
+    indexer_tc_kernel<32><<<num_sms(), THREADS, SMEM_BYTES, st>>>(mk, mq, kp);
+  return check_launch("indexer_tc");
 }
 
 }  // namespace mtpsd
