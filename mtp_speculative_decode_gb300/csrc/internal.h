@@ -7,6 +7,12 @@
 
 namespace mtpsd {
 
+// 2D tensor map with the 128-byte swizzle (map: a 64-byte aligned CUtensorMap).
+// dtype_u8_or_bf16: 0 = uint8 elements, 1 = bf16 elements.
+bool tma_available();
+bool make_tma_2d(void* map, int dtype_u8_or_bf16, const void* base, uint64_t inner_elems, uint64_t rows,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, bool l2_256);
+
 int launch_merge_tokens(const int64_t* prompt, int64_t S, const uint32_t* po, const int64_t* draft,
                         int B, int K, int64_t* out, uint32_t* mo, cudaStream_t st);
 int launch_quantize_fp8(const float* x, int64_t n_blocks, uint8_t* codes, float* scales, cudaStream_t st);
@@ -53,6 +59,10 @@ struct MlaPlan {
   int32_t* status;
 };
 size_t mla_workspace_bytes(int R, int H, int n_idx, int n_append, int dtype);
+bool mla_tc_supported(const MlaPlan& p);
+int mla_tc_per_split(int R, int H, int64_t total);
+int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* part_o, float* part_ml,
+                         cudaStream_t st);
 int launch_sparse_mla(const MlaPlan& p, cudaStream_t st);
 
 }  // namespace mtpsd

@@ -31,7 +31,6 @@
 // MTPSD_STATUS_WAIT_TIMEOUT, drains its own copies in flight, frees TMEM and
 // returns.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -482,30 +481,8 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
 }  // namespace itc
 
 // ------------------------------------------------------------------ host side
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
-  }
-  return fn;
-}
-
 static bool make_map_rows128(CUtensorMap* map, const void* base, int64_t rows, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {128};
-  cuuint32_t box[2] = {128, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return make_tma_2d(map, 0, base, 128, (uint64_t)rows, 128, 128, box_rows, true);
 }
 
 static bool tc_device_ok() {
@@ -533,7 +510,7 @@ bool indexer_tc_supported(const IndexerPlan& p) {
   if (p.pool < 1 || p.pool > 0x7fffffffLL || (int64_t)p.R * p.H > 0x7fffffffLL) return false;
   if (p.max_visible > 0x7fffffffLL - itc::TILE_M) return false;
   if (!p.plan_ws) return false;
-  return tc_device_ok() && encode_fn() != nullptr;
+  return tc_device_ok() && tma_available();
 }
 
 int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {

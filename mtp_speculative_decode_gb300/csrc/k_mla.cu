@@ -421,8 +421,26 @@ static MlaSplit choose_split(int R, int H, int n_idx, int n_append, int dtype) {
   return sp;
 }
 
+static bool use_tc(int H, int dtype) {
+  MlaPlan q{};
+  q.H = H; q.dtype = dtype; q.d_latent = MLA_DL; q.d_v = MLA_DV;
+  return mla_tc_supported(q);
+}
+
+// splits of the selected list for the kernel that will run
+static MlaSplit plan_split(int R, int H, int n_idx, int n_append, int dtype) {
+  if (use_tc(H, dtype)) {
+    int64_t total = (int64_t)n_idx + n_append;
+    MlaSplit sp;
+    sp.per_split = mla_tc_per_split(R, H, total);
+    sp.n_splits = total > 0 ? (int)ceil_div(total, sp.per_split) : 1;
+    return sp;
+  }
+  return choose_split(R, H, n_idx, n_append, dtype);
+}
+
 size_t mla_workspace_bytes(int R, int H, int n_idx, int n_append, int dtype) {
-  MlaSplit sp = choose_split(R, H, n_idx, n_append, dtype);
+  MlaSplit sp = plan_split(R, H, n_idx, n_append, dtype);
   if (sp.n_splits == 1) return 0;
   size_t rh = (size_t)R * H * sp.n_splits;
   return rh * MLA_DV * sizeof(float) + rh * 2 * sizeof(float) + 256;
@@ -430,7 +448,7 @@ size_t mla_workspace_bytes(int R, int H, int n_idx, int n_append, int dtype) {
 
 int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
   if (p.R == 0) return MTPSD_OK;
-  MlaSplit sp = choose_split(p.R, p.H, p.n_idx, p.n_append, p.dtype);
+  MlaSplit sp = plan_split(p.R, p.H, p.n_idx, p.n_append, p.dtype);
   float* part_o = nullptr;
   float* part_ml = nullptr;
   if (sp.n_splits > 1) {
@@ -441,6 +459,16 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
     }
     part_o = (float*)p.ws;
     part_ml = part_o + (size_t)p.R * p.H * sp.n_splits * MLA_DV;
+  }
+  if (p.dtype == MTPSD_BF16 && mla_tc_supported(p)) {
+    int rc = launch_sparse_mla_tc(p, sp.n_splits, (int)sp.per_split, part_o, part_ml, st);
+    if (rc) return rc;
+    if (sp.n_splits > 1) {
+      mla_combine_kernel<__nv_bfloat16><<<(unsigned)((int64_t)p.R * p.H), 128, 0, st>>>(p, sp.n_splits, part_o,
+                                                                                        part_ml);
+      return check_launch("sparse_mla_combine");
+    }
+    return MTPSD_OK;
   }
   if (p.dtype == MTPSD_BF16) {
     static bool attr = false;

@@ -1,0 +1,632 @@
+// Sparse MLA decode on the 5th-generation tensor cores (tcgen05 kind::f16,
+// bf16 operands, fp32 accumulators in TMEM).
+//
+// [P2] "验证段的逐层算子" op 7 / [P3] "稀疏 MLA 的前向路径": per query row r and
+// head h, softmax attention over the selected latent rows c[s_j, 0:576] with
+// values c[s_j, 0:512].
+//
+// One CTA owns (row, 128-head group, half of the 512 value dims, split of the
+// selected list).  The 128 heads are the MMA's M.  A full [128 x 512] fp32
+// output needs all 512 TMEM columns, so the value dims are split over two
+// CTAs that both form the scores:
+//   TMEM  [  0,128) query dims 0..255 (A operand of QK^T, bf16 pairs)
+//         [128,192) [192,256) two score buffers S of 64 positions (fp32),
+//                   P aliased in their first 32 columns (bf16 pairs)
+//         [256,512) O: 128 heads x this CTA's 256 value dims (fp32)
+//   SMEM  query dims 256..575 (A operand, 128-byte swizzle, 80 KB) and two
+//         pair buffers of 64 gathered latent rows (72 KB each).  A pair
+//         buffer is filled as two 32-row tiles and laid out per 64-dim chunk:
+//         chunk c = 64 rows x 128 B (rows 0..31 from the first tile, 32..63
+//         from the second), 128-byte swizzle.  The same bytes are the K-major
+//         B operand of S = Q C^T (N = 64 positions) and the MN-major B
+//         operand of O += P V (K = positions, N = this CTA's 256 dims).
+// Per 64-position pair: QK^T = 16 MMAs with A from TMEM + 20 with A from
+// shared memory (M=128, N=64, K=16); the softmax warps (thread = head) read
+// S, apply the lazy max (O is rescaled only when a head's max grows by more
+// than 2^8), write P as bf16 into the S columns, and PV = 4 MMAs (M=128,
+// N=256, K=16) with A = P from TMEM accumulate into O.  QK(P) is issued
+// before PV(P-1) so the tensor cores work while the softmax runs.  (With A
+// in shared memory an N=32 MMA is bound by re-reading the 4 KB A tile; N=64
+// halves that cost per position.)
+//
+// Roles (224 threads): warps 0-3 softmax/epilogue (TMEM lanes = heads);
+// warps 4-5 produce: each turns its 16 positions of every 32-row tile into
+// pool rows (the selection entries are prefetched one tile ahead) and
+// gathers them with TMA tile::gather4 loads (4 rows x 64 dims per
+// instruction, invalid positions read as zeros through an out-of-range row);
+// the first also loads the shared part of the query; warp 6 allocates TMEM
+// and issues the MMAs.  The producer and MMA roles run with the whole warp so
+// that descriptors and coordinates stay in uniform registers, and one elected
+// lane issues.  Every mbarrier wait is bounded (2 s) and flags
+// MTPSD_STATUS_WAIT_TIMEOUT on expiry.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mtpsd {
+namespace mtc {
+
+constexpr int DL = 576, DV = 512, DVH = 256;
+constexpr int HG = 128;                 // heads per CTA (MMA M)
+constexpr int NT = 32;                  // positions per gathered tile
+constexpr int NP = 64;                  // positions per MMA step (a pair of tiles)
+constexpr int NSTAGE = 4;               // tiles in the ring = 2 pair buffers
+constexpr int QLO = 256;                // query dims held in TMEM
+constexpr int QHI_CHUNKS = (DL - QLO) / 64;   // 5 chunks of 64 dims in shared memory
+constexpr int C_CHUNKS = DL / 64;             // 9
+constexpr int CHUNK_BYTES = NP * 128;         // 8192: one chunk of a pair buffer
+constexpr int PAIR_BYTES = C_CHUNKS * CHUNK_BYTES;   // 73728
+constexpr int TILE_BYTES = PAIR_BYTES / 2;           // 36864 gathered per tile
+constexpr int OFF_QHI = 0;
+constexpr int OFF_C = OFF_QHI + QHI_CHUNKS * HG * 128;       // 81920
+constexpr int OFF_MASK = OFF_C + 2 * PAIR_BYTES;             // 229376: [NSTAGE][N_PROD] uint32 validity bits
+constexpr int OFF_BAR = OFF_MASK + NSTAGE * 2 * 4;
+// barriers: c_full[4], c_empty[2], s_full[2], p_full[2], pv_done[2], q_ready, drain
+constexpr int N_BARS = NSTAGE + 2 + 6 + 2;
+constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;               // tmem base, abort flag
+constexpr int SMEM_USED = OFF_MISC + 16;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;                 // alignment slack
+constexpr int THREADS = 224;
+constexpr int PROD_WARP = 4, N_PROD = 2, MMA_WARP = 6;
+constexpr int TM_Q = 0, TM_S0 = 128, TM_O = 256;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float RESCALE_LOG2 = 8.0f;
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+
+struct Params {
+  int B, R, H, n_idx, n_append;
+  float sl2;                  // softmax scale * log2(e)
+  int64_t row_pos_add;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* latent;
+  int64_t pool;
+  const int64_t* cache_start;
+  const uint32_t* row_offsets;
+  const int64_t* row_pos;
+  const int32_t* idx;
+  const int64_t* append_base;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;              // split partials (unnormalised O), or null
+  float* part_ml;
+  int n_splits;
+  int per_split;              // positions per split (multiple of NP)
+  int32_t* status;
+};
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(b)),
+               "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"((uint32_t)__cvta_generic_to_shared(bar)) : "memory");
+}
+// 4 rows (y0..y3) x one box of columns starting at x
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2,
+                                            int y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"((uint32_t)__cvta_generic_to_shared(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t c) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(c));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t par) {
+  uint32_t ok;
+  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(ok) : "r"(saddr(b)), "r"(par) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t par, volatile int* abort_flag, int32_t* status) {
+  if (mbar_try(b, par)) return true;
+  uint64_t t0 = gtimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(b, par)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (gtimer() - t0 > WAIT_LIMIT_NS) {
+        *abort_flag = 1;
+        flag_status(status, MTPSD_STATUS_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+// One lane of a converged warp (the lowest), as a warp-uniform branch: the
+// issuing role runs with all 32 lanes so that addresses and descriptors stay
+// in uniform registers, and only the elected lane issues TMA / MMA.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n .reg .b32 rx;\n .reg .pred px;\n elect.sync rx|px, 0xffffffff;\n selp.b32 %0, 1, 0, px;\n}\n"
+               : "=r"(pred));
+  return pred != 0;
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void commit(uint64_t* b) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(b)) : "memory");
+}
+
+// K-major (or MN-major) 128-byte-swizzle descriptor.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// kind::f16 instruction descriptors: D = F32, A = B = BF16, A K-major.
+constexpr uint32_t IDESC_QK = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NP >> 3) << 17) | ((uint32_t)(HG >> 4) << 24);
+constexpr uint32_t IDESC_PV =
+    (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(DVH >> 3) << 17) | ((uint32_t)(HG >> 4) << 24);
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+               ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
+#define TM_REGS32(r) \
+  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), \
+  "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),      \
+  "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),     \
+  "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+#define TM_IN32(r) \
+  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), \
+  "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),  \
+  "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),   \
+  "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+
+__device__ __forceinline__ void tm_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+               "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : TM_REGS32(r) : "r"(taddr));
+}
+__device__ __forceinline__ void tm_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+               "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+               ::"r"(taddr), TM_IN32(r) : "memory");
+}
+__device__ __forceinline__ void tm_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+               ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+               "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+               : "memory");
+}
+__device__ __forceinline__ void tm_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tm_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32); -inf -> +0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);   // .x (low half) = lo
+  return *(uint32_t*)&v;
+}
+
+// Selection entry j of row r: the position (>= 0), -1 for padding, or -2 past the split.
+__device__ __forceinline__ int64_t entry(const Params& p, int r, int64_t j, int64_t j1) {
+  if (j >= j1) return -2;
+  if (j < p.n_idx) return p.idx[(int64_t)r * p.n_idx + j];
+  return p.append_base[r] + 1 + (j - p.n_idx);
+}
+// Pool row of an entry, or -1 (padding, past the split, or out of range: flagged).
+__device__ __forceinline__ int64_t entry_row(const Params& p, int64_t s, int64_t base, int64_t limit) {
+  if (s == -1 || s == -2) return -1;
+  if (s < 0 || s > limit) {
+    flag_status(p.status, MTPSD_STATUS_INDEX_RANGE);
+    return -1;
+  }
+  const int64_t row = base + s;
+  if (row < 0 || row >= p.pool) {
+    flag_status(p.status, MTPSD_STATUS_ROW_RANGE);
+    return -1;
+  }
+  return row;
+}
+
+__global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
+                                                                   const __grid_constant__ CUtensorMap tm_q, Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(sm + OFF_BAR);
+  uint64_t* c_full = bars;                 // per tile stage: both producers' bytes landed
+  uint64_t* c_empty = bars + NSTAGE;       // per pair buffer: its PV completed
+  uint64_t* s_full = c_empty + 2;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* q_ready = pv_done + 2;
+  uint64_t* drain = q_ready + 1;
+  uint32_t* tmem_slot = (uint32_t*)(sm + OFF_MISC);
+  volatile int* abort_flag = (volatile int*)(sm + OFF_MISC + 4);
+  uint32_t* mask_s = (uint32_t*)(sm + OFF_MASK);   // [stage][producer]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x;
+  const int hg = blockIdx.y >> 1, vh = blockIdx.y & 1;
+  const int split = blockIdx.z;
+  const int h0 = hg * HG;
+  const int b = request_of_row(p.row_offsets, p.B, (uint32_t)r);
+  const int64_t base = p.cache_start[b];
+  const int64_t limit = p.row_pos[r] + p.row_pos_add;
+  const int64_t total = (int64_t)p.n_idx + p.n_append;
+  const int64_t j0 = (int64_t)split * p.per_split;
+  const int64_t j1 = min(total, j0 + (int64_t)p.per_split);
+  const int n_pairs = j1 > j0 ? (int)((j1 - j0 + NP - 1) / NP) : 0;
+  const int n_tiles = 2 * n_pairs;        // a last half pair is filled with zero rows
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSTAGE; ++i) mbar_init(&c_full[i], N_PROD);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(q_ready, 129);          // 128 softmax threads (TMEM part) + the first producer (TMA bytes)
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == MMA_WARP) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)), "r"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const __nv_bfloat16* qrow = p.q + ((int64_t)r * p.H + h0) * DL;
+
+  if (warp < 4) {
+    // ------------------------------------------------ softmax / epilogue: thread = head
+    const int h = threadIdx.x;                 // 0..127 = TMEM lane
+    const bool head_ok = (h0 + h) < p.H;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    {   // query dims 0..255 -> TMEM columns [0,128) as bf16 pairs
+      const uint4* src = (const uint4*)(qrow + (int64_t)h * DL);
+#pragma unroll
+      for (int c = 0; c < QLO / 64; ++c) {
+        uint32_t v[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint4 x = head_ok ? src[c * 8 + i] : make_uint4(0, 0, 0, 0);
+          v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+        }
+        tm_st32(tmem + lane_off + TM_Q + c * 32, v);
+      }
+      tm_wait_st();
+      fence_before();
+      mbar_arrive(q_ready);
+    }
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int P = 0; P < n_pairs && ok; ++P) {
+      const int q = P & 1;
+      const uint32_t par = (P >> 1) & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[q], par, abort_flag, p.status));
+      // the validity bits were written by the producers before they released the two tiles
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[2 * q], par, abort_flag, p.status));
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[2 * q + 1], par, abort_flag, p.status));
+      if (!ok) break;
+      fence_after();
+      uint32_t sr[64];
+      tm_ld32(tmem + lane_off + TM_S0 + q * 64, sr);
+      tm_ld32(tmem + lane_off + TM_S0 + q * 64 + 32, sr + 32);
+      tm_wait_ld();
+      const uint64_t mask = (uint64_t)(mask_s[(2 * q) * 2] | mask_s[(2 * q) * 2 + 1]) |
+                            ((uint64_t)(mask_s[(2 * q + 1) * 2] | mask_s[(2 * q + 1) * 2 + 1]) << 32);
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        float v = ((mask >> j) & 1ull) ? __uint_as_float(sr[j]) * p.sl2 : -INFINITY;
+        sr[j] = __float_as_uint(v);
+        mx[j & 3] = fmaxf(mx[j & 3], v);
+      }
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      if (mt > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mt > -INFINITY)) {
+        // new reference max for this head; rescale what O already holds
+        if (m_ref > -INFINITY) {
+          const float alpha = ex2(m_ref - mt);
+          // O must not be touched while the previous PV is still accumulating
+          mbar_wait(&pv_done[(P - 1) & 1], ((P - 1) >> 1) & 1, abort_flag, p.status);
+          fence_after();
+          l *= alpha;
+#pragma unroll 1
+          for (int c = 0; c < DVH / 32; ++c) {
+            uint32_t o[32];
+            tm_ld32(tmem + lane_off + TM_O + c * 32, o);
+            tm_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tm_st32(tmem + lane_off + TM_O + c * 32, o);
+          }
+          tm_wait_st();
+        }
+        m_ref = mt;
+      }
+      // p = 2^(s - m_ref); a masked -inf gives 0, and a head with no valid position so far
+      // (m_ref = -inf, every s = -inf) uses offset 0
+      const float mo = m_ref == -INFINITY ? 0.f : m_ref;
+      uint32_t pk[32];
+      float psum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float a = ex2(__uint_as_float(sr[2 * j]) - mo);
+        const float c = ex2(__uint_as_float(sr[2 * j + 1]) - mo);
+        pk[j] = pack_bf16(a, c);
+        __nv_bfloat162 bv = *(__nv_bfloat162*)&pk[j];
+        float2 f = __bfloat1622float2(bv);   // the sum uses the rounded values PV multiplies
+        psum[j & 3] += f.x + f.y;
+      }
+      l += (psum[0] + psum[1]) + (psum[2] + psum[3]);
+      tm_st32(tmem + lane_off + TM_S0 + q * 64, pk);
+      tm_wait_st();
+      fence_before();
+      mbar_arrive(&p_full[q]);
+    }
+    // ------------------------------------------------ epilogue
+    if (ok && n_pairs > 0) {
+      const int last = n_pairs - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[last & 1], (last >> 1) & 1, abort_flag, p.status));
+    }
+    if (ok) fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    if (p.n_splits == 1) {
+      __nv_bfloat16* og = p.out + ((int64_t)r * p.H + h0 + h) * DV + vh * DVH;
+#pragma unroll 1
+      for (int c = 0; c < DVH / 32; ++c) {
+        uint32_t o[32];
+        if (n_pairs > 0 && ok) {
+          tm_ld32(tmem + lane_off + TM_O + c * 32, o);
+          tm_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+        if (head_ok) {
+          uint4* dst = (uint4*)(og + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (head_ok && vh == 0 && p.lse)
+        p.lse[(int64_t)r * p.H + h0 + h] = l > 0.f ? (m_ref + log2f(l)) / LOG2E : -INFINITY;
+    } else {
+      float* po = p.part_o + (((int64_t)r * p.H + h0 + h) * p.n_splits + split) * DV + vh * DVH;
+#pragma unroll 1
+      for (int c = 0; c < DVH / 32; ++c) {
+        uint32_t o[32];
+        if (n_pairs > 0 && ok) {
+          tm_ld32(tmem + lane_off + TM_O + c * 32, o);
+          tm_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        if (head_ok) {
+          float4* dst = (float4*)(po + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]), __uint_as_float(o[4 * i + 2]),
+                                 __uint_as_float(o[4 * i + 3]));
+        }
+      }
+      if (head_ok && vh == 0) {
+        float* ml = p.part_ml + (((int64_t)r * p.H + h0 + h) * p.n_splits + split) * 2;
+        ml[0] = l > 0.f ? m_ref : -INFINITY;
+        ml[1] = l;
+      }
+    }
+  } else if (warp < PROD_WARP + N_PROD) {
+    // ------------------------------------------------ producers
+    // Producer pw gathers the 4-row groups g = pw, pw + 2, pw + 4, pw + 6 of
+    // every 32-row tile: lane l (< 16) owns position 4*g + (l & 3) of group
+    // g = pw + 2*(l >> 2); lanes 16..31 mirror lanes 0..15.
+    const int pw = warp - PROD_WARP;
+    const int ln = lane & 15;
+    const int my_pos = 4 * (pw + 2 * (ln >> 2)) + (ln & 3);
+    const int32_t oob = (int32_t)p.pool;   // a row outside the tensor map: TMA reads zeros
+    if (pw == 0 && elect_one()) {   // query dims 256..575 of the 128 heads: 5 boxes of 64 dims x 128 rows
+      mbar_arrive_expect_tx(q_ready, QHI_CHUNKS * HG * 128);
+      for (int c = 0; c < QHI_CHUNKS; ++c)
+        tma_load_2d(saddr(sm + OFF_QHI + c * (HG * 128)), &tm_q, QLO + c * 64, r * p.H + h0, q_ready);
+    }
+    __syncwarp();
+    int64_t nxt = n_tiles > 0 ? entry(p, r, j0 + my_pos, j1) : -2;
+    int issued = 0;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int64_t cur = nxt;
+      if (t + 1 < n_tiles) nxt = entry(p, r, j0 + (int64_t)(t + 1) * NT + my_pos, j1);   // prefetch
+      const int st = t % NSTAGE, P = t >> 1, q = P & 1, R = P >> 1;
+      if (R > 0 && !__all_sync(0xffffffffu, mbar_wait(&c_empty[q], (R - 1) & 1, abort_flag, p.status))) break;
+      const int64_t row = entry_row(p, cur, base, limit);
+      const bool valid = row >= 0 && lane < 16;
+      const uint32_t bits = __reduce_or_sync(0xffffffffu, valid ? (1u << my_pos) : 0u);
+      if (lane == 0) mask_s[st * 2 + pw] = bits;
+      const int yv = row >= 0 ? (int)row : oob;
+      int y[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) y[i] = __shfl_sync(0xffffffffu, yv, i);
+      const uint32_t dst = saddr(sm + OFF_C + q * PAIR_BYTES + (t & 1) * (NT * 128));
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&c_full[st], TILE_BYTES / N_PROD);
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+          const int g = pw + 2 * gi;
+#pragma unroll
+          for (int c = 0; c < C_CHUNKS; ++c)
+            tma_gather4(dst + c * CHUNK_BYTES + g * 512, &tm_lat, c * 64, y[4 * gi], y[4 * gi + 1], y[4 * gi + 2],
+                        y[4 * gi + 3], &c_full[st]);
+        }
+      }
+      __syncwarp();
+      issued = t + 1;
+    }
+    if (*abort_flag && lane == 0) {   // wait (bounded) for this CTA's copies still in flight
+      volatile int dummy = 0;
+      for (int st = 0; st < NSTAGE; ++st) {
+        const int n = issued / NSTAGE + (st < issued % NSTAGE ? 1 : 0);
+        if (n > 0) mbar_wait(&c_full[st], (n - 1) & 1, &dummy, p.status);
+      }
+      if (pw == 0) mbar_wait(q_ready, 0, &dummy, p.status);
+    }
+  } else {
+    // ------------------------------------------------ MMA issue (warp 6; one elected lane issues)
+    bool ok = __all_sync(0xffffffffu, mbar_wait(q_ready, 0, abort_flag, p.status));
+    if (ok) fence_after();
+    const uint64_t qhi_desc = desc_sw128(saddr(sm + OFF_QHI), 16, 1024);
+    const uint64_t c_desc0 = desc_sw128(saddr(sm + OFF_C), 16, 1024);
+    const uint64_t v_desc0 = desc_sw128(saddr(sm + OFF_C) + vh * 4 * CHUNK_BYTES, CHUNK_BYTES, 1024);
+    for (int P = 0; P <= n_pairs && ok; ++P) {
+      if (P < n_pairs) {
+        const int q = P & 1;
+        const uint32_t par = (P >> 1) & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&c_full[2 * q], par, abort_flag, p.status));
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[2 * q + 1], par, abort_flag, p.status));
+        if (!ok) break;
+        fence_after();
+        const uint64_t cd = c_desc0 + (uint64_t)((q * PAIR_BYTES) >> 4);
+        const uint32_t d = tmem + TM_S0 + q * 64;
+        if (elect_one()) {
+          // S = Q C^T over 64 positions: dims 0..255 with A from TMEM, 256..575 with A from shared memory
+#pragma unroll
+          for (int k = 0; k < DL / 16; ++k) {
+            const uint32_t boff = (uint32_t)((k >> 2) * CHUNK_BYTES + (k & 3) * 32);   // chunk, 32-byte K step
+            if (k < QLO / 16) {
+              mma_ts(d, tmem + TM_Q + k * 8, cd + (boff >> 4), IDESC_QK, k > 0 ? 1u : 0u);
+            } else {
+              const int kq = k - QLO / 16;
+              const uint32_t aoff = (uint32_t)((kq >> 2) * (HG * 128) + (kq & 3) * 32);
+              mma_ss(d, qhi_desc + (aoff >> 4), cd + (boff >> 4), IDESC_QK, 1u);
+            }
+          }
+          commit(&s_full[q]);
+        }
+        __syncwarp();
+      }
+      if (P >= 1) {
+        // O += P(P-1) V(P-1): A = P from TMEM, B = the pair buffer as MN-major (N = this CTA's 256 dims)
+        const int Pp = P - 1, qp = Pp & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&p_full[qp], (Pp >> 1) & 1, abort_flag, p.status));
+        if (!ok) break;
+        fence_after();
+        const uint64_t vd = v_desc0 + (uint64_t)((qp * PAIR_BYTES) >> 4);
+        if (elect_one()) {
+#pragma unroll
+          for (int k = 0; k < NP / 16; ++k)
+            mma_ts(tmem + TM_O, tmem + TM_S0 + qp * 64 + k * 8, vd + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV,
+                   (Pp > 0 || k > 0) ? 1u : 0u);
+          commit(&pv_done[qp]);
+          commit(&c_empty[qp]);
+        }
+        __syncwarp();
+      }
+    }
+    if (elect_one()) commit(drain);
+    __syncwarp();
+    volatile int dummy = 0;
+    mbar_wait(drain, 0, &dummy, p.status);
+  }
+
+  fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+  }
+}
+
+}  // namespace mtc
+
+bool mla_tc_supported(const MlaPlan& p) {
+  if (p.dtype != MTPSD_BF16 || p.d_latent != 576 || p.d_v != 512) return false;
+  if (p.H % mtc::HG != 0) return false;
+  int dev = 0, major = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (major != 10) return false;
+  const char* env = getenv("MTPSD_MLA");
+  if (env && env[0] == 'm') return false;   // "mma": the mma.sync kernel
+  if (p.pool > 0x7ffffffeLL || (int64_t)p.R * p.H > 0x7fffffffLL) return false;
+  if (((uintptr_t)p.latent % 16) || ((uintptr_t)p.q % 16)) return false;
+  return tma_available();
+}
+
+// Splits of the selected list that balance whole waves of one-CTA-per-SM
+// work.  Returns the positions per
+// split (a multiple of NT).
+int mla_tc_per_split(int R, int H, int64_t total) {
+  const int64_t tiles = (total + mtc::NP - 1) / mtc::NP;
+  const int64_t units = (int64_t)R * (H / mtc::HG) * 2;
+  const int sms = num_sms();
+  int64_t best = 1;
+  double best_cost = 1e30;
+  for (int64_t s = best; s <= best + 64 && s <= tiles; ++s) {
+    const int64_t per = (tiles + s - 1) / s;
+    const int64_t waves = (units * s + sms - 1) / sms;
+    const double cost = (double)waves * (per + 2.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  const int64_t per = ((tiles + best - 1) / best) * mtc::NP;
+  return (int)(per > 0 ? per : mtc::NP);
+}
+
+int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* part_o, float* part_ml,
+                         cudaStream_t st) {
+  using namespace mtc;
+  Params k;
+  k.B = p.B; k.R = p.R; k.H = p.H; k.n_idx = p.n_idx; k.n_append = p.n_append;
+  k.sl2 = p.scale * LOG2E; k.row_pos_add = p.row_pos_add;
+  k.q = (const __nv_bfloat16*)p.q; k.latent = (const __nv_bfloat16*)p.latent; k.pool = p.pool;
+  k.cache_start = p.cache_start; k.row_offsets = p.row_offsets; k.row_pos = p.row_pos; k.idx = p.idx;
+  k.append_base = p.append_base; k.out = (__nv_bfloat16*)p.out; k.lse = p.lse; k.part_o = part_o; k.part_ml = part_ml;
+  k.n_splits = n_splits; k.per_split = per_split; k.status = p.status;
+  alignas(64) CUtensorMap tm_lat, tm_q;
+  if (!make_tma_2d(&tm_lat, 1, p.latent, DL, (uint64_t)p.pool, DL * 2, 64, 1, false) ||
+      !make_tma_2d(&tm_q, 1, p.q, DL, (uint64_t)p.R * p.H, DL * 2, 64, HG, true)) {
+    set_error("sparse_mla: cuTensorMapEncodeTiled failed");
+    return MTPSD_ECUDA;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr = true;
+  }
+  dim3 grid(p.R, (p.H / HG) * 2, n_splits);
+  sparse_mla_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(tm_lat, tm_q, k);
+  return check_launch("sparse_mla_tc");
+}
+
+}  // namespace mtpsd
