@@ -61,15 +61,15 @@ constexpr int PAIR_BYTES = C_CHUNKS * CHUNK_BYTES;   // 73728
 constexpr int TILE_BYTES = PAIR_BYTES / 2;           // 36864 gathered per tile
 constexpr int OFF_QHI = 0;
 constexpr int OFF_C = OFF_QHI + QHI_CHUNKS * HG * 128;       // 81920
-constexpr int OFF_MASK = OFF_C + 2 * PAIR_BYTES;             // 229376: [NSTAGE][N_PROD] uint32 validity bits
-constexpr int OFF_BAR = OFF_MASK + NSTAGE * 2 * 4;
+constexpr int OFF_MASK = OFF_C + 2 * PAIR_BYTES;             // 229376: [NSTAGE][4] uint32 validity bits
+constexpr int OFF_BAR = OFF_MASK + NSTAGE * 4 * 4;
 // barriers: c_full[4], c_empty[2], s_full[2], p_full[2], pv_done[2], q_ready, drain
 constexpr int N_BARS = NSTAGE + 2 + 6 + 2;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;               // tmem base, abort flag
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;                 // alignment slack
-constexpr int THREADS = 224;
-constexpr int PROD_WARP = 4, N_PROD = 2, MMA_WARP = 6;
+constexpr int THREADS = 288;
+constexpr int PROD_WARP = 4, N_PROD = 4, MMA_WARP = 8;
 constexpr int TM_Q = 0, TM_S0 = 128, TM_O = 256;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -228,12 +228,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *(uint32_t*)&v;
 }
 
-// Selection entry j of row r: the position (>= 0), -1 for padding, or -2 past the split.
-__device__ __forceinline__ int64_t entry(const Params& p, int r, int64_t j, int64_t j1) {
-  if (j >= j1) return -2;
-  if (j < p.n_idx) return p.idx[(int64_t)r * p.n_idx + j];
-  return p.append_base[r] + 1 + (j - p.n_idx);
-}
 // Pool row of an entry, or -1 (padding, past the split, or out of range: flagged).
 __device__ __forceinline__ int64_t entry_row(const Params& p, int64_t s, int64_t base, int64_t limit) {
   if (s == -1 || s == -2) return -1;
@@ -338,8 +332,9 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       tm_ld32(tmem + lane_off + TM_S0 + q * 64, sr);
       tm_ld32(tmem + lane_off + TM_S0 + q * 64 + 32, sr + 32);
       tm_wait_ld();
-      const uint64_t mask = (uint64_t)(mask_s[(2 * q) * 2] | mask_s[(2 * q) * 2 + 1]) |
-                            ((uint64_t)(mask_s[(2 * q + 1) * 2] | mask_s[(2 * q + 1) * 2 + 1]) << 32);
+      const uint32_t* m0 = mask_s + (2 * q) * 4;
+      const uint32_t* m1 = mask_s + (2 * q + 1) * 4;
+      const uint64_t mask = (uint64_t)(m0[0] | m0[1] | m0[2] | m0[3]) | ((uint64_t)(m1[0] | m1[1] | m1[2] | m1[3]) << 32);
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
@@ -448,12 +443,13 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     }
   } else if (warp < PROD_WARP + N_PROD) {
     // ------------------------------------------------ producers
-    // Producer pw gathers the 4-row groups g = pw, pw + 2, pw + 4, pw + 6 of
-    // every 32-row tile: lane l (< 16) owns position 4*g + (l & 3) of group
-    // g = pw + 2*(l >> 2); lanes 16..31 mirror lanes 0..15.
+    // Producer pw gathers the 4-row groups g = pw and g = pw + 4 of every
+    // 32-row tile: lane l (< 8) owns position 4*g + (l & 3) of group
+    // g = pw + 4*(l >> 2); the other lanes mirror lanes 0..7.  The selection
+    // entries of the next tile are loaded one iteration ahead.
     const int pw = warp - PROD_WARP;
-    const int ln = lane & 15;
-    const int my_pos = 4 * (pw + 2 * (ln >> 2)) + (ln & 3);
+    const int ln = lane & 7;
+    const int my_pos = 4 * (pw + 4 * (ln >> 2)) + (ln & 3);
     const int32_t oob = (int32_t)p.pool;   // a row outside the tensor map: TMA reads zeros
     if (pw == 0 && elect_one()) {   // query dims 256..575 of the 128 heads: 5 boxes of 64 dims x 128 rows
       mbar_arrive_expect_tx(q_ready, QHI_CHUNKS * HG * 128);
@@ -461,27 +457,32 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
         tma_load_2d(saddr(sm + OFF_QHI + c * (HG * 128)), &tm_q, QLO + c * 64, r * p.H + h0, q_ready);
     }
     __syncwarp();
-    int64_t nxt = n_tiles > 0 ? entry(p, r, j0 + my_pos, j1) : -2;
+    const int32_t* idx_row = p.idx + (int64_t)r * p.n_idx;
+    // raw selected entry of position j (or a clamped dummy when j is an appended / past-the-split position)
+    auto raw = [&](int64_t j) -> int32_t { return p.n_idx > 0 ? idx_row[min(j, (int64_t)p.n_idx - 1)] : 0; };
+    int32_t nraw = n_tiles > 0 ? raw(j0 + my_pos) : 0;
     int issued = 0;
     for (int t = 0; t < n_tiles; ++t) {
-      const int64_t cur = nxt;
-      if (t + 1 < n_tiles) nxt = entry(p, r, j0 + (int64_t)(t + 1) * NT + my_pos, j1);   // prefetch
+      const int32_t craw = nraw;
+      if (t + 1 < n_tiles) nraw = raw(j0 + (int64_t)(t + 1) * NT + my_pos);   // prefetch
       const int st = t % NSTAGE, P = t >> 1, q = P & 1, R = P >> 1;
       if (R > 0 && !__all_sync(0xffffffffu, mbar_wait(&c_empty[q], (R - 1) & 1, abort_flag, p.status))) break;
-      const int64_t row = entry_row(p, cur, base, limit);
-      const bool valid = row >= 0 && lane < 16;
+      const int64_t j = j0 + (int64_t)t * NT + my_pos;
+      const int64_t e = j >= j1 ? -2 : (j < p.n_idx ? (int64_t)craw : p.append_base[r] + 1 + (j - p.n_idx));
+      const int64_t row = entry_row(p, e, base, limit);
+      const bool valid = row >= 0 && lane < 8;
       const uint32_t bits = __reduce_or_sync(0xffffffffu, valid ? (1u << my_pos) : 0u);
-      if (lane == 0) mask_s[st * 2 + pw] = bits;
+      if (lane == 0) mask_s[st * 4 + pw] = bits;
       const int yv = row >= 0 ? (int)row : oob;
-      int y[16];
+      int y[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = __shfl_sync(0xffffffffu, yv, i);
+      for (int i = 0; i < 8; ++i) y[i] = __shfl_sync(0xffffffffu, yv, i);
       const uint32_t dst = saddr(sm + OFF_C + q * PAIR_BYTES + (t & 1) * (NT * 128));
       if (elect_one()) {
         mbar_arrive_expect_tx(&c_full[st], TILE_BYTES / N_PROD);
 #pragma unroll
-        for (int gi = 0; gi < 4; ++gi) {
-          const int g = pw + 2 * gi;
+        for (int gi = 0; gi < 2; ++gi) {
+          const int g = pw + 4 * gi;
 #pragma unroll
           for (int c = 0; c < C_CHUNKS; ++c)
             tma_gather4(dst + c * CHUNK_BYTES + g * 512, &tm_lat, c * 64, y[4 * gi], y[4 * gi + 1], y[4 * gi + 2],
@@ -506,49 +507,72 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     const uint64_t qhi_desc = desc_sw128(saddr(sm + OFF_QHI), 16, 1024);
     const uint64_t c_desc0 = desc_sw128(saddr(sm + OFF_C), 16, 1024);
     const uint64_t v_desc0 = desc_sw128(saddr(sm + OFF_C) + vh * 4 * CHUNK_BYTES, CHUNK_BYTES, 1024);
-    for (int P = 0; P <= n_pairs && ok; ++P) {
-      if (P < n_pairs) {
-        const int q = P & 1;
-        const uint32_t par = (P >> 1) & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(&c_full[2 * q], par, abort_flag, p.status));
-        ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[2 * q + 1], par, abort_flag, p.status));
-        if (!ok) break;
-        fence_after();
-        const uint64_t cd = c_desc0 + (uint64_t)((q * PAIR_BYTES) >> 4);
-        const uint32_t d = tmem + TM_S0 + q * 64;
-        if (elect_one()) {
-          // S = Q C^T over 64 positions: dims 0..255 with A from TMEM, 256..575 with A from shared memory
+    // Issue whichever is ready: QK(nq) once its pair has landed (and PV(nq-2),
+    // which last read the S columns QK(nq) overwrites, has been issued: the
+    // MMAs execute in issue order), or PV(np) once the softmax published P.
+    int nq = 0, np = 0;
+    uint64_t t0 = gtimer();
+    uint32_t spins = 0;
+    while (np < n_pairs && ok) {
+      bool did = false;
+      if (nq < n_pairs && nq <= np + 1) {
+        const int q = nq & 1;
+        const uint32_t par = (nq >> 1) & 1;
+        if (__all_sync(0xffffffffu, mbar_try(&c_full[2 * q], par) && mbar_try(&c_full[2 * q + 1], par))) {
+          fence_after();
+          const uint64_t cd = c_desc0 + (uint64_t)((q * PAIR_BYTES) >> 4);
+          const uint32_t d = tmem + TM_S0 + q * 64;
+          if (elect_one()) {
+            // S = Q C^T over 64 positions: dims 0..255 with A from TMEM, 256..575 with A from shared memory
 #pragma unroll
-          for (int k = 0; k < DL / 16; ++k) {
-            const uint32_t boff = (uint32_t)((k >> 2) * CHUNK_BYTES + (k & 3) * 32);   // chunk, 32-byte K step
-            if (k < QLO / 16) {
-              mma_ts(d, tmem + TM_Q + k * 8, cd + (boff >> 4), IDESC_QK, k > 0 ? 1u : 0u);
-            } else {
-              const int kq = k - QLO / 16;
-              const uint32_t aoff = (uint32_t)((kq >> 2) * (HG * 128) + (kq & 3) * 32);
-              mma_ss(d, qhi_desc + (aoff >> 4), cd + (boff >> 4), IDESC_QK, 1u);
+            for (int k = 0; k < DL / 16; ++k) {
+              const uint32_t boff = (uint32_t)((k >> 2) * CHUNK_BYTES + (k & 3) * 32);   // chunk, 32-byte K step
+              if (k < QLO / 16) {
+                mma_ts(d, tmem + TM_Q + k * 8, cd + (boff >> 4), IDESC_QK, k > 0 ? 1u : 0u);
+              } else {
+                const int kq = k - QLO / 16;
+                const uint32_t aoff = (uint32_t)((kq >> 2) * (HG * 128) + (kq & 3) * 32);
+                mma_ss(d, qhi_desc + (aoff >> 4), cd + (boff >> 4), IDESC_QK, 1u);
+              }
             }
+            commit(&s_full[q]);
           }
-          commit(&s_full[q]);
+          __syncwarp();
+          ++nq;
+          did = true;
         }
-        __syncwarp();
       }
-      if (P >= 1) {
-        // O += P(P-1) V(P-1): A = P from TMEM, B = the pair buffer as MN-major (N = this CTA's 256 dims)
-        const int Pp = P - 1, qp = Pp & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(&p_full[qp], (Pp >> 1) & 1, abort_flag, p.status));
-        if (!ok) break;
-        fence_after();
-        const uint64_t vd = v_desc0 + (uint64_t)((qp * PAIR_BYTES) >> 4);
-        if (elect_one()) {
+      if (np < nq) {
+        // O += P(np) V(np): A = P from TMEM, B = the pair buffer as MN-major (N = this CTA's 256 dims)
+        const int qp = np & 1;
+        if (__all_sync(0xffffffffu, mbar_try(&p_full[qp], (np >> 1) & 1))) {
+          fence_after();
+          const uint64_t vd = v_desc0 + (uint64_t)((qp * PAIR_BYTES) >> 4);
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < NP / 16; ++k)
-            mma_ts(tmem + TM_O, tmem + TM_S0 + qp * 64 + k * 8, vd + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV,
-                   (Pp > 0 || k > 0) ? 1u : 0u);
-          commit(&pv_done[qp]);
-          commit(&c_empty[qp]);
+            for (int k = 0; k < NP / 16; ++k)
+              mma_ts(tmem + TM_O, tmem + TM_S0 + qp * 64 + k * 8, vd + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV,
+                     (np > 0 || k > 0) ? 1u : 0u);
+            commit(&pv_done[qp]);
+            commit(&c_empty[qp]);
+          }
+          __syncwarp();
+          ++np;
+          did = true;
         }
-        __syncwarp();
+      }
+      if (did) {
+        t0 = gtimer();
+        spins = 0;
+      } else if ((++spins & 255u) == 0) {   // bounded: give up after the wait limit
+        if (*abort_flag) {
+          ok = false;
+        } else if (gtimer() - t0 > WAIT_LIMIT_NS) {
+          *abort_flag = 1;
+          flag_status(p.status, MTPSD_STATUS_WAIT_TIMEOUT);
+          ok = false;
+        }
+        ok = __all_sync(0xffffffffu, ok);
       }
     }
     if (elect_one()) commit(drain);
