@@ -6,7 +6,8 @@
 // selects its own.  Ties at the k-th score go to the lower position; the
 // output lists the selected positions in ascending order, -1 padded.
 //
-// One CTA of 1024 threads per row.  Scores map to order-preserving uint32
+// Rows of up to 40960 keys use the register kernel below.  Longer rows: one
+// CTA of 1024 threads per row.  Scores map to order-preserving uint32
 // keys; four 8-bit radix passes (most significant first) over the row find
 // the k-th largest key T with warp-aggregated shared-memory histograms.  The
 // row's keys stay in shared memory when they fit (<= TOPK_SMEM_KEYS), else
@@ -22,7 +23,7 @@ constexpr int TOPK_THREADS = 1024;
 constexpr int TOPK_SMEM_KEYS = 48 * 1024;   // 192 KB of keys
 
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -32,7 +33,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
   if (lane == 31) warp_sums[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    int w = (lane < (TOPK_THREADS / 32)) ? warp_sums[lane] : 0;
+    int w = (lane < nw) ? warp_sums[lane] : 0;
     int incl = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -163,8 +164,114 @@ __global__ void __launch_bounds__(TOPK_THREADS, 1) topk_kernel(TopkPlan p, int64
   }
 }
 
+// Rows of up to 40960 keys: each thread holds KPT consecutive keys in
+// registers (positions t*KPT .. t*KPT+KPT-1) and the CTA finds the k-th
+// largest key T exactly by a bitwise search from the most significant bit:
+// T grows by bit b when at least k keys are >= T | 2^b (32 counting rounds,
+// one warp reduction and one barrier each).  The ordered compaction is the
+// same as above.
+template <int KPT, int NTH>
+__global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
+  __shared__ int wsum[2][32];
+  __shared__ int warp_sums[32];
+  __shared__ int total_s;
+  const int r = blockIdx.x;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  constexpr int NW = NTH / 32;
+  int64_t V = p.row_len[r] + (p.len_plus_one ? 1 : 0);
+  if (V > p.max_len) {
+    if (threadIdx.x == 0) flag_status(p.status, MTPSD_STATUS_INDEX_RANGE);
+    V = p.max_len;
+  }
+  if (V < 0) V = 0;
+  const int k = p.k;
+  int32_t* out = p.out_idx + (int64_t)r * k;
+  float* outs = p.out_score ? p.out_score + (int64_t)r * k : nullptr;
+  const float* row = p.scores + (int64_t)r * p.ld;
+  if (V <= k) {  // everything visible is selected
+    for (int64_t i = threadIdx.x; i < k; i += blockDim.x) {
+      out[i] = i < V ? (int32_t)i : -1;
+      if (outs) outs[i] = i < V ? row[i] : -INFINITY;
+    }
+    return;
+  }
+  // keys of this thread's positions; 0 (below every finite key) past the row
+  const int a = threadIdx.x * KPT;
+  uint32_t key[KPT];
+#pragma unroll
+  for (int i = 0; i < KPT; i += 4) {
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (a + i < p.ld) f = *(const float4*)(row + a + i);   // ld is a multiple of 4 and rows are 16-byte aligned
+    key[i] = a + i < V ? float_key(f.x) : 0u;
+    key[i + 1] = a + i + 1 < V ? float_key(f.y) : 0u;
+    key[i + 2] = a + i + 2 < V ? float_key(f.z) : 0u;
+    key[i + 3] = a + i + 3 < V ? float_key(f.w) : 0u;
+  }
+  uint32_t T = 0;
+#pragma unroll 1
+  for (int b = 31; b >= 0; --b) {
+    const uint32_t cand = T | (1u << b);
+    unsigned c = 0;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) c += key[i] >= cand ? 1u : 0u;
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0) wsum[b & 1][wid] = (int)c;
+    __syncthreads();   // the other buffer is rewritten only after the next barrier
+    int tot = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) tot += wsum[b & 1][w];
+    if (tot >= k) T = cand;
+  }
+  int n_gt = 0, n_eq = 0;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    n_gt += key[i] > T;
+    n_eq += key[i] == T;
+  }
+  const int gt_before = block_exclusive_scan(n_gt, warp_sums, &total_s);
+  const int need_eq = k - total_s;   // equal keys taken, lowest positions first
+  const int eq_before = block_exclusive_scan(n_eq, warp_sums, &total_s);
+  int take_eq = max(0, min(n_eq, need_eq - eq_before));
+  int out_pos = gt_before + min(eq_before, need_eq);
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    bool take = key[i] > T;
+    if (key[i] == T && take_eq > 0) {
+      take = true;
+      --take_eq;
+    }
+    if (take && out_pos < k) {
+      out[out_pos] = a + i;
+      if (outs) outs[out_pos] = key_float(key[i]);
+      ++out_pos;
+    }
+  }
+}
+
+template <int NTH>
+static int launch_topk_reg(const TopkPlan& p, int kpt, cudaStream_t st) {
+  switch (kpt) {
+#define MTPSD_TOPK_CASE(K) \
+  case K: topk_reg_kernel<K, NTH><<<p.R, NTH, 0, st>>>(p); break;
+    MTPSD_TOPK_CASE(4) MTPSD_TOPK_CASE(8) MTPSD_TOPK_CASE(12) MTPSD_TOPK_CASE(16) MTPSD_TOPK_CASE(20)
+    MTPSD_TOPK_CASE(24) MTPSD_TOPK_CASE(28) MTPSD_TOPK_CASE(32) MTPSD_TOPK_CASE(36) MTPSD_TOPK_CASE(40)
+#undef MTPSD_TOPK_CASE
+    default: return -1;
+  }
+  return check_launch("topk");
+}
+
 int launch_topk(const TopkPlan& p, cudaStream_t st) {
   if (p.R == 0) return MTPSD_OK;
+  const bool aligned = ((uintptr_t)p.scores % 16) == 0 && (p.ld % 4) == 0;
+  if (aligned && p.max_len <= 40960) {
+    const int nth = p.max_len <= 16384 ? 512 : 1024;
+    int kpt = (int)((p.max_len + nth - 1) / nth);
+    kpt = (kpt + 3) & ~3;
+    if (kpt < 4) kpt = 4;
+    if (nth == 512 && kpt <= 32) return launch_topk_reg<512>(p, kpt, st);
+    if (nth == 1024 && kpt <= 40) return launch_topk_reg<1024>(p, kpt, st);
+  }
   int64_t cache_keys = p.max_len <= TOPK_SMEM_KEYS ? p.max_len : 0;
   size_t smem = (size_t)cache_keys * sizeof(uint32_t);
   if (smem > 48 * 1024)
