@@ -327,6 +327,58 @@ __global__ void mla_combine_kernel(MlaPlan p, int n_splits, const float* __restr
   if (threadIdx.x == 0 && p.lse) p.lse[rh] = l > 0.f ? (m + log2f(l)) / LOG2E : -INFINITY;
 }
 
+// The same merge for 512 value dims with 16-byte accesses: four heads per
+// 256-thread block, 64 threads per head, 8 dims per thread; one weight
+// 2^(m_s - m) per split.
+template <typename OutT>
+__global__ void __launch_bounds__(256) mla_combine512_kernel(MlaPlan p, int n_splits, const float* __restrict__ part_o,
+                                                             const float* __restrict__ part_ml) {
+  const int64_t rh = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 6);
+  if (rh >= (int64_t)p.R * p.H) return;
+  const int t = threadIdx.x & 63;
+  const float* ml = part_ml + rh * n_splits * 2;
+  float m = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) m = fmaxf(m, ml[2 * s]);
+  float l = 0.f;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < n_splits; ++s) {
+    const float ms = ml[2 * s];
+    if (ms == -INFINITY) continue;
+    const float w = exp2f(ms - m);
+    l += w * ml[2 * s + 1];
+    const float4* src = (const float4*)(part_o + (rh * n_splits + s) * MLA_DV) + 2 * t;
+    const float4 a = src[0], b = src[1];
+    acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+    acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  if constexpr (sizeof(OutT) == 2) {
+    uint32_t w4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+      w4[i] = *(uint32_t*)&v;
+    }
+    *((uint4*)((__nv_bfloat16*)p.out + rh * MLA_DV) + t) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  } else {
+    float4* dst = (float4*)((float*)p.out + rh * MLA_DV) + 2 * t;
+    dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+  }
+  if (t == 0 && p.lse) p.lse[rh] = l > 0.f ? (m + log2f(l)) / LOG2E : -INFINITY;
+}
+
+template <typename OutT>
+static int launch_combine(const MlaPlan& p, int n_splits, const float* part_o, const float* part_ml, cudaStream_t st) {
+  const int64_t rh = (int64_t)p.R * p.H;
+  if (p.d_v == MLA_DV && ((uintptr_t)p.out % 16) == 0) {
+    mla_combine512_kernel<OutT><<<(unsigned)((rh + 3) / 4), 256, 0, st>>>(p, n_splits, part_o, part_ml);
+  } else {
+    mla_combine_kernel<OutT><<<(unsigned)rh, 128, 0, st>>>(p, n_splits, part_o, part_ml);
+  }
+  return check_launch("sparse_mla_combine");
+}
+
 // float32 path: one CTA per (row, head, split); logits of the split in shared.
 __global__ void __launch_bounds__(256) sparse_mla_f32_kernel(MlaPlan p, MlaSplit sp, float* __restrict__ part_o,
                                                               float* __restrict__ part_ml) {
@@ -464,9 +516,7 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
     int rc = launch_sparse_mla_tc(p, sp.n_splits, (int)sp.per_split, part_o, part_ml, st);
     if (rc) return rc;
     if (sp.n_splits > 1) {
-      mla_combine_kernel<__nv_bfloat16><<<(unsigned)((int64_t)p.R * p.H), 128, 0, st>>>(p, sp.n_splits, part_o,
-                                                                                        part_ml);
-      return check_launch("sparse_mla_combine");
+      return launch_combine<__nv_bfloat16>(p, sp.n_splits, part_o, part_ml, st);
     }
     return MTPSD_OK;
   }
@@ -481,9 +531,7 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
     int rc = check_launch("sparse_mla_bf16");
     if (rc) return rc;
     if (sp.n_splits > 1) {
-      mla_combine_kernel<__nv_bfloat16><<<(unsigned)((int64_t)p.R * p.H), 128, 0, st>>>(p, sp.n_splits, part_o,
-                                                                                        part_ml);
-      return check_launch("sparse_mla_combine");
+      return launch_combine<__nv_bfloat16>(p, sp.n_splits, part_o, part_ml, st);
     }
     return MTPSD_OK;
   }
@@ -496,8 +544,7 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
   int rc = check_launch("sparse_mla_f32");
   if (rc) return rc;
   if (sp.n_splits > 1) {
-    mla_combine_kernel<float><<<(unsigned)((int64_t)p.R * p.H), 128, 0, st>>>(p, sp.n_splits, part_o, part_ml);
-    return check_launch("sparse_mla_combine");
+    return launch_combine<float>(p, sp.n_splits, part_o, part_ml, st);
   }
   return MTPSD_OK;
 }
