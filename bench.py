@@ -23,6 +23,7 @@ benchmark) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -314,13 +315,17 @@ def run_ours(a, world, rank, local):
 
 
 def _traffic_from_profile():
-    """DRAM bytes per launch of the profiled kernel, when a summary for the
-    current kernel build is committed (profiles/traffic.json), else None."""
+    """DRAM bytes per launch of the profiled kernel (profiles/traffic.json),
+    or None when there is no capture or the kernel source changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
+        src = os.path.join(ROOT, d["source"])
+        with open(src, "rb") as f:
+            if hashlib.sha1(f.read()).hexdigest() != d["source_sha1"]:
+                return None
         return d.get("sparse_mla_verify_dram_bytes")
     except Exception:
         return None
