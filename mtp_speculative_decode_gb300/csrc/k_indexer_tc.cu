@@ -410,8 +410,9 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const int pos_in_tile = quarter * 32 + lane;
     constexpr int rows_per_wg = 64 / H;    // 1 (H = 64) or 2 (H = 32)
-    int n_chunk = 0, cur_g = -1, nrows = 0, row0 = 0, nch = 0;
+    int n_chunk = 0, cur_g = -1, nrows = 0, row0 = 0, nch = 0, ks_tile = -1;
     int64_t vmax = 0, cstart = 0;
+    float ks_next = 0.f;
     bool ok = true;
     Cursor c;
     c.start(p, n_groups, it0);
@@ -424,15 +425,36 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
         vmax = p.g_vmax[g];
         cstart = p.cache_start[p.g_b[g]];
         nch = (nrows * H + SLOT_COLS - 1) / SLOT_COLS;
-        for (int e = lane; e < nrows * H; e += 32)
-          wq[e] = p.w[(int64_t)row0 * H + e] * p.q_scale[(int64_t)row0 * H + e];
+        {   // all of the group's (row, head) weights in flight at once
+          float wv[Q_ROWS / 32], qv[Q_ROWS / 32];
+#pragma unroll
+          for (int k = 0; k < Q_ROWS / 32; ++k) {
+            const int e = lane + 32 * k;
+            const bool in = e < nrows * H;
+            wv[k] = in ? p.w[(int64_t)row0 * H + e] : 0.f;
+            qv[k] = in ? p.q_scale[(int64_t)row0 * H + e] : 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < Q_ROWS / 32; ++k)
+            if (lane + 32 * k < nrows * H) wq[lane + 32 * k] = wv[k] * qv[k];
+        }
         for (int i = lane; i < nrows; i += 32) vis[i] = min(p.row_pos[row0 + i] + 1, p.max_visible);
         __syncwarp();
         cur_g = g;
+        ks_tile = -1;
+      }
+      // this position's key scale; the next tile's (same group) is loaded a tile ahead
+      auto load_ks = [&](int tile) -> float {
+        const int64_t ss = (int64_t)tile * TILE_M + pos_in_tile;
+        const int64_t pr = cstart + ss;
+        return (ss < vmax && pr >= 0 && pr < p.pool) ? p.k_scale[pr] : 0.f;
+      };
+      const float ks = ks_tile == c.tile ? ks_next : load_ks(c.tile);
+      if ((int64_t)(c.tile + 1) * TILE_M < vmax) {
+        ks_next = load_ks(c.tile + 1);
+        ks_tile = c.tile + 1;
       }
       const int64_t s = (int64_t)c.tile * TILE_M + pos_in_tile;
-      const int64_t prow = cstart + s;
-      const float ks = (s < vmax && prow >= 0 && prow < p.pool) ? p.k_scale[prow] : 0.f;
       for (int ch = 0; ch < nch; ++ch) {
         const int slot = n_chunk % NSLOT, sround = n_chunk / NSLOT;
         // warp-uniform outcome: tcgen05.ld below is a warp-collective instruction
