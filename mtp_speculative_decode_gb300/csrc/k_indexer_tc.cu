@@ -21,7 +21,9 @@
 //              weight, head sum, k_scale, coalesced score store
 //   warp 8     TMA producer: query rows of the current request group and a
 //              6-stage ring of key tiles
-//   warp 9     TMEM allocation and the single-thread MMA issue
+//   warp 9     TMEM allocation and the MMA issue
+// The producer and MMA roles run with the whole warp (uniform loop state,
+// bounded waits taken by all lanes) and one elected lane issues.
 // Work: the rows of each request are cut into groups of up to 512/H rows
 // (the query block kept in shared memory); each group scans
 // ceil(max visible / 128) key tiles; the flattened (group, tile) list is split
@@ -133,6 +135,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(saddr(bar))
       : "memory");
+}
+
+// One lane of a converged warp (the lowest), as a warp-uniform branch: the
+// producer and MMA roles run with the whole warp so that their loop state
+// stays in uniform registers, and only the elected lane issues.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n .reg .b32 rx;\n .reg .pred px;\n elect.sync rx|px, 0xffffffff;\n selp.b32 %0, 1, 0, px;\n}\n"
+               : "=r"(pred));
+  return pred != 0;
 }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms of
@@ -323,87 +335,102 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == PRODUCER_WARP) {
-    if (lane == 0) {
+    if (elect_one()) {
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_k) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_q) : "memory");
-      int n_load = 0, gq = 0, cur_g = -1;
-      bool ok = true;
-      Cursor c;
-      c.start(p, n_groups, it0);
-      for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups)) {
-        const int g = c.g;
-        if (g != cur_g) {
-          if (gq > 0) ok = mbar_wait(q_empty, (gq - 1) & 1, abort_flag, p.status);
-          if (!ok) break;
-          const int nrows = p.g_nrows[g], row0 = p.g_row0[g];
+    }
+    __syncwarp();
+    int n_load = 0, gq = 0, cur_g = -1;
+    int64_t cstart = 0;
+    bool ok = true;
+    Cursor c;
+    c.start(p, n_groups, it0);
+    for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups)) {
+      const int g = c.g;
+      if (g != cur_g) {
+        if (gq > 0) ok = __all_sync(0xffffffffu, mbar_wait(q_empty, (gq - 1) & 1, abort_flag, p.status));
+        if (!ok) break;
+        const int nrows = p.g_nrows[g], row0 = p.g_row0[g];
+        cstart = p.cache_start[p.g_b[g]];
+        if (elect_one()) {
           mbar_expect_tx(q_full, (uint32_t)(nrows * H * KB));
           for (int i = 0; i < nrows; ++i)
             tma_load_2d(saddr(sm + OFF_Q + i * H * KB), &tmap_q, 0, (row0 + i) * H, q_full);
-          ++gq;
-          cur_g = g;
         }
-        const int stage = n_load % NSTAGE, round = n_load / NSTAGE;
-        if (round > 0) ok = mbar_wait(&k_empty[stage], (round - 1) & 1, abort_flag, p.status);
-        if (!ok) break;
+        __syncwarp();
+        ++gq;
+        cur_g = g;
+      }
+      const int stage = n_load % NSTAGE, round = n_load / NSTAGE;
+      if (round > 0) ok = __all_sync(0xffffffffu, mbar_wait(&k_empty[stage], (round - 1) & 1, abort_flag, p.status));
+      if (!ok) break;
+      const int64_t y = cstart + (int64_t)c.tile * TILE_M;
+      if (elect_one()) {
         mbar_expect_tx(&k_full[stage], TILE_M * KB);
-        const int64_t y = p.cache_start[p.g_b[g]] + (int64_t)c.tile * TILE_M;
         tma_load_2d(saddr(sm + OFF_K + stage * TILE_M * KB), &tmap_k, 0, (int)y, &k_full[stage]);
-        ++n_load;
       }
-      if (*abort_flag) {   // drain this CTA's copies still in flight (bounded)
-        volatile int dummy = 0;
-        for (int s = 0; s < NSTAGE; ++s) {
-          const int issued = n_load / NSTAGE + (s < n_load % NSTAGE ? 1 : 0);   // loads of stage s
-          if (issued > 0) mbar_wait(&k_full[s], (issued - 1) & 1, &dummy, p.status);
-        }
-        if (gq > 0) mbar_wait(q_full, (gq - 1) & 1, &dummy, p.status);
+      __syncwarp();
+      ++n_load;
+    }
+    if (*abort_flag && lane == 0) {   // drain this CTA's copies still in flight (bounded)
+      volatile int dummy = 0;
+      for (int s = 0; s < NSTAGE; ++s) {
+        const int issued = n_load / NSTAGE + (s < n_load % NSTAGE ? 1 : 0);   // loads of stage s
+        if (issued > 0) mbar_wait(&k_full[s], (issued - 1) & 1, &dummy, p.status);
       }
+      if (gq > 0) mbar_wait(q_full, (gq - 1) & 1, &dummy, p.status);
     }
   } else if (warp == MMA_WARP) {
-    if (lane == 0) {
-      int n_cons = 0, n_chunk = 0, gq = 0, cur_g = -1, nch = 0;
-      bool ok = true;
-      Cursor c;
-      c.start(p, n_groups, it0);
-      for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups)) {
-        const int g = c.g;
-        if (g != cur_g) {
-          if (cur_g >= 0) mma_commit(q_empty);
-          ok = mbar_wait(q_full, gq & 1, abort_flag, p.status);
-          if (!ok) break;
-          ++gq;
-          cur_g = g;
-          nch = (p.g_nrows[g] * H + SLOT_COLS - 1) / SLOT_COLS;
+    int n_cons = 0, n_chunk = 0, gq = 0, cur_g = -1, nch = 0;
+    bool ok = true;
+    Cursor c;
+    c.start(p, n_groups, it0);
+    for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups)) {
+      const int g = c.g;
+      if (g != cur_g) {
+        if (cur_g >= 0) {
+          if (elect_one()) mma_commit(q_empty);
+          __syncwarp();
         }
-        const int stage = n_cons % NSTAGE, round = n_cons / NSTAGE;
-        ok = mbar_wait(&k_full[stage], round & 1, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, mbar_wait(q_full, gq & 1, abort_flag, p.status));
         if (!ok) break;
-        tc_fence_after();
-        const uint32_t a_base = saddr(sm + OFF_K + stage * TILE_M * KB);
-        for (int ch = 0; ch < nch && ok; ++ch) {
-          const int slot = n_chunk % NSLOT, sround = n_chunk / NSLOT;
-          if (sround > 0) {
-            ok = mbar_wait(&slot_empty[slot], (sround - 1) & 1, abort_flag, p.status);
-            if (!ok) break;
-            tc_fence_after();
-          }
-          const uint32_t b_base = saddr(sm + OFF_Q + ch * SLOT_COLS * KB);
-          const uint32_t d = tmem_base + (uint32_t)(slot * SLOT_COLS);
+        ++gq;
+        cur_g = g;
+        nch = (p.g_nrows[g] * H + SLOT_COLS - 1) / SLOT_COLS;
+      }
+      const int stage = n_cons % NSTAGE, round = n_cons / NSTAGE;
+      ok = __all_sync(0xffffffffu, mbar_wait(&k_full[stage], round & 1, abort_flag, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a_base = saddr(sm + OFF_K + stage * TILE_M * KB);
+      for (int ch = 0; ch < nch && ok; ++ch) {
+        const int slot = n_chunk % NSLOT, sround = n_chunk / NSLOT;
+        if (sround > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&slot_empty[slot], (sround - 1) & 1, abort_flag, p.status));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const uint32_t b_base = saddr(sm + OFF_Q + ch * SLOT_COLS * KB);
+        const uint32_t d = tmem_base + (uint32_t)(slot * SLOT_COLS);
+        if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < KB / 32; ++kk)
             mma_fp8(d, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), kk > 0 ? 1u : 0u);
           mma_commit(&slot_full[slot]);
-          ++n_chunk;
         }
-        if (!ok) break;
-        mma_commit(&k_empty[stage]);
-        ++n_cons;
+        __syncwarp();
+        ++n_chunk;
       }
-      // all issued MMAs complete before TMEM is released
-      mma_commit(drain);
-      volatile int dummy = 0;
-      mbar_wait(drain, 0, &dummy, p.status);
+      if (!ok) break;
+      if (elect_one()) mma_commit(&k_empty[stage]);
+      __syncwarp();
+      ++n_cons;
     }
+    // all issued MMAs complete before TMEM is released
+    if (elect_one()) mma_commit(drain);
+    __syncwarp();
+    volatile int dummy = 0;
+    mbar_wait(drain, 0, &dummy, p.status);
   } else {
     // ------------------------------------------------------------ epilogue
     const int wg = warp >> 2;              // which 64 of the slot's 128 columns
