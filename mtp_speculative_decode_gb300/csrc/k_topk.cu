@@ -166,10 +166,11 @@ __global__ void __launch_bounds__(TOPK_THREADS, 1) topk_kernel(TopkPlan p, int64
 
 // Rows of up to 40960 keys: each thread holds KPT consecutive keys in
 // registers (positions t*KPT .. t*KPT+KPT-1) and the CTA finds the k-th
-// largest key T exactly by a bitwise search from the most significant bit:
-// T grows by bit b when at least k keys are >= T | 2^b (32 counting rounds,
-// one warp reduction and one barrier each).  The ordered compaction is the
-// same as above.
+// largest key T exactly by a bitwise search: the bits shared by all visible
+// keys are T's, and below them T grows by bit b when at least k keys are
+// >= T | 2^b (one counting round per bit: a warp reduction, one barrier, and
+// a second warp reduction over the per-warp counts).  The ordered compaction
+// is the same as above.
 template <int KPT, int NTH>
 __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
   __shared__ int wsum[2][32];
@@ -207,9 +208,30 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
     key[i + 2] = a + i + 2 < V ? float_key(f.z) : 0u;
     key[i + 3] = a + i + 3 < V ? float_key(f.w) : 0u;
   }
-  uint32_t T = 0;
+  // bits shared by every visible key (the sign and most exponent bits of these
+  // scores) are T's as well; the search starts below them
+  uint32_t kand = ~0u, kor = 0u;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i)
+    if (a + i < V) {
+      kand &= key[i];
+      kor |= key[i];
+    }
+  kand = __reduce_and_sync(0xffffffffu, kand);
+  kor = __reduce_or_sync(0xffffffffu, kor);
+  if (lane == 0) {
+    wsum[0][wid] = (int)kand;
+    wsum[1][wid] = (int)kor;
+  }
+  __syncthreads();
+  kand = __reduce_and_sync(0xffffffffu, lane < NW ? (uint32_t)wsum[0][lane] : ~0u);
+  kor = __reduce_or_sync(0xffffffffu, lane < NW ? (uint32_t)wsum[1][lane] : 0u);
+  __syncthreads();   // wsum is reused below
+  const uint32_t diff = kand ^ kor;
+  const int b0 = diff ? 31 - __clz(diff) : -1;   // highest bit where visible keys differ
+  uint32_t T = b0 >= 31 ? 0u : (b0 < 0 ? kand : (kand & (~0u << (b0 + 1))));
 #pragma unroll 1
-  for (int b = 31; b >= 0; --b) {
+  for (int b = b0; b >= 0; --b) {
     const uint32_t cand = T | (1u << b);
     unsigned c = 0;
 #pragma unroll
@@ -217,10 +239,8 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
     c = __reduce_add_sync(0xffffffffu, c);
     if (lane == 0) wsum[b & 1][wid] = (int)c;
     __syncthreads();   // the other buffer is rewritten only after the next barrier
-    int tot = 0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) tot += wsum[b & 1][w];
-    if (tot >= k) T = cand;
+    const unsigned tot = __reduce_add_sync(0xffffffffu, lane < NW ? (unsigned)wsum[b & 1][lane] : 0u);
+    if (tot >= (unsigned)k) T = cand;
   }
   int n_gt = 0, n_eq = 0;
 #pragma unroll
