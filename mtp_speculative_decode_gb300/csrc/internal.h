@@ -61,6 +61,7 @@ struct MlaPlan {
 size_t mla_workspace_bytes(int R, int H, int n_idx, int n_append, int dtype);
 bool mla_tc_supported(const MlaPlan& p);
 int mla_tc_per_split(int R, int H, int64_t total);
+int mla_tc_ml_halves();
 int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* part_o, float* part_ml,
                          cudaStream_t st);
 int launch_sparse_mla(const MlaPlan& p, cudaStream_t st);

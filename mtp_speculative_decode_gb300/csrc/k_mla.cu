@@ -304,48 +304,60 @@ __global__ void __launch_bounds__(256, 1) sparse_mla_bf16_kernel(MlaPlan p, MlaS
   }
 }
 
-// Merge split partials: o = sum_s 2^(m_s - m) o_s / sum_s 2^(m_s - m) l_s.
+// Merge split partials: o = sum_s 2^(m_s - m) o_s / sum_s 2^(m_s - m) l_s.  The partials carry
+// `halves` (max, sum) pairs per split: with 2, the two halves of the value dims were accumulated
+// with their own maxima and sums, and each half is merged with its own.
 template <typename OutT>
-__global__ void mla_combine_kernel(MlaPlan p, int n_splits, const float* __restrict__ part_o,
+__global__ void mla_combine_kernel(MlaPlan p, int n_splits, int halves, const float* __restrict__ part_o,
                                    const float* __restrict__ part_ml) {
   const int64_t rh = blockIdx.x;   // r * H + h
-  const float* ml = part_ml + rh * n_splits * 2;
-  float m = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) m = fmaxf(m, ml[2 * s]);
-  float l = 0.f;
-  for (int s = 0; s < n_splits; ++s)
-    if (ml[2 * s] != -INFINITY) l += exp2f(ml[2 * s] - m) * ml[2 * s + 1];
-  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float* ml = part_ml + rh * n_splits * halves * 2;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  for (int v = 0; v < halves; ++v) {
+    for (int s = 0; s < n_splits; ++s) m[v] = fmaxf(m[v], ml[(s * halves + v) * 2]);
+    for (int s = 0; s < n_splits; ++s) {
+      const float ms = ml[(s * halves + v) * 2];
+      if (ms != -INFINITY) l[v] += exp2f(ms - m[v]) * ml[(s * halves + v) * 2 + 1];
+    }
+  }
+  const int dh = p.d_v / halves;
   for (int d = threadIdx.x; d < p.d_v; d += blockDim.x) {
+    const int v = halves == 2 && d >= dh ? 1 : 0;
     float acc = 0.f;
-    for (int s = 0; s < n_splits; ++s)
-      if (ml[2 * s] != -INFINITY) acc += exp2f(ml[2 * s] - m) * part_o[(rh * n_splits + s) * p.d_v + d];
+    for (int s = 0; s < n_splits; ++s) {
+      const float ms = ml[(s * halves + v) * 2];
+      if (ms != -INFINITY) acc += exp2f(ms - m[v]) * part_o[(rh * n_splits + s) * p.d_v + d];
+    }
+    const float inv = l[v] > 0.f ? 1.f / l[v] : 0.f;
     OutT* og = (OutT*)p.out + rh * p.d_v + d;
     if constexpr (sizeof(OutT) == 2) *og = __float2bfloat16_rn(acc * inv);
     else *og = acc * inv;
   }
-  if (threadIdx.x == 0 && p.lse) p.lse[rh] = l > 0.f ? (m + log2f(l)) / LOG2E : -INFINITY;
+  if (threadIdx.x == 0 && p.lse) p.lse[rh] = l[0] > 0.f ? (m[0] + log2f(l[0])) / LOG2E : -INFINITY;
 }
 
 // The same merge for 512 value dims with 16-byte accesses: four heads per
 // 256-thread block, 64 threads per head, 8 dims per thread; one weight
 // 2^(m_s - m) per split.
 template <typename OutT>
-__global__ void __launch_bounds__(256) mla_combine512_kernel(MlaPlan p, int n_splits, const float* __restrict__ part_o,
+__global__ void __launch_bounds__(256) mla_combine512_kernel(MlaPlan p, int n_splits, int halves,
+                                                             const float* __restrict__ part_o,
                                                              const float* __restrict__ part_ml) {
   const int64_t rh = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 6);
   if (rh >= (int64_t)p.R * p.H) return;
   const int t = threadIdx.x & 63;
-  const float* ml = part_ml + rh * n_splits * 2;
+  // dims 8t..8t+7 lie in value half t / 32 when the halves carry their own (max, sum)
+  const int ms_stride = halves * 2;
+  const float* ml = part_ml + rh * n_splits * ms_stride + (halves == 2 ? (t >> 5) * 2 : 0);
   float m = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) m = fmaxf(m, ml[2 * s]);
+  for (int s = 0; s < n_splits; ++s) m = fmaxf(m, ml[s * ms_stride]);
   float l = 0.f;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int s = 0; s < n_splits; ++s) {
-    const float ms = ml[2 * s];
+    const float ms = ml[s * ms_stride];
     if (ms == -INFINITY) continue;
     const float w = exp2f(ms - m);
-    l += w * ml[2 * s + 1];
+    l += w * ml[s * ms_stride + 1];
     const float4* src = (const float4*)(part_o + (rh * n_splits + s) * MLA_DV) + 2 * t;
     const float4 a = src[0], b = src[1];
     acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
@@ -369,12 +381,13 @@ __global__ void __launch_bounds__(256) mla_combine512_kernel(MlaPlan p, int n_sp
 }
 
 template <typename OutT>
-static int launch_combine(const MlaPlan& p, int n_splits, const float* part_o, const float* part_ml, cudaStream_t st) {
+static int launch_combine(const MlaPlan& p, int n_splits, int halves, const float* part_o, const float* part_ml,
+                          cudaStream_t st) {
   const int64_t rh = (int64_t)p.R * p.H;
   if (p.d_v == MLA_DV && ((uintptr_t)p.out % 16) == 0) {
-    mla_combine512_kernel<OutT><<<(unsigned)((rh + 3) / 4), 256, 0, st>>>(p, n_splits, part_o, part_ml);
+    mla_combine512_kernel<OutT><<<(unsigned)((rh + 3) / 4), 256, 0, st>>>(p, n_splits, halves, part_o, part_ml);
   } else {
-    mla_combine_kernel<OutT><<<(unsigned)rh, 128, 0, st>>>(p, n_splits, part_o, part_ml);
+    mla_combine_kernel<OutT><<<(unsigned)rh, 128, 0, st>>>(p, n_splits, halves, part_o, part_ml);
   }
   return check_launch("sparse_mla_combine");
 }
@@ -495,7 +508,7 @@ size_t mla_workspace_bytes(int R, int H, int n_idx, int n_append, int dtype) {
   MlaSplit sp = plan_split(R, H, n_idx, n_append, dtype);
   if (sp.n_splits == 1) return 0;
   size_t rh = (size_t)R * H * sp.n_splits;
-  return rh * MLA_DV * sizeof(float) + rh * 2 * sizeof(float) + 256;
+  return rh * MLA_DV * sizeof(float) + rh * 4 * sizeof(float) + 256;   // up to two (max, sum) pairs per split
 }
 
 int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
@@ -516,7 +529,7 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
     int rc = launch_sparse_mla_tc(p, sp.n_splits, (int)sp.per_split, part_o, part_ml, st);
     if (rc) return rc;
     if (sp.n_splits > 1) {
-      return launch_combine<__nv_bfloat16>(p, sp.n_splits, part_o, part_ml, st);
+      return launch_combine<__nv_bfloat16>(p, sp.n_splits, mla_tc_ml_halves(), part_o, part_ml, st);
     }
     return MTPSD_OK;
   }
@@ -531,7 +544,7 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
     int rc = check_launch("sparse_mla_bf16");
     if (rc) return rc;
     if (sp.n_splits > 1) {
-      return launch_combine<__nv_bfloat16>(p, sp.n_splits, part_o, part_ml, st);
+      return launch_combine<__nv_bfloat16>(p, sp.n_splits, 1, part_o, part_ml, st);
     }
     return MTPSD_OK;
   }
@@ -544,7 +557,7 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
   int rc = check_launch("sparse_mla_f32");
   if (rc) return rc;
   if (sp.n_splits > 1) {
-    return launch_combine<float>(p, sp.n_splits, part_o, part_ml, st);
+    return launch_combine<float>(p, sp.n_splits, 1, part_o, part_ml, st);
   }
   return MTPSD_OK;
 }

@@ -5,42 +5,53 @@
 // head h, softmax attention over the selected latent rows c[s_j, 0:576] with
 // values c[s_j, 0:512].
 //
-// One CTA owns (row, 128-head group, half of the 512 value dims, split of the
-// selected list).  The 128 heads are the MMA's M.  A full [128 x 512] fp32
-// output needs all 512 TMEM columns, so the value dims are split over two
-// CTAs that both form the scores:
-//   TMEM  [  0,128) query dims 0..255 (A operand of QK^T, bf16 pairs)
-//         [128,192) [192,256) two score buffers S of 64 positions (fp32),
-//                   P aliased in their first 32 columns (bf16 pairs)
+// A cluster of two CTAs owns (row, 128-head group, split of the selected
+// list); the 128 heads are the MMA's M.  The two CTAs split the 576 latent
+// dims instead of duplicating them, so every selected row is gathered once:
+//   rank 0: dims 0..255 and the rope dims 512..575 (5 chunks of 64 dims);
+//           its value dims are 0..255
+//   rank 1: dims 256..511 (4 chunks); its value dims are 256..511
+// Each CTA forms the partial scores of its dims, S_k = Q[:, D_k] C[:, D_k]^T,
+// in TMEM.  Its sender warps scale them to log2 units, round them to fp16
+// and store them into the other CTA's receive slot (st.async, 16 KB per 64
+// positions, completing bytes on that CTA's mbarrier); its softmax warps add
+// the received half to their own fp32 partial, S = S_own + S_other, and run
+// the softmax for this CTA's 256 value dims.  The two CTAs see the other
+// half rounded differently, so each value half keeps its own running
+// (max, sum); split partials carry one (max, sum) per half.
+//   TMEM  [  0,128) this CTA's first 256 query dims (A operand, bf16 pairs)
+//         [128,192) [192,256) two partial-score buffers of 64 positions
+//                   (fp32), P aliased in their first 32 columns (bf16 pairs)
 //         [256,512) O: 128 heads x this CTA's 256 value dims (fp32)
-//   SMEM  query dims 256..575 (A operand, 128-byte swizzle, 80 KB) and two
-//         pair buffers of 64 gathered latent rows (72 KB each).  A pair
-//         buffer is filled as two 32-row tiles and laid out per 64-dim chunk:
-//         chunk c = 64 rows x 128 B (rows 0..31 from the first tile, 32..63
-//         from the second), 128-byte swizzle.  The same bytes are the K-major
-//         B operand of S = Q C^T (N = 64 positions) and the MN-major B
-//         operand of O += P V (K = positions, N = this CTA's 256 dims).
-// Per 64-position pair: QK^T = 16 MMAs with A from TMEM + 20 with A from
-// shared memory (M=128, N=64, K=16); the softmax warps (thread = head) read
-// S, apply the lazy max (O is rescaled only when a head's max grows by more
-// than 2^8), write P as bf16 into the S columns, and PV = 4 MMAs (M=128,
-// N=256, K=16) with A = P from TMEM accumulate into O.  QK(P) is issued
-// before PV(P-1) so the tensor cores work while the softmax runs.  (With A
-// in shared memory an N=32 MMA is bound by re-reading the 4 KB A tile; N=64
-// halves that cost per position.)
+//   SMEM  rank 0's rope query dims (16 KB, 128-byte swizzle); a ring of four
+//         pair buffers of 64 gathered positions (40 KB each), laid out per
+//         64-dim chunk (64 rows x 128 B, 128-byte swizzle), which are both the
+//         K-major B operand of the scores (N = 64 positions) and, for chunks
+//         0..3, the MN-major B operand of O += P V (K = positions, N = 256);
+//         two receive slots for the other CTA's fp16 partial scores.
+// Per pair: QK^T is 16 MMAs with A from TMEM (+4 with A from shared memory on
+// rank 0), M=128, N=64, K=16; PV is 4 MMAs (M=128, N=256, K=16) with A = P
+// from TMEM.  QK(P) is issued before PV(P-1) so the tensor cores work while
+// the softmax runs.  The softmax (thread = head) applies a lazy max: O is
+// rescaled only when a head's max grows by more than 2^8.
 //
-// Roles (224 threads): warps 0-3 softmax/epilogue (TMEM lanes = heads);
-// warps 4-5 produce: each turns its 16 positions of every 32-row tile into
-// pool rows (the selection entries are prefetched one tile ahead) and
-// gathers them with TMA tile::gather4 loads (4 rows x 64 dims per
-// instruction, invalid positions read as zeros through an out-of-range row);
-// the first also loads the shared part of the query; warp 6 allocates TMEM
-// and issues the MMAs.  The producer and MMA roles run with the whole warp so
-// that descriptors and coordinates stay in uniform registers, and one elected
-// lane issues.  Every mbarrier wait is bounded (2 s) and flags
-// MTPSD_STATUS_WAIT_TIMEOUT on expiry.
+// Roles (416 threads): warps 0-3 softmax/epilogue (TMEM lanes = heads);
+// warps 4-7 send the partial scores (thread = head of TMEM quadrant warp%4),
+// so the DSMEM stores, which drain at about 13 bytes per cycle per SM, run
+// beside the softmax instead of in it; warps 8-11 produce: each turns its 8
+// positions of every 32-row tile into pool rows and gathers this CTA's
+// chunks of them with TMA tile::gather4 loads (4 rows x 64 dims per
+// instruction; invalid positions read as zeros through an out-of-range row);
+// the first also loads rank 0's rope query dims; warp 12 allocates TMEM and
+// issues the MMAs.  A receive slot is refilled (pair P+2) only after the
+// other CTA's softmax warps have consumed it (one remote arrival per warp).  The producer
+// and MMA roles run with the whole warp so that descriptors and coordinates
+// stay in uniform registers, and one elected lane issues.  Every mbarrier
+// wait is bounded (2 s) and flags MTPSD_STATUS_WAIT_TIMEOUT on expiry; a CTA
+// whose partner stops sending times out the same way.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -52,28 +63,31 @@ constexpr int DL = 576, DV = 512, DVH = 256;
 constexpr int HG = 128;                 // heads per CTA (MMA M)
 constexpr int NT = 32;                  // positions per gathered tile
 constexpr int NP = 64;                  // positions per MMA step (a pair of tiles)
-constexpr int NSTAGE = 4;               // tiles in the ring = 2 pair buffers
-constexpr int QLO = 256;                // query dims held in TMEM
-constexpr int QHI_CHUNKS = (DL - QLO) / 64;   // 5 chunks of 64 dims in shared memory
-constexpr int C_CHUNKS = DL / 64;             // 9
-constexpr int CHUNK_BYTES = NP * 128;         // 8192: one chunk of a pair buffer
-constexpr int PAIR_BYTES = C_CHUNKS * CHUNK_BYTES;   // 73728
-constexpr int TILE_BYTES = PAIR_BYTES / 2;           // 36864 gathered per tile
-constexpr int OFF_QHI = 0;
-constexpr int OFF_C = OFF_QHI + QHI_CHUNKS * HG * 128;       // 81920
-constexpr int OFF_MASK = OFF_C + 2 * PAIR_BYTES;             // 229376: [NSTAGE][4] uint32 validity bits
+constexpr int NPAIR = 4;                // pair buffers in the ring
+constexpr int NSTAGE = 2 * NPAIR;       // 32-row tiles in the ring
+constexpr int NCH_MAX = 5;              // 64-dim chunks one CTA gathers (rank 0)
+constexpr int QTM = 256;                // query dims held in TMEM
+constexpr int CHUNK_BYTES = NP * 128;   // 8192: one chunk of a pair buffer
+constexpr int PAIR_STRIDE = NCH_MAX * CHUNK_BYTES;   // 40960
+constexpr int XSLOT_BYTES = HG * NP * 2;             // 16384: one pair's fp16 partial scores
+constexpr int OFF_QR = 0;                                    // rope query dims (rank 0)
+constexpr int OFF_C = OFF_QR + HG * 128;                     // 16384
+constexpr int OFF_X = OFF_C + NPAIR * PAIR_STRIDE;           // 180224
+constexpr int OFF_MASK = OFF_X + 2 * XSLOT_BYTES;            // 212992: [NSTAGE][4] uint32 validity bits
 constexpr int OFF_BAR = OFF_MASK + NSTAGE * 4 * 4;
-// barriers: c_full[4], c_empty[2], s_full[2], p_full[2], pv_done[2], q_ready, drain
-constexpr int N_BARS = NSTAGE + 2 + 6 + 2;
+// barriers: c_full[NSTAGE], c_empty[NPAIR], s_full[2], p_full[2], pv_done[2], x_full[2], s_read[2], x_free[2],
+// q_ready, drain
+constexpr int N_BARS = NSTAGE + NPAIR + 12 + 2;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;               // tmem base, abort flag
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;                 // alignment slack
-constexpr int THREADS = 288;
-constexpr int PROD_WARP = 4, N_PROD = 4, MMA_WARP = 8;
+constexpr int THREADS = 416;
+constexpr int SEND_WARP = 4, PROD_WARP = 8, N_PROD = 4, MMA_WARP = 12;
 constexpr int TM_Q = 0, TM_S0 = 128, TM_O = 256;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct Params {
   int B, R, H, n_idx, n_append;
@@ -130,6 +144,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
 __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t par) {
   uint32_t ok;
   asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(ok) : "r"(saddr(b)), "r"(par) : "memory");
+  return ok != 0;
+}
+// Non-blocking test, for loops that poll several barriers: try_wait may suspend the thread until
+// the phase completes, which would hold up the other conditions the loop serves.
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t par) {
+  uint32_t ok;
+  asm volatile("{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
                : "=r"(ok) : "r"(saddr(b)), "r"(par) : "memory");
   return ok != 0;
 }
@@ -228,6 +250,68 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *(uint32_t*)&v;
 }
 
+// The same wait with cluster-scope acquire, for barriers whose bytes the other CTA completes.
+__device__ __forceinline__ bool mbar_try_cl(uint64_t* b, uint32_t par) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, "
+      "p;\n}\n"
+      : "=r"(ok) : "r"(saddr(b)), "r"(par) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* b, uint32_t par, volatile int* abort_flag, int32_t* status) {
+  if (mbar_try_cl(b, par)) return true;
+  uint64_t t0 = gtimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_cl(b, par)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (gtimer() - t0 > WAIT_LIMIT_NS) {
+        *abort_flag = 1;
+        flag_status(status, MTPSD_STATUS_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+// shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_rank(uint32_t cta_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(cta_addr), "r"(rank));
+  return r;
+}
+// 16 bytes into the other CTA's shared memory; completes 16 bytes on its barrier
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// (lo, hi) -> fp16 pair with lo in the low half; out-of-range values saturate to +-65504
+__device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+// Arrive on a barrier of the other CTA.  Relaxed: the callers arrive after the values they read have
+// been consumed (so the reads are complete), and a release at cluster scope costs thousands of cycles.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// fp16 pair -> two floats (exact)
+__device__ __forceinline__ float2 f16x2_to_f32(uint32_t u) {
+  __half2 h = *(__half2*)&u;
+  return __half22float2(h);
+}
+
 // Pool row of an entry, or -1 (padding, past the split, or out of range: flagged).
 __device__ __forceinline__ int64_t entry_row(const Params& p, int64_t s, int64_t base, int64_t limit) {
   if (s == -1 || s == -2) return -1;
@@ -248,20 +332,26 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + OFF_BAR);
-  uint64_t* c_full = bars;                 // per tile stage: both producers' bytes landed
+  uint64_t* c_full = bars;                 // per tile stage: the producers' bytes landed
   uint64_t* c_empty = bars + NSTAGE;       // per pair buffer: its PV completed
-  uint64_t* s_full = c_empty + 2;
+  uint64_t* s_full = c_empty + NPAIR;      // partial scores of the pair in score buffer s are in TMEM
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
-  uint64_t* q_ready = pv_done + 2;
+  uint64_t* x_full = pv_done + 2;          // receive slot s holds the other CTA's partial scores
+  uint64_t* s_read = x_full + 2;           // the senders have read score buffer s
+  uint64_t* x_free = s_read + 2;           // the other CTA has consumed what this CTA sent into its slot s
+  uint64_t* q_ready = x_free + 2;
   uint64_t* drain = q_ready + 1;
   uint32_t* tmem_slot = (uint32_t*)(sm + OFF_MISC);
   volatile int* abort_flag = (volatile int*)(sm + OFF_MISC + 4);
   uint32_t* mask_s = (uint32_t*)(sm + OFF_MASK);   // [stage][producer]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();    // = the value half this CTA owns
+  const uint32_t peer = rank ^ 1u;
+  const int nch = rank == 0 ? 5 : 4;       // 64-dim chunks this CTA gathers
   const int r = blockIdx.x;
-  const int hg = blockIdx.y >> 1, vh = blockIdx.y & 1;
+  const int hg = blockIdx.y >> 1;
   const int split = blockIdx.z;
   const int h0 = hg * HG;
   const int b = request_of_row(p.row_offsets, p.B, (uint32_t)r);
@@ -275,13 +365,17 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSTAGE; ++i) mbar_init(&c_full[i], N_PROD);
+    for (int i = 0; i < NPAIR; ++i) mbar_init(&c_empty[i], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&c_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&pv_done[i], 1);
+      mbar_init(&x_full[i], 1);
+      mbar_init(&s_read[i], 128);
+      mbar_init(&x_free[i], 4);           // one arrival per softmax warp of the other CTA
     }
-    mbar_init(q_ready, 129);          // 128 softmax threads (TMEM part) + the first producer (TMA bytes)
+    // 128 softmax threads (query dims in TMEM), plus on rank 0 the first producer (rope dims by TMA)
+    mbar_init(q_ready, rank == 0 ? 129 : 128);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -293,6 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   fence_before();
   __syncthreads();
   fence_after();
+  cluster_sync();                          // both CTAs' barriers exist before any remote arrival
   const uint32_t tmem = *tmem_slot;
   const __nv_bfloat16* qrow = p.q + ((int64_t)r * p.H + h0) * DL;
 
@@ -301,10 +396,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     const int h = threadIdx.x;                 // 0..127 = TMEM lane
     const bool head_ok = (h0 + h) < p.H;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    {   // query dims 0..255 -> TMEM columns [0,128) as bf16 pairs
-      const uint4* src = (const uint4*)(qrow + (int64_t)h * DL);
+    {   // this CTA's 256 query dims -> TMEM columns [0,128) as bf16 pairs
+      const uint4* src = (const uint4*)(qrow + (int64_t)h * DL + rank * QTM);
 #pragma unroll
-      for (int c = 0; c < QLO / 64; ++c) {
+      for (int c = 0; c < QTM / 64; ++c) {
         uint32_t v[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -317,31 +412,59 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       fence_before();
       mbar_arrive(q_ready);
     }
+    // receive slot layout: head h's 64 fp16 scores are 8 pieces of 16 bytes, piece c at (c ^ (h & 7)),
+    // so that eight consecutive heads touch all 32 banks
+    const uint32_t x_own = saddr(sm + OFF_X) + (uint32_t)h * 128u;
+    const uint32_t xfree_peer = map_rank(saddr(x_free), peer);
+    const uint32_t swz = (uint32_t)(h & 7);
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int P = 0; P < n_pairs && ok; ++P) {
-      const int q = P & 1;
+      const int s = P & 1;
       const uint32_t par = (P >> 1) & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[q], par, abort_flag, p.status));
+      const int st0 = 2 * (P % NPAIR);
+      const uint32_t cpar = (P / NPAIR) & 1;
+      if (h == 0) mbar_arrive_expect_tx(&x_full[s], XSLOT_BYTES);
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s], par, abort_flag, p.status));
       // the validity bits were written by the producers before they released the two tiles
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[2 * q], par, abort_flag, p.status));
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[2 * q + 1], par, abort_flag, p.status));
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[st0], cpar, abort_flag, p.status));
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[st0 + 1], cpar, abort_flag, p.status));
       if (!ok) break;
       fence_after();
       uint32_t sr[64];
-      tm_ld32(tmem + lane_off + TM_S0 + q * 64, sr);
-      tm_ld32(tmem + lane_off + TM_S0 + q * 64 + 32, sr + 32);
+      tm_ld32(tmem + lane_off + TM_S0 + s * 64, sr);
+      tm_ld32(tmem + lane_off + TM_S0 + s * 64 + 32, sr + 32);
       tm_wait_ld();
-      const uint32_t* m0 = mask_s + (2 * q) * 4;
-      const uint32_t* m1 = mask_s + (2 * q + 1) * 4;
+      // the other CTA's fp16 partial scores of the same pair
+      ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_full[s], par, abort_flag, p.status));
+      if (!ok) break;
+      const uint32_t xo = x_own + (uint32_t)s * XSLOT_BYTES;
+      const uint32_t* m0 = mask_s + st0 * 4;
+      const uint32_t* m1 = mask_s + (st0 + 1) * 4;
       const uint64_t mask = (uint64_t)(m0[0] | m0[1] | m0[2] | m0[3]) | ((uint64_t)(m1[0] | m1[1] | m1[2] | m1[3]) << 32);
+      // S = this CTA's partial (fp32) + the other's (fp16), in log2 units
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        float v = ((mask >> j) & 1ull) ? __uint_as_float(sr[j]) * p.sl2 : -INFINITY;
-        sr[j] = __float_as_uint(v);
-        mx[j & 3] = fmaxf(mx[j & 3], v);
+      for (int c = 0; c < 8; ++c) {
+        uint32_t px[4];
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(px[0]), "=r"(px[1]), "=r"(px[2]), "=r"(px[3])
+                     : "r"(xo + ((c ^ swz) << 4))
+                     : "memory");
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int j = 8 * c + 2 * i;
+          const float2 o = f16x2_to_f32(px[i]);
+          const float v0 = ((mask >> j) & 1ull) ? fmaf(__uint_as_float(sr[j]), p.sl2, o.x) : -INFINITY;
+          const float v1 = ((mask >> (j + 1)) & 1ull) ? fmaf(__uint_as_float(sr[j + 1]), p.sl2, o.y) : -INFINITY;
+          sr[j] = __float_as_uint(v0);
+          sr[j + 1] = __float_as_uint(v1);
+          mx[i] = fmaxf(mx[i], fmaxf(v0, v1));
+        }
       }
+      // slot s may be written again (pair P+2) once all four warps have consumed it
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(xfree_peer + (uint32_t)s * 8u);
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       if (mt > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mt > -INFINITY)) {
         // new reference max for this head; rescale what O already holds
@@ -374,15 +497,17 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
         const float a = ex2(__uint_as_float(sr[2 * j]) - mo);
         const float c = ex2(__uint_as_float(sr[2 * j + 1]) - mo);
         pk[j] = pack_bf16(a, c);
-        __nv_bfloat162 bv = *(__nv_bfloat162*)&pk[j];
-        float2 f = __bfloat1622float2(bv);   // the sum uses the rounded values PV multiplies
-        psum[j & 3] += f.x + f.y;
+        // the sum uses the rounded values PV multiplies (bf16 -> f32 is a shift)
+        psum[j & 3] += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
       }
       l += (psum[0] + psum[1]) + (psum[2] + psum[3]);
-      tm_st32(tmem + lane_off + TM_S0 + q * 64, pk);
+      // P overwrites the scores: the senders must have read them
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_read[s], par, abort_flag, p.status));
+      if (!ok) break;
+      tm_st32(tmem + lane_off + TM_S0 + s * 64, pk);
       tm_wait_st();
       fence_before();
-      mbar_arrive(&p_full[q]);
+      mbar_arrive(&p_full[s]);
     }
     // ------------------------------------------------ epilogue
     if (ok && n_pairs > 0) {
@@ -392,7 +517,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     if (ok) fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
     if (p.n_splits == 1) {
-      __nv_bfloat16* og = p.out + ((int64_t)r * p.H + h0 + h) * DV + vh * DVH;
+      __nv_bfloat16* og = p.out + ((int64_t)r * p.H + h0 + h) * DV + rank * DVH;
 #pragma unroll 1
       for (int c = 0; c < DVH / 32; ++c) {
         uint32_t o[32];
@@ -413,10 +538,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
-      if (head_ok && vh == 0 && p.lse)
+      if (head_ok && rank == 0 && p.lse)
         p.lse[(int64_t)r * p.H + h0 + h] = l > 0.f ? (m_ref + log2f(l)) / LOG2E : -INFINITY;
     } else {
-      float* po = p.part_o + (((int64_t)r * p.H + h0 + h) * p.n_splits + split) * DV + vh * DVH;
+      float* po = p.part_o + (((int64_t)r * p.H + h0 + h) * p.n_splits + split) * DV + rank * DVH;
 #pragma unroll 1
       for (int c = 0; c < DVH / 32; ++c) {
         uint32_t o[32];
@@ -435,11 +560,46 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
                                  __uint_as_float(o[4 * i + 3]));
         }
       }
-      if (head_ok && vh == 0) {
-        float* ml = p.part_ml + (((int64_t)r * p.H + h0 + h) * p.n_splits + split) * 2;
+      if (head_ok) {   // each value half carries its own (max, sum)
+        float* ml = p.part_ml + ((((int64_t)r * p.H + h0 + h) * p.n_splits + split) * 2 + rank) * 2;
         ml[0] = l > 0.f ? m_ref : -INFINITY;
         ml[1] = l;
       }
+    }
+  } else if (warp < SEND_WARP + 4) {
+    // ------------------------------------------------ senders: thread = head of TMEM quadrant warp % 4
+    // Each reads the partial scores of its head, scales them to log2 units, rounds them to fp16 and
+    // stores them into the other CTA's receive slot (st.async, completing bytes on its x_full).
+    const int h = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t x_peer = map_rank(saddr(sm + OFF_X) + (uint32_t)h * 128u, peer);
+    const uint32_t xfull_peer = map_rank(saddr(x_full), peer);
+    const uint32_t swz = (uint32_t)(h & 7);
+    bool ok = true;
+    for (int P = 0; P < n_pairs && ok; ++P) {
+      const int s = P & 1;
+      const uint32_t par = (P >> 1) & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s], par, abort_flag, p.status));
+      if (!ok) break;
+      fence_after();
+      uint32_t sr[64];
+      tm_ld32(tmem + lane_off + TM_S0 + s * 64, sr);
+      tm_ld32(tmem + lane_off + TM_S0 + s * 64 + 32, sr + 32);
+      tm_wait_ld();
+      fence_before();
+      mbar_arrive(&s_read[s]);
+      uint32_t hx[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        hx[j] = pack_f16_sat(__uint_as_float(sr[2 * j]) * p.sl2, __uint_as_float(sr[2 * j + 1]) * p.sl2);
+      // the other CTA has consumed what was sent into this slot two pairs ago
+      if (P >= 2) ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_free[s], ((P - 2) >> 1) & 1, abort_flag, p.status));
+      if (!ok) break;
+      const uint32_t xo = x_peer + (uint32_t)s * XSLOT_BYTES;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_async_v4(xo + ((c ^ swz) << 4), hx[4 * c], hx[4 * c + 1], hx[4 * c + 2], hx[4 * c + 3],
+                    xfull_peer + (uint32_t)s * 8u);
     }
   } else if (warp < PROD_WARP + N_PROD) {
     // ------------------------------------------------ producers
@@ -451,10 +611,11 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     const int ln = lane & 7;
     const int my_pos = 4 * (pw + 4 * (ln >> 2)) + (ln & 3);
     const int32_t oob = (int32_t)p.pool;   // a row outside the tensor map: TMA reads zeros
-    if (pw == 0 && elect_one()) {   // query dims 256..575 of the 128 heads: 5 boxes of 64 dims x 128 rows
-      mbar_arrive_expect_tx(q_ready, QHI_CHUNKS * HG * 128);
-      for (int c = 0; c < QHI_CHUNKS; ++c)
-        tma_load_2d(saddr(sm + OFF_QHI + c * (HG * 128)), &tm_q, QLO + c * 64, r * p.H + h0, q_ready);
+    // first latent column of local chunk c
+    auto chunk_x = [&](int c) -> int { return rank == 0 ? (c < 4 ? c * 64 : 512) : 256 + c * 64; };
+    if (rank == 0 && pw == 0 && elect_one()) {   // rope query dims of the 128 heads: one box of 64 dims x 128 rows
+      mbar_arrive_expect_tx(q_ready, HG * 128);
+      tma_load_2d(saddr(sm + OFF_QR), &tm_q, 512, r * p.H + h0, q_ready);
     }
     __syncwarp();
     const int32_t* idx_row = p.idx + (int64_t)r * p.n_idx;
@@ -465,7 +626,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     for (int t = 0; t < n_tiles; ++t) {
       const int32_t craw = nraw;
       if (t + 1 < n_tiles) nraw = raw(j0 + (int64_t)(t + 1) * NT + my_pos);   // prefetch
-      const int st = t % NSTAGE, P = t >> 1, q = P & 1, R = P >> 1;
+      const int st = t % NSTAGE, P = t >> 1, q = P % NPAIR, R = P / NPAIR;
       if (R > 0 && !__all_sync(0xffffffffu, mbar_wait(&c_empty[q], (R - 1) & 1, abort_flag, p.status))) break;
       const int64_t j = j0 + (int64_t)t * NT + my_pos;
       const int64_t e = j >= j1 ? -2 : (j < p.n_idx ? (int64_t)craw : p.append_base[r] + 1 + (j - p.n_idx));
@@ -477,16 +638,17 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       int y[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) y[i] = __shfl_sync(0xffffffffu, yv, i);
-      const uint32_t dst = saddr(sm + OFF_C + q * PAIR_BYTES + (t & 1) * (NT * 128));
+      const uint32_t dst = saddr(sm + OFF_C + q * PAIR_STRIDE + (t & 1) * (NT * 128));
       if (elect_one()) {
-        mbar_arrive_expect_tx(&c_full[st], TILE_BYTES / N_PROD);
+        mbar_arrive_expect_tx(&c_full[st], (uint32_t)nch * 1024u);
 #pragma unroll
         for (int gi = 0; gi < 2; ++gi) {
           const int g = pw + 4 * gi;
 #pragma unroll
-          for (int c = 0; c < C_CHUNKS; ++c)
-            tma_gather4(dst + c * CHUNK_BYTES + g * 512, &tm_lat, c * 64, y[4 * gi], y[4 * gi + 1], y[4 * gi + 2],
-                        y[4 * gi + 3], &c_full[st]);
+          for (int c = 0; c < NCH_MAX; ++c)
+            if (c < nch)
+              tma_gather4(dst + c * CHUNK_BYTES + g * 512, &tm_lat, chunk_x(c), y[4 * gi], y[4 * gi + 1],
+                          y[4 * gi + 2], y[4 * gi + 3], &c_full[st]);
         }
       }
       __syncwarp();
@@ -498,15 +660,16 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
         const int n = issued / NSTAGE + (st < issued % NSTAGE ? 1 : 0);
         if (n > 0) mbar_wait(&c_full[st], (n - 1) & 1, &dummy, p.status);
       }
-      if (pw == 0) mbar_wait(q_ready, 0, &dummy, p.status);
+      if (rank == 0 && pw == 0) mbar_wait(q_ready, 0, &dummy, p.status);
     }
   } else {
-    // ------------------------------------------------ MMA issue (warp 6; one elected lane issues)
+    // ------------------------------------------------ MMA issue (warp 12; one elected lane issues)
     bool ok = __all_sync(0xffffffffu, mbar_wait(q_ready, 0, abort_flag, p.status));
     if (ok) fence_after();
-    const uint64_t qhi_desc = desc_sw128(saddr(sm + OFF_QHI), 16, 1024);
+    const uint64_t qr_desc = desc_sw128(saddr(sm + OFF_QR), 16, 1024);
     const uint64_t c_desc0 = desc_sw128(saddr(sm + OFF_C), 16, 1024);
-    const uint64_t v_desc0 = desc_sw128(saddr(sm + OFF_C) + vh * 4 * CHUNK_BYTES, CHUNK_BYTES, 1024);
+    const uint64_t v_desc0 = desc_sw128(saddr(sm + OFF_C), CHUNK_BYTES, 1024);
+    const int nk = nch * 4;
     // Issue whichever is ready: QK(nq) once its pair has landed (and PV(nq-2),
     // which last read the S columns QK(nq) overwrites, has been issued: the
     // MMAs execute in issue order), or PV(np) once the softmax published P.
@@ -516,26 +679,25 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     while (np < n_pairs && ok) {
       bool did = false;
       if (nq < n_pairs && nq <= np + 1) {
-        const int q = nq & 1;
-        const uint32_t par = (nq >> 1) & 1;
-        if (__all_sync(0xffffffffu, mbar_try(&c_full[2 * q], par) && mbar_try(&c_full[2 * q + 1], par))) {
+        const int bq = nq % NPAIR;
+        const uint32_t par = (nq / NPAIR) & 1;
+        if (__all_sync(0xffffffffu, mbar_test(&c_full[2 * bq], par) && mbar_test(&c_full[2 * bq + 1], par))) {
           fence_after();
-          const uint64_t cd = c_desc0 + (uint64_t)((q * PAIR_BYTES) >> 4);
-          const uint32_t d = tmem + TM_S0 + q * 64;
+          const uint64_t cd = c_desc0 + (uint64_t)((bq * PAIR_STRIDE) >> 4);
+          const uint32_t d = tmem + TM_S0 + (nq & 1) * 64;
           if (elect_one()) {
-            // S = Q C^T over 64 positions: dims 0..255 with A from TMEM, 256..575 with A from shared memory
+            // partial S over this CTA's chunks: 0..3 with A from TMEM, rank 0's rope chunk with A from shared memory
 #pragma unroll
-            for (int k = 0; k < DL / 16; ++k) {
-              const uint32_t boff = (uint32_t)((k >> 2) * CHUNK_BYTES + (k & 3) * 32);   // chunk, 32-byte K step
-              if (k < QLO / 16) {
-                mma_ts(d, tmem + TM_Q + k * 8, cd + (boff >> 4), IDESC_QK, k > 0 ? 1u : 0u);
-              } else {
-                const int kq = k - QLO / 16;
-                const uint32_t aoff = (uint32_t)((kq >> 2) * (HG * 128) + (kq & 3) * 32);
-                mma_ss(d, qhi_desc + (aoff >> 4), cd + (boff >> 4), IDESC_QK, 1u);
+            for (int k = 0; k < NCH_MAX * 4; ++k) {
+              if (k < nk) {
+                const uint32_t boff = (uint32_t)((k >> 2) * CHUNK_BYTES + (k & 3) * 32);   // chunk, 32-byte K step
+                if (k < QTM / 16)
+                  mma_ts(d, tmem + TM_Q + k * 8, cd + (boff >> 4), IDESC_QK, k > 0 ? 1u : 0u);
+                else
+                  mma_ss(d, qr_desc + (uint64_t)(((k & 3) * 32) >> 4), cd + (boff >> 4), IDESC_QK, 1u);
               }
             }
-            commit(&s_full[q]);
+            commit(&s_full[nq & 1]);
           }
           __syncwarp();
           ++nq;
@@ -543,18 +705,19 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
         }
       }
       if (np < nq) {
-        // O += P(np) V(np): A = P from TMEM, B = the pair buffer as MN-major (N = this CTA's 256 dims)
-        const int qp = np & 1;
-        if (__all_sync(0xffffffffu, mbar_try(&p_full[qp], (np >> 1) & 1))) {
+        // O += P(np) V(np): A = P from TMEM, B = chunks 0..3 of the pair buffer as MN-major (N = 256 dims)
+        const int sp = np & 1;
+        if (__all_sync(0xffffffffu, mbar_test(&p_full[sp], (np >> 1) & 1))) {
           fence_after();
-          const uint64_t vd = v_desc0 + (uint64_t)((qp * PAIR_BYTES) >> 4);
+          const int bp = np % NPAIR;
+          const uint64_t vd = v_desc0 + (uint64_t)((bp * PAIR_STRIDE) >> 4);
           if (elect_one()) {
 #pragma unroll
             for (int k = 0; k < NP / 16; ++k)
-              mma_ts(tmem + TM_O, tmem + TM_S0 + qp * 64 + k * 8, vd + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV,
+              mma_ts(tmem + TM_O, tmem + TM_S0 + sp * 64 + k * 8, vd + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV,
                      (np > 0 || k > 0) ? 1u : 0u);
-            commit(&pv_done[qp]);
-            commit(&c_empty[qp]);
+            commit(&pv_done[sp]);
+            commit(&c_empty[bp]);
           }
           __syncwarp();
           ++np;
@@ -587,6 +750,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
   }
+  cluster_sync();                          // the other CTA no longer writes into this CTA's shared memory
 }
 
 }  // namespace mtc
@@ -605,19 +769,62 @@ bool mla_tc_supported(const MlaPlan& p) {
   return tma_available();
 }
 
-// Splits of the selected list that balance whole waves of one-CTA-per-SM
-// work.  Returns the positions per
-// split (a multiple of NT).
+namespace {
+cudaLaunchConfig_t mla_tc_config(dim3 grid, cudaStream_t st, cudaLaunchAttribute* attrs) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(mtc::THREADS);
+  cfg.dynamicSmemBytes = mtc::SMEM_BYTES;
+  cfg.stream = st;
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 1;
+  attrs[0].val.clusterDim.y = 2;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+bool mla_tc_prepare() {
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(mtc::sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             mtc::SMEM_BYTES) != cudaSuccess)
+      return false;
+    attr = true;
+  }
+  return true;
+}
+// CTAs of this kernel that run at once: two per co-resident cluster.
+int mla_tc_resident_ctas() {
+  static int n = 0;
+  if (!n) {
+    int clusters = 0;
+    cudaLaunchAttribute attrs[1];
+    cudaLaunchConfig_t cfg = mla_tc_config(dim3(1, 2, 1), 0, attrs);
+    if (mla_tc_prepare() &&
+        cudaOccupancyMaxActiveClusters(&clusters, (void*)mtc::sparse_mla_tc_kernel, &cfg) == cudaSuccess &&
+        clusters > 0)
+      n = 2 * clusters;
+    else
+      n = num_sms() & ~1;
+    cudaGetLastError();
+  }
+  return n;
+}
+}  // namespace
+
+// Splits of the selected list that balance whole waves of resident clusters.
+// Returns the positions per split (a multiple of NP).
 int mla_tc_per_split(int R, int H, int64_t total) {
   const int64_t tiles = (total + mtc::NP - 1) / mtc::NP;
   const int64_t units = (int64_t)R * (H / mtc::HG) * 2;
-  const int sms = num_sms();
+  const int slots = mla_tc_resident_ctas();
   int64_t best = 1;
   double best_cost = 1e30;
   for (int64_t s = best; s <= best + 64 && s <= tiles; ++s) {
     const int64_t per = (tiles + s - 1) / s;
-    const int64_t waves = (units * s + sms - 1) / sms;
-    const double cost = (double)waves * (per + 2.0);
+    const int64_t waves = (units * s + slots - 1) / slots;
+    const double cost = (double)waves * (per + 4.0);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = s;
@@ -626,6 +833,9 @@ int mla_tc_per_split(int R, int H, int64_t total) {
   const int64_t per = ((tiles + best - 1) / best) * mtc::NP;
   return (int)(per > 0 ? per : mtc::NP);
 }
+
+// (max, sum) pairs per split that the kernel writes: one per value half
+int mla_tc_ml_halves() { return 2; }
 
 int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* part_o, float* part_ml,
                          cudaStream_t st) {
@@ -643,13 +853,17 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
     set_error("sparse_mla: cuTensorMapEncodeTiled failed");
     return MTPSD_ECUDA;
   }
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    attr = true;
+  if (!mla_tc_prepare()) {
+    set_error("sparse_mla_tc: cudaFuncSetAttribute failed");
+    return MTPSD_ECUDA;
   }
-  dim3 grid(p.R, (p.H / HG) * 2, n_splits);
-  sparse_mla_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(tm_lat, tm_q, k);
+  cudaLaunchAttribute attrs[1];
+  cudaLaunchConfig_t cfg = mla_tc_config(dim3(p.R, (p.H / HG) * 2, n_splits), st, attrs);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel, tm_lat, tm_q, k);
+  if (e != cudaSuccess) {
+    set_error("sparse_mla_tc: launch failed: %s", cudaGetErrorString(e));
+    return MTPSD_ECUDA;
+  }
   return check_launch("sparse_mla_tc");
 }
 
