@@ -13,12 +13,13 @@
 //   rank 1: dims 256..511 (4 chunks); its value dims are 256..511
 // Each CTA forms the partial scores of its dims, S_k = Q[:, D_k] C[:, D_k]^T,
 // in TMEM.  Its sender warps scale them to log2 units, round them to fp16
-// and store them into the other CTA's receive slot (st.async, 16 KB per 64
-// positions, completing bytes on that CTA's mbarrier); its softmax warps add
-// the received half to their own fp32 partial, S = S_own + S_other, and run
-// the softmax for this CTA's 256 value dims.  The two CTAs see the other
-// half rounded differently, so each value half keeps its own running
-// (max, sum); split partials carry one (max, sum) per half.
+// and stage them in shared memory; one lane then moves the 16 KB of a pair
+// into the other CTA's receive slot with a single bulk copy (completing bytes
+// on that CTA's mbarrier).  Its softmax warps add the received half to their
+// own fp32 partial, S = S_own + S_other, and run the softmax for this CTA's
+// 256 value dims.  The two CTAs see the other half rounded differently, so
+// each value half keeps its own running (max, sum); split partials carry one
+// (max, sum) per half.
 //   TMEM  [  0,128) this CTA's first 256 query dims (A operand, bf16 pairs)
 //         [128,192) [192,256) two partial-score buffers of 64 positions
 //                   (fp32), P aliased in their first 32 columns (bf16 pairs)
@@ -28,27 +29,34 @@
 //         64-dim chunk (64 rows x 128 B, 128-byte swizzle), which are both the
 //         K-major B operand of the scores (N = 64 positions) and, for chunks
 //         0..3, the MN-major B operand of O += P V (K = positions, N = 256);
-//         two receive slots for the other CTA's fp16 partial scores.
+//         two receive slots for the other CTA's fp16 partial scores and one
+//         staging slot for this CTA's (16 KB each: row = head, 64 positions
+//         in 128 bytes, 16-byte piece c at (c ^ (head & 7))).
 // Per pair: QK^T is 16 MMAs with A from TMEM (+4 with A from shared memory on
 // rank 0), M=128, N=64, K=16; PV is 4 MMAs (M=128, N=256, K=16) with A = P
-// from TMEM.  QK(P) is issued before PV(P-1) so the tensor cores work while
-// the softmax runs.  The softmax (thread = head) applies a lazy max: O is
-// rescaled only when a head's max grows by more than 2^8.
+// from TMEM.  The MMA warp issues, in this fixed order, QK(P+1) (its buffer
+// was last read by PV(P-1), issued before it) and PV(P) once the softmax
+// published P, and sleeps in its waits: a polling or a blocked issue there
+// takes issue slots and memory-instruction slots from the softmax warp that
+// shares its scheduler.  The softmax (thread = head) applies a lazy max: O
+// is rescaled only when a head's max grows by more than 2^8.
 //
 // Roles (416 threads): warps 0-3 softmax/epilogue (TMEM lanes = heads);
-// warps 4-7 send the partial scores (thread = head of TMEM quadrant warp%4),
-// so the DSMEM stores, which drain at about 13 bytes per cycle per SM, run
-// beside the softmax instead of in it; warps 8-11 produce: each turns its 8
-// positions of every 32-row tile into pool rows and gathers this CTA's
-// chunks of them with TMA tile::gather4 loads (4 rows x 64 dims per
-// instruction; invalid positions read as zeros through an out-of-range row);
-// the first also loads rank 0's rope query dims; warp 12 allocates TMEM and
-// issues the MMAs.  A receive slot is refilled (pair P+2) only after the
-// other CTA's softmax warps have consumed it (one remote arrival per warp).  The producer
-// and MMA roles run with the whole warp so that descriptors and coordinates
-// stay in uniform registers, and one elected lane issues.  Every mbarrier
-// wait is bounded (2 s) and flags MTPSD_STATUS_WAIT_TIMEOUT on expiry; a CTA
-// whose partner stops sending times out the same way.
+// warps 4-7 send the partial scores (thread = head of TMEM quadrant warp%4).
+// Per-thread DSMEM stores (st.async) drain at about 13 bytes per cycle per
+// SM and hold up the memory instructions of every warp on the issuing
+// scheduler, so the senders only stage and one bulk copy per pair crosses
+// to the other SM.  Warps 8-11 produce: each turns its 8 positions of every
+// 32-row tile into pool rows and gathers this CTA's chunks of them with TMA
+// tile::gather4 loads (4 rows x 64 dims per instruction; invalid positions
+// read as zeros through an out-of-range row); the first also loads rank 0's
+// rope query dims; warp 12 allocates TMEM and issues the MMAs.  A receive
+// slot is refilled (pair P+2) only after the other CTA's softmax warps have
+// consumed it (one remote arrival per warp).  The producer and MMA roles run
+// with the whole warp so that descriptors and coordinates stay in uniform
+// registers, and one elected lane issues.  Every mbarrier wait is bounded
+// (2 s) and flags MTPSD_STATUS_WAIT_TIMEOUT on expiry; a CTA whose partner
+// stops sending times out the same way.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -72,12 +80,13 @@ constexpr int PAIR_STRIDE = NCH_MAX * CHUNK_BYTES;   // 40960
 constexpr int XSLOT_BYTES = HG * NP * 2;             // 16384: one pair's fp16 partial scores
 constexpr int OFF_QR = 0;                                    // rope query dims (rank 0)
 constexpr int OFF_C = OFF_QR + HG * 128;                     // 16384
-constexpr int OFF_X = OFF_C + NPAIR * PAIR_STRIDE;           // 180224
-constexpr int OFF_MASK = OFF_X + 2 * XSLOT_BYTES;            // 212992: [NSTAGE][4] uint32 validity bits
+constexpr int OFF_X = OFF_C + NPAIR * PAIR_STRIDE;           // 180224: [2] receive slots
+constexpr int OFF_STG = OFF_X + 2 * XSLOT_BYTES;             // 212992: own fp16 partials staged for the copy
+constexpr int OFF_MASK = OFF_STG + XSLOT_BYTES;              // 229376: [NSTAGE][4] uint32 validity bits
 constexpr int OFF_BAR = OFF_MASK + NSTAGE * 4 * 4;
 // barriers: c_full[NSTAGE], c_empty[NPAIR], s_full[2], p_full[2], pv_done[2], x_full[2], s_read[2], x_free[2],
 // q_ready, drain
-constexpr int N_BARS = NSTAGE + NPAIR + 12 + 2;
+constexpr int N_BARS = NSTAGE + NPAIR + 12 + 2 + 2;   // + stg_full, stg_free
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;               // tmem base, abort flag
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;                 // alignment slack
@@ -144,14 +153,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
 __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t par) {
   uint32_t ok;
   asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-               : "=r"(ok) : "r"(saddr(b)), "r"(par) : "memory");
-  return ok != 0;
-}
-// Non-blocking test, for loops that poll several barriers: try_wait may suspend the thread until
-// the phase completes, which would hold up the other conditions the loop serves.
-__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t par) {
-  uint32_t ok;
-  asm volatile("{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
                : "=r"(ok) : "r"(saddr(b)), "r"(par) : "memory");
   return ok != 0;
 }
@@ -340,7 +341,9 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   uint64_t* x_full = pv_done + 2;          // receive slot s holds the other CTA's partial scores
   uint64_t* s_read = x_full + 2;           // the senders have read score buffer s
   uint64_t* x_free = s_read + 2;           // the other CTA has consumed what this CTA sent into its slot s
-  uint64_t* q_ready = x_free + 2;
+  uint64_t* stg_full = x_free + 2;        // the senders staged a pair (one phase per pair)
+  uint64_t* stg_free = stg_full + 1;       // the copy of the previous pair has read the staging slot
+  uint64_t* q_ready = stg_free + 1;
   uint64_t* drain = q_ready + 1;
   uint32_t* tmem_slot = (uint32_t*)(sm + OFF_MISC);
   volatile int* abort_flag = (volatile int*)(sm + OFF_MISC + 4);
@@ -374,6 +377,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       mbar_init(&s_read[i], 128);
       mbar_init(&x_free[i], 4);           // one arrival per softmax warp of the other CTA
     }
+    mbar_init(stg_full, 128);
+    mbar_init(stg_free, 1);
     // 128 softmax threads (query dims in TMEM), plus on rank 0 the first producer (rope dims by TMA)
     mbar_init(q_ready, rank == 0 ? 129 : 128);
     mbar_init(drain, 1);
@@ -572,8 +577,9 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     // stores them into the other CTA's receive slot (st.async, completing bytes on its x_full).
     const int h = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t x_peer = map_rank(saddr(sm + OFF_X) + (uint32_t)h * 128u, peer);
+    const uint32_t x_peer0 = map_rank(saddr(sm + OFF_X), peer);
     const uint32_t xfull_peer = map_rank(saddr(x_full), peer);
+    const uint32_t stg_row = saddr(sm + OFF_STG) + (uint32_t)h * 128u;   // one staging slot
     const uint32_t swz = (uint32_t)(h & 7);
     bool ok = true;
     for (int P = 0; P < n_pairs && ok; ++P) {
@@ -592,15 +598,43 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         hx[j] = pack_f16_sat(__uint_as_float(sr[2 * j]) * p.sl2, __uint_as_float(sr[2 * j + 1]) * p.sl2);
-      // the other CTA has consumed what was sent into this slot two pairs ago
-      if (P >= 2) ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_free[s], ((P - 2) >> 1) & 1, abort_flag, p.status));
-      if (!ok) break;
-      const uint32_t xo = x_peer + (uint32_t)s * XSLOT_BYTES;
+      // the staging slot: the copy of pair P-1 has read it (the issuing lane checks, then releases it)
+      if (P >= 1) {
+        if (warp == SEND_WARP) {
+          if (elect_one()) {
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            mbar_arrive(stg_free);
+          }
+          __syncwarp();
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(stg_free, (P - 1) & 1, abort_flag, p.status));
+        if (!ok) break;
+      }
 #pragma unroll
       for (int c = 0; c < 8; ++c)
-        st_async_v4(xo + ((c ^ swz) << 4), hx[4 * c], hx[4 * c + 1], hx[4 * c + 2], hx[4 * c + 3],
-                    xfull_peer + (uint32_t)s * 8u);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg_row + ((c ^ swz) << 4)),
+                     "r"(hx[4 * c]), "r"(hx[4 * c + 1]), "r"(hx[4 * c + 2]), "r"(hx[4 * c + 3])
+                     : "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the bulk copy
+      mbar_arrive(stg_full);
+      if (warp == SEND_WARP) {
+        // one bulk copy of the 16 KB slot into the other CTA's receive slot, once it consumed pair P-2
+        ok = __all_sync(0xffffffffu, mbar_wait(stg_full, P & 1, abort_flag, p.status));
+        if (ok && P >= 2) ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_free[s], ((P - 2) >> 1) & 1, abort_flag, p.status));
+        if (!ok) break;
+        if (elect_one()) {
+          asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                       ::"r"(x_peer0 + (uint32_t)s * XSLOT_BYTES), "r"(saddr(sm + OFF_STG)), "r"(XSLOT_BYTES),
+                       "r"(xfull_peer + (uint32_t)s * 8u)
+                       : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        __syncwarp();
+      }
     }
+    if (warp == SEND_WARP && elect_one())   // this CTA's staged bytes have been read before it exits
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
   } else if (warp < PROD_WARP + N_PROD) {
     // ------------------------------------------------ producers
     // Producer pw gathers the 4-row groups g = pw and g = pw + 4 of every
@@ -670,73 +704,54 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     const uint64_t c_desc0 = desc_sw128(saddr(sm + OFF_C), 16, 1024);
     const uint64_t v_desc0 = desc_sw128(saddr(sm + OFF_C), CHUNK_BYTES, 1024);
     const int nk = nch * 4;
-    // Issue whichever is ready: QK(nq) once its pair has landed (and PV(nq-2),
-    // which last read the S columns QK(nq) overwrites, has been issued: the
-    // MMAs execute in issue order), or PV(np) once the softmax published P.
-    int nq = 0, np = 0;
-    uint64_t t0 = gtimer();
-    uint32_t spins = 0;
-    while (np < n_pairs && ok) {
-      bool did = false;
-      if (nq < n_pairs && nq <= np + 1) {
-        const int bq = nq % NPAIR;
-        const uint32_t par = (nq / NPAIR) & 1;
-        if (__all_sync(0xffffffffu, mbar_test(&c_full[2 * bq], par) && mbar_test(&c_full[2 * bq + 1], par))) {
-          fence_after();
-          const uint64_t cd = c_desc0 + (uint64_t)((bq * PAIR_STRIDE) >> 4);
-          const uint32_t d = tmem + TM_S0 + (nq & 1) * 64;
-          if (elect_one()) {
-            // partial S over this CTA's chunks: 0..3 with A from TMEM, rank 0's rope chunk with A from shared memory
+    // The MMAs follow a fixed order: QK(0), then for every pair P, QK(P+1) (its S buffer was last read
+    // by PV(P-1), issued before it: the MMAs execute in issue order) and PV(P) once the softmax
+    // published P.  The waits suspend the warp (try_wait) instead of polling, so the softmax warp that
+    // shares this scheduler keeps its issue slots.
+    auto issue_qk = [&](int nq) -> bool {
+      const int bq = nq % NPAIR;
+      const uint32_t par = (nq / NPAIR) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&c_full[2 * bq], par, abort_flag, p.status) &&
+                                       mbar_wait(&c_full[2 * bq + 1], par, abort_flag, p.status)))
+        return false;
+      fence_after();
+      const uint64_t cd = c_desc0 + (uint64_t)((bq * PAIR_STRIDE) >> 4);
+      const uint32_t d = tmem + TM_S0 + (nq & 1) * 64;
+      if (elect_one()) {
+        // partial S over this CTA's chunks: 0..3 with A from TMEM, rank 0's rope chunk with A from shared memory
 #pragma unroll
-            for (int k = 0; k < NCH_MAX * 4; ++k) {
-              if (k < nk) {
-                const uint32_t boff = (uint32_t)((k >> 2) * CHUNK_BYTES + (k & 3) * 32);   // chunk, 32-byte K step
-                if (k < QTM / 16)
-                  mma_ts(d, tmem + TM_Q + k * 8, cd + (boff >> 4), IDESC_QK, k > 0 ? 1u : 0u);
-                else
-                  mma_ss(d, qr_desc + (uint64_t)(((k & 3) * 32) >> 4), cd + (boff >> 4), IDESC_QK, 1u);
-              }
-            }
-            commit(&s_full[nq & 1]);
+        for (int k = 0; k < NCH_MAX * 4; ++k) {
+          if (k < nk) {
+            const uint32_t boff = (uint32_t)((k >> 2) * CHUNK_BYTES + (k & 3) * 32);   // chunk, 32-byte K step
+            if (k < QTM / 16)
+              mma_ts(d, tmem + TM_Q + k * 8, cd + (boff >> 4), IDESC_QK, k > 0 ? 1u : 0u);
+            else
+              mma_ss(d, qr_desc + (uint64_t)(((k & 3) * 32) >> 4), cd + (boff >> 4), IDESC_QK, 1u);
           }
-          __syncwarp();
-          ++nq;
-          did = true;
         }
+        commit(&s_full[nq & 1]);
       }
-      if (np < nq) {
-        // O += P(np) V(np): A = P from TMEM, B = chunks 0..3 of the pair buffer as MN-major (N = 256 dims)
-        const int sp = np & 1;
-        if (__all_sync(0xffffffffu, mbar_test(&p_full[sp], (np >> 1) & 1))) {
-          fence_after();
-          const int bp = np % NPAIR;
-          const uint64_t vd = v_desc0 + (uint64_t)((bp * PAIR_STRIDE) >> 4);
-          if (elect_one()) {
+      __syncwarp();
+      return true;
+    };
+    if (ok && n_pairs > 0) ok = issue_qk(0);
+    for (int np = 0; np < n_pairs && ok; ++np) {
+      if (np + 1 < n_pairs && !issue_qk(np + 1)) break;
+      // O += P(np) V(np): A = P from TMEM, B = chunks 0..3 of the pair buffer as MN-major (N = 256 dims)
+      const int sp = np & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&p_full[sp], (np >> 1) & 1, abort_flag, p.status))) break;
+      fence_after();
+      const int bp = np % NPAIR;
+      const uint64_t vd = v_desc0 + (uint64_t)((bp * PAIR_STRIDE) >> 4);
+      if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < NP / 16; ++k)
-              mma_ts(tmem + TM_O, tmem + TM_S0 + sp * 64 + k * 8, vd + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV,
-                     (np > 0 || k > 0) ? 1u : 0u);
-            commit(&pv_done[sp]);
-            commit(&c_empty[bp]);
-          }
-          __syncwarp();
-          ++np;
-          did = true;
-        }
+        for (int k = 0; k < NP / 16; ++k)
+          mma_ts(tmem + TM_O, tmem + TM_S0 + sp * 64 + k * 8, vd + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV,
+                 (np > 0 || k > 0) ? 1u : 0u);
+        commit(&pv_done[sp]);
+        commit(&c_empty[bp]);
       }
-      if (did) {
-        t0 = gtimer();
-        spins = 0;
-      } else if ((++spins & 255u) == 0) {   // bounded: give up after the wait limit
-        if (*abort_flag) {
-          ok = false;
-        } else if (gtimer() - t0 > WAIT_LIMIT_NS) {
-          *abort_flag = 1;
-          flag_status(p.status, MTPSD_STATUS_WAIT_TIMEOUT);
-          ok = false;
-        }
-        ok = __all_sync(0xffffffffu, ok);
-      }
+      __syncwarp();
     }
     if (elect_one()) commit(drain);
     __syncwarp();
