@@ -13,9 +13,9 @@
 //   rank 1: dims 256..511 (4 chunks); its value dims are 256..511
 // Each CTA forms the partial scores of its dims, S_k = Q[:, D_k] C[:, D_k]^T,
 // in TMEM.  Its sender warps scale them to log2 units, round them to fp16
-// and stage them in shared memory; one lane then moves the 16 KB of a pair
-// into the other CTA's receive slot with a single bulk copy (completing bytes
-// on that CTA's mbarrier).  Its softmax warps add the received half to their
+// and stage them in shared memory; lane 0 of each sender warp then moves the
+// warp's 32 heads (4 KB of a pair's 16 KB) into the other CTA's receive slot
+// with one bulk copy (completing bytes on that CTA's mbarrier).  Its softmax warps add the received half to their
 // own fp32 partial, S = S_own + S_other, and run the softmax for this CTA's
 // 256 value dims.  The two CTAs see the other half rounded differently, so
 // each value half keeps its own running (max, sum); split partials carry one
@@ -45,8 +45,9 @@
 // warps 4-7 send the partial scores (thread = head of TMEM quadrant warp%4).
 // Per-thread DSMEM stores (st.async) drain at about 13 bytes per cycle per
 // SM and hold up the memory instructions of every warp on the issuing
-// scheduler, so the senders only stage and one bulk copy per pair crosses
-// to the other SM.  Warps 8-11 produce: each turns its 8 positions of every
+// scheduler, so the senders only stage and one bulk copy per warp and pair
+// crosses to the other SM; a warp rewrites its staging rows only after its
+// previous copy has read them.  Warps 8-11 produce: each turns its 8 positions of every
 // 32-row tile into pool rows and gathers this CTA's chunks of them with TMA
 // tile::gather4 loads (4 rows x 64 dims per instruction; invalid positions
 // read as zeros through an out-of-range row); the first also loads rank 0's
@@ -86,7 +87,7 @@ constexpr int OFF_MASK = OFF_STG + XSLOT_BYTES;              // 229376: [NSTAGE]
 constexpr int OFF_BAR = OFF_MASK + NSTAGE * 4 * 4;
 // barriers: c_full[NSTAGE], c_empty[NPAIR], s_full[2], p_full[2], pv_done[2], x_full[2], s_read[2], x_free[2],
 // q_ready, drain
-constexpr int N_BARS = NSTAGE + NPAIR + 12 + 2 + 2;   // + stg_full, stg_free
+constexpr int N_BARS = NSTAGE + NPAIR + 12 + 2;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;               // tmem base, abort flag
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;                 // alignment slack
@@ -341,9 +342,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   uint64_t* x_full = pv_done + 2;          // receive slot s holds the other CTA's partial scores
   uint64_t* s_read = x_full + 2;           // the senders have read score buffer s
   uint64_t* x_free = s_read + 2;           // the other CTA has consumed what this CTA sent into its slot s
-  uint64_t* stg_full = x_free + 2;        // the senders staged a pair (one phase per pair)
-  uint64_t* stg_free = stg_full + 1;       // the copy of the previous pair has read the staging slot
-  uint64_t* q_ready = stg_free + 1;
+  uint64_t* q_ready = x_free + 2;
   uint64_t* drain = q_ready + 1;
   uint32_t* tmem_slot = (uint32_t*)(sm + OFF_MISC);
   volatile int* abort_flag = (volatile int*)(sm + OFF_MISC + 4);
@@ -377,8 +376,6 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       mbar_init(&s_read[i], 128);
       mbar_init(&x_free[i], 4);           // one arrival per softmax warp of the other CTA
     }
-    mbar_init(stg_full, 128);
-    mbar_init(stg_free, 1);
     // 128 softmax threads (query dims in TMEM), plus on rank 0 the first producer (rope dims by TMA)
     mbar_init(q_ready, rank == 0 ? 129 : 128);
     mbar_init(drain, 1);
@@ -574,7 +571,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   } else if (warp < SEND_WARP + 4) {
     // ------------------------------------------------ senders: thread = head of TMEM quadrant warp % 4
     // Each reads the partial scores of its head, scales them to log2 units, rounds them to fp16 and
-    // stores them into the other CTA's receive slot (st.async, completing bytes on its x_full).
+    // stages them in its row of the staging slot; lane 0 of each warp then copies the warp's 32 rows
+    // (4 KB) into the other CTA's receive slot with one bulk copy, completing bytes on its x_full.
     const int h = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t x_peer0 = map_rank(saddr(sm + OFF_X), peer);
@@ -598,17 +596,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         hx[j] = pack_f16_sat(__uint_as_float(sr[2 * j]) * p.sl2, __uint_as_float(sr[2 * j + 1]) * p.sl2);
-      // the staging slot: the copy of pair P-1 has read it (the issuing lane checks, then releases it)
+      // this warp's 32 rows of the staging slot (4 KB): lane 0's copy of pair P-1 has read them
       if (P >= 1) {
-        if (warp == SEND_WARP) {
-          if (elect_one()) {
-            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-            mbar_arrive(stg_free);
-          }
-          __syncwarp();
-        }
-        ok = __all_sync(0xffffffffu, mbar_wait(stg_free, (P - 1) & 1, abort_flag, p.status));
-        if (!ok) break;
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
       }
 #pragma unroll
       for (int c = 0; c < 8; ++c)
@@ -616,23 +607,21 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
                      "r"(hx[4 * c]), "r"(hx[4 * c + 1]), "r"(hx[4 * c + 2]), "r"(hx[4 * c + 3])
                      : "memory");
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the bulk copy
-      mbar_arrive(stg_full);
-      if (warp == SEND_WARP) {
-        // one bulk copy of the 16 KB slot into the other CTA's receive slot, once it consumed pair P-2
-        ok = __all_sync(0xffffffffu, mbar_wait(stg_full, P & 1, abort_flag, p.status));
-        if (ok && P >= 2) ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_free[s], ((P - 2) >> 1) & 1, abort_flag, p.status));
-        if (!ok) break;
-        if (elect_one()) {
-          asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                       ::"r"(x_peer0 + (uint32_t)s * XSLOT_BYTES), "r"(saddr(sm + OFF_STG)), "r"(XSLOT_BYTES),
-                       "r"(xfull_peer + (uint32_t)s * 8u)
-                       : "memory");
-          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        }
-        __syncwarp();
+      // the other CTA has consumed what was sent into its slot s two pairs ago
+      if (P >= 2) ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_free[s], ((P - 2) >> 1) & 1, abort_flag, p.status));
+      else __syncwarp();
+      if (!ok) break;
+      if (lane == 0) {
+        const uint32_t off = (uint32_t)(warp & 3) * 32u * 128u;   // this warp's rows
+        asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(x_peer0 + (uint32_t)s * XSLOT_BYTES + off), "r"(saddr(sm + OFF_STG) + off), "r"(32 * 128),
+                     "r"(xfull_peer + (uint32_t)s * 8u)
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
+      __syncwarp();
     }
-    if (warp == SEND_WARP && elect_one())   // this CTA's staged bytes have been read before it exits
+    if (lane == 0)   // this warp's staged bytes have been read before the CTA exits
       asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     __syncwarp();
   } else if (warp < PROD_WARP + N_PROD) {
