@@ -17,6 +17,8 @@ constexpr int IDX_TILE = 64;
 
 template <bool FP8>
 __global__ void __launch_bounds__(256) indexer_scores_kernel(IndexerPlan p) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   extern __shared__ float smem[];
   const int H = p.H, D = p.D, DP = p.D + 1;
   float* ks = smem;                      // [64][D+1] dequantized keys
@@ -105,11 +107,11 @@ int launch_indexer_scores(const IndexerPlan& p, cudaStream_t st) {
   if (p.dtype == MTPSD_FP8_E4M3) {
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(indexer_scores_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    indexer_scores_kernel<true><<<grid, 256, smem, st>>>(p);
+    launch_k(indexer_scores_kernel<true>, grid, 256, smem, st, p);
   } else {
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(indexer_scores_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    indexer_scores_kernel<false><<<grid, 256, smem, st>>>(p);
+    launch_k(indexer_scores_kernel<false>, grid, 256, smem, st, p);
   }
   return check_launch("indexer_scores");
 }

@@ -221,6 +221,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const uint32_t* __restrict__
                                                     int B, int64_t max_visible, int group_rows, int* g_b,
                                                     int* g_row0, int* g_nrows, int* g_vmax, int* g_tile0,
                                                     int* n_groups) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   __shared__ int s_groups[1024], s_tiles[1024];
   __shared__ int carry_g, carry_t;
   if (threadIdx.x == 0) carry_g = carry_t = 0;
@@ -284,6 +286,8 @@ template <int H>
 __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                 const __grid_constant__ CUtensorMap tmap_q,
                                                                 Params p) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + OFF_BAR);
@@ -578,7 +582,7 @@ int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {
   int* g_tile0 = g_vmax + n;
   int* n_groups = g_tile0 + n;
   const int group_rows = Q_ROWS / p.H;
-  plan_kernel<<<1, 1024, 0, st>>>(p.row_offsets, p.row_pos, p.B, p.max_visible, group_rows, g_b, g_row0, g_nrows,
+  launch_k(plan_kernel, 1, 1024, 0, st, p.row_offsets, p.row_pos, p.B, p.max_visible, group_rows, g_b, g_row0, g_nrows,
                                   g_vmax, g_tile0, n_groups);
   int rc = check_launch("indexer_tc_plan");
   if (rc) return rc;
@@ -594,9 +598,9 @@ int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {
     attr = true;
   }
   if (p.H == 64)
-    indexer_tc_kernel<64><<<num_sms(), THREADS, SMEM_BYTES, st>>>(mk, mq, kp);
+    launch_k(indexer_tc_kernel<64>, num_sms(), THREADS, SMEM_BYTES, st, mk, mq, kp);
   else
-    indexer_tc_kernel<32><<<num_sms(), THREADS, SMEM_BYTES, st>>>(mk, mq, kp);
+    launch_k(indexer_tc_kernel<32>, num_sms(), THREADS, SMEM_BYTES, st, mk, mq, kp);
   return check_launch("indexer_tc");
 }
 

@@ -100,6 +100,8 @@ struct MlaSmem {
 
 __global__ void __launch_bounds__(256, 1) sparse_mla_bf16_kernel(MlaPlan p, MlaSplit sp, float* __restrict__ part_o,
                                                                   float* __restrict__ part_ml) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   extern __shared__ __align__(128) uint8_t sm[];
   const int r = blockIdx.x;
   const int hg = blockIdx.y;
@@ -310,6 +312,8 @@ __global__ void __launch_bounds__(256, 1) sparse_mla_bf16_kernel(MlaPlan p, MlaS
 template <typename OutT>
 __global__ void mla_combine_kernel(MlaPlan p, int n_splits, int halves, const float* __restrict__ part_o,
                                    const float* __restrict__ part_ml) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   const int64_t rh = blockIdx.x;   // r * H + h
   const float* ml = part_ml + rh * n_splits * halves * 2;
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
@@ -343,6 +347,8 @@ template <typename OutT>
 __global__ void __launch_bounds__(256) mla_combine512_kernel(MlaPlan p, int n_splits, int halves,
                                                              const float* __restrict__ part_o,
                                                              const float* __restrict__ part_ml) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   const int64_t rh = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 6);
   if (rh >= (int64_t)p.R * p.H) return;
   const int t = threadIdx.x & 63;
@@ -385,9 +391,9 @@ static int launch_combine(const MlaPlan& p, int n_splits, int halves, const floa
                           cudaStream_t st) {
   const int64_t rh = (int64_t)p.R * p.H;
   if (p.d_v == MLA_DV && ((uintptr_t)p.out % 16) == 0) {
-    mla_combine512_kernel<OutT><<<(unsigned)((rh + 3) / 4), 256, 0, st>>>(p, n_splits, halves, part_o, part_ml);
+    launch_k(mla_combine512_kernel<OutT>, (unsigned)((rh + 3) / 4), 256, 0, st, p, n_splits, halves, part_o, part_ml);
   } else {
-    mla_combine_kernel<OutT><<<(unsigned)rh, 128, 0, st>>>(p, n_splits, halves, part_o, part_ml);
+    launch_k(mla_combine_kernel<OutT>, (unsigned)rh, 128, 0, st, p, n_splits, halves, part_o, part_ml);
   }
   return check_launch("sparse_mla_combine");
 }
@@ -395,6 +401,8 @@ static int launch_combine(const MlaPlan& p, int n_splits, int halves, const floa
 // float32 path: one CTA per (row, head, split); logits of the split in shared.
 __global__ void __launch_bounds__(256) sparse_mla_f32_kernel(MlaPlan p, MlaSplit sp, float* __restrict__ part_o,
                                                               float* __restrict__ part_ml) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   extern __shared__ float fsm[];
   const int r = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
   const int H = p.H, DL = p.d_latent, DV = p.d_v;
@@ -540,7 +548,7 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
       attr = true;
     }
     dim3 grid(p.R, (unsigned)ceil_div(p.H, MLA_HG), sp.n_splits);
-    sparse_mla_bf16_kernel<<<grid, 256, MlaSmem::BYTES, st>>>(p, sp, part_o, part_ml);
+    launch_k(sparse_mla_bf16_kernel, grid, 256, MlaSmem::BYTES, st, p, sp, part_o, part_ml);
     int rc = check_launch("sparse_mla_bf16");
     if (rc) return rc;
     if (sp.n_splits > 1) {
@@ -553,7 +561,7 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(sparse_mla_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(p.R, p.H, sp.n_splits);
-  sparse_mla_f32_kernel<<<grid, 256, smem, st>>>(p, sp, part_o, part_ml);
+  launch_k(sparse_mla_f32_kernel, grid, 256, smem, st, p, sp, part_o, part_ml);
   int rc = check_launch("sparse_mla_f32");
   if (rc) return rc;
   if (sp.n_splits > 1) {

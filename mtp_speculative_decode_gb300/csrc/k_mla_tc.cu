@@ -331,6 +331,8 @@ __device__ __forceinline__ int64_t entry_row(const Params& p, int64_t s, int64_t
 
 __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                                                                    const __grid_constant__ CUtensorMap tm_q, Params p) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + OFF_BAR);
@@ -861,8 +863,11 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
     set_error("sparse_mla_tc: cudaFuncSetAttribute failed");
     return MTPSD_ECUDA;
   }
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
   cudaLaunchConfig_t cfg = mla_tc_config(dim3(p.R, (p.H / HG) * 2, n_splits), st, attrs);
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see launch_k()
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel, tm_lat, tm_q, k);
   if (e != cudaSuccess) {
     set_error("sparse_mla_tc: launch failed: %s", cudaGetErrorString(e));

@@ -14,6 +14,8 @@ namespace mtpsd {
 __global__ void merge_tokens_kernel(const int64_t* __restrict__ prompt, const uint32_t* __restrict__ po,
                                     const int64_t* __restrict__ draft, int B, int K, int64_t total,
                                     int64_t* __restrict__ out, uint32_t* __restrict__ mo) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t <= B && t < (int64_t)B + 1) mo[t] = po[t] + (uint32_t)(t * K);
   for (; t < total; t += (int64_t)gridDim.x * blockDim.x) {
@@ -39,7 +41,7 @@ int launch_merge_tokens(const int64_t* prompt, int64_t S, const uint32_t* po, co
   if (blocks < 1) blocks = 1;
   // the first B+1 threads also write merged offsets; make sure they exist
   if ((int64_t)blocks * 256 < B + 1) blocks = (int)((B + 1 + 255) / 256);
-  merge_tokens_kernel<<<blocks, 256, 0, st>>>(prompt, po, draft, B, K, total, out, mo);
+  launch_k(merge_tokens_kernel, blocks, 256, 0, st, prompt, po, draft, B, K, total, out, mo);
   return check_launch("merge_tokens");
 }
 
@@ -50,6 +52,8 @@ int launch_merge_tokens(const int64_t* prompt, int64_t S, const uint32_t* po, co
 // conversion to E4M3.
 __global__ void quantize_fp8_kernel(const float4* __restrict__ x, int64_t n_blocks,
                                     uint32_t* __restrict__ codes, float* __restrict__ scales) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   int lane = threadIdx.x & 31;
   int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -73,7 +77,7 @@ int launch_quantize_fp8(const float* x, int64_t n_blocks, uint8_t* codes, float*
   int64_t warps = n_blocks;
   int64_t blocks = (warps * 32 + 255) / 256;
   if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
-  quantize_fp8_kernel<<<(int)blocks, 256, 0, st>>>((const float4*)x, n_blocks, (uint32_t*)codes, scales);
+  launch_k(quantize_fp8_kernel, (int)blocks, 256, 0, st, (const float4*)x, n_blocks, (uint32_t*)codes, scales);
   return check_launch("quantize_fp8_block128");
 }
 
@@ -82,6 +86,8 @@ int launch_quantize_fp8(const float* x, int64_t n_blocks, uint8_t* codes, float*
 __global__ void accept_greedy_kernel(const int64_t* __restrict__ draft, const int64_t* __restrict__ tgt,
                                      int B, int K, int64_t magic, int32_t* __restrict__ n_acc,
                                      int64_t* __restrict__ next) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int64_t* d = draft + (int64_t)b * K;
@@ -98,7 +104,7 @@ __global__ void accept_greedy_kernel(const int64_t* __restrict__ draft, const in
 
 int launch_accept_greedy(const int64_t* draft, const int64_t* tgt, int B, int K, int64_t magic,
                          int32_t* n_acc, int64_t* next, cudaStream_t st) {
-  accept_greedy_kernel<<<(B + 127) / 128, 128, 0, st>>>(draft, tgt, B, K, magic, n_acc, next);
+  launch_k(accept_greedy_kernel, (B + 127) / 128, 128, 0, st, draft, tgt, B, K, magic, n_acc, next);
   return check_launch("accept_greedy");
 }
 
@@ -114,6 +120,8 @@ __global__ void kv_writeback_kernel(const uint4* __restrict__ src_l, const uint4
                                     const int64_t* __restrict__ cache_start, const int64_t* __restrict__ dst_pos,
                                     int64_t pool,
                                     int64_t* __restrict__ next_pos, int32_t* __restrict__ status) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   int b = blockIdx.y;
   int i = blockIdx.x;
   int n = n_acc[b] + 1;                 // accept_len, bonus included
@@ -138,7 +146,7 @@ int launch_kv_writeback(const void* src_l, const uint8_t* src_k, const float* sr
                         int64_t* next_pos,
                         int32_t* status, cudaStream_t st) {
   dim3 grid(W, B);
-  kv_writeback_kernel<<<grid, 64, 0, st>>>((const uint4*)src_l, (const uint4*)src_k, src_s, W, lat_bytes / 16,
+  launch_k(kv_writeback_kernel, grid, 64, 0, st, (const uint4*)src_l, (const uint4*)src_k, src_s, W, lat_bytes / 16,
                                            idx_bytes / 16, n_acc, (uint4*)dst_l, (uint4*)dst_k, dst_s,
                                            cache_start, dst_pos, pool, next_pos, status);
   return check_launch("kv_writeback");
@@ -150,6 +158,8 @@ int launch_kv_writeback(const void* src_l, const uint8_t* src_k, const float* sr
 __global__ void share_gather_kernel(const int32_t* __restrict__ s0, const uint32_t* __restrict__ ro,
                                     const int32_t* __restrict__ n_acc, int k, int32_t* __restrict__ out,
                                     int32_t* __restrict__ status) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   int b = blockIdx.x;
   int64_t first = ro[b], last = (int64_t)ro[b + 1] - 1;
   if (last < first) {  // empty segment: nothing to share
@@ -173,7 +183,7 @@ __global__ void share_gather_kernel(const int32_t* __restrict__ s0, const uint32
 
 int launch_share_gather(const int32_t* s0, const uint32_t* ro, const int32_t* n_acc, int B, int k,
                         int32_t* out, int32_t* status, cudaStream_t st) {
-  share_gather_kernel<<<B, 128, 0, st>>>(s0, ro, n_acc, k, out, status);
+  launch_k(share_gather_kernel, B, 128, 0, st, s0, ro, n_acc, k, out, status);
   return check_launch("topk_share_gather");
 }
 

@@ -50,6 +50,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
 }
 
 __global__ void __launch_bounds__(TOPK_THREADS, 1) topk_kernel(TopkPlan p, int64_t cache_cap) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   extern __shared__ uint32_t keys_s[];
   __shared__ int hist[256];
   __shared__ int warp_sums[32];
@@ -173,6 +175,8 @@ __global__ void __launch_bounds__(TOPK_THREADS, 1) topk_kernel(TopkPlan p, int64
 // is the same as above.
 template <int KPT, int NTH>
 __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
   __shared__ int wsum[2][32];
   __shared__ int warp_sums[32];
   __shared__ int total_s;
@@ -272,7 +276,7 @@ template <int NTH>
 static int launch_topk_reg(const TopkPlan& p, int kpt, cudaStream_t st) {
   switch (kpt) {
 #define MTPSD_TOPK_CASE(K) \
-  case K: topk_reg_kernel<K, NTH><<<p.R, NTH, 0, st>>>(p); break;
+  case K: launch_k(topk_reg_kernel<K, NTH>, p.R, NTH, 0, st, p); break;
     MTPSD_TOPK_CASE(4) MTPSD_TOPK_CASE(8) MTPSD_TOPK_CASE(12) MTPSD_TOPK_CASE(16) MTPSD_TOPK_CASE(20)
     MTPSD_TOPK_CASE(24) MTPSD_TOPK_CASE(28) MTPSD_TOPK_CASE(32) MTPSD_TOPK_CASE(36) MTPSD_TOPK_CASE(40)
 #undef MTPSD_TOPK_CASE
@@ -296,7 +300,7 @@ int launch_topk(const TopkPlan& p, cudaStream_t st) {
   size_t smem = (size_t)cache_keys * sizeof(uint32_t);
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  topk_kernel<<<p.R, TOPK_THREADS, smem, st>>>(p, cache_keys);
+  launch_k(topk_kernel, p.R, TOPK_THREADS, smem, st, p, cache_keys);
   return check_launch("topk");
 }
 
