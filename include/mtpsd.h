@@ -133,6 +133,10 @@ typedef struct {
 int64_t mtpsd_scores_ld(int64_t max_visible);
 size_t mtpsd_indexer_topk_workspace_size(int32_t B, int32_t R, int64_t max_visible, int32_t topk);
 int mtpsd_indexer_topk(const mtpsd_indexer_args* args, void* stream);
+/* Kernel launches one mtpsd_indexer_topk call with R > 0 makes on the current device: 3 on the
+ * tensor-core path (group plan, FP8 score GEMM, top-k: MTPSD_FP8_E4M3, head_dim 128, 32 or 64 heads,
+ * 16-byte aligned q and k_cache, which this count assumes), else 2 (scores, top-k). */
+int32_t mtpsd_indexer_topk_launch_count(int32_t n_heads, int32_t head_dim, int32_t dtype);
 
 /* ------------------------------------------------------------------------
  * Allocation-free variant of mtpsd_indexer_topk (the source pages have no
@@ -213,6 +217,11 @@ typedef struct {
 
 size_t mtpsd_sparse_mla_workspace_size(int32_t R, int32_t n_heads, int32_t n_idx, int32_t n_append,
                                        int32_t dtype);
+/* Kernel launches one mtpsd_sparse_mla_decode call with these sizes makes on the current device: 1, or 2
+ * when the selected list is split and the split partials are merged by a second kernel (they are merged
+ * inside the first when the splits of a row fit one thread-block cluster and `out` is 16-byte aligned,
+ * which this count assumes).  0 for sizes that launch nothing. */
+int32_t mtpsd_sparse_mla_launch_count(int32_t R, int32_t n_heads, int32_t n_idx, int32_t n_append, int32_t dtype);
 int mtpsd_sparse_mla_decode(const mtpsd_mla_args* args, void* stream);
 
 /* ------------------------------------------------------------------------

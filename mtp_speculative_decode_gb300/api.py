@@ -171,6 +171,16 @@ def sparse_mla_workspace_size(R, H, n_idx, n_append, dtype) -> int:
     return int(lib().mtpsd_sparse_mla_workspace_size(R, H, n_idx, n_append, dtype))
 
 
+def indexer_topk_launch_count(H, D, dtype) -> int:
+    """Kernel launches of one indexer_topk call (aligned q and k_cache)."""
+    return int(lib().mtpsd_indexer_topk_launch_count(H, D, dtype))
+
+
+def sparse_mla_launch_count(R, H, n_idx, n_append, dtype) -> int:
+    """Kernel launches of one sparse_mla_decode call (16-byte aligned output)."""
+    return int(lib().mtpsd_sparse_mla_launch_count(R, H, n_idx, n_append, dtype))
+
+
 def sparse_mla_decode(q, latent, cache_start, row_offsets, row_pos, idx, softmax_scale: float,
                       n_append: int = 0, append_base=None, row_pos_add: int = 0, out=None, lse=None,
                       workspace=None, dev_status=None, stream=None):

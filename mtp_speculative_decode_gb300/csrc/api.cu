@@ -116,6 +116,10 @@ int mtpsd_indexer_topk(const mtpsd_indexer_args* a, void* stream) {
   return launch_topk(t, st);
 }
 
+int32_t mtpsd_indexer_topk_launch_count(int32_t n_heads, int32_t head_dim, int32_t dtype) {
+  return indexer_launch_count(n_heads, head_dim, dtype);
+}
+
 size_t mtpsd_topk_workspace_size(int32_t R, int32_t topk) {
   (void)R; (void)topk;
   return 0;
@@ -139,6 +143,11 @@ int mtpsd_topk(const float* scores, int64_t ld, int32_t R, const int64_t* row_le
 size_t mtpsd_sparse_mla_workspace_size(int32_t R, int32_t n_heads, int32_t n_idx, int32_t n_append, int32_t dtype) {
   if (R <= 0 || n_heads <= 0 || n_idx < 0 || n_append < 0) return 0;
   return mla_workspace_bytes(R, n_heads, n_idx, n_append, dtype);
+}
+
+int32_t mtpsd_sparse_mla_launch_count(int32_t R, int32_t n_heads, int32_t n_idx, int32_t n_append, int32_t dtype) {
+  if (R <= 0 || n_heads <= 0 || n_idx < 0 || n_append < 0) return 0;
+  return mla_launch_count(R, n_heads, n_idx, n_append, dtype);
 }
 
 int mtpsd_sparse_mla_decode(const mtpsd_mla_args* a, void* stream) {

@@ -37,6 +37,7 @@ struct IndexerPlan {
 };
 int launch_indexer_scores(const IndexerPlan& p, cudaStream_t st);
 size_t indexer_tc_plan_bytes(int B, int R);
+int indexer_launch_count(int H, int D, int dtype);
 bool indexer_tc_supported(const IndexerPlan& p);
 int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st);
 
@@ -62,8 +63,11 @@ size_t mla_workspace_bytes(int R, int H, int n_idx, int n_append, int dtype);
 bool mla_tc_supported(const MlaPlan& p);
 int mla_tc_per_split(int R, int H, int64_t total);
 int mla_tc_ml_halves();
+bool mla_tc_fuse(int n_splits);
+int mla_launch_count(int R, int H, int n_idx, int n_append, int dtype);
+// Launches the tensor-core kernel; *combined tells whether it also merged the split partials.
 int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* part_o, float* part_ml,
-                         cudaStream_t st);
+                         cudaStream_t st, bool* combined);
 int launch_sparse_mla(const MlaPlan& p, cudaStream_t st);
 
 }  // namespace mtpsd

@@ -507,17 +507,18 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
           const int i = ch * (SLOT_COLS / H) + wg * rows_per_wg + j;   // row within the group
           if (i >= nrows) break;
           const float4* wr = (const float4*)(wq + i * H);
-          float acc = 0.f;
+          // four independent sums (heads h = 4k + m go to acc[m]) instead of one 64-long chain
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
           const int hb = j * H;   // first column of row i within this warp's 64
 #pragma unroll
           for (int h4 = 0; h4 < H / 4; ++h4) {
             float4 ww = wr[h4];
-            acc = fmaf(ww.x, fmaxf(v[hb + h4 * 4 + 0], 0.f), acc);
-            acc = fmaf(ww.y, fmaxf(v[hb + h4 * 4 + 1], 0.f), acc);
-            acc = fmaf(ww.z, fmaxf(v[hb + h4 * 4 + 2], 0.f), acc);
-            acc = fmaf(ww.w, fmaxf(v[hb + h4 * 4 + 3], 0.f), acc);
+            acc[0] = fmaf(ww.x, fmaxf(v[hb + h4 * 4 + 0], 0.f), acc[0]);
+            acc[1] = fmaf(ww.y, fmaxf(v[hb + h4 * 4 + 1], 0.f), acc[1]);
+            acc[2] = fmaf(ww.z, fmaxf(v[hb + h4 * 4 + 2], 0.f), acc[2]);
+            acc[3] = fmaf(ww.w, fmaxf(v[hb + h4 * 4 + 3], 0.f), acc[3]);
           }
-          if (s < vis[i]) p.scores[(int64_t)(row0 + i) * p.ld + s] = acc * ks;
+          if (s < vis[i]) p.scores[(int64_t)(row0 + i) * p.ld + s] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * ks;
         }
       }
     }
@@ -564,6 +565,13 @@ bool indexer_tc_supported(const IndexerPlan& p) {
   if (p.max_visible > 0x7fffffffLL - itc::TILE_M) return false;
   if (!p.plan_ws) return false;
   return tc_device_ok() && tma_available();
+}
+
+int indexer_launch_count(int H, int D, int dtype) {
+  const char* env = getenv("MTPSD_INDEXER");
+  const bool tc = !(env && strcmp(env, "generic") == 0) && dtype == MTPSD_FP8_E4M3 && D == 128 &&
+                  (H == 64 || H == 32) && tc_device_ok() && tma_available();
+  return tc ? 3 : 2;
 }
 
 int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {

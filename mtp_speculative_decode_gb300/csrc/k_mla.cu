@@ -512,6 +512,14 @@ static MlaSplit plan_split(int R, int H, int n_idx, int n_append, int dtype) {
   return choose_split(R, H, n_idx, n_append, dtype);
 }
 
+int mla_launch_count(int R, int H, int n_idx, int n_append, int dtype) {
+  if (R <= 0) return 0;
+  MlaSplit sp = plan_split(R, H, n_idx, n_append, dtype);
+  if (sp.n_splits <= 1) return 1;
+  if (dtype == MTPSD_BF16 && use_tc(H, dtype) && mla_tc_fuse(sp.n_splits)) return 1;
+  return 2;
+}
+
 size_t mla_workspace_bytes(int R, int H, int n_idx, int n_append, int dtype) {
   MlaSplit sp = plan_split(R, H, n_idx, n_append, dtype);
   if (sp.n_splits == 1) return 0;
@@ -534,9 +542,10 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
     part_ml = part_o + (size_t)p.R * p.H * sp.n_splits * MLA_DV;
   }
   if (p.dtype == MTPSD_BF16 && mla_tc_supported(p)) {
-    int rc = launch_sparse_mla_tc(p, sp.n_splits, (int)sp.per_split, part_o, part_ml, st);
+    bool combined = false;
+    int rc = launch_sparse_mla_tc(p, sp.n_splits, (int)sp.per_split, part_o, part_ml, st, &combined);
     if (rc) return rc;
-    if (sp.n_splits > 1) {
+    if (sp.n_splits > 1 && !combined) {
       return launch_combine<__nv_bfloat16>(p, sp.n_splits, mla_tc_ml_halves(), part_o, part_ml, st);
     }
     return MTPSD_OK;

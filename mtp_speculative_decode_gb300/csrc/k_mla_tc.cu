@@ -97,6 +97,7 @@ constexpr int TM_Q = 0, TM_S0 = 128, TM_O = 256;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+constexpr int MAX_FUSED_SPLITS_K = 4;     // splits of a row that share one cluster and merge in the kernel
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct Params {
@@ -117,6 +118,7 @@ struct Params {
   float* part_ml;
   int n_splits;
   int per_split;              // positions per split (multiple of NP)
+  int fused_combine;          // the splits of a row share one cluster and merge their partials in-kernel
   int32_t* status;
 };
 
@@ -329,10 +331,61 @@ __device__ __forceinline__ int64_t entry_row(const Params& p, int64_t s, int64_t
   return row;
 }
 
+// Merge of the S split partials of heads [hlo, hhi) for one value half (the fused combine):
+// o = sum_s 2^(m_s - m) o_s / sum_s 2^(m_s - m) l_s, 8 value dims per thread.  Warp w takes heads
+// hlo + w + 13 i; the loads of HB heads are issued together before their arithmetic.
+template <int S>
+__device__ __noinline__ void merge_splits(const Params& p, int r, int h0, int hlo, int hhi, uint32_t rank) {
+  constexpr int NW = THREADS / 32, HB = S == 2 ? 3 : (S == 3 ? 2 : 1);
+  const int warp = threadIdx.x >> 5, d8 = threadIdx.x & 31;   // dims 8*d8 .. +7 of the half
+  for (int i0 = 0; hlo + warp + NW * i0 < hhi; i0 += HB) {
+    float2 mlv[HB][S];
+    float4 ov[HB][S][2];
+#pragma unroll
+    for (int i = 0; i < HB; ++i) {
+      const int hh = hlo + warp + NW * (i0 + i);
+      if (hh < hhi) {
+        const int64_t rh = (int64_t)r * p.H + h0 + hh;
+#pragma unroll
+        for (int t = 0; t < S; ++t) {
+          mlv[i][t] = *(const float2*)(p.part_ml + ((rh * S + t) * 2 + rank) * 2);
+          const float4* src = (const float4*)(p.part_o + (rh * S + t) * DV + rank * DVH) + 2 * d8;
+          ov[i][t][0] = src[0];
+          ov[i][t][1] = src[1];
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < HB; ++i) {
+      const int hh = hlo + warp + NW * (i0 + i);
+      if (hh >= hhi) break;
+      const int64_t rh = (int64_t)r * p.H + h0 + hh;
+      float m = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < S; ++t) m = fmaxf(m, mlv[i][t].x);
+      float l = 0.f;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int t = 0; t < S; ++t) {
+        if (mlv[i][t].x == -INFINITY) continue;
+        const float w = ex2(mlv[i][t].x - m);
+        l += w * mlv[i][t].y;
+        const float4 a = ov[i][t][0], c = ov[i][t][1];
+        acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+        acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint32_t w4[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) w4[k] = pack_bf16(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+      *((uint4*)(p.out + rh * DV + rank * DVH) + d8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      if (rank == 0 && d8 == 0 && p.lse) p.lse[rh] = l > 0.f ? (m + log2f(l)) / LOG2E : -INFINITY;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                                                                    const __grid_constant__ CUtensorMap tm_q, Params p) {
-  griddep_wait();                // the previous kernel's writes are visible from here on
-  griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + OFF_BAR);
@@ -351,16 +404,15 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   uint32_t* mask_s = (uint32_t*)(sm + OFF_MASK);   // [stage][producer]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();    // = the value half this CTA owns
-  const uint32_t peer = rank ^ 1u;
+  // cluster (1, 2, S): rank = value half + 2 * split; the other half of the same split is crank ^ 1
+  const uint32_t crank = cluster_rank();
+  const uint32_t rank = crank & 1u;        // = the value half this CTA owns
+  const uint32_t peer = crank ^ 1u;
   const int nch = rank == 0 ? 5 : 4;       // 64-dim chunks this CTA gathers
   const int r = blockIdx.x;
   const int hg = blockIdx.y >> 1;
   const int split = blockIdx.z;
   const int h0 = hg * HG;
-  const int b = request_of_row(p.row_offsets, p.B, (uint32_t)r);
-  const int64_t base = p.cache_start[b];
-  const int64_t limit = p.row_pos[r] + p.row_pos_add;
   const int64_t total = (int64_t)p.n_idx + p.n_append;
   const int64_t j0 = (int64_t)split * p.per_split;
   const int64_t j1 = min(total, j0 + (int64_t)p.per_split);
@@ -388,10 +440,21 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)), "r"(512));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  if (warp == PROD_WARP && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_lat) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_q) : "memory");
+  }
   fence_before();
   __syncthreads();
   fence_after();
   cluster_sync();                          // both CTAs' barriers exist before any remote arrival
+  // Everything above touches no global memory and overlaps the previous kernel's tail (programmatic
+  // dependent launch); its writes are visible from here on.
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = request_of_row(p.row_offsets, p.B, (uint32_t)r);
+  const int64_t base = p.cache_start[b];
+  const int64_t limit = p.row_pos[r] + p.row_pos_add;
   const uint32_t tmem = *tmem_slot;
   const __nv_bfloat16* qrow = p.q + ((int64_t)r * p.H + h0) * DL;
 
@@ -756,7 +819,17 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
   }
-  cluster_sync();                          // the other CTA no longer writes into this CTA's shared memory
+  // the other CTA no longer writes into this CTA's shared memory; with a fused combine, every split of
+  // this row has also written its partials (the barrier releases and acquires at cluster scope)
+  cluster_sync();
+  if (p.fused_combine) {
+    const int hlo = split * HG / p.n_splits, hhi = (split + 1) * HG / p.n_splits;
+    switch (p.n_splits) {
+      case 2: merge_splits<2>(p, r, h0, hlo, hhi, rank); break;
+      case 3: merge_splits<3>(p, r, h0, hlo, hhi, rank); break;
+      default: merge_splits<4>(p, r, h0, hlo, hhi, rank); break;
+    }
+  }
 }
 
 }  // namespace mtc
@@ -776,7 +849,10 @@ bool mla_tc_supported(const MlaPlan& p) {
 }
 
 namespace {
-cudaLaunchConfig_t mla_tc_config(dim3 grid, cudaStream_t st, cudaLaunchAttribute* attrs) {
+// Largest split count whose splits share one cluster (2 CTAs per split, 8 CTAs at most).
+constexpr int MAX_FUSED_SPLITS = mtc::MAX_FUSED_SPLITS_K;
+
+cudaLaunchConfig_t mla_tc_config(dim3 grid, int cluster_z, cudaStream_t st, cudaLaunchAttribute* attrs) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(mtc::THREADS);
@@ -785,7 +861,7 @@ cudaLaunchConfig_t mla_tc_config(dim3 grid, cudaStream_t st, cudaLaunchAttribute
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = 1;
   attrs[0].val.clusterDim.y = 2;
-  attrs[0].val.clusterDim.z = 1;
+  attrs[0].val.clusterDim.z = cluster_z;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
   return cfg;
@@ -800,35 +876,41 @@ bool mla_tc_prepare() {
   }
   return true;
 }
-// CTAs of this kernel that run at once: two per co-resident cluster.
-int mla_tc_resident_ctas() {
-  static int n = 0;
-  if (!n) {
+// CTAs of this kernel that run at once with clusters of 2 x cluster_z CTAs.
+int mla_tc_resident_ctas(int cluster_z) {
+  static int n[MAX_FUSED_SPLITS + 1] = {0};
+  if (!n[cluster_z]) {
     int clusters = 0;
     cudaLaunchAttribute attrs[1];
-    cudaLaunchConfig_t cfg = mla_tc_config(dim3(1, 2, 1), 0, attrs);
+    cudaLaunchConfig_t cfg = mla_tc_config(dim3(1, 2, cluster_z), cluster_z, 0, attrs);
     if (mla_tc_prepare() &&
         cudaOccupancyMaxActiveClusters(&clusters, (void*)mtc::sparse_mla_tc_kernel, &cfg) == cudaSuccess &&
         clusters > 0)
-      n = 2 * clusters;
+      n[cluster_z] = 2 * cluster_z * clusters;
     else
-      n = num_sms() & ~1;
+      n[cluster_z] = cluster_z == 1 ? (num_sms() & ~1) : 0;
     cudaGetLastError();
   }
-  return n;
+  return n[cluster_z];
 }
 }  // namespace
+
+// The splits of a row share one cluster (and merge in the kernel) when there are few of them and
+// such clusters fit on the device.
+bool mla_tc_fuse(int n_splits) {
+  return n_splits >= 2 && n_splits <= MAX_FUSED_SPLITS && mla_tc_resident_ctas(n_splits) > 0;
+}
 
 // Splits of the selected list that balance whole waves of resident clusters.
 // Returns the positions per split (a multiple of NP).
 int mla_tc_per_split(int R, int H, int64_t total) {
   const int64_t tiles = (total + mtc::NP - 1) / mtc::NP;
   const int64_t units = (int64_t)R * (H / mtc::HG) * 2;
-  const int slots = mla_tc_resident_ctas();
   int64_t best = 1;
   double best_cost = 1e30;
   for (int64_t s = best; s <= best + 64 && s <= tiles; ++s) {
     const int64_t per = (tiles + s - 1) / s;
+    const int slots = mla_tc_fuse((int)s) ? mla_tc_resident_ctas((int)s) : mla_tc_resident_ctas(1);
     const int64_t waves = (units * s + slots - 1) / slots;
     const double cost = (double)waves * (per + 4.0);
     if (cost < best_cost - 1e-9) {
@@ -844,7 +926,7 @@ int mla_tc_per_split(int R, int H, int64_t total) {
 int mla_tc_ml_halves() { return 2; }
 
 int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* part_o, float* part_ml,
-                         cudaStream_t st) {
+                         cudaStream_t st, bool* combined) {
   using namespace mtc;
   Params k;
   k.B = p.B; k.R = p.R; k.H = p.H; k.n_idx = p.n_idx; k.n_append = p.n_append;
@@ -853,6 +935,8 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
   k.cache_start = p.cache_start; k.row_offsets = p.row_offsets; k.row_pos = p.row_pos; k.idx = p.idx;
   k.append_base = p.append_base; k.out = (__nv_bfloat16*)p.out; k.lse = p.lse; k.part_o = part_o; k.part_ml = part_ml;
   k.n_splits = n_splits; k.per_split = per_split; k.status = p.status;
+  k.fused_combine = mla_tc_fuse(n_splits) && ((uintptr_t)p.out % 16) == 0 ? 1 : 0;   // 16-byte output stores
+  if (combined) *combined = k.fused_combine != 0;
   alignas(64) CUtensorMap tm_lat, tm_q;
   if (!make_tma_2d(&tm_lat, 1, p.latent, DL, (uint64_t)p.pool, DL * 2, 64, 1, false) ||
       !make_tma_2d(&tm_q, 1, p.q, DL, (uint64_t)p.R * p.H, DL * 2, 64, HG, true)) {
@@ -864,7 +948,7 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
     return MTPSD_ECUDA;
   }
   cudaLaunchAttribute attrs[2];
-  cudaLaunchConfig_t cfg = mla_tc_config(dim3(p.R, (p.H / HG) * 2, n_splits), st, attrs);
+  cudaLaunchConfig_t cfg = mla_tc_config(dim3(p.R, (p.H / HG) * 2, n_splits), k.fused_combine ? n_splits : 1, st, attrs);
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see launch_k()
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 2;

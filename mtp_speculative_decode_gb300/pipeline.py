@@ -22,6 +22,7 @@ from typing import Dict, Optional
 import numpy as np
 import torch
 
+from . import _native as N
 from . import api
 from . import workloads as W
 
@@ -195,14 +196,16 @@ class DecodeStep:
     def launches_per_step(self) -> int:
         """Kernel launches of one step (for the benchmark's launch count)."""
         n = 0
+        quant = 1 if self.fp8 else 0
+        _, H_I, D_I = self.q_idx_raw.shape
+        idx = api.indexer_topk_launch_count(H_I, D_I, N.MTPSD_FP8_E4M3 if self.fp8 else N.MTPSD_F32)
         if self.spec.verify:
-            n += 1 + (1 if self.fp8 else 0) + 2 + self._mla_launches(self.spec.topk, 0, self.R)
+            n += 1 + quant + idx + self._mla_launches(self.spec.topk, 0, self.R)
         n += 1
         if self.has_draft:
-            n += 1 + (1 if self.fp8 else 0) + 2 + 1
+            n += 1 + quant + idx + 1
             n += sum(self._mla_launches(self.spec.topk, j, self.B) for j in range(self.spec.draft_steps))
         return n
 
     def _mla_launches(self, n_idx, n_append, R):
-        return 1 + (1 if api.sparse_mla_workspace_size(R, self.spec.H_Q, n_idx, n_append,
-                                                        1 if self.fp8 else 0) else 0)
+        return api.sparse_mla_launch_count(R, self.spec.H_Q, n_idx, n_append, 1 if self.fp8 else 0)
