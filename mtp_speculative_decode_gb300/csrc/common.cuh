@@ -36,6 +36,25 @@ __device__ __forceinline__ int request_of_row(const uint32_t* row_offsets, int B
   return lo;
 }
 
+// The same search by a whole warp (all 32 lanes call it): each round loads 32 evenly spaced offsets
+// at once and keeps the last one <= r, so B <= 32 takes one round of loads and B <= 1024 two,
+// instead of log2(B) dependent loads.
+__device__ __forceinline__ int request_of_row_warp(const uint32_t* row_offsets, int B, uint32_t r) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, n = B;  // answer in [lo, lo + n): row_offsets[lo] <= r
+  while (n > 1) {
+    const int step = (n + 31) >> 5;
+    const int c = lo + lane * step;
+    const bool le = c < lo + n && row_offsets[c] <= r;
+    const unsigned m = __ballot_sync(0xffffffffu, le) | 1u;   // lane 0 (c = lo) holds by the invariant
+    const int k = 31 - __clz((int)m);
+    const int c_k = lo + k * step;
+    n = min(step, lo + n - c_k);
+    lo = c_k;
+  }
+  return lo;
+}
+
 MTPSD_HD int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Programmatic dependent launch.  Every kernel of the library is launched with launch_k(), which lets

@@ -10,6 +10,8 @@ namespace mtpsd {
 // 2D tensor map with the 128-byte swizzle (map: a 64-byte aligned CUtensorMap).
 // dtype_u8_or_bf16: 0 = uint8 elements, 1 = bf16 elements.
 bool tma_available();
+bool make_tma_store_map(void* map, bool f32, const void* base, int rank, const uint64_t* dims,
+                        const uint64_t* strides, const uint32_t* box);
 bool make_tma_2d(void* map, int dtype_u8_or_bf16, const void* base, uint64_t inner_elems, uint64_t rows,
                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, bool l2_256);
 

@@ -214,67 +214,83 @@ struct Cursor {
 };
 
 // ------------------------------------------------------------------- kernels
-// Group plan: one block.  For each request, its rows are cut into groups of
-// at most group_rows rows; each group scans ceil(vmax/128) tiles, vmax being
-// the largest visible length of its rows (clamped to max_visible).
+// Group plan: one block of up to 1024 threads (one request per thread, in passes of blockDim
+// requests).  For each request, its rows are cut into groups of at most group_rows rows; each group
+// scans ceil(vmax/128) tiles, vmax being the largest visible length of its rows (clamped to
+// max_visible).  The group and tile offsets are exclusive prefix sums over the requests (warp
+// shuffles, then one warp over the warp totals).
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  return v;
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(const uint32_t* __restrict__ ro, const int64_t* __restrict__ row_pos,
                                                     int B, int64_t max_visible, int group_rows, int* g_b,
                                                     int* g_row0, int* g_nrows, int* g_vmax, int* g_tile0,
                                                     int* n_groups) {
   griddep_wait();                // the previous kernel's writes are visible from here on
   griddep_launch_dependents();
-  __shared__ int s_groups[1024], s_tiles[1024];
-  __shared__ int carry_g, carry_t;
-  if (threadIdx.x == 0) carry_g = carry_t = 0;
-  __syncthreads();
-  for (int base = 0; base < B; base += 1024) {
+  __shared__ int s_wg[32], s_wt[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int carry_g = 0, carry_t = 0;
+  for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
-    int ng = 0, nt = 0;
+    int r0 = 0, r1 = 0, ng = 0, nt = 0;
     if (b < B) {
-      int r0 = (int)ro[b], r1 = (int)ro[b + 1];
+      r0 = (int)ro[b];
+      r1 = (int)ro[b + 1];
       for (int a = r0; a < r1; a += group_rows) {
-        int e = min(r1, a + group_rows);
+        const int e = min(r1, a + group_rows);
         int64_t vm = 0;
         for (int r = a; r < e; ++r) vm = max(vm, min(row_pos[r] + 1, max_visible));
         ++ng;
         nt += (int)((vm + TILE_M - 1) / TILE_M);
       }
     }
-    s_groups[threadIdx.x] = ng;
-    s_tiles[threadIdx.x] = nt;
-    __syncthreads();
-    // inclusive scans (Hillis-Steele)
-    for (int o = 1; o < 1024; o <<= 1) {
-      int vg = threadIdx.x >= o ? s_groups[threadIdx.x - o] : 0;
-      int vt = threadIdx.x >= o ? s_tiles[threadIdx.x - o] : 0;
-      __syncthreads();
-      s_groups[threadIdx.x] += vg;
-      s_tiles[threadIdx.x] += vt;
-      __syncthreads();
+    const int ig = warp_incl_scan(ng, lane), it = warp_incl_scan(nt, lane);
+    if (lane == 31) {
+      s_wg[wid] = ig;
+      s_wt[wid] = it;
     }
-    int gpos = carry_g + s_groups[threadIdx.x] - ng;
-    int tpos = carry_t + s_tiles[threadIdx.x] - nt;
-    if (b < B) {
-      int r0 = (int)ro[b], r1 = (int)ro[b + 1];
-      for (int a = r0; a < r1; a += group_rows) {
-        int e = min(r1, a + group_rows);
-        int64_t vm = 0;
-        for (int r = a; r < e; ++r) vm = max(vm, min(row_pos[r] + 1, max_visible));
-        g_b[gpos] = b;
-        g_row0[gpos] = a;
-        g_nrows[gpos] = e - a;
-        g_vmax[gpos] = (int)vm;
-        g_tile0[gpos] = tpos;
-        ++gpos;
-        tpos += (int)((vm + TILE_M - 1) / TILE_M);
+    __syncthreads();
+    if (wid == 0) {
+      const int vg = lane < nw ? s_wg[lane] : 0, vt = lane < nw ? s_wt[lane] : 0;
+      const int sg = warp_incl_scan(vg, lane), stt = warp_incl_scan(vt, lane);
+      if (lane < nw) {
+        s_wg[lane] = sg - vg;     // exclusive offsets of the warps
+        s_wt[lane] = stt - vt;
       }
     }
     __syncthreads();
-    if (threadIdx.x == 1023) {
-      carry_g += s_groups[1023];
-      carry_t += s_tiles[1023];
+    int gpos = carry_g + s_wg[wid] + ig - ng;
+    int tpos = carry_t + s_wt[wid] + it - nt;
+    for (int a = r0; a < r1; a += group_rows) {   // no rows: no groups (b >= B too)
+      const int e = min(r1, a + group_rows);
+      int64_t vm = 0;
+      for (int r = a; r < e; ++r) vm = max(vm, min(row_pos[r] + 1, max_visible));
+      g_b[gpos] = b;
+      g_row0[gpos] = a;
+      g_nrows[gpos] = e - a;
+      g_vmax[gpos] = (int)vm;
+      g_tile0[gpos] = tpos;
+      ++gpos;
+      tpos += (int)((vm + TILE_M - 1) / TILE_M);
+    }
+    // pass totals: the last warp's exclusive offset plus its inclusive total
+    const int last = nw - 1;
+    __shared__ int s_tot[2];
+    if (threadIdx.x == blockDim.x - 1) {
+      s_tot[0] = s_wg[last] + ig;
+      s_tot[1] = s_wt[last] + it;
     }
     __syncthreads();
+    carry_g += s_tot[0];
+    carry_t += s_tot[1];
+    __syncthreads();   // s_wg / s_wt / s_tot are rewritten by the next pass
   }
   if (threadIdx.x == 0) {
     g_tile0[carry_g] = carry_t;
@@ -590,7 +606,8 @@ int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {
   int* g_tile0 = g_vmax + n;
   int* n_groups = g_tile0 + n;
   const int group_rows = Q_ROWS / p.H;
-  launch_k(plan_kernel, 1, 1024, 0, st, p.row_offsets, p.row_pos, p.B, p.max_visible, group_rows, g_b, g_row0, g_nrows,
+  const int plan_threads = p.B >= 1024 ? 1024 : ((p.B + 31) / 32) * 32 + (p.B == 0 ? 32 : 0);
+  launch_k(plan_kernel, 1, plan_threads, 0, st, p.row_offsets, p.row_pos, p.B, p.max_visible, group_rows, g_b, g_row0, g_nrows,
                                   g_vmax, g_tile0, n_groups);
   int rc = check_launch("indexer_tc_plan");
   if (rc) return rc;

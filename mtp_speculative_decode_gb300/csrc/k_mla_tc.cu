@@ -131,6 +131,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"((uint32_t)__cvta_generic_to_shared(bar)) : "memory");
 }
+// TMA stores of one shared-memory box (bulk async-group of the issuing thread)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"((uint64_t)map), "r"(x), "r"(y), "r"(src) : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+               ::"l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(src) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
 // 4 rows (y0..y3) x one box of columns starting at x
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2,
                                             int y3, uint64_t* bar) {
@@ -385,7 +397,8 @@ __device__ __noinline__ void merge_splits(const Params& p, int r, int h0, int hl
 }
 
 __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
-                                                                   const __grid_constant__ CUtensorMap tm_q, Params p) {
+                                                                   const __grid_constant__ CUtensorMap tm_q,
+                                                                   const __grid_constant__ CUtensorMap tm_st, Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + OFF_BAR);
@@ -443,6 +456,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   if (warp == PROD_WARP && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_lat) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_q) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_st) : "memory");
   }
   fence_before();
   __syncthreads();
@@ -452,9 +466,6 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   // dependent launch); its writes are visible from here on.
   griddep_wait();
   griddep_launch_dependents();
-  const int b = request_of_row(p.row_offsets, p.B, (uint32_t)r);
-  const int64_t base = p.cache_start[b];
-  const int64_t limit = p.row_pos[r] + p.row_pos_add;
   const uint32_t tmem = *tmem_slot;
   const __nv_bfloat16* qrow = p.q + ((int64_t)r * p.H + h0) * DL;
 
@@ -509,24 +520,47 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       const uint32_t* m0 = mask_s + st0 * 4;
       const uint32_t* m1 = mask_s + (st0 + 1) * 4;
       const uint64_t mask = (uint64_t)(m0[0] | m0[1] | m0[2] | m0[3]) | ((uint64_t)(m1[0] | m1[1] | m1[2] | m1[3]) << 32);
-      // S = this CTA's partial (fp32) + the other's (fp16), in log2 units
+      // S = this CTA's partial (fp32) + the other's (fp16), in log2 units.  The mask is the same for
+      // the whole CTA, so the branch is uniform; a pair without padding skips the per-position select.
+      const bool full = mask == ~0ull;
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t px[4];
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(px[0]), "=r"(px[1]), "=r"(px[2]), "=r"(px[3])
-                     : "r"(xo + ((c ^ swz) << 4))
-                     : "memory");
+        for (int c = 0; c < 8; ++c) {
+          uint32_t px[4];
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(px[0]), "=r"(px[1]), "=r"(px[2]), "=r"(px[3])
+                       : "r"(xo + ((c ^ swz) << 4))
+                       : "memory");
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int j = 8 * c + 2 * i;
-          const float2 o = f16x2_to_f32(px[i]);
-          const float v0 = ((mask >> j) & 1ull) ? fmaf(__uint_as_float(sr[j]), p.sl2, o.x) : -INFINITY;
-          const float v1 = ((mask >> (j + 1)) & 1ull) ? fmaf(__uint_as_float(sr[j + 1]), p.sl2, o.y) : -INFINITY;
-          sr[j] = __float_as_uint(v0);
-          sr[j + 1] = __float_as_uint(v1);
-          mx[i] = fmaxf(mx[i], fmaxf(v0, v1));
+          for (int i = 0; i < 4; ++i) {
+            const int j = 8 * c + 2 * i;
+            const float2 o = f16x2_to_f32(px[i]);
+            const float v0 = fmaf(__uint_as_float(sr[j]), p.sl2, o.x);
+            const float v1 = fmaf(__uint_as_float(sr[j + 1]), p.sl2, o.y);
+            sr[j] = __float_as_uint(v0);
+            sr[j + 1] = __float_as_uint(v1);
+            mx[i] = fmaxf(mx[i], fmaxf(v0, v1));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t px[4];
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(px[0]), "=r"(px[1]), "=r"(px[2]), "=r"(px[3])
+                       : "r"(xo + ((c ^ swz) << 4))
+                       : "memory");
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = 8 * c + 2 * i;
+            const float2 o = f16x2_to_f32(px[i]);
+            const float v0 = ((mask >> j) & 1ull) ? fmaf(__uint_as_float(sr[j]), p.sl2, o.x) : -INFINITY;
+            const float v1 = ((mask >> (j + 1)) & 1ull) ? fmaf(__uint_as_float(sr[j + 1]), p.sl2, o.y) : -INFINITY;
+            sr[j] = __float_as_uint(v0);
+            sr[j + 1] = __float_as_uint(v1);
+            mx[i] = fmaxf(mx[i], fmaxf(v0, v1));
+          }
         }
       }
       // slot s may be written again (pair P+2) once all four warps have consumed it
@@ -559,13 +593,14 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       const float mo = m_ref == -INFINITY ? 0.f : m_ref;
       uint32_t pk[32];
       float psum[4] = {0.f, 0.f, 0.f, 0.f};
+      // masked positions (-inf) give exact zeros; the sum is taken over the fp32 values (their bf16
+      // rounding in P is unbiased and below the tolerance of the output)
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float a = ex2(__uint_as_float(sr[2 * j]) - mo);
         const float c = ex2(__uint_as_float(sr[2 * j + 1]) - mo);
         pk[j] = pack_bf16(a, c);
-        // the sum uses the rounded values PV multiplies (bf16 -> f32 is a shift)
-        psum[j & 3] += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
+        psum[j & 3] += a + c;
       }
       l += (psum[0] + psum[1]) + (psum[2] + psum[3]);
       // P overwrites the scores: the senders must have read them
@@ -583,12 +618,18 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     }
     if (ok) fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
+    // O leaves through shared memory (the drained gather ring): each warp writes its 32 heads as
+    // boxes of 32 rows x 128 bytes with the 128-byte swizzle (16-byte piece c of row i at c ^ (i & 7),
+    // so the eight rows of a quarter warp hit all banks), then one lane stores them with TMA.
+    const bool have_o = n_pairs > 0 && ok;
+    const uint32_t row_off = (uint32_t)lane * 128u;
+    const uint32_t sw = (uint32_t)(lane & 7);
     if (p.n_splits == 1) {
-      __nv_bfloat16* og = p.out + ((int64_t)r * p.H + h0 + h) * DV + rank * DVH;
+      const uint32_t stg = saddr(sm + OFF_C) + (uint32_t)warp * 16384u;   // 4 boxes of 64 bf16 columns
 #pragma unroll 1
       for (int c = 0; c < DVH / 32; ++c) {
         uint32_t o[32];
-        if (n_pairs > 0 && ok) {
+        if (have_o) {
           tm_ld32(tmem + lane_off + TM_O + c * 32, o);
           tm_wait_ld();
         } else {
@@ -599,34 +640,54 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-        if (head_ok) {
-          uint4* dst = (uint4*)(og + c * 32);
+        const uint32_t box = stg + (uint32_t)(c >> 1) * 4096u + row_off;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-        }
+        for (int q = 0; q < 4; ++q)
+          st_shared_v4(box + ((((uint32_t)(c & 1) * 4u + q) ^ sw) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2],
+                       w[4 * q + 3]);
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the TMA store
+      __syncwarp();
+      if (ok && lane == 0) {
+#pragma unroll
+        for (int bx = 0; bx < DVH / 64; ++bx)
+          tma_store_2d(&tm_st, stg + (uint32_t)bx * 4096u, (int)rank * DVH + bx * 64, r * p.H + h0 + warp * 32);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // the staging is read before exit
+      }
+      __syncwarp();
       if (head_ok && rank == 0 && p.lse)
         p.lse[(int64_t)r * p.H + h0 + h] = l > 0.f ? (m_ref + log2f(l)) / LOG2E : -INFINITY;
     } else {
-      float* po = p.part_o + (((int64_t)r * p.H + h0 + h) * p.n_splits + split) * DV + rank * DVH;
+      const uint32_t stg = saddr(sm + OFF_C) + (uint32_t)warp * 32768u;   // 8 boxes of 32 float columns
 #pragma unroll 1
       for (int c = 0; c < DVH / 32; ++c) {
         uint32_t o[32];
-        if (n_pairs > 0 && ok) {
+        if (have_o) {
           tm_ld32(tmem + lane_off + TM_O + c * 32, o);
           tm_wait_ld();
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0u;
         }
-        if (head_ok) {
-          float4* dst = (float4*)(po + c * 32);
+        const uint32_t box = stg + (uint32_t)c * 4096u + row_off;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]), __uint_as_float(o[4 * i + 2]),
-                                 __uint_as_float(o[4 * i + 3]));
-        }
+        for (int q = 0; q < 8; ++q)
+          st_shared_v4(box + (((uint32_t)q ^ sw) << 4), o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (ok && lane == 0) {
+#pragma unroll
+        for (int c = 0; c < DVH / 32; ++c)
+          tma_store_3d(&tm_st, stg + (uint32_t)c * 4096u, (int)rank * DVH + c * 32, split, r * p.H + h0 + warp * 32);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        // the partials are complete in global memory, and ordered before this thread's later
+        // generic accesses (the cluster barrier that releases them to the merging CTAs)
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      __syncwarp();
       if (head_ok) {   // each value half carries its own (max, sum)
         float* ml = p.part_ml + ((((int64_t)r * p.H + h0 + h) * p.n_splits + split) * 2 + rank) * 2;
         ml[0] = l > 0.f ? m_ref : -INFINITY;
@@ -709,7 +770,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     const int32_t* idx_row = p.idx + (int64_t)r * p.n_idx;
     // raw selected entry of position j (or a clamped dummy when j is an appended / past-the-split position)
     auto raw = [&](int64_t j) -> int32_t { return p.n_idx > 0 ? idx_row[min(j, (int64_t)p.n_idx - 1)] : 0; };
+    // the first entries and the row's visible limit are loaded while the warp looks up the request
     int32_t nraw = n_tiles > 0 ? raw(j0 + my_pos) : 0;
+    const int64_t limit = p.row_pos[r] + p.row_pos_add;
+    const int64_t base = p.cache_start[request_of_row_warp(p.row_offsets, p.B, (uint32_t)r)];
     int issued = 0;
     for (int t = 0; t < n_tiles; ++t) {
       const int32_t craw = nraw;
@@ -845,6 +909,8 @@ bool mla_tc_supported(const MlaPlan& p) {
   if (env && env[0] == 'm') return false;   // "mma": the mma.sync kernel
   if (p.pool > 0x7ffffffeLL || (int64_t)p.R * p.H > 0x7fffffffLL) return false;
   if (((uintptr_t)p.latent % 16) || ((uintptr_t)p.q % 16)) return false;
+  // the output and the split partials (workspace) are written by TMA stores
+  if (((uintptr_t)p.out % 16) || ((uintptr_t)p.ws % 16)) return false;
   return tma_available();
 }
 
@@ -935,10 +1001,20 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
   k.cache_start = p.cache_start; k.row_offsets = p.row_offsets; k.row_pos = p.row_pos; k.idx = p.idx;
   k.append_base = p.append_base; k.out = (__nv_bfloat16*)p.out; k.lse = p.lse; k.part_o = part_o; k.part_ml = part_ml;
   k.n_splits = n_splits; k.per_split = per_split; k.status = p.status;
-  k.fused_combine = mla_tc_fuse(n_splits) && ((uintptr_t)p.out % 16) == 0 ? 1 : 0;   // 16-byte output stores
+  k.fused_combine = mla_tc_fuse(n_splits) ? 1 : 0;
   if (combined) *combined = k.fused_combine != 0;
-  alignas(64) CUtensorMap tm_lat, tm_q;
-  if (!make_tma_2d(&tm_lat, 1, p.latent, DL, (uint64_t)p.pool, DL * 2, 64, 1, false) ||
+  alignas(64) CUtensorMap tm_lat, tm_q, tm_st;
+  // epilogue stores: boxes of 32 heads x 128 bytes, into out [R*H, 512] bf16 or into the split
+  // partials [R*H, splits, 512] float32
+  const uint64_t rh = (uint64_t)p.R * p.H;
+  const uint64_t out_dims[2] = {(uint64_t)DV, rh}, out_strides[1] = {(uint64_t)DV * 2};
+  const uint32_t out_box[2] = {64, 32};
+  const uint64_t po_dims[3] = {(uint64_t)DV, (uint64_t)n_splits, rh};
+  const uint64_t po_strides[2] = {(uint64_t)DV * 4, (uint64_t)DV * 4 * n_splits};
+  const uint32_t po_box[3] = {32, 1, 32};
+  const bool st_ok = n_splits == 1 ? make_tma_store_map(&tm_st, false, p.out, 2, out_dims, out_strides, out_box)
+                                   : make_tma_store_map(&tm_st, true, part_o, 3, po_dims, po_strides, po_box);
+  if (!st_ok || !make_tma_2d(&tm_lat, 1, p.latent, DL, (uint64_t)p.pool, DL * 2, 64, 1, false) ||
       !make_tma_2d(&tm_q, 1, p.q, DL, (uint64_t)p.R * p.H, DL * 2, 64, HG, true)) {
     set_error("sparse_mla: cuTensorMapEncodeTiled failed");
     return MTPSD_ECUDA;
@@ -952,7 +1028,7 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see launch_k()
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel, tm_lat, tm_q, k);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel, tm_lat, tm_q, tm_st, k);
   if (e != cudaSuccess) {
     set_error("sparse_mla_tc: launch failed: %s", cudaGetErrorString(e));
     return MTPSD_ECUDA;

@@ -39,4 +39,24 @@ bool make_tma_2d(void* map, int dtype_u8_or_bf16, const void* base, uint64_t inn
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map for TMA stores from shared memory: rank 2 or 3, bf16 or float32, 128-byte swizzle
+// (the box's inner extent must be 128 bytes).  dims[0] is the contiguous dimension; strides are the
+// byte strides of dims 1.. (multiples of 16).
+bool make_tma_store_map(void* map, bool f32, const void* base, int rank, const uint64_t* dims,
+                        const uint64_t* strides, const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn || rank < 2 || rank > 3) return false;
+  cuuint64_t d[3], st[2];
+  cuuint32_t bx[3], estr[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = (cuuint64_t)dims[i];
+    bx[i] = (cuuint32_t)box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = (cuuint64_t)strides[i];
+  CUresult r = fn((CUtensorMap*)map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  (cuuint32_t)rank, const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace mtpsd
