@@ -79,15 +79,16 @@ constexpr int QTM = 256;                // query dims held in TMEM
 constexpr int CHUNK_BYTES = NP * 128;   // 8192: one chunk of a pair buffer
 constexpr int PAIR_STRIDE = NCH_MAX * CHUNK_BYTES;   // 40960
 constexpr int XSLOT_BYTES = HG * NP * 2;             // 16384: one pair's fp16 partial scores
+constexpr int XHALF_BYTES = XSLOT_BYTES / 2;         // 8192: positions 0..31 or 32..63 of the pair
 constexpr int OFF_QR = 0;                                    // rope query dims (rank 0)
 constexpr int OFF_C = OFF_QR + HG * 128;                     // 16384
 constexpr int OFF_X = OFF_C + NPAIR * PAIR_STRIDE;           // 180224: [2] receive slots
 constexpr int OFF_STG = OFF_X + 2 * XSLOT_BYTES;             // 212992: own fp16 partials staged for the copy
 constexpr int OFF_MASK = OFF_STG + XSLOT_BYTES;              // 229376: [NSTAGE][4] uint32 validity bits
 constexpr int OFF_BAR = OFF_MASK + NSTAGE * 4 * 4;
-// barriers: c_full[NSTAGE], c_empty[NPAIR], s_full[2], p_full[2], pv_done[2], x_full[2], s_read[2], x_free[2],
-// q_ready, drain
-constexpr int N_BARS = NSTAGE + NPAIR + 12 + 2;
+// barriers: c_full[NSTAGE], c_empty[NPAIR], s_full[2], p_full[2], pv_done[2], x_full[2][2], s_read[2], x_free[2],
+// stg_free, q_ready, drain
+constexpr int N_BARS = NSTAGE + NPAIR + 14 + 3;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;               // tmem base, abort flag
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;                 // alignment slack
@@ -407,10 +408,11 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   uint64_t* s_full = c_empty + NPAIR;      // partial scores of the pair in score buffer s are in TMEM
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
-  uint64_t* x_full = pv_done + 2;          // receive slot s holds the other CTA's partial scores
-  uint64_t* s_read = x_full + 2;           // the senders have read score buffer s
+  uint64_t* x_full = pv_done + 2;          // [slot][half]: half of receive slot s holds the other CTA's scores
+  uint64_t* s_read = x_full + 4;           // the senders have read score buffer s
   uint64_t* x_free = s_read + 2;           // the other CTA has consumed what this CTA sent into its slot s
-  uint64_t* q_ready = x_free + 2;
+  uint64_t* stg_free = x_free + 2;         // the other CTA received the last staged pair (staging reusable)
+  uint64_t* q_ready = stg_free + 1;
   uint64_t* drain = q_ready + 1;
   uint32_t* tmem_slot = (uint32_t*)(sm + OFF_MISC);
   volatile int* abort_flag = (volatile int*)(sm + OFF_MISC + 4);
@@ -439,11 +441,13 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&pv_done[i], 1);
-      mbar_init(&x_full[i], 1);
+      mbar_init(&x_full[2 * i], 1);
+      mbar_init(&x_full[2 * i + 1], 1);
       mbar_init(&s_read[i], 128);
       mbar_init(&x_free[i], 4);           // one arrival per softmax warp of the other CTA
     }
     // 128 softmax threads (query dims in TMEM), plus on rank 0 the first producer (rope dims by TMA)
+    mbar_init(stg_free, 1);                 // one arrival by the other CTA's first softmax thread
     mbar_init(q_ready, rank == 0 ? 129 : 128);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -490,11 +494,13 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       fence_before();
       mbar_arrive(q_ready);
     }
-    // receive slot layout: head h's 64 fp16 scores are 8 pieces of 16 bytes, piece c at (c ^ (h & 7)),
-    // so that eight consecutive heads touch all 32 banks
-    const uint32_t x_own = saddr(sm + OFF_X) + (uint32_t)h * 128u;
+    // receive slot layout: two halves (positions 0..31, 32..63) that arrive separately; head h's 32
+    // fp16 scores of a half are 4 pieces of 16 bytes at h*64, piece c at (c ^ ((h >> 1) & 3)), so that
+    // eight consecutive heads touch all 32 banks
+    const uint32_t x_own = saddr(sm + OFF_X) + (uint32_t)h * 64u;
     const uint32_t xfree_peer = map_rank(saddr(x_free), peer);
-    const uint32_t swz = (uint32_t)(h & 7);
+    const uint32_t stgfree_peer = map_rank(saddr(stg_free), peer);
+    const uint32_t swz = (uint32_t)((h >> 1) & 3);
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int P = 0; P < n_pairs && ok; ++P) {
@@ -502,31 +508,38 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       const uint32_t par = (P >> 1) & 1;
       const int st0 = 2 * (P % NPAIR);
       const uint32_t cpar = (P / NPAIR) & 1;
-      if (h == 0) mbar_arrive_expect_tx(&x_full[s], XSLOT_BYTES);
+      if (h == 0) {
+        mbar_arrive_expect_tx(&x_full[2 * s], XHALF_BYTES);
+        mbar_arrive_expect_tx(&x_full[2 * s + 1], XHALF_BYTES);
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s], par, abort_flag, p.status));
       // the validity bits were written by the producers before they released the two tiles
       ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[st0], cpar, abort_flag, p.status));
       ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[st0 + 1], cpar, abort_flag, p.status));
       if (!ok) break;
       fence_after();
-      uint32_t sr[64];
-      tm_ld32(tmem + lane_off + TM_S0 + s * 64, sr);
-      tm_ld32(tmem + lane_off + TM_S0 + s * 64 + 32, sr + 32);
-      tm_wait_ld();
-      // the other CTA's fp16 partial scores of the same pair
-      ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_full[s], par, abort_flag, p.status));
-      if (!ok) break;
-      const uint32_t xo = x_own + (uint32_t)s * XSLOT_BYTES;
       const uint32_t* m0 = mask_s + st0 * 4;
       const uint32_t* m1 = mask_s + (st0 + 1) * 4;
       const uint64_t mask = (uint64_t)(m0[0] | m0[1] | m0[2] | m0[3]) | ((uint64_t)(m1[0] | m1[1] | m1[2] | m1[3]) << 32);
-      // S = this CTA's partial (fp32) + the other's (fp16), in log2 units.  The mask is the same for
-      // the whole CTA, so the branch is uniform; a pair without padding skips the per-position select.
+      // S = this CTA's partial (fp32, TMEM) + the other's (fp16, receive slot), in log2 units, and in the
+      // same pass p = 2^(S - m_ref) against the current reference max (lazy max: the reference moves only
+      // when a head's max grows by more than 2^RESCALE_LOG2, and then the pass runs again from TMEM and
+      // the slot, which stay intact until P is published and the slot released).  The two halves of the
+      // pair (positions 0..31, 32..63) are processed as they land.  The mask is the same for the whole
+      // CTA, so the branch is uniform; a pair without padding skips the per-position select.  Masked
+      // positions (-inf) give exact zeros.  The sum is taken over the fp32 values (their bf16 rounding
+      // in P is unbiased and below the output tolerance).
       const bool full = mask == ~0ull;
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (full) {
+      float psum[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[32];
+      auto half_pass = [&](const int half, const bool masked, const float mo) {
+        uint32_t sr[32];
+        tm_ld32(tmem + lane_off + TM_S0 + s * 64 + half * 32, sr);
+        tm_wait_ld();
+        const uint32_t xo = x_own + (uint32_t)s * XSLOT_BYTES + (uint32_t)half * XHALF_BYTES;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
           uint32_t px[4];
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(px[0]), "=r"(px[1]), "=r"(px[2]), "=r"(px[3])
@@ -534,38 +547,31 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
                        : "memory");
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int j = 8 * c + 2 * i;
+            const int j = 8 * c + 2 * i;   // within the half
             const float2 o = f16x2_to_f32(px[i]);
-            const float v0 = fmaf(__uint_as_float(sr[j]), p.sl2, o.x);
-            const float v1 = fmaf(__uint_as_float(sr[j + 1]), p.sl2, o.y);
-            sr[j] = __float_as_uint(v0);
-            sr[j + 1] = __float_as_uint(v1);
+            float v0 = fmaf(__uint_as_float(sr[j]), p.sl2, o.x);
+            float v1 = fmaf(__uint_as_float(sr[j + 1]), p.sl2, o.y);
+            if (masked) {
+              v0 = ((mask >> (32 * half + j)) & 1ull) ? v0 : -INFINITY;
+              v1 = ((mask >> (32 * half + j + 1)) & 1ull) ? v1 : -INFINITY;
+            }
             mx[i] = fmaxf(mx[i], fmaxf(v0, v1));
+            const float e0 = ex2(v0 - mo), e1 = ex2(v1 - mo);
+            pk[16 * half + (j >> 1)] = pack_bf16(e0, e1);
+            psum[i] += e0 + e1;
           }
         }
-      } else {
+      };
+      const float mo0 = m_ref == -INFINITY ? 0.f : m_ref;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t px[4];
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(px[0]), "=r"(px[1]), "=r"(px[2]), "=r"(px[3])
-                       : "r"(xo + ((c ^ swz) << 4))
-                       : "memory");
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j = 8 * c + 2 * i;
-            const float2 o = f16x2_to_f32(px[i]);
-            const float v0 = ((mask >> j) & 1ull) ? fmaf(__uint_as_float(sr[j]), p.sl2, o.x) : -INFINITY;
-            const float v1 = ((mask >> (j + 1)) & 1ull) ? fmaf(__uint_as_float(sr[j + 1]), p.sl2, o.y) : -INFINITY;
-            sr[j] = __float_as_uint(v0);
-            sr[j + 1] = __float_as_uint(v1);
-            mx[i] = fmaxf(mx[i], fmaxf(v0, v1));
-          }
-        }
+      for (int half = 0; half < 2; ++half) {
+        ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_full[2 * s + half], par, abort_flag, p.status));
+        if (!ok) break;
+        if (half == 1 && h == 0) mbar_arrive_remote(stgfree_peer);   // the other CTA may restage
+        if (full) half_pass(half, false, mo0);
+        else half_pass(half, true, mo0);
       }
-      // slot s may be written again (pair P+2) once all four warps have consumed it
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(xfree_peer + (uint32_t)s * 8u);
+      if (!ok) break;
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       if (mt > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mt > -INFINITY)) {
         // new reference max for this head; rescale what O already holds
@@ -587,21 +593,20 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
           tm_wait_st();
         }
         m_ref = mt;
-      }
-      // p = 2^(s - m_ref); a masked -inf gives 0, and a head with no valid position so far
-      // (m_ref = -inf, every s = -inf) uses offset 0
-      const float mo = m_ref == -INFINITY ? 0.f : m_ref;
-      uint32_t pk[32];
-      float psum[4] = {0.f, 0.f, 0.f, 0.f};
-      // masked positions (-inf) give exact zeros; the sum is taken over the fp32 values (their bf16
-      // rounding in P is unbiased and below the tolerance of the output)
+        // this pair's exponentials again, against the new reference
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float a = ex2(__uint_as_float(sr[2 * j]) - mo);
-        const float c = ex2(__uint_as_float(sr[2 * j + 1]) - mo);
-        pk[j] = pack_bf16(a, c);
-        psum[j & 3] += a + c;
+        for (int i = 0; i < 4; ++i) psum[i] = 0.f;
+        if (full) {
+          half_pass(0, false, m_ref);
+          half_pass(1, false, m_ref);
+        } else {
+          half_pass(0, true, m_ref);
+          half_pass(1, true, m_ref);
+        }
       }
+      // slot s may be written again (pair P+2) once all four warps have consumed it
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(xfree_peer + (uint32_t)s * 8u);
       l += (psum[0] + psum[1]) + (psum[2] + psum[3]);
       // P overwrites the scores: the senders must have read them
       ok = __all_sync(0xffffffffu, mbar_wait(&s_read[s], par, abort_flag, p.status));
@@ -697,14 +702,20 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   } else if (warp < SEND_WARP + 4) {
     // ------------------------------------------------ senders: thread = head of TMEM quadrant warp % 4
     // Each reads the partial scores of its head, scales them to log2 units, rounds them to fp16 and
-    // stages them in its row of the staging slot; lane 0 of each warp then copies the warp's 32 rows
-    // (4 KB) into the other CTA's receive slot with one bulk copy, completing bytes on its x_full.
+    // stages them in its rows of the staging slot (same layout as a receive slot); lane 0 of each warp
+    // then copies the warp's 32 rows of each half (2 KB) into the other CTA's receive slot with one bulk
+    // copy per half, completing bytes on that half's x_full, so that the first half is on its way
+    // while the second is converted.  The staging slot is rewritten only after the other CTA reported
+    // that the previous pair landed (stg_free): a shared-to-cluster bulk copy has no completion
+    // this CTA can wait on.
     const int h = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t x_peer0 = map_rank(saddr(sm + OFF_X), peer);
     const uint32_t xfull_peer = map_rank(saddr(x_full), peer);
-    const uint32_t stg_row = saddr(sm + OFF_STG) + (uint32_t)h * 128u;   // one staging slot
-    const uint32_t swz = (uint32_t)(h & 7);
+    const uint32_t stg0 = saddr(sm + OFF_STG);
+    const uint32_t stg_row = stg0 + (uint32_t)h * 64u;
+    const uint32_t swz = (uint32_t)((h >> 1) & 3);
+    const uint32_t off = (uint32_t)(warp & 3) * 32u * 64u;   // this warp's rows within a half
     bool ok = true;
     for (int P = 0; P < n_pairs && ok; ++P) {
       const int s = P & 1;
@@ -718,38 +729,40 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       tm_wait_ld();
       fence_before();
       mbar_arrive(&s_read[s]);
-      uint32_t hx[32];
+      // the other CTA received pair P-1 (so its copies have read the staging slot)
+      if (P >= 1) ok = __all_sync(0xffffffffu, mbar_wait_cl(stg_free, (P - 1) & 1, abort_flag, p.status));
+      if (!ok) break;
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        hx[j] = pack_f16_sat(__uint_as_float(sr[2 * j]) * p.sl2, __uint_as_float(sr[2 * j + 1]) * p.sl2);
-      // this warp's 32 rows of the staging slot (4 KB): lane 0's copy of pair P-1 has read them
-      if (P >= 1) {
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      for (int half = 0; half < 2; ++half) {
+        uint32_t hx[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          hx[j] = pack_f16_sat(__uint_as_float(sr[32 * half + 2 * j]) * p.sl2,
+                               __uint_as_float(sr[32 * half + 2 * j + 1]) * p.sl2);
+        const uint32_t row = stg_row + (uint32_t)half * XHALF_BYTES;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c ^ swz) << 4)),
+                       "r"(hx[4 * c]), "r"(hx[4 * c + 1]), "r"(hx[4 * c + 2]), "r"(hx[4 * c + 3])
+                       : "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the bulk copy
+        // the other CTA has consumed what was sent into its slot s two pairs ago
+        if (half == 0 && P >= 2)
+          ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_free[s], ((P - 2) >> 1) & 1, abort_flag, p.status));
+        else
+          __syncwarp();
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t ho = (uint32_t)s * XSLOT_BYTES + (uint32_t)half * XHALF_BYTES + off;
+          asm volatile(
+              "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+              ::"r"(x_peer0 + ho), "r"(stg0 + (uint32_t)half * XHALF_BYTES + off), "r"(32 * 64),
+              "r"(xfull_peer + (uint32_t)(2 * s + half) * 8u)
+              : "memory");
+        }
         __syncwarp();
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg_row + ((c ^ swz) << 4)),
-                     "r"(hx[4 * c]), "r"(hx[4 * c + 1]), "r"(hx[4 * c + 2]), "r"(hx[4 * c + 3])
-                     : "memory");
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the bulk copy
-      // the other CTA has consumed what was sent into its slot s two pairs ago
-      if (P >= 2) ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_free[s], ((P - 2) >> 1) & 1, abort_flag, p.status));
-      else __syncwarp();
-      if (!ok) break;
-      if (lane == 0) {
-        const uint32_t off = (uint32_t)(warp & 3) * 32u * 128u;   // this warp's rows
-        asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                     ::"r"(x_peer0 + (uint32_t)s * XSLOT_BYTES + off), "r"(saddr(sm + OFF_STG) + off), "r"(32 * 128),
-                     "r"(xfull_peer + (uint32_t)s * 8u)
-                     : "memory");
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-      }
-      __syncwarp();
     }
-    if (lane == 0)   // this warp's staged bytes have been read before the CTA exits
-      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-    __syncwarp();
   } else if (warp < PROD_WARP + N_PROD) {
     // ------------------------------------------------ producers
     // Producer pw gathers the 4-row groups g = pw and g = pw + 4 of every
