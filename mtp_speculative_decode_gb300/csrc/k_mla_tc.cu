@@ -768,7 +768,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     // Producer pw gathers the 4-row groups g = pw and g = pw + 4 of every
     // 32-row tile: lane l (< 8) owns position 4*g + (l & 3) of group
     // g = pw + 4*(l >> 2); the other lanes mirror lanes 0..7.  The selection
-    // entries of the next tile are loaded one iteration ahead.
+    // entries are loaded PF tiles ahead (a register queue), so that the second
+    // tile of a pair issues right after the first instead of waiting for an L2 load.
     const int pw = warp - PROD_WARP;
     const int ln = lane & 7;
     const int my_pos = 4 * (pw + 4 * (ln >> 2)) + (ln & 3);
@@ -784,17 +785,23 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     // raw selected entry of position j (or a clamped dummy when j is an appended / past-the-split position)
     auto raw = [&](int64_t j) -> int32_t { return p.n_idx > 0 ? idx_row[min(j, (int64_t)p.n_idx - 1)] : 0; };
     // the first entries and the row's visible limit are loaded while the warp looks up the request
-    int32_t nraw = n_tiles > 0 ? raw(j0 + my_pos) : 0;
+    constexpr int PF = 4;
+    int32_t rq[PF];
+#pragma unroll
+    for (int i = 0; i < PF; ++i) rq[i] = i < n_tiles ? raw(j0 + (int64_t)i * NT + my_pos) : 0;
     const int64_t limit = p.row_pos[r] + p.row_pos_add;
+    const int64_t abase = p.n_append > 0 ? p.append_base[r] + 1 : 0;   // first appended position
     const int64_t base = p.cache_start[request_of_row_warp(p.row_offsets, p.B, (uint32_t)r)];
     int issued = 0;
     for (int t = 0; t < n_tiles; ++t) {
-      const int32_t craw = nraw;
-      if (t + 1 < n_tiles) nraw = raw(j0 + (int64_t)(t + 1) * NT + my_pos);   // prefetch
+      const int32_t craw = rq[0];
+#pragma unroll
+      for (int i = 0; i + 1 < PF; ++i) rq[i] = rq[i + 1];
+      rq[PF - 1] = t + PF < n_tiles ? raw(j0 + (int64_t)(t + PF) * NT + my_pos) : 0;
       const int st = t % NSTAGE, P = t >> 1, q = P % NPAIR, R = P / NPAIR;
       if (R > 0 && !__all_sync(0xffffffffu, mbar_wait(&c_empty[q], (R - 1) & 1, abort_flag, p.status))) break;
       const int64_t j = j0 + (int64_t)t * NT + my_pos;
-      const int64_t e = j >= j1 ? -2 : (j < p.n_idx ? (int64_t)craw : p.append_base[r] + 1 + (j - p.n_idx));
+      const int64_t e = j >= j1 ? -2 : (j < p.n_idx ? (int64_t)craw : abase + (j - p.n_idx));
       const int64_t row = entry_row(p, e, base, limit);
       const bool valid = row >= 0 && lane < 8;
       const uint32_t bits = __reduce_or_sync(0xffffffffu, valid ? (1u << my_pos) : 0u);
