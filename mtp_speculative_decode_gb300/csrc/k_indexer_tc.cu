@@ -194,14 +194,10 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 // (group, tile) cursor over the flattened work list
 struct Cursor {
   int g, tile;
+  // called by all 32 lanes of a warp: the last g with g_tile0[g] <= it (which skips groups without
+  // tiles), found with rounds of 32 parallel loads
   __device__ void start(const Params& p, int n_groups, int it) {
-    int lo = 0, hi = n_groups;   // last g with g_tile0[g] <= it
-    while (hi - lo > 1) {
-      int mid = (lo + hi) >> 1;
-      if (p.g_tile0[mid] <= it) lo = mid; else hi = mid;
-    }
-    g = lo;
-    while (g + 1 < n_groups && p.g_tile0[g + 1] <= it) ++g;   // skip groups without tiles
+    g = request_of_row_warp((const uint32_t*)p.g_tile0, n_groups, (uint32_t)it);
     tile = it - p.g_tile0[g];
   }
   __device__ void next(const Params& p, int n_groups) {
@@ -302,8 +298,6 @@ template <int H>
 __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                 const __grid_constant__ CUtensorMap tmap_q,
                                                                 Params p) {
-  griddep_wait();                // the previous kernel's writes are visible from here on
-  griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + OFF_BAR);
@@ -322,12 +316,8 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
   int64_t* vis = (int64_t*)(sm + OFF_VIS) + (threadIdx.x >> 5) * MAX_GROUP_ROWS;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_groups = *p.n_groups;
-  const int total = n_groups > 0 ? p.g_tile0[n_groups] : 0;
-  const int it0 = (int)(((int64_t)blockIdx.x * total) / gridDim.x);
-  const int it1 = (int)(((int64_t)(blockIdx.x + 1) * total) / gridDim.x);
-  if (it0 >= it1) return;   // uniform per CTA, before any barrier or TMEM use
-
+  // The set-up below touches no global memory, so it overlaps the previous kernel's tail
+  // (programmatic dependent launch); the plan it wrote is read after griddep_wait().
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&k_full[i], 1);
@@ -349,17 +339,27 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
                  "r"(NSLOT * SLOT_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  if (warp == PRODUCER_WARP && elect_one()) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_k) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_q) : "memory");
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
+  const int n_groups = *p.n_groups;
+  const int total = n_groups > 0 ? p.g_tile0[n_groups] : 0;
+  const int it0 = (int)(((int64_t)blockIdx.x * total) / gridDim.x);
+  const int it1 = (int)(((int64_t)(blockIdx.x + 1) * total) / gridDim.x);
+  if (it0 >= it1) {   // no work: uniform per CTA; the TMEM allocated above is released
+    if (warp == MMA_WARP)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(NSLOT * SLOT_COLS));
+    return;
+  }
 
   if (warp == PRODUCER_WARP) {
-    if (elect_one()) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_k) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_q) : "memory");
-    }
-    __syncwarp();
     int n_load = 0, gq = 0, cur_g = -1;
     int64_t cstart = 0;
     bool ok = true;
