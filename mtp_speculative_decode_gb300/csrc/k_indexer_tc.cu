@@ -62,6 +62,7 @@ constexpr int OFF_BAR = OFF_VIS + EPI_WARPS * MAX_GROUP_ROWS * 8;
 constexpr int N_BARS = 2 * NSTAGE + 2 + 2 * NSLOT + 1;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;         // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
 
@@ -457,9 +458,14 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const int pos_in_tile = quarter * 32 + lane;
     constexpr int rows_per_wg = 64 / H;    // 1 (H = 64) or 2 (H = 32)
-    int n_chunk = 0, cur_g = -1, nrows = 0, row0 = 0, nch = 0, ks_tile = -1;
+    int n_chunk = 0, cur_g = -1, nrows = 0, row0 = 0, nch = 0, kq_tile = -1;
     int64_t vmax = 0, cstart = 0;
-    float ks_next = 0.f;
+    // key scales of this lane's position in the next KQ tiles of the group (loaded KQ tiles ahead:
+    // one tile of work is shorter than a DRAM round trip)
+    constexpr int KQ = 4;
+    float kq[KQ];
+#pragma unroll
+    for (int i = 0; i < KQ; ++i) kq[i] = 0.f;
     bool ok = true;
     Cursor c;
     c.start(p, n_groups, it0);
@@ -488,19 +494,23 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
         for (int i = lane; i < nrows; i += 32) vis[i] = min(p.row_pos[row0 + i] + 1, p.max_visible);
         __syncwarp();
         cur_g = g;
-        ks_tile = -1;
+        kq_tile = -1;
       }
-      // this position's key scale; the next tile's (same group) is loaded a tile ahead
+      // this position's key scale (0 past the group's visible length)
       auto load_ks = [&](int tile) -> float {
         const int64_t ss = (int64_t)tile * TILE_M + pos_in_tile;
         const int64_t pr = cstart + ss;
         return (ss < vmax && pr >= 0 && pr < p.pool) ? p.k_scale[pr] : 0.f;
       };
-      const float ks = ks_tile == c.tile ? ks_next : load_ks(c.tile);
-      if ((int64_t)(c.tile + 1) * TILE_M < vmax) {
-        ks_next = load_ks(c.tile + 1);
-        ks_tile = c.tile + 1;
+      if (kq_tile != c.tile) {   // first tile of the group in this CTA: fill the queue
+#pragma unroll
+        for (int i = 0; i < KQ; ++i) kq[i] = load_ks(c.tile + i);
       }
+      const float ks = kq[0];
+#pragma unroll
+      for (int i = 0; i + 1 < KQ; ++i) kq[i] = kq[i + 1];
+      kq[KQ - 1] = load_ks(c.tile + KQ);
+      kq_tile = c.tile + 1;
       const int64_t s = (int64_t)c.tile * TILE_M + pos_in_tile;
       for (int ch = 0; ch < nch; ++ch) {
         const int slot = n_chunk % NSLOT, sround = n_chunk / NSLOT;

@@ -289,7 +289,9 @@ int launch_topk(const TopkPlan& p, cudaStream_t st) {
   if (p.R == 0) return MTPSD_OK;
   const bool aligned = ((uintptr_t)p.scores % 16) == 0 && (p.ld % 4) == 0;
   if (aligned && p.max_len <= 40960) {
-    const int nth = p.max_len <= 16384 ? 512 : 1024;
+    // 512 threads per row up to 16384 keys, unless there are too few rows to fill the SMs: then
+    // 1024 threads hold fewer keys each and every counting round is shorter
+    const int nth = (p.max_len <= 16384 && p.R > num_sms() / 2) ? 512 : 1024;
     int kpt = (int)((p.max_len + nth - 1) / nth);
     kpt = (kpt + 3) & ~3;
     if (kpt < 4) kpt = 4;
