@@ -172,8 +172,12 @@ __global__ void __launch_bounds__(TOPK_THREADS, 1) topk_kernel(TopkPlan p, int64
 // keys are T's, and below them T grows by bit b when at least k keys are
 // >= T | 2^b (one counting round per bit: a warp reduction, one barrier, and
 // a second warp reduction over the per-warp counts).  The ordered compaction
-// is the same as above.
-template <int KPT, int NTH>
+// is the same as above.  With XT, the row may run past KPT*NTH by at most NTH
+// keys: thread t also holds the tail key at position KPT*NTH + t (so a row of
+// 8198 keys takes 16 keys per thread and a tail of 6, not 20 per thread), and
+// the tail keys, whose positions follow every regular one, are compacted after
+// them.
+template <int KPT, int NTH, bool XT>
 __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
   griddep_wait();                // the previous kernel's writes are visible from here on
   griddep_launch_dependents();
@@ -212,6 +216,9 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
     key[i + 2] = a + i + 2 < V ? float_key(f.z) : 0u;
     key[i + 3] = a + i + 3 < V ? float_key(f.w) : 0u;
   }
+  const int ax = KPT * NTH + threadIdx.x;   // this thread's tail position (XT)
+  const bool xv = XT && ax < V;
+  const uint32_t xkey = xv ? float_key(row[ax]) : 0u;
   // bits shared by every visible key (the sign and most exponent bits of these
   // scores) are T's as well; the search starts below them
   uint32_t kand = ~0u, kor = 0u;
@@ -221,6 +228,10 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
       kand &= key[i];
       kor |= key[i];
     }
+  if (xv) {
+    kand &= xkey;
+    kor |= xkey;
+  }
   kand = __reduce_and_sync(0xffffffffu, kand);
   kor = __reduce_or_sync(0xffffffffu, kor);
   if (lane == 0) {
@@ -240,6 +251,7 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
     unsigned c = 0;
 #pragma unroll
     for (int i = 0; i < KPT; ++i) c += key[i] >= cand ? 1u : 0u;
+    if constexpr (XT) c += xkey >= cand ? 1u : 0u;
     c = __reduce_add_sync(0xffffffffu, c);
     if (lane == 0) wsum[b & 1][wid] = (int)c;
     __syncthreads();   // the other buffer is rewritten only after the next barrier
@@ -251,6 +263,41 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
   for (int i = 0; i < KPT; ++i) {
     n_gt += key[i] > T;
     n_eq += key[i] == T;
+  }
+  if constexpr (XT) {
+    // counts of the regular keys and of the tail keys, each as two 16-bit fields (> T, == T): every
+    // total is below 65536 (at most 40960 keys), so one scan carries both fields without a carry
+    const int xg = xkey > T, xe = xv && xkey == T;
+    const int pr = block_exclusive_scan(n_gt | (n_eq << 16), warp_sums, &total_s);
+    const int tr = total_s;
+    const int px = block_exclusive_scan(xg | (xe << 16), warp_sums, &total_s);
+    const int tx = total_s;
+    const int gt_before = pr & 0xffff, eq_before = pr >> 16, tot_gt = (tr & 0xffff) + (tx & 0xffff);
+    const int tot_eq_r = tr >> 16;
+    const int need_eq = k - tot_gt;   // equal keys taken, lowest positions first: regular ones, then the tail
+    int take_eq = max(0, min(n_eq, need_eq - eq_before));
+    int out_pos = gt_before + min(eq_before, need_eq);
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      bool take = key[i] > T;
+      if (key[i] == T && take_eq > 0) {
+        take = true;
+        --take_eq;
+      }
+      if (take && out_pos < k) {
+        out[out_pos] = a + i;
+        if (outs) outs[out_pos] = key_float(key[i]);
+        ++out_pos;
+      }
+    }
+    const int need_eq_x = max(0, need_eq - tot_eq_r);
+    const int gx_before = px & 0xffff, ex_before = px >> 16;
+    const int x_pos = (tr & 0xffff) + min(tot_eq_r, need_eq) + gx_before + min(ex_before, need_eq_x);
+    if ((xg || (xe && ex_before < need_eq_x)) && x_pos < k) {
+      out[x_pos] = ax;
+      if (outs) outs[x_pos] = key_float(xkey);
+    }
+    return;
   }
   const int gt_before = block_exclusive_scan(n_gt, warp_sums, &total_s);
   const int need_eq = k - total_s;   // equal keys taken, lowest positions first
@@ -272,11 +319,11 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
   }
 }
 
-template <int NTH>
+template <int NTH, bool XT>
 static int launch_topk_reg(const TopkPlan& p, int kpt, cudaStream_t st) {
   switch (kpt) {
 #define MTPSD_TOPK_CASE(K) \
-  case K: launch_k(topk_reg_kernel<K, NTH>, p.R, NTH, 0, st, p); break;
+  case K: launch_k(topk_reg_kernel<K, NTH, XT>, p.R, NTH, 0, st, p); break;
     MTPSD_TOPK_CASE(4) MTPSD_TOPK_CASE(8) MTPSD_TOPK_CASE(12) MTPSD_TOPK_CASE(16) MTPSD_TOPK_CASE(20)
     MTPSD_TOPK_CASE(24) MTPSD_TOPK_CASE(28) MTPSD_TOPK_CASE(32) MTPSD_TOPK_CASE(36) MTPSD_TOPK_CASE(40)
 #undef MTPSD_TOPK_CASE
@@ -292,11 +339,15 @@ int launch_topk(const TopkPlan& p, cudaStream_t st) {
     // 512 threads per row up to 16384 keys, unless there are too few rows to fill the SMs: then
     // 1024 threads hold fewer keys each and every counting round is shorter
     const int nth = (p.max_len <= 16384 && p.R > num_sms() / 2) ? 512 : 1024;
-    int kpt = (int)((p.max_len + nth - 1) / nth);
+    // keys per thread in registers (a multiple of 4 for the 16-byte loads), plus one tail key per
+    // thread when that covers the rest of the row
+    const int kdown = (int)(p.max_len / nth) & ~3;
+    const bool xt = kdown >= 4 && p.max_len - (int64_t)kdown * nth <= nth && p.max_len > (int64_t)kdown * nth;
+    int kpt = xt ? kdown : (int)((p.max_len + nth - 1) / nth);
     kpt = (kpt + 3) & ~3;
     if (kpt < 4) kpt = 4;
-    if (nth == 512 && kpt <= 32) return launch_topk_reg<512>(p, kpt, st);
-    if (nth == 1024 && kpt <= 40) return launch_topk_reg<1024>(p, kpt, st);
+    if (nth == 512 && kpt <= 32) return xt ? launch_topk_reg<512, true>(p, kpt, st) : launch_topk_reg<512, false>(p, kpt, st);
+    if (nth == 1024 && kpt <= 40) return xt ? launch_topk_reg<1024, true>(p, kpt, st) : launch_topk_reg<1024, false>(p, kpt, st);
   }
   int64_t cache_keys = p.max_len <= TOPK_SMEM_KEYS ? p.max_len : 0;
   size_t smem = (size_t)cache_keys * sizeof(uint32_t);
