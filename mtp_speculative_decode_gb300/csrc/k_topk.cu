@@ -245,8 +245,60 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
   const uint32_t diff = kand ^ kor;
   const int b0 = diff ? 31 - __clz(diff) : -1;   // highest bit where visible keys differ
   uint32_t T = b0 >= 31 ? 0u : (b0 < 0 ? kand : (kand & (~0u << (b0 + 1))));
+  // Eleven bits at a time while at least eleven are left: a 2048-bin histogram of bits b-10..b of the
+  // keys that share T's bits above b (keys above that prefix are only counted), then the bin where the
+  // count from the top reaches k.  Thread t owns bins BPT*t .. BPT*t+BPT-1.
+  constexpr int BPT = 2048 / NTH;
+  __shared__ int hist[2048];
+  __shared__ int dsel;
+  int bl = b0;
 #pragma unroll 1
-  for (int b = b0; b >= 0; --b) {
+  while (bl >= 10) {
+    const int sh = bl - 10;
+#pragma unroll
+    for (int e = 0; e < BPT; ++e) hist[threadIdx.x * BPT + e] = 0;
+    __syncthreads();
+    const uint32_t preT = bl >= 31 ? 0u : (T >> (bl + 1));
+    int above = 0;
+    auto put = [&](uint32_t kv, bool valid) {
+      if (!valid) return;
+      const uint32_t pre = bl >= 31 ? 0u : (kv >> (bl + 1));
+      if (pre > preT) ++above;
+      else if (pre == preT) atomicAdd(&hist[(kv >> sh) & 2047u], 1);
+    };
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) put(key[i], a + i < V);
+    if constexpr (XT) put(xkey, xv);
+    __syncthreads();
+    int hv[BPT], lsum = 0;
+#pragma unroll
+    for (int e = 0; e < BPT; ++e) {
+      hv[e] = hist[threadIdx.x * BPT + e];
+      lsum += hv[e];
+    }
+    // both fields stay below 65536 (at most 40960 keys): one scan carries the bin counts and the
+    // keys above the prefix
+    const int pk = block_exclusive_scan(lsum | (above << 16), warp_sums, &total_s);
+    const int tot = total_s & 0xffff, A = total_s >> 16;
+    const int U = A + tot - (pk & 0xffff) - lsum;   // keys in the bins above this thread's, and above the prefix
+    if (U < k && k <= U + lsum) {
+      int run = U, d = threadIdx.x * BPT;
+#pragma unroll
+      for (int e = BPT - 1; e >= 0; --e) {
+        run += hv[e];
+        if (run >= k) {
+          d = threadIdx.x * BPT + e;
+          break;
+        }
+      }
+      dsel = d;
+    }
+    __syncthreads();
+    T |= (uint32_t)dsel << sh;
+    bl -= 11;
+  }
+#pragma unroll 1
+  for (int b = bl; b >= 0; --b) {
     const uint32_t cand = T | (1u << b);
     unsigned c = 0;
 #pragma unroll
