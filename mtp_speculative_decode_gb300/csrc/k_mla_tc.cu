@@ -14,11 +14,13 @@
 // Each CTA forms the partial scores of its dims, S_k = Q[:, D_k] C[:, D_k]^T,
 // in TMEM.  Its sender warps scale them to log2 units, round them to fp16
 // and stage them in shared memory; lane 0 of each sender warp then moves the
-// warp's 32 heads (4 KB of a pair's 16 KB) into the other CTA's receive slot
-// with one bulk copy (completing bytes on that CTA's mbarrier).  Its softmax warps add the received half to their
-// own fp32 partial, S = S_own + S_other, and run the softmax for this CTA's
-// 256 value dims.  The two CTAs see the other half rounded differently, so
-// each value half keeps its own running (max, sum); split partials carry one
+// warp's 32 heads into the other CTA's receive slot with one bulk copy per
+// half pair (positions 0..31 and 32..63, 2 KB each), each completing bytes on
+// its own mbarrier of that CTA.  Its softmax warps take each half as it lands:
+// add it to their own fp32 partial, S = S_own + S_other, and exponentiate
+// against the current reference max in the same pass, for this CTA's 256
+// value dims.  The two CTAs see the other half rounded differently, so each
+// value half keeps its own running (max, sum); split partials carry one
 // (max, sum) per half.
 //   TMEM  [  0,128) this CTA's first 256 query dims (A operand, bf16 pairs)
 //         [128,192) [192,256) two partial-score buffers of 64 positions
@@ -30,8 +32,11 @@
 //         K-major B operand of the scores (N = 64 positions) and, for chunks
 //         0..3, the MN-major B operand of O += P V (K = positions, N = 256);
 //         two receive slots for the other CTA's fp16 partial scores and one
-//         staging slot for this CTA's (16 KB each: row = head, 64 positions
-//         in 128 bytes, 16-byte piece c at (c ^ (head & 7))).
+//         staging slot for this CTA's (16 KB each: two halves of 8 KB, each
+//         row = head with 32 positions in 64 bytes, 16-byte piece c at
+//         (c ^ ((head >> 1) & 3))).  After the last pair the drained ring
+//         stages O as 128-byte-swizzled boxes of 32 heads for TMA stores (bf16
+//         output, or float32 split partials).
 // Per pair: QK^T is 16 MMAs with A from TMEM (+4 with A from shared memory on
 // rank 0), M=128, N=64, K=16; PV is 4 MMAs (M=128, N=256, K=16) with A = P
 // from TMEM.  The MMA warp issues, in this fixed order, QK(P+1) (its buffer
@@ -39,15 +44,18 @@
 // published P, and sleeps in its waits: a polling or a blocked issue there
 // takes issue slots and memory-instruction slots from the softmax warp that
 // shares its scheduler.  The softmax (thread = head) applies a lazy max: O
-// is rescaled only when a head's max grows by more than 2^8.
+// is rescaled, and the pair's exponentials taken again, only when a head's
+// max grows by more than 2^8.
 //
 // Roles (416 threads): warps 0-3 softmax/epilogue (TMEM lanes = heads);
 // warps 4-7 send the partial scores (thread = head of TMEM quadrant warp%4).
 // Per-thread DSMEM stores (st.async) drain at about 13 bytes per cycle per
 // SM and hold up the memory instructions of every warp on the issuing
-// scheduler, so the senders only stage and one bulk copy per warp and pair
-// crosses to the other SM; a warp rewrites its staging rows only after its
-// previous copy has read them.  Warps 8-11 produce: each turns its 8 positions of every
+// scheduler, so the senders only stage and bulk copies cross to the other SM.
+// A shared-to-cluster bulk copy completes only on the receiver's mbarrier, so
+// the receiver's first softmax thread reports each landed pair back (a relaxed
+// remote arrival on stg_free) and the senders restage only after it.  Warps
+// 8-11 produce, with the selection entries queued four tiles ahead: each turns its 8 positions of every
 // 32-row tile into pool rows and gathers this CTA's chunks of them with TMA
 // tile::gather4 loads (4 rows x 64 dims per instruction; invalid positions
 // read as zeros through an out-of-range row); the first also loads rank 0's
