@@ -101,3 +101,16 @@ def test_workspace_queries(native):
     assert lib.mtpsd_scores_ld(8198) % 4 == 0 and lib.mtpsd_scores_ld(8198) >= 8198
     ws = lib.mtpsd_indexer_topk_workspace_size(32, 192, 8198, 2048)
     assert ws >= 192 * 8198 * 4
+
+
+def test_launch_count_queries(native):
+    """The launch-count queries answer on any machine (without a device they describe the portable
+    kernels): nothing for an empty call, one or two launches otherwise."""
+    lib = native.lib()
+    assert lib.mtpsd_sparse_mla_launch_count(0, 128, 2048, 0, native.MTPSD_BF16) == 0
+    for R, n_append in ((192, 0), (32, 3), (1, 0)):
+        assert lib.mtpsd_sparse_mla_launch_count(R, 128, 2048, n_append, native.MTPSD_BF16) in (1, 2)
+        assert lib.mtpsd_sparse_mla_launch_count(R, 128, 2048, n_append, native.MTPSD_F32) in (1, 2)
+    assert lib.mtpsd_indexer_topk_launch_count(64, 128, native.MTPSD_FP8_E4M3) in (2, 3)
+    assert lib.mtpsd_indexer_topk_launch_count(64, 128, native.MTPSD_F32) == 2
+    assert lib.mtpsd_indexer_topk_launch_count(48, 128, native.MTPSD_FP8_E4M3) == 2   # no tensor-core shape
