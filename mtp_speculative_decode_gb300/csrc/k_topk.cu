@@ -22,29 +22,32 @@ namespace mtpsd {
 constexpr int TOPK_THREADS = 1024;
 constexpr int TOPK_SMEM_KEYS = 48 * 1024;   // 192 KB of keys
 
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+// Exclusive prefix sum over the block (T = int, or uint32_t for the packed two-field counts below,
+// whose upper field may reach bit 31: unsigned addition carries no sign).
+template <typename T>
+__device__ __forceinline__ T block_exclusive_scan(T v, T* warp_sums, T* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int x = v;
+  T x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
+    T y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) warp_sums[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    int w = (lane < nw) ? warp_sums[lane] : 0;
-    int incl = w;
+    T w = (lane < nw) ? warp_sums[lane] : T(0);
+    T incl = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, incl, o);
+      T y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
     warp_sums[lane] = incl - w;
     if (lane == 31) *total = incl;
   }
   __syncthreads();
-  int res = warp_sums[wid] + x - v;
+  T res = warp_sums[wid] + x - v;
   __syncthreads();
   return res;
 }
@@ -184,6 +187,8 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
   __shared__ int wsum[2][32];
   __shared__ int warp_sums[32];
   __shared__ int total_s;
+  __shared__ uint32_t uwarp_sums[32];
+  __shared__ uint32_t utotal_s;
   const int r = blockIdx.x;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   constexpr int NW = NTH / 32;
@@ -276,11 +281,11 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
       hv[e] = hist[threadIdx.x * BPT + e];
       lsum += hv[e];
     }
-    // both fields stay below 65536 (at most 40960 keys): one scan carries the bin counts and the
-    // keys above the prefix
-    const int pk = block_exclusive_scan(lsum | (above << 16), warp_sums, &total_s);
-    const int tot = total_s & 0xffff, A = total_s >> 16;
-    const int U = A + tot - (pk & 0xffff) - lsum;   // keys in the bins above this thread's, and above the prefix
+    // both fields stay below 65536 (at most 40960 keys): one unsigned scan carries the bin counts in
+    // the low half and the keys above the prefix in the high half
+    const uint32_t pk = block_exclusive_scan<uint32_t>((uint32_t)lsum | ((uint32_t)above << 16), uwarp_sums, &utotal_s);
+    const int tot = (int)(utotal_s & 0xffffu), A = (int)(utotal_s >> 16);
+    const int U = A + tot - (int)(pk & 0xffffu) - lsum;   // keys in the bins above this thread's, and above the prefix
     if (U < k && k <= U + lsum) {
       int run = U, d = threadIdx.x * BPT;
 #pragma unroll
@@ -317,15 +322,17 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
     n_eq += key[i] == T;
   }
   if constexpr (XT) {
-    // counts of the regular keys and of the tail keys, each as two 16-bit fields (> T, == T): every
-    // total is below 65536 (at most 40960 keys), so one scan carries both fields without a carry
+    // counts of the regular keys and of the tail keys, each as two 16-bit fields (> T, == T) of an
+    // unsigned word: every total is below 65536 (at most 40960 keys), so one scan carries both fields
+    // without a carry, and the upper field may use bit 31 (32768 or more equal keys)
     const int xg = xkey > T, xe = xv && xkey == T;
-    const int pr = block_exclusive_scan(n_gt | (n_eq << 16), warp_sums, &total_s);
-    const int tr = total_s;
-    const int px = block_exclusive_scan(xg | (xe << 16), warp_sums, &total_s);
-    const int tx = total_s;
-    const int gt_before = pr & 0xffff, eq_before = pr >> 16, tot_gt = (tr & 0xffff) + (tx & 0xffff);
-    const int tot_eq_r = tr >> 16;
+    const uint32_t pr = block_exclusive_scan<uint32_t>((uint32_t)n_gt | ((uint32_t)n_eq << 16), uwarp_sums, &utotal_s);
+    const uint32_t tr = utotal_s;
+    const uint32_t px = block_exclusive_scan<uint32_t>((uint32_t)xg | ((uint32_t)xe << 16), uwarp_sums, &utotal_s);
+    const uint32_t tx = utotal_s;
+    const int gt_before = (int)(pr & 0xffffu), eq_before = (int)(pr >> 16);
+    const int tot_gt = (int)(tr & 0xffffu) + (int)(tx & 0xffffu);
+    const int tot_eq_r = (int)(tr >> 16);
     const int need_eq = k - tot_gt;   // equal keys taken, lowest positions first: regular ones, then the tail
     int take_eq = max(0, min(n_eq, need_eq - eq_before));
     int out_pos = gt_before + min(eq_before, need_eq);
@@ -343,8 +350,8 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
       }
     }
     const int need_eq_x = max(0, need_eq - tot_eq_r);
-    const int gx_before = px & 0xffff, ex_before = px >> 16;
-    const int x_pos = (tr & 0xffff) + min(tot_eq_r, need_eq) + gx_before + min(ex_before, need_eq_x);
+    const int gx_before = (int)(px & 0xffffu), ex_before = (int)(px >> 16);
+    const int x_pos = (int)(tr & 0xffffu) + min(tot_eq_r, need_eq) + gx_before + min(ex_before, need_eq_x);
     if ((xg || (xe && ex_before < need_eq_x)) && x_pos < k) {
       out[x_pos] = ax;
       if (outs) outs[x_pos] = key_float(xkey);

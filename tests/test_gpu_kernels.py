@@ -156,7 +156,9 @@ def test_share_gather(mt):
 
 @pytest.mark.parametrize("V,k,ties", [(10, 32, False), (32, 32, False), (33, 32, True), (5000, 2048, False),
                                       (8198, 2048, True), (60000, 2048, False), (70000, 2048, True),
-                                      (3000, 1, True), (4096, 4096, False), (9000, 4096, True)])
+                                      (3000, 1, True), (4096, 4096, False), (9000, 4096, True),
+                                      # one tail key per thread at 1024 threads, 32768+ equal keys in a row
+                                      (33000, 2048, True), (37000, 2048, True), (33000, 2048, False)])
 def test_topk_exact(mt, V, k, ties):
     rng = np.random.default_rng(V + k)
     R = 7
