@@ -131,7 +131,11 @@ typedef struct {
 
 /* Row stride (floats) of the score matrix for a given max_visible. */
 int64_t mtpsd_scores_ld(int64_t max_visible);
+/* Workspace bytes of mtpsd_indexer_topk: the score matrix (R x mtpsd_scores_ld(max_visible) floats,
+ * 256-byte padded) followed by the work plan.  When args->scores is given (16-byte aligned) the scores
+ * go there and the workspace needs only mtpsd_indexer_topk_plan_bytes(B, R). */
 size_t mtpsd_indexer_topk_workspace_size(int32_t B, int32_t R, int64_t max_visible, int32_t topk);
+size_t mtpsd_indexer_topk_plan_bytes(int32_t B, int32_t R);
 int mtpsd_indexer_topk(const mtpsd_indexer_args* args, void* stream);
 /* Kernel launches one mtpsd_indexer_topk call with R > 0 makes on the current device: 3 on the
  * tensor-core path (group plan, FP8 score GEMM, top-k: MTPSD_FP8_E4M3, head_dim 128, 32 or 64 heads,
@@ -152,7 +156,9 @@ int32_t mtpsd_indexer_topk_launch_count(int32_t n_heads, int32_t head_dim, int32
  * process exits.  The caller still passes every input and output.
  * - A call needing more than MTPSD_NOALLOC_SCRATCH_BYTES of scratch
  *   (mtpsd_indexer_topk_workspace_size(B, R, max_visible, topk), about
- *   R * max_visible * 4 bytes) returns MTPSD_EWORKSPACE before any launch.
+ *   R * max_visible * 4 bytes; only mtpsd_indexer_topk_plan_bytes(B, R) when
+ *   args->scores is given, since the scores then go to the caller's buffer)
+ *   returns MTPSD_EWORKSPACE before any launch.
  * - The first call on a device (the current device) looks up the array's
  *   device address; make that first call before any stream capture.
  * - All calls share the one array, which keeps the last call's contents
@@ -276,6 +282,21 @@ int mtpsd_kv_writeback(const void* src_latent, const uint8_t* src_idxk, const fl
 int mtpsd_topk_share_gather(const int32_t* step0_topk, const uint32_t* row_offsets,
                             const int32_t* num_accepted, int32_t B, int32_t k, int32_t* shared_idx,
                             int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Check of the device-side bounded wait (the source pages have no
+ * counterpart: it makes the library's failure path testable without a fault).
+ * Every tensor-core kernel waits on its mbarrier phases through one helper
+ * that gives up after a limit (2 s in the kernels), flags
+ * MTPSD_STATUS_WAIT_TIMEOUT, lets the kernel release what it holds and return.
+ * This call launches one small kernel in which two warps wait, with that
+ * helper (CTA-scope and cluster-scope acquire), on a barrier phase that
+ * nothing completes, with the given limit (1 ns .. 1 s).  Afterwards
+ * *dev_status has MTPSD_STATUS_WAIT_TIMEOUT set and result [4] int64 (device)
+ * holds, per warp, the nanoseconds waited and 1 if the wait succeeded (0:
+ * it gave up, as it must).  The device stays usable.
+ */
+int mtpsd_check_bounded_wait(int64_t limit_ns, int32_t* dev_status, int64_t* result, void* stream);
 
 /* ------------------------------------------------------------------------ */
 const char* mtpsd_last_error(void);

@@ -60,6 +60,7 @@ SIGNATURES = {
     "mtpsd_quantize_fp8_block128": (C.c_int, [vp, i64, vp, vp, vp]),
     "mtpsd_scores_ld": (i64, [i64]),
     "mtpsd_indexer_topk_workspace_size": (C.c_size_t, [i32, i32, i64, i32]),
+    "mtpsd_indexer_topk_plan_bytes": (C.c_size_t, [i32, i32]),
     "mtpsd_indexer_topk": (C.c_int, [C.POINTER(IndexerArgs), vp]),
     "mtpsd_indexer_topk_noalloc": (C.c_int, [C.POINTER(IndexerArgs), vp]),
     "mtpsd_topk_workspace_size": (C.c_size_t, [i32, i32]),
@@ -71,6 +72,7 @@ SIGNATURES = {
     "mtpsd_accept_greedy": (C.c_int, [vp, vp, i32, i32, i64, vp, vp, vp]),
     "mtpsd_kv_writeback": (C.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp]),
     "mtpsd_topk_share_gather": (C.c_int, [vp, vp, vp, i32, i32, vp, vp, vp]),
+    "mtpsd_check_bounded_wait": (C.c_int, [i64, vp, vp, vp]),
     "mtpsd_last_error": (C.c_char_p, []),
     "mtpsd_version": (i32, []),
 }

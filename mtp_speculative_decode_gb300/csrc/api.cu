@@ -68,6 +68,8 @@ int mtpsd_quantize_fp8_block128(const float* x, int64_t n_blocks, uint8_t* codes
 
 int64_t mtpsd_scores_ld(int64_t max_visible) { return (int64_t)align_up((size_t)(max_visible > 0 ? max_visible : 1), 4); }
 
+size_t mtpsd_indexer_topk_plan_bytes(int32_t B, int32_t R) { return (B < 0 || R < 0) ? 0 : indexer_tc_plan_bytes(B, R); }
+
 size_t mtpsd_indexer_topk_workspace_size(int32_t B, int32_t R, int64_t max_visible, int32_t topk) {
   (void)topk;
   size_t scores = (size_t)R * (size_t)mtpsd_scores_ld(max_visible) * sizeof(float);
@@ -93,10 +95,13 @@ int mtpsd_indexer_topk(const mtpsd_indexer_args* a, void* stream) {
   if (a->R == 0) return MTPSD_OK;
   if (!a->q || !a->weights || !a->k_cache || !a->cache_start || !a->row_offsets || !a->row_pos || !a->topk_idx)
     return fail(MTPSD_EINVAL, "indexer_topk: null pointer");
-  size_t need = mtpsd_indexer_topk_workspace_size(a->B, a->R, a->max_visible, a->topk);
+  // with a caller score buffer the workspace holds only the work plan, else the scores and then the plan
+  size_t need = a->scores ? indexer_tc_plan_bytes(a->B, a->R)
+                          : mtpsd_indexer_topk_workspace_size(a->B, a->R, a->max_visible, a->topk);
   if (!a->workspace || a->workspace_bytes < need)
     return fail(MTPSD_EWORKSPACE, "indexer_topk: workspace of %zu bytes needed, %zu given", need, a->workspace_bytes);
   if (!aligned(a->workspace, 256)) return fail(MTPSD_EINVAL, "indexer_topk: workspace must be 256-byte aligned");
+  if (a->scores && !aligned(a->scores, 16)) return fail(MTPSD_EINVAL, "indexer_topk: scores must be 16-byte aligned");
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t ld = mtpsd_scores_ld(a->max_visible);
   float* scores = a->scores ? a->scores : (float*)a->workspace;
@@ -105,7 +110,7 @@ int mtpsd_indexer_topk(const mtpsd_indexer_args* a, void* stream) {
   p.q = a->q; p.q_scale = a->q_scale; p.w = a->weights; p.k = a->k_cache; p.k_scale = a->k_scale;
   p.pool = a->pool_tokens; p.cache_start = a->cache_start; p.row_offsets = a->row_offsets; p.row_pos = a->row_pos;
   p.max_visible = a->max_visible; p.scores = scores; p.ld = ld;
-  p.plan_ws = (char*)a->workspace + align_up((size_t)a->R * ld * sizeof(float), 256);
+  p.plan_ws = a->scores ? a->workspace : (void*)((char*)a->workspace + align_up((size_t)a->R * ld * sizeof(float), 256));
   p.status = a->dev_status;
   int rc = indexer_tc_supported(p) ? launch_indexer_scores_tc(p, st) : launch_indexer_scores(p, st);
   if (rc) return rc;
@@ -219,6 +224,14 @@ int mtpsd_topk_share_gather(const int32_t* step0_topk, const uint32_t* row_offse
   if ((k & 3) == 0 && (!aligned(step0_topk, 16) || !aligned(shared_idx, 16)))
     return fail(MTPSD_EINVAL, "topk_share_gather: buffers must be 16-byte aligned when k % 4 == 0");
   return launch_share_gather(step0_topk, row_offsets, num_accepted, B, k, shared_idx, dev_status, (cudaStream_t)stream);
+}
+
+int mtpsd_check_bounded_wait(int64_t limit_ns, int32_t* dev_status, int64_t* result, void* stream) {
+  g_err[0] = 0;
+  if (limit_ns < 1 || limit_ns > 1000000000LL) return fail(MTPSD_EINVAL, "check_bounded_wait: limit_ns must be 1..1e9");
+  if (!dev_status || !result) return fail(MTPSD_EINVAL, "check_bounded_wait: null pointer");
+  if (!aligned(result, 8)) return fail(MTPSD_EINVAL, "check_bounded_wait: result must be 8-byte aligned");
+  return launch_bounded_wait_check(limit_ns, dev_status, result, (cudaStream_t)stream);
 }
 
 }  // extern "C"

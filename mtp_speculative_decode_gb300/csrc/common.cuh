@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/mtpsd.h"
 
 #define MTPSD_HD __host__ __device__ __forceinline__
@@ -81,15 +83,50 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-inline int num_sms() {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
+// Device facts and once-per-device set-up, keyed by the current device ordinal, so a process that
+// drives several GPUs gets each one's own values.  Thread-safe: the caches are atomics, and two threads
+// that race only repeat an idempotent query or attribute call.
+constexpr int kMaxCachedDevices = 64;
+
+inline int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  return dev;
+}
+
+inline int device_attr_cached(std::atomic<int>* cache, cudaDeviceAttr attr, int fallback) {
+  const int dev = current_device();
+  if (dev >= 0 && dev < kMaxCachedDevices) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v) return v;
   }
-  return sms;
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, attr, dev) != cudaSuccess || v <= 0) v = fallback;
+  if (dev >= 0 && dev < kMaxCachedDevices) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+inline int num_sms() {
+  static std::atomic<int> cache[kMaxCachedDevices];
+  return device_attr_cached(cache, cudaDevAttrMultiProcessorCount, 148);
+}
+
+inline int cc_major() {
+  static std::atomic<int> cache[kMaxCachedDevices];
+  return device_attr_cached(cache, cudaDevAttrComputeCapabilityMajor, -1);
+}
+
+// Raises a kernel's dynamic shared-memory limit on the current device, once per device (done: one
+// bit per device ordinal, owned by the caller for that kernel).  False when the call failed.
+template <typename Kernel>
+inline bool set_smem_limit_once(Kernel kernel, int bytes, std::atomic<uint64_t>& done) {
+  const int dev = current_device();
+  const bool cacheable = dev >= 0 && dev < kMaxCachedDevices;
+  const uint64_t bit = cacheable ? (1ull << dev) : 0;
+  if (cacheable && (done.load(std::memory_order_acquire) & bit)) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  if (cacheable) done.fetch_or(bit, std::memory_order_acq_rel);
+  return true;
 }
 
 // Order-preserving map of a float to uint32 (larger float -> larger key).

@@ -38,6 +38,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "mbar.cuh"
 
 namespace mtpsd {
 namespace itc {
@@ -64,7 +65,7 @@ constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;         // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+constexpr unsigned long long WAIT_LIMIT_NS = mbar::DEFAULT_LIMIT_NS;
 
 struct Params {
   const float* q_scale;
@@ -89,12 +90,6 @@ struct Params {
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(bar)), "r"(count));
 }
@@ -104,31 +99,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(bar)) : "memory");
 }
-__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(saddr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait: false when it gave up (time limit or another role aborted).
+// Bounded wait (the shared helper with this kernel's limit): false when it gave up (time limit or
+// another role aborted).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int32_t* status) {
-  if (mbar_try(bar, parity)) return true;
-  uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-        *abort_flag = 1;
-        flag_status(status, MTPSD_STATUS_WAIT_TIMEOUT);
-        return false;
-      }
-    }
-  }
+  return mbar::wait<false>(bar, parity, abort_flag, status, WAIT_LIMIT_NS);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -565,16 +540,7 @@ static bool make_map_rows128(CUtensorMap* map, const void* base, int64_t rows, u
   return make_tma_2d(map, 0, base, 128, (uint64_t)rows, 128, 128, box_rows, true);
 }
 
-static bool tc_device_ok() {
-  static int ok = -1;
-  if (ok < 0) {
-    int dev = 0, major = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    ok = (major == 10) ? 1 : 0;
-  }
-  return ok == 1;
-}
+static bool tc_device_ok() { return cc_major() == 10; }
 
 size_t indexer_tc_plan_bytes(int B, int R) {
   size_t n = (size_t)B + (size_t)R + 2;
@@ -626,11 +592,11 @@ int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {
   kp.row_pos = p.row_pos; kp.pool = p.pool; kp.max_visible = p.max_visible; kp.scores = p.scores; kp.ld = p.ld;
   kp.H = p.H; kp.g_b = g_b; kp.g_row0 = g_row0; kp.g_nrows = g_nrows; kp.g_vmax = g_vmax; kp.g_tile0 = g_tile0;
   kp.n_groups = n_groups; kp.status = p.status;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(indexer_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    cudaFuncSetAttribute(indexer_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    attr = true;
+  static std::atomic<uint64_t> attr64{0}, attr32{0};
+  if (!(p.H == 64 ? set_smem_limit_once(indexer_tc_kernel<64>, SMEM_BYTES, attr64)
+                  : set_smem_limit_once(indexer_tc_kernel<32>, SMEM_BYTES, attr32))) {
+    set_error("indexer_tc: cudaFuncSetAttribute failed");
+    return MTPSD_ECUDA;
   }
   if (p.H == 64)
     launch_k(indexer_tc_kernel<64>, num_sms(), THREADS, SMEM_BYTES, st, mk, mq, kp);

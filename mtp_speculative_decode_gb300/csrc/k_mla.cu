@@ -551,10 +551,10 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
     return MTPSD_OK;
   }
   if (p.dtype == MTPSD_BF16) {
-    static bool attr = false;
-    if (!attr) {
-      cudaFuncSetAttribute(sparse_mla_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MlaSmem::BYTES);
-      attr = true;
+    static std::atomic<uint64_t> attr{0};
+    if (!set_smem_limit_once(sparse_mla_bf16_kernel, MlaSmem::BYTES, attr)) {
+      set_error("sparse_mla_bf16: cudaFuncSetAttribute failed");
+      return MTPSD_ECUDA;
     }
     dim3 grid(p.R, (unsigned)ceil_div(p.H, MLA_HG), sp.n_splits);
     launch_k(sparse_mla_bf16_kernel, grid, 256, MlaSmem::BYTES, st, p, sp, part_o, part_ml);

@@ -72,6 +72,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "mbar.cuh"
 
 namespace mtpsd {
 namespace mtc {
@@ -105,7 +106,7 @@ constexpr int SEND_WARP = 4, PROD_WARP = 8, N_PROD = 4, MMA_WARP = 12;
 constexpr int TM_Q = 0, TM_S0 = 128, TM_O = 256;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+constexpr unsigned long long WAIT_LIMIT_NS = mbar::DEFAULT_LIMIT_NS;
 constexpr int MAX_FUSED_SPLITS_K = 4;     // splits of a row that share one cluster and merge in the kernel
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
@@ -163,37 +164,14 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
 }
 
 __device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ uint64_t gtimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t c) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(c));
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
 }
-__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t par) {
-  uint32_t ok;
-  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-               : "=r"(ok) : "r"(saddr(b)), "r"(par) : "memory");
-  return ok != 0;
-}
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t par, volatile int* abort_flag, int32_t* status) {
-  if (mbar_try(b, par)) return true;
-  uint64_t t0 = gtimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try(b, par)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (gtimer() - t0 > WAIT_LIMIT_NS) {
-        *abort_flag = 1;
-        flag_status(status, MTPSD_STATUS_WAIT_TIMEOUT);
-        return false;
-      }
-    }
-  }
+  return mbar::wait<false>(b, par, abort_flag, status, WAIT_LIMIT_NS);
 }
 // One lane of a converged warp (the lowest), as a warp-uniform branch: the
 // issuing role runs with all 32 lanes so that addresses and descriptors stay
@@ -276,28 +254,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // The same wait with cluster-scope acquire, for barriers whose bytes the other CTA completes.
-__device__ __forceinline__ bool mbar_try_cl(uint64_t* b, uint32_t par) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, "
-      "p;\n}\n"
-      : "=r"(ok) : "r"(saddr(b)), "r"(par) : "memory");
-  return ok != 0;
-}
 __device__ __forceinline__ bool mbar_wait_cl(uint64_t* b, uint32_t par, volatile int* abort_flag, int32_t* status) {
-  if (mbar_try_cl(b, par)) return true;
-  uint64_t t0 = gtimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_cl(b, par)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (gtimer() - t0 > WAIT_LIMIT_NS) {
-        *abort_flag = 1;
-        flag_status(status, MTPSD_STATUS_WAIT_TIMEOUT);
-        return false;
-      }
-    }
-  }
+  return mbar::wait<true>(b, par, abort_flag, status, WAIT_LIMIT_NS);
 }
 // shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
 __device__ __forceinline__ uint32_t map_rank(uint32_t cta_addr, uint32_t rank) {
@@ -929,10 +887,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
 bool mla_tc_supported(const MlaPlan& p) {
   if (p.dtype != MTPSD_BF16 || p.d_latent != 576 || p.d_v != 512) return false;
   if (p.H % mtc::HG != 0) return false;
-  int dev = 0, major = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  if (major != 10) return false;
+  if (cc_major() != 10) return false;
   const char* env = getenv("MTPSD_MLA");
   if (env && env[0] == 'm') return false;   // "mma": the mma.sync kernel
   if (p.pool > 0x7ffffffeLL || (int64_t)p.R * p.H > 0x7fffffffLL) return false;
@@ -961,31 +916,31 @@ cudaLaunchConfig_t mla_tc_config(dim3 grid, int cluster_z, cudaStream_t st, cuda
   return cfg;
 }
 bool mla_tc_prepare() {
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(mtc::sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             mtc::SMEM_BYTES) != cudaSuccess)
-      return false;
-    attr = true;
-  }
-  return true;
+  static std::atomic<uint64_t> attr{0};
+  return set_smem_limit_once(mtc::sparse_mla_tc_kernel, mtc::SMEM_BYTES, attr);
 }
-// CTAs of this kernel that run at once with clusters of 2 x cluster_z CTAs.
+// CTAs of this kernel that run at once with clusters of 2 x cluster_z CTAs (cached per device; -1 in
+// the cache stands for "none fit").
 int mla_tc_resident_ctas(int cluster_z) {
-  static int n[MAX_FUSED_SPLITS + 1] = {0};
-  if (!n[cluster_z]) {
-    int clusters = 0;
-    cudaLaunchAttribute attrs[1];
-    cudaLaunchConfig_t cfg = mla_tc_config(dim3(1, 2, cluster_z), cluster_z, 0, attrs);
-    if (mla_tc_prepare() &&
-        cudaOccupancyMaxActiveClusters(&clusters, (void*)mtc::sparse_mla_tc_kernel, &cfg) == cudaSuccess &&
-        clusters > 0)
-      n[cluster_z] = 2 * cluster_z * clusters;
-    else
-      n[cluster_z] = cluster_z == 1 ? (num_sms() & ~1) : 0;
-    cudaGetLastError();
+  static std::atomic<int> cache[kMaxCachedDevices][MAX_FUSED_SPLITS + 1];
+  const int dev = current_device();
+  const bool cacheable = dev >= 0 && dev < kMaxCachedDevices;
+  if (cacheable) {
+    const int v = cache[dev][cluster_z].load(std::memory_order_relaxed);
+    if (v) return v < 0 ? 0 : v;
   }
-  return n[cluster_z];
+  int n = 0, clusters = 0;
+  cudaLaunchAttribute attrs[1];
+  cudaLaunchConfig_t cfg = mla_tc_config(dim3(1, 2, cluster_z), cluster_z, 0, attrs);
+  if (mla_tc_prepare() &&
+      cudaOccupancyMaxActiveClusters(&clusters, (void*)mtc::sparse_mla_tc_kernel, &cfg) == cudaSuccess &&
+      clusters > 0)
+    n = 2 * cluster_z * clusters;
+  else
+    n = cluster_z == 1 ? (num_sms() & ~1) : 0;
+  cudaGetLastError();
+  if (cacheable) cache[dev][cluster_z].store(n > 0 ? n : -1, std::memory_order_relaxed);
+  return n;
 }
 }  // namespace
 

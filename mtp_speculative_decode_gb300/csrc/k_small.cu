@@ -5,6 +5,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "mbar.cuh"
 
 namespace mtpsd {
 
@@ -185,6 +186,39 @@ int launch_share_gather(const int32_t* s0, const uint32_t* ro, const int32_t* n_
                         int32_t* out, int32_t* status, cudaStream_t st) {
   launch_k(share_gather_kernel, B, 128, 0, st, s0, ro, n_acc, k, out, status);
   return check_launch("topk_share_gather");
+}
+
+// ---------------------------------------------------------------------------
+// Check of the bounded mbarrier wait that every tensor-core kernel uses: warp 0
+// waits at CTA scope and warp 1 at cluster scope on one barrier phase that
+// nothing completes, with the caller's limit.  Each gives up (the first at the
+// limit, the other at the limit or on the abort flag the first set), flags
+// MTPSD_STATUS_WAIT_TIMEOUT and records [waited ns, 1 if the wait succeeded].
+__global__ void bounded_wait_check_kernel(unsigned long long limit_ns, int32_t* status, int64_t* out) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(&bar)));
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t t0 = mbar::globaltimer_ns();
+  const bool ok = warp == 0 ? mbar::wait<false>(&bar, 0, &abort_flag, status, limit_ns)
+                            : mbar::wait<true>(&bar, 0, &abort_flag, status, limit_ns);
+  const uint64_t t1 = mbar::globaltimer_ns();
+  if (lane == 0) {
+    out[2 * warp] = (int64_t)(t1 - t0);
+    out[2 * warp + 1] = ok ? 1 : 0;
+  }
+}
+
+int launch_bounded_wait_check(int64_t limit_ns, int32_t* status, int64_t* out, cudaStream_t st) {
+  launch_k(bounded_wait_check_kernel, 1, 64, 0, st, (unsigned long long)limit_ns, status, out);
+  return check_launch("bounded_wait_check");
 }
 
 }  // namespace mtpsd

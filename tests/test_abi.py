@@ -85,6 +85,9 @@ def test_host_checks_reject_before_launch(native):
     assert lib.mtpsd_kv_writeback(None, None, None, 1, 6, 7, 128, None, None, None, None, None, None, 10, None,
                                   None, None) == native.MTPSD_EUNSUPPORTED
     assert lib.mtpsd_topk(None, 10, 1, None, 20, 4, None, None, None, 0, None, None) == native.MTPSD_EINVAL
+    assert lib.mtpsd_check_bounded_wait(0, 8, 8, None) == native.MTPSD_EINVAL
+    assert lib.mtpsd_check_bounded_wait(2_000_000_000, 8, 8, None) == native.MTPSD_EINVAL
+    assert lib.mtpsd_check_bounded_wait(1000, None, 8, None) == native.MTPSD_EINVAL
 
 
 def test_host_merged_offsets_mirror(native):
@@ -101,6 +104,10 @@ def test_workspace_queries(native):
     assert lib.mtpsd_scores_ld(8198) % 4 == 0 and lib.mtpsd_scores_ld(8198) >= 8198
     ws = lib.mtpsd_indexer_topk_workspace_size(32, 192, 8198, 2048)
     assert ws >= 192 * 8198 * 4
+    plan = lib.mtpsd_indexer_topk_plan_bytes(32, 192)
+    assert 0 < plan < 64 * 1024 and plan % 256 == 0
+    # the workspace is the padded score matrix followed by the plan
+    assert ws == (192 * lib.mtpsd_scores_ld(8198) * 4 + 255) // 256 * 256 + plan
 
 
 def test_launch_count_queries(native):
