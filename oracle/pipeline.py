@@ -88,16 +88,6 @@ class OracleStep:
         acc_len = np.clip(np.asarray(num_accepted) + 1, 1, W)
         return self.w.L + acc_len
 
-    def written_back(self, num_accepted, b: int, pos: int, name: str):
-        """Draft-layer content at position `pos` of request b after the
-        write-back (the source row when pos is inside the accepted segment)."""
-        W = self.spec.K + 1
-        n = int(min(max(num_accepted[b] + 1, 1), W))
-        start = int(self.w.L[b])
-        if start <= pos < start + n:
-            return ("src", pos - start)
-        return ("pool", pos)
-
     def draft_keys(self, num_accepted, b: int, upto: int):
         """Dequantized draft indexer keys of request b after the write-back."""
         base = int(self.w.cache_start[b])

@@ -354,3 +354,99 @@ def test_shared_steps_equal_rerun_when_context_below_k():
                                                         np.array([P + j]), fp8=False)[0], k)
         shared = share.shared_step_positions(s0, P, j)
         assert sorted(shared) == sorted(int(x) for x in rerun if x >= 0)
+
+
+# --------------------------------------------------------------------- k-th score (tie band)
+
+def test_kth_score_hand_worked():
+    s = np.array([3.0, 1.0, 4.0, 1.0, 5.0, 9.0, 2.0, 6.0])
+    # descending: 9 6 5 4 3 2 1 1
+    assert topk.kth_score(s, 1) == 9.0
+    assert topk.kth_score(s, 3) == 5.0
+    assert topk.kth_score(s, 8) == 1.0
+    assert topk.kth_score(s, 20) == 1.0            # fewer than k: the smallest
+    t = np.array([2.0, 2.0, 2.0, 1.0])
+    assert topk.kth_score(t, 2) == 2.0             # ties count once per position
+    assert topk.kth_score(t, 3) == 2.0
+    assert topk.kth_score(t, 4) == 1.0
+    assert topk.kth_score(np.array([-0.5]), 2048) == -0.5
+
+
+def test_kth_score_is_the_score_of_the_last_selected():
+    """The k-th score equals the smallest score topk_select takes (brute
+    force over small rows with ties)."""
+    rng = np.random.default_rng(21)
+    for _ in range(50):
+        V = int(rng.integers(1, 9))
+        k = int(rng.integers(1, 10))
+        sc = rng.integers(-3, 4, V).astype(np.float64)
+        sub = _brute_topk(sc, k)
+        assert topk.kth_score(sc, k) == min(sc[i] for i in sub)
+
+
+# --------------------------------------------------------------------- draft inputs after the write-back
+
+def _marker_step(fp8_keys: bool):
+    """Two requests, contexts L = [5, 7], window W = 4 (K = 3).  Pool row t of
+    the draft layer holds the constant 100 + t in every element; window row i
+    of request b holds -(1 + 10 b + i).  Positions are pool rows minus
+    cache_start = [0, 20]."""
+    import types
+
+    import torch
+    from oracle.pipeline import OracleStep
+    T, D = 40, 128
+    spec = types.SimpleNamespace(K=3, topk=8, latent_f32=not fp8_keys)
+    w = types.SimpleNamespace(spec=spec, L=np.array([5, 7]), cache_start=np.array([0, 20]), tensors={})
+    pool_k = np.repeat((100.0 + np.arange(T))[:, None], D, axis=1).astype(np.float32)
+    pool_l = np.repeat((100.0 + np.arange(T))[:, None], 576, axis=1).astype(np.float32)
+    win = -(1.0 + 10.0 * np.arange(2)[:, None] + np.arange(4)[None, :])          # [B, W]
+    d = {"d_k_idx": torch.from_numpy(pool_k),
+         "src_k_idx": torch.from_numpy(np.repeat(win[:, :, None], D, axis=2).astype(np.float32)),
+         "d_latent": torch.from_numpy(pool_l),
+         "src_latent": torch.from_numpy(np.repeat(win[:, :, None], 576, axis=2).astype(np.float32))}
+    return OracleStep(w, d)
+
+
+def test_next_pos_hand_worked():
+    """The draft step-0 row sits right after the written-back accepted segment
+    (bonus included): P = L + num_accepted + 1."""
+    o = _marker_step(False)
+    assert o.next_pos(np.array([0, 3])).tolist() == [6, 11]
+    assert o.next_pos(np.array([2, 0])).tolist() == [8, 8]
+
+
+def test_draft_keys_overlay_hand_worked():
+    o = _marker_step(False)
+    n_acc = np.array([0, 3])
+    k0 = o.draft_keys(n_acc, 0, 8)[:, 0]
+    # request 0: one accepted row (the bonus) overwrites position 5 only
+    assert k0.tolist() == [100, 101, 102, 103, 104, -1, 106, 107]
+    k1 = o.draft_keys(n_acc, 1, 12)[:, 0]
+    # request 1: positions 7..10 take window rows 0..3; position 11 (= L + n) keeps the pool row
+    assert k1.tolist() == [120, 121, 122, 123, 124, 125, 126, -11, -12, -13, -14, 131]
+    # a visible prefix that ends inside the segment takes only the rows inside it
+    assert o.draft_keys(n_acc, 1, 9)[:, 0].tolist() == [120, 121, 122, 123, 124, 125, 126, -11, -12]
+
+
+def test_draft_keys_requantized_per_token():
+    """With FP8 keys every overlaid row carries its own block-128 scale: a
+    constant row c quantizes to the code of +-448 with scale |c|/448 and so
+    decodes back to c (to float32 rounding of the scale)."""
+    o = _marker_step(True)
+    k1 = o.draft_keys(np.array([0, 3]), 1, 12)
+    want = [120, 121, 122, 123, 124, 125, 126, -11, -12, -13, -14, 131]
+    for row, c in zip(k1, want):
+        assert np.allclose(row, c, rtol=2 ** -23, atol=0)
+
+
+def test_draft_latent_rows_overlay_hand_worked():
+    o = _marker_step(False)
+    n_acc = np.array([1, 0])
+    # request 0: accept length 2 -> positions 5, 6 take window rows 0, 1; 7 keeps the pool row
+    rows = o.draft_latent_rows(n_acc, 0, [0, 4, 5, 6, 7])
+    assert rows[:, 0].tolist() == [100, 104, -1, -2, 107]
+    assert rows.shape == (5, 576) and np.all(rows == rows[:, :1])
+    # request 1: accept length 1 -> only position 7; position 8 is the pool row (pool row 28)
+    rows = o.draft_latent_rows(n_acc, 1, [8, 7, 3])
+    assert rows[:, 0].tolist() == [128, -11, 123]
