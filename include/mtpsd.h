@@ -142,6 +142,17 @@ int mtpsd_indexer_topk(const mtpsd_indexer_args* args, void* stream);
  * 16-byte aligned q and k_cache, which this count assumes), else 2 (scores, top-k). */
 int32_t mtpsd_indexer_topk_launch_count(int32_t n_heads, int32_t head_dim, int32_t dtype);
 
+/* The scoring half of mtpsd_indexer_topk, for callers that select (or time the
+ * selection) themselves: writes the score matrix args->scores [R, ld] (ld =
+ * mtpsd_scores_ld(max_visible); row r holds positions 0..row_pos[r], the rest of
+ * the row is not written) and launches nothing else.  args->scores is required
+ * (16-byte aligned); topk, topk_idx and topk_score are ignored; the workspace
+ * needs mtpsd_indexer_topk_plan_bytes(B, R).  mtpsd_topk over the result with
+ * row_len[r] = row_pos[r] + 1 gives exactly what mtpsd_indexer_topk returns. */
+int mtpsd_indexer_scores(const mtpsd_indexer_args* args, void* stream);
+/* Kernel launches of one mtpsd_indexer_scores call with R > 0 (2 on the tensor-core path, else 1). */
+int32_t mtpsd_indexer_scores_launch_count(int32_t n_heads, int32_t head_dim, int32_t dtype);
+
 /* ------------------------------------------------------------------------
  * Allocation-free variant of mtpsd_indexer_topk (the source pages have no
  * counterpart: this is a deployment convenience of this library).
@@ -172,13 +183,17 @@ int mtpsd_indexer_topk_noalloc(const mtpsd_indexer_args* args, void* stream);
 /* ------------------------------------------------------------------------
  * Standalone per-row top-k over a score matrix (the selection half of the
  * call above, for callers that produce scores themselves).
- *   scores [R, ld] float32, row_len [R] int64 (valid prefix of each row)
+ *   scores [R, ld] float32 (16-byte aligned rows with ld % 4 == 0 take the
+ *   register-resident kernel), row_len [R] int64: row r's valid prefix has
+ *   row_len[r] + row_len_add scores (pass row_pos with row_len_add = 1 for the
+ *   indexer's visible lengths), clamped to max_len (flagged
+ *   MTPSD_STATUS_INDEX_RANGE when a length exceeds it)
  *   -> out_idx [R, topk] (ascending positions, -1 padded), out_score nullable.
  * NaN scores are not supported.
  */
 size_t mtpsd_topk_workspace_size(int32_t R, int32_t topk);
-int mtpsd_topk(const float* scores, int64_t ld, int32_t R, const int64_t* row_len, int64_t max_len,
-               int32_t topk, int32_t* out_idx, float* out_score, void* workspace,
+int mtpsd_topk(const float* scores, int64_t ld, int32_t R, const int64_t* row_len, int64_t row_len_add,
+               int64_t max_len, int32_t topk, int32_t* out_idx, float* out_score, void* workspace,
                size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------

@@ -117,9 +117,12 @@ def indexer_topk_workspace_size(B, R, max_visible, topk) -> int:
     return int(lib().mtpsd_indexer_topk_workspace_size(B, R, max_visible, topk))
 
 
-def indexer_topk(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets, row_pos, topk: int,
-                 max_visible: int, topk_idx=None, topk_score=None, scores=None, workspace=None,
-                 dev_status=None, stream=None):
+def indexer_plan_bytes(B, R) -> int:
+    return int(lib().mtpsd_indexer_topk_plan_bytes(B, R))
+
+
+def _indexer_args(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets, row_pos, topk, max_visible,
+                  topk_idx, topk_score, scores, ws, dev_status):
     fp8 = q.dtype == torch.uint8
     _need(q, "q", torch.uint8 if fp8 else torch.float32, 3)
     _need(k_cache, "k_cache", q.dtype, 2)
@@ -130,37 +133,64 @@ def indexer_topk(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets
     if fp8:
         _need(q_scale, "q_scale", torch.float32)
         _need(k_scale, "k_scale", torch.float32)
+    if scores is not None:
+        _need(scores, "scores", torch.float32, 2)
+        if scores.shape[0] != q.shape[0] or scores.shape[1] != scores_ld(max_visible):
+            raise ValueError("scores must be [R, scores_ld(max_visible)]")
     R, H, D = q.shape
+    return N.IndexerArgs(B=cache_start.numel(), R=R, n_heads=H, head_dim=D, topk=topk,
+                         dtype=N.MTPSD_FP8_E4M3 if fp8 else N.MTPSD_F32,
+                         q=q.data_ptr(), q_scale=q_scale.data_ptr() if fp8 else None,
+                         weights=weights.data_ptr(), k_cache=k_cache.data_ptr(),
+                         k_scale=k_scale.data_ptr() if fp8 else None, pool_tokens=k_cache.shape[0],
+                         cache_start=cache_start.data_ptr(), row_offsets=row_offsets.data_ptr(),
+                         row_pos=row_pos.data_ptr(), max_visible=max_visible,
+                         topk_idx=None if topk_idx is None else topk_idx.data_ptr(),
+                         topk_score=None if topk_score is None else topk_score.data_ptr(),
+                         scores=None if scores is None else scores.data_ptr(),
+                         workspace=ws.data_ptr(), workspace_bytes=ws.numel(),
+                         dev_status=None if dev_status is None else dev_status.data_ptr())
+
+
+def indexer_topk(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets, row_pos, topk: int,
+                 max_visible: int, topk_idx=None, topk_score=None, scores=None, workspace=None,
+                 dev_status=None, stream=None):
+    R = q.shape[0]
     B = cache_start.numel()
-    dev = q.device
     if topk_idx is None:
-        topk_idx = torch.empty(R, topk, dtype=torch.int32, device=dev)
-    nbytes = indexer_topk_workspace_size(B, R, max_visible, topk)
-    ws = _ws(workspace, nbytes, dev)
-    a = N.IndexerArgs(B=B, R=R, n_heads=H, head_dim=D, topk=topk,
-                      dtype=N.MTPSD_FP8_E4M3 if fp8 else N.MTPSD_F32,
-                      q=q.data_ptr(), q_scale=q_scale.data_ptr() if fp8 else None,
-                      weights=weights.data_ptr(), k_cache=k_cache.data_ptr(),
-                      k_scale=k_scale.data_ptr() if fp8 else None, pool_tokens=k_cache.shape[0],
-                      cache_start=cache_start.data_ptr(), row_offsets=row_offsets.data_ptr(),
-                      row_pos=row_pos.data_ptr(), max_visible=max_visible,
-                      topk_idx=topk_idx.data_ptr(),
-                      topk_score=None if topk_score is None else topk_score.data_ptr(),
-                      scores=None if scores is None else scores.data_ptr(),
-                      workspace=ws.data_ptr(), workspace_bytes=ws.numel(),
-                      dev_status=None if dev_status is None else dev_status.data_ptr())
+        topk_idx = torch.empty(R, topk, dtype=torch.int32, device=q.device)
+    nbytes = indexer_plan_bytes(B, R) if scores is not None else indexer_topk_workspace_size(B, R, max_visible, topk)
+    ws = _ws(workspace, nbytes, q.device)
+    a = _indexer_args(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets, row_pos, topk, max_visible,
+                      topk_idx, topk_score, scores, ws, dev_status)
     check("mtpsd_indexer_topk", lib().mtpsd_indexer_topk(C.byref(a), _stream(stream)))
     return topk_idx
 
 
-def topk(scores, row_len, max_len: int, k: int, out_idx=None, out_score=None, dev_status=None, stream=None):
+def indexer_scores(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets, row_pos, max_visible: int,
+                   scores=None, workspace=None, dev_status=None, stream=None):
+    """The score matrix [R, scores_ld(max_visible)] alone (row r valid up to row_pos[r])."""
+    R = q.shape[0]
+    B = cache_start.numel()
+    if scores is None:
+        scores = torch.empty(R, scores_ld(max_visible), dtype=torch.float32, device=q.device)
+    ws = _ws(workspace, indexer_plan_bytes(B, R), q.device)
+    a = _indexer_args(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets, row_pos, 1, max_visible,
+                      None, None, scores, ws, dev_status)
+    check("mtpsd_indexer_scores", lib().mtpsd_indexer_scores(C.byref(a), _stream(stream)))
+    return scores
+
+
+def topk(scores, row_len, max_len: int, k: int, out_idx=None, out_score=None, dev_status=None, stream=None,
+         row_len_add: int = 0):
+    """Top-k per row; row r's valid prefix has row_len[r] + row_len_add scores."""
     _need(scores, "scores", torch.float32, 2)
     _need(row_len, "row_len", torch.int64, 1)
     R, ld = scores.shape
     if out_idx is None:
         out_idx = torch.empty(R, k, dtype=torch.int32, device=scores.device)
     check("mtpsd_topk", lib().mtpsd_topk(
-        _ptr(scores), ld, R, _ptr(row_len), max_len, k, _ptr(out_idx), _ptr(out_score), None, 0,
+        _ptr(scores), ld, R, _ptr(row_len), row_len_add, max_len, k, _ptr(out_idx), _ptr(out_score), None, 0,
         _ptr(dev_status), _stream(stream)))
     return out_idx
 
@@ -174,6 +204,11 @@ def sparse_mla_workspace_size(R, H, n_idx, n_append, dtype) -> int:
 def indexer_topk_launch_count(H, D, dtype) -> int:
     """Kernel launches of one indexer_topk call (aligned q and k_cache)."""
     return int(lib().mtpsd_indexer_topk_launch_count(H, D, dtype))
+
+
+def indexer_scores_launch_count(H, D, dtype) -> int:
+    """Kernel launches of one indexer_scores call (aligned q and k_cache)."""
+    return int(lib().mtpsd_indexer_scores_launch_count(H, D, dtype))
 
 
 def sparse_mla_launch_count(R, H, n_idx, n_append, dtype) -> int:

@@ -37,7 +37,7 @@ extern "C" {
 
 const char* mtpsd_last_error(void) { return g_err; }
 
-int32_t mtpsd_version(void) { return 100; }
+int32_t mtpsd_version(void) { return 101; }
 
 int mtpsd_merge_tokens(const int64_t* prompt_tokens, int64_t S, const uint32_t* prompt_offsets,
                        const int64_t* draft_tokens, int32_t B, int32_t K, int64_t* merged_tokens,
@@ -76,33 +76,41 @@ size_t mtpsd_indexer_topk_workspace_size(int32_t B, int32_t R, int64_t max_visib
   return align_up(scores, 256) + indexer_tc_plan_bytes(B, R);
 }
 
-int mtpsd_indexer_topk(const mtpsd_indexer_args* a, void* stream) {
-  g_err[0] = 0;
-  if (!a) return fail(MTPSD_EINVAL, "indexer_topk: null args");
-  if (a->B < 1 || a->R < 0 || a->n_heads < 1 || a->topk < 1 || a->topk > 4096)
-    return fail(MTPSD_EINVAL, "indexer_topk: need B >= 1, R >= 0, n_heads >= 1, 1 <= topk <= 4096");
+}  // extern "C"
+
+namespace mtpsd {
+// Checks the indexer arguments and launches the score kernels (plan + tensor-core GEMM, or the CUDA-core
+// kernel) into `*scores_out` (args->scores, else the head of the workspace).  need_scores: the call
+// requires a caller score buffer (mtpsd_indexer_scores).
+static int indexer_scores_checked(const mtpsd_indexer_args* a, bool need_scores, bool need_topk,
+                                  cudaStream_t st, float** scores_out) {
+  if (!a) return fail(MTPSD_EINVAL, "indexer: null args");
+  if (a->B < 1 || a->R < 0 || a->n_heads < 1)
+    return fail(MTPSD_EINVAL, "indexer: need B >= 1, R >= 0, n_heads >= 1");
   if (a->max_visible < 0 || a->max_visible > 0x7fffffffLL)
-    return fail(MTPSD_EINVAL, "indexer_topk: max_visible out of range");
+    return fail(MTPSD_EINVAL, "indexer: max_visible out of range");
   if (a->dtype == MTPSD_FP8_E4M3) {
-    if (a->head_dim != 128) return fail(MTPSD_EUNSUPPORTED, "indexer_topk: FP8 needs head_dim 128 (one block-128 scale per head)");
-    if (!a->q_scale || !a->k_scale) return fail(MTPSD_EINVAL, "indexer_topk: FP8 needs q_scale and k_scale");
+    if (a->head_dim != 128) return fail(MTPSD_EUNSUPPORTED, "indexer: FP8 needs head_dim 128 (one block-128 scale per head)");
+    if (!a->q_scale || !a->k_scale) return fail(MTPSD_EINVAL, "indexer: FP8 needs q_scale and k_scale");
   } else if (a->dtype == MTPSD_F32) {
-    if (a->head_dim < 1 || a->head_dim > 256) return fail(MTPSD_EUNSUPPORTED, "indexer_topk: float32 head_dim 1..256");
+    if (a->head_dim < 1 || a->head_dim > 256) return fail(MTPSD_EUNSUPPORTED, "indexer: float32 head_dim 1..256");
   } else {
-    return fail(MTPSD_EUNSUPPORTED, "indexer_topk: dtype must be MTPSD_FP8_E4M3 or MTPSD_F32");
+    return fail(MTPSD_EUNSUPPORTED, "indexer: dtype must be MTPSD_FP8_E4M3 or MTPSD_F32");
   }
-  if ((size_t)a->n_heads * a->head_dim > 16384) return fail(MTPSD_EUNSUPPORTED, "indexer_topk: n_heads*head_dim > 16384");
+  if ((size_t)a->n_heads * a->head_dim > 16384) return fail(MTPSD_EUNSUPPORTED, "indexer: n_heads*head_dim > 16384");
+  if (need_topk && (a->topk < 1 || a->topk > 4096)) return fail(MTPSD_EINVAL, "indexer_topk: need 1 <= topk <= 4096");
+  if (need_scores && !a->scores) return fail(MTPSD_EINVAL, "indexer_scores: args->scores is required");
   if (a->R == 0) return MTPSD_OK;
-  if (!a->q || !a->weights || !a->k_cache || !a->cache_start || !a->row_offsets || !a->row_pos || !a->topk_idx)
-    return fail(MTPSD_EINVAL, "indexer_topk: null pointer");
+  if (!a->q || !a->weights || !a->k_cache || !a->cache_start || !a->row_offsets || !a->row_pos ||
+      (need_topk && !a->topk_idx))
+    return fail(MTPSD_EINVAL, "indexer: null pointer");
   // with a caller score buffer the workspace holds only the work plan, else the scores and then the plan
   size_t need = a->scores ? indexer_tc_plan_bytes(a->B, a->R)
                           : mtpsd_indexer_topk_workspace_size(a->B, a->R, a->max_visible, a->topk);
   if (!a->workspace || a->workspace_bytes < need)
-    return fail(MTPSD_EWORKSPACE, "indexer_topk: workspace of %zu bytes needed, %zu given", need, a->workspace_bytes);
-  if (!aligned(a->workspace, 256)) return fail(MTPSD_EINVAL, "indexer_topk: workspace must be 256-byte aligned");
-  if (a->scores && !aligned(a->scores, 16)) return fail(MTPSD_EINVAL, "indexer_topk: scores must be 16-byte aligned");
-  cudaStream_t st = (cudaStream_t)stream;
+    return fail(MTPSD_EWORKSPACE, "indexer: workspace of %zu bytes needed, %zu given", need, a->workspace_bytes);
+  if (!aligned(a->workspace, 256)) return fail(MTPSD_EINVAL, "indexer: workspace must be 256-byte aligned");
+  if (a->scores && !aligned(a->scores, 16)) return fail(MTPSD_EINVAL, "indexer: scores must be 16-byte aligned");
   const int64_t ld = mtpsd_scores_ld(a->max_visible);
   float* scores = a->scores ? a->scores : (float*)a->workspace;
   IndexerPlan p;
@@ -112,10 +120,31 @@ int mtpsd_indexer_topk(const mtpsd_indexer_args* a, void* stream) {
   p.max_visible = a->max_visible; p.scores = scores; p.ld = ld;
   p.plan_ws = a->scores ? a->workspace : (void*)((char*)a->workspace + align_up((size_t)a->R * ld * sizeof(float), 256));
   p.status = a->dev_status;
-  int rc = indexer_tc_supported(p) ? launch_indexer_scores_tc(p, st) : launch_indexer_scores(p, st);
-  if (rc) return rc;
+  *scores_out = scores;
+  return indexer_tc_supported(p) ? launch_indexer_scores_tc(p, st) : launch_indexer_scores(p, st);
+}
+}  // namespace mtpsd
+
+extern "C" {
+
+int mtpsd_indexer_scores(const mtpsd_indexer_args* a, void* stream) {
+  g_err[0] = 0;
+  float* scores = nullptr;
+  return indexer_scores_checked(a, true, false, (cudaStream_t)stream, &scores);
+}
+
+int32_t mtpsd_indexer_scores_launch_count(int32_t n_heads, int32_t head_dim, int32_t dtype) {
+  return indexer_launch_count(n_heads, head_dim, dtype) - 1;
+}
+
+int mtpsd_indexer_topk(const mtpsd_indexer_args* a, void* stream) {
+  g_err[0] = 0;
+  cudaStream_t st = (cudaStream_t)stream;
+  float* scores = nullptr;
+  int rc = indexer_scores_checked(a, false, true, st, &scores);
+  if (rc || a->R == 0) return rc;
   TopkPlan t;
-  t.scores = scores; t.ld = ld; t.R = a->R; t.row_len = a->row_pos; t.len_plus_one = 1;
+  t.scores = scores; t.ld = mtpsd_scores_ld(a->max_visible); t.R = a->R; t.row_len = a->row_pos; t.len_add = 1;
   t.max_len = a->max_visible; t.k = a->topk; t.out_idx = a->topk_idx; t.out_score = a->topk_score;
   t.status = a->dev_status;
   return launch_topk(t, st);
@@ -130,17 +159,18 @@ size_t mtpsd_topk_workspace_size(int32_t R, int32_t topk) {
   return 0;
 }
 
-int mtpsd_topk(const float* scores, int64_t ld, int32_t R, const int64_t* row_len, int64_t max_len, int32_t topk,
-               int32_t* out_idx, float* out_score, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-               void* stream) {
+int mtpsd_topk(const float* scores, int64_t ld, int32_t R, const int64_t* row_len, int64_t row_len_add,
+               int64_t max_len, int32_t topk, int32_t* out_idx, float* out_score, void* workspace,
+               size_t workspace_bytes, int32_t* dev_status, void* stream) {
   g_err[0] = 0;
   (void)workspace; (void)workspace_bytes;
   if (R < 0 || topk < 1 || topk > 4096 || max_len < 0 || max_len > 0x7fffffffLL || ld < max_len)
     return fail(MTPSD_EINVAL, "topk: need R >= 0, 1 <= topk <= 4096, 0 <= max_len <= ld");
+  if (row_len_add < -0x7fffffffLL || row_len_add > 0x7fffffffLL) return fail(MTPSD_EINVAL, "topk: row_len_add out of range");
   if (R == 0) return MTPSD_OK;
   if (!scores || !row_len || !out_idx) return fail(MTPSD_EINVAL, "topk: null pointer");
   TopkPlan t;
-  t.scores = scores; t.ld = ld; t.R = R; t.row_len = row_len; t.len_plus_one = 0; t.max_len = max_len;
+  t.scores = scores; t.ld = ld; t.R = R; t.row_len = row_len; t.len_add = row_len_add; t.max_len = max_len;
   t.k = topk; t.out_idx = out_idx; t.out_score = out_score; t.status = dev_status;
   return launch_topk(t, (cudaStream_t)stream);
 }

@@ -44,9 +44,9 @@ int indexer_launch_count(int H, int D, int dtype);
 bool indexer_tc_supported(const IndexerPlan& p);
 int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st);
 
-// top-k over rows of a score matrix; row length = row_len[r] or row_pos[r]+1
+// top-k over rows of a score matrix; row length = row_len[r] + len_add
 struct TopkPlan {
-  const float* scores; int64_t ld; int R; const int64_t* row_len; int len_plus_one;
+  const float* scores; int64_t ld; int R; const int64_t* row_len; int64_t len_add;
   int64_t max_len; int k; int32_t* out_idx; float* out_score; int32_t* status;
 };
 int launch_topk(const TopkPlan& p, cudaStream_t st);

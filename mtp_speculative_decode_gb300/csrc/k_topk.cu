@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(TOPK_THREADS, 1) topk_kernel(TopkPlan p, int64
   __shared__ int remaining_s;
 
   const int r = blockIdx.x;
-  int64_t V = p.row_len[r] + (p.len_plus_one ? 1 : 0);
+  int64_t V = p.row_len[r] + p.len_add;
   if (V > p.max_len) {
     if (threadIdx.x == 0) flag_status(p.status, MTPSD_STATUS_INDEX_RANGE);
     V = p.max_len;
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
   const int r = blockIdx.x;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   constexpr int NW = NTH / 32;
-  int64_t V = p.row_len[r] + (p.len_plus_one ? 1 : 0);
+  int64_t V = p.row_len[r] + p.len_add;
   if (V > p.max_len) {
     if (threadIdx.x == 0) flag_status(p.status, MTPSD_STATUS_INDEX_RANGE);
     V = p.max_len;

@@ -31,6 +31,14 @@ def _dev_u32(x, device):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.uint32)).to(device)
 
 
+def _gen(src, name, device):
+    """An input tensor on the device: generated there chunk by chunk when the
+    source is the workload's on-demand set, else copied."""
+    if hasattr(src, "to_device"):
+        return src.to_device(name, device)
+    return _dev(src[name], device)
+
+
 def _dev(x, device, dtype=None):
     t = torch.as_tensor(x)
     if dtype is not None:
@@ -50,14 +58,14 @@ class DecodeStep:
         t = w.tensors
         # --- resident caches (target layer)
         self.cache_start = _dev(w.cache_start, device, torch.int64)
-        self.latent = _dev(t["latent"], device)
+        self.latent = _gen(t, "latent", device)
         if self.fp8:
-            k_raw = _dev(t["k_idx"], device)
+            k_raw = _gen(t, "k_idx", device)
             self.k_cache, k_scale = api.quantize_fp8_block128(k_raw)
             self.k_scale = k_scale.reshape(-1).contiguous()
             del k_raw
         else:
-            self.k_cache = _dev(t["k_idx"], device)
+            self.k_cache = _gen(t, "k_idx", device)
             self.k_scale = None
         # --- verify rows (host-known layout)
         self.row_pos = _dev(w.row_pos, device, torch.int64)
@@ -67,9 +75,9 @@ class DecodeStep:
         self.prompt_offsets = _dev_u32(w.prompt_offsets, device)
         self.draft_tokens = _dev(w.draft_tokens, device, torch.int64)
         self.target_argmax = _dev(w.target_argmax, device, torch.int64)
-        self.q_idx_raw = _dev(t["q_idx"], device)
-        self.w_idx = _dev(t["w_idx"], device)
-        self.q_mla = _dev(t["q_mla"], device)
+        self.q_idx_raw = _gen(t, "q_idx", device)
+        self.w_idx = _gen(t, "w_idx", device)
+        self.q_mla = _gen(t, "q_mla", device)
         # --- outputs / intermediates
         S = w.prompt_tokens.shape[0]
         self.merged_tokens = torch.empty(S + B * K, dtype=torch.int64, device=device)
@@ -91,40 +99,41 @@ class DecodeStep:
         self.num_accepted = torch.empty(B, dtype=torch.int32, device=device)
         self.next_tokens = torch.empty(B, dtype=torch.int64, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.ws_idx = torch.empty(api.indexer_topk_workspace_size(B, R, self.max_visible, spec.topk),
-                                  dtype=torch.uint8, device=device)
+        # the indexer's score matrix (read back by the top-k) and its small work plan
+        self.scores = torch.empty(R, api.scores_ld(self.max_visible), dtype=torch.float32, device=device)
+        self.ws_plan = torch.empty(max(api.indexer_plan_bytes(B, R), 256), dtype=torch.uint8, device=device)
         n = api.sparse_mla_workspace_size(R, spec.H_Q, spec.topk, 0, 1 if self.fp8 else 0)
         self.ws_mla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
         # --- draft layer
         self.has_draft = spec.draft_steps > 0
         if self.has_draft:
             d = draft if draft is not None else W.draft_tensors(w)
-            self.d_latent = _dev(d["d_latent"], device)
+            self.d_latent = _gen(d, "d_latent", device)
             if self.fp8:
-                kr = _dev(d["d_k_idx"], device)
+                kr = _gen(d, "d_k_idx", device)
                 self.d_k_cache, ks = api.quantize_fp8_block128(kr)
                 self.d_k_scale = ks.reshape(-1).contiguous()
-                sr = _dev(d["src_k_idx"], device)
+                sr = _gen(d, "src_k_idx", device)
                 self.src_idxk, ss = api.quantize_fp8_block128(sr)
                 self.src_idxs = ss.reshape(B, -1).contiguous()
                 del kr, sr
             else:
                 # float32 keys move as raw bytes, without a scale
-                self.d_k_cache = _dev(d["d_k_idx"], device)
+                self.d_k_cache = _gen(d, "d_k_idx", device)
                 self.d_k_scale = None
-                self.src_idxk = _dev(d["src_k_idx"], device).view(torch.uint8)
+                self.src_idxk = _gen(d, "src_k_idx", device).view(torch.uint8)
                 self.src_idxs = None
-            self.src_latent = _dev(d["src_latent"], device)
+            self.src_latent = _gen(d, "src_latent", device)
             self.dst_pos = _dev(w.L, device, torch.int64)    # accepted segment starts at L_b
             self.next_pos = torch.empty(B, dtype=torch.int64, device=device)
-            self.d_q_idx_raw = _dev(d["d_q_idx"], device)
-            self.d_w_idx = _dev(d["d_w_idx"], device)
+            self.d_q_idx_raw = _gen(d, "d_q_idx", device)
+            self.d_w_idx = _gen(d, "d_w_idx", device)
             if self.fp8:
                 self.d_q_idx = torch.empty(self.d_q_idx_raw.shape, dtype=torch.uint8, device=device)
                 self.d_q_scale = torch.empty(self.d_q_idx_raw.shape[:2], dtype=torch.float32, device=device)
             else:
                 self.d_q_idx, self.d_q_scale = self.d_q_idx_raw, None
-            self.d_q_mla = [_dev(d[f"d_q_mla{j}"], device) for j in range(spec.draft_steps)]
+            self.d_q_mla = [_gen(d, f"d_q_mla{j}", device) for j in range(spec.draft_steps)]
             self.d_row_offsets = _dev_u32(np.arange(B + 1), device)
             self.d_max_visible = int(w.L.max()) + (K + 1) + 1
             self.d_topk = torch.empty(B, spec.topk, dtype=torch.int32, device=device)
@@ -133,8 +142,8 @@ class DecodeStep:
                           for _ in range(spec.draft_steps)]
             self.d_lse = [torch.empty(B, spec.H_Q, dtype=torch.float32, device=device)
                           for _ in range(spec.draft_steps)]
-            self.ws_didx = torch.empty(api.indexer_topk_workspace_size(B, B, self.d_max_visible, spec.topk),
-                                       dtype=torch.uint8, device=device)
+            self.d_scores = torch.empty(B, api.scores_ld(self.d_max_visible), dtype=torch.float32, device=device)
+            self.ws_dplan = torch.empty(max(api.indexer_plan_bytes(B, B), 256), dtype=torch.uint8, device=device)
             n = max(api.sparse_mla_workspace_size(B, spec.H_Q, spec.topk, j, 1 if self.fp8 else 0)
                     for j in range(spec.draft_steps))
             self.ws_dmla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
@@ -144,12 +153,21 @@ class DecodeStep:
         api.merge_tokens(self.prompt_tokens, self.prompt_offsets, self.draft_tokens, self.merged_tokens,
                          self.merged_offsets, stream=stream)
 
-    def verify_indexer(self, stream=None):
+    def verify_scores(self, stream=None):
+        """FP8 quantization of the indexer queries, then the indexer score GEMM."""
         if self.fp8:
             api.quantize_fp8_block128(self.q_idx_raw, self.q_idx, self.q_scale, stream=stream)
-        api.indexer_topk(self.q_idx, self.q_scale, self.w_idx, self.k_cache, self.k_scale, self.cache_start,
-                         self.row_offsets, self.row_pos, self.spec.topk, self.max_visible, topk_idx=self.topk_idx,
-                         workspace=self.ws_idx, dev_status=self.status, stream=stream)
+        api.indexer_scores(self.q_idx, self.q_scale, self.w_idx, self.k_cache, self.k_scale, self.cache_start,
+                           self.row_offsets, self.row_pos, self.max_visible, scores=self.scores,
+                           workspace=self.ws_plan, dev_status=self.status, stream=stream)
+
+    def verify_topk(self, stream=None):
+        api.topk(self.scores, self.row_pos, self.max_visible, self.spec.topk, out_idx=self.topk_idx,
+                 dev_status=self.status, stream=stream, row_len_add=1)
+
+    def verify_indexer(self, stream=None):
+        self.verify_scores(stream)
+        self.verify_topk(stream)
 
     def verify_mla(self, stream=None):
         api.sparse_mla_decode(self.q_mla, self.latent, self.cache_start, self.row_offsets, self.row_pos,
@@ -165,14 +183,25 @@ class DecodeStep:
                          self.d_k_cache.view(torch.uint8), self.d_k_scale, self.cache_start, self.dst_pos,
                          next_pos=self.next_pos, dev_status=self.status, stream=stream)
 
-    def draft_indexer(self, stream=None):
+    def draft_scores(self, stream=None):
+        """Draft step 0: FP8 quantization of the draft indexer query, then the score GEMM at the position
+        after the written-back segment."""
         if self.fp8:
             api.quantize_fp8_block128(self.d_q_idx_raw, self.d_q_idx, self.d_q_scale, stream=stream)
-        api.indexer_topk(self.d_q_idx, self.d_q_scale, self.d_w_idx, self.d_k_cache, self.d_k_scale,
-                         self.cache_start, self.d_row_offsets, self.next_pos, self.spec.topk, self.d_max_visible,
-                         topk_idx=self.d_topk, workspace=self.ws_didx, dev_status=self.status, stream=stream)
+        api.indexer_scores(self.d_q_idx, self.d_q_scale, self.d_w_idx, self.d_k_cache, self.d_k_scale,
+                           self.cache_start, self.d_row_offsets, self.next_pos, self.d_max_visible,
+                           scores=self.d_scores, workspace=self.ws_dplan, dev_status=self.status, stream=stream)
+
+    def draft_topk(self, stream=None):
+        """Draft step 0 selection, then the share gather that steps 1.. reuse."""
+        api.topk(self.d_scores, self.next_pos, self.d_max_visible, self.spec.topk, out_idx=self.d_topk,
+                 dev_status=self.status, stream=stream, row_len_add=1)
         api.topk_share_gather(self.d_topk, self.d_row_offsets, None, self.shared_idx, dev_status=self.status,
                               stream=stream)
+
+    def draft_indexer(self, stream=None):
+        self.draft_scores(stream)
+        self.draft_topk(stream)
 
     def draft_mla(self, j: int, stream=None):
         api.sparse_mla_decode(self.d_q_mla[j], self.d_latent, self.cache_start, self.d_row_offsets, self.next_pos,
@@ -180,18 +209,23 @@ class DecodeStep:
                               append_base=self.next_pos if j else None, row_pos_add=j, out=self.d_out[j],
                               lse=self.d_lse[j], workspace=self.ws_dmla, dev_status=self.status, stream=stream)
 
+    def phases(self):
+        """The step as an ordered list of (name, callable(stream)): what step() runs."""
+        ph = []
+        if self.spec.verify:
+            ph += [("merge", self.merge), ("verify_scores", self.verify_scores), ("verify_topk", self.verify_topk),
+                   ("verify_mla", self.verify_mla)]
+        ph.append(("accept", self.accept))
+        if self.has_draft:
+            ph += [("writeback", self.writeback), ("draft_scores", self.draft_scores), ("draft_topk", self.draft_topk)]
+            ph += [(f"draft_mla{j}", (lambda stream=None, j=j: self.draft_mla(j, stream)))
+                   for j in range(self.spec.draft_steps)]
+        return ph
+
     def step(self, stream=None):
         """The whole hot path once."""
-        if self.spec.verify:
-            self.merge(stream)
-            self.verify_indexer(stream)
-            self.verify_mla(stream)
-        self.accept(stream)
-        if self.has_draft:
-            self.writeback(stream)
-            self.draft_indexer(stream)
-            for j in range(self.spec.draft_steps):
-                self.draft_mla(j, stream)
+        for _, fn in self.phases():
+            fn(stream)
 
     def launches_per_step(self) -> int:
         """Kernel launches of one step (for the benchmark's launch count)."""

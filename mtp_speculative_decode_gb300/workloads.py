@@ -6,6 +6,14 @@ to the CUDA path and to the CPU oracle.  Each tensor has its own random stream
 derived from (seed, tensor name), drawn with torch's CPU generator seeded per
 stream, so any tensor can be regenerated on its own.
 
+Generation: every tensor is drawn in blocks of 65536 consecutive elements
+(row-major), block i from its own numpy PCG64 stream seeded by (workload seed,
+CRC-32 of the tensor name, i).  Any range of rows can therefore be regenerated
+on its own (the oracle reads only the requests it checks), the blocks are
+drawn in parallel threads, and a device copy is filled chunk by chunk without
+a full host copy.  Normal values are float32 samples (then rounded to the
+tensor's dtype, bf16 by round-to-nearest-even); uniforms are float32.
+
 Workloads (shapes of the MTP decode step of a GLM-5.x / DeepSeek-V3.2 style
 model: index_topk 2048, 576-wide latent = 512 + 64, 64 indexer heads of 128,
 128 query heads, 1 bonus + 5 draft tokens per request):
@@ -31,7 +39,10 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
+import threading
 import zlib
+from concurrent.futures import ThreadPoolExecutor
 from typing import Dict, List, Optional
 
 import numpy as np
@@ -40,6 +51,7 @@ import torch
 SOFTMAX_SCALE = 1.0 / math.sqrt(576.0)
 ACCEPT_P = 0.67065
 GLM_VOCAB = 154880
+BLOCK = 1 << 16                     # elements per random stream
 
 
 @dataclasses.dataclass
@@ -76,29 +88,177 @@ SPECS: Dict[str, Spec] = {
 }
 
 
-def _stream(seed: int, name: str) -> torch.Generator:
-    g = torch.Generator()
-    g.manual_seed((seed * 1_000_003 + zlib.crc32(name.encode())) % (2 ** 63))
-    return g
+# ----------------------------------------------------------------------------- block streams
+
+def _key(name: str) -> int:
+    return zlib.crc32(name.encode())
+
+
+def _block_rng(seed: int, name: str, block: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, _key(name), block])))
+
+
+def _draw(seed: int, name: str, kind: str, e0: int, e1: int) -> np.ndarray:
+    """Elements [e0, e1) of a tensor's float32 stream ("normal" or "uniform")."""
+    out = np.empty(e1 - e0, dtype=np.float32)
+    b = e0 // BLOCK
+    pos = 0
+    while pos < e1 - e0:
+        lo = b * BLOCK
+        g = _block_rng(seed, name, b)
+        blk = g.standard_normal(BLOCK, dtype=np.float32) if kind == "normal" else g.random(BLOCK, dtype=np.float32)
+        a = max(e0, lo) - lo
+        n = min(e1, lo + BLOCK) - lo - a
+        out[pos:pos + n] = blk[a:a + n]
+        pos += n
+        b += 1
+    return out
+
+
+_POOL = None
+_POOL_LOCK = threading.Lock()
+
+
+def _pool() -> ThreadPoolExecutor:
+    global _POOL
+    with _POOL_LOCK:
+        if _POOL is None:
+            _POOL = ThreadPoolExecutor(max(1, min(32, os.cpu_count() or 1)))
+        return _POOL
 
 
 def normal(seed: int, name: str, shape, std: float = 1.0, dtype=torch.float32) -> torch.Tensor:
-    """N(0, std^2) samples, generated in float32 then cast to dtype (CPU)."""
-    g = _stream(seed, name)
-    x = torch.randn(*shape, generator=g, dtype=torch.float32)
-    if std != 1.0:
-        x.mul_(std)
-    return x.to(dtype)
+    """N(0, std^2) samples of the given shape (CPU), from the tensor's block streams."""
+    return TensorSpec(tuple(shape), "normal", std, dtype).generate(seed, name)
 
 
 def uniform(seed: int, name: str, shape, lo=0.0, hi=1.0) -> torch.Tensor:
-    g = _stream(seed, name)
-    return torch.rand(*shape, generator=g, dtype=torch.float32) * (hi - lo) + lo
+    x = TensorSpec(tuple(shape), "uniform", 1.0, torch.float32).generate(seed, name)
+    return x * (hi - lo) + lo
 
 
 def integers(seed: int, name: str, shape, lo: int, hi: int) -> torch.Tensor:
-    g = _stream(seed, name)
-    return torch.randint(lo, hi, tuple(shape), generator=g, dtype=torch.int64)
+    """Uniform integers in [lo, hi) (one stream per tensor: these tensors are small)."""
+    g = _block_rng(seed, name, 0)
+    return torch.from_numpy(g.integers(lo, hi, tuple(shape), dtype=np.int64))
+
+
+@dataclasses.dataclass
+class TensorSpec:
+    shape: tuple
+    kind: str            # "normal" or "uniform"
+    std: float
+    dtype: torch.dtype
+
+    @property
+    def row_elems(self) -> int:
+        return int(np.prod(self.shape[1:], dtype=np.int64)) if len(self.shape) > 1 else 1
+
+    def _rows_f32(self, seed, name, a, b) -> np.ndarray:
+        x = _draw(seed, name, self.kind, a * self.row_elems, b * self.row_elems)
+        if self.std != 1.0:
+            x *= np.float32(self.std)
+        return x
+
+    def _cast(self, x: np.ndarray, rows: int) -> torch.Tensor:
+        t = torch.from_numpy(x).reshape((rows,) + tuple(self.shape[1:]))
+        return t if self.dtype == torch.float32 else t.to(self.dtype)
+
+    def rows(self, seed, name, a: int, b: int) -> torch.Tensor:
+        """Rows [a, b) along the first dimension, generated in parallel blocks."""
+        a, b = max(0, a), min(self.shape[0], b)
+        if b <= a:
+            return self._cast(np.empty(0, np.float32), 0)
+        per = max(1, (1 << 22) // self.row_elems)          # about 4M elements per task
+        starts = list(range(a, b, per))
+        parts = list(_pool().map(lambda s: self._cast(self._rows_f32(seed, name, s, min(b, s + per)),
+                                                      min(b, s + per) - s), starts))
+        return parts[0] if len(parts) == 1 else torch.cat(parts)
+
+    def generate(self, seed, name) -> torch.Tensor:
+        return self.rows(seed, name, 0, self.shape[0]) if len(self.shape) else \
+            self._cast(self._rows_f32(seed, name, 0, 1), 1).reshape(())
+
+    def to_device(self, seed, name, device) -> torch.Tensor:
+        """The tensor on `device`, filled in chunks (about 64M elements each) as they are generated."""
+        out = torch.empty(self.shape, dtype=self.dtype, device=device)
+        n = self.shape[0]
+        per = max(1, (1 << 26) // self.row_elems)
+        for s in range(0, n, per):
+            e = min(n, s + per)
+            out[s:e].copy_(self.rows(seed, name, s, e))
+        return out
+
+
+class Tensors:
+    """The named input tensors of a workload, generated on demand.
+
+    t[name] is the whole tensor (CPU, cached); t.rows(name, a, b) and
+    t.take(name, index) regenerate only the rows asked for;
+    t.to_device(name, device) fills a device tensor chunk by chunk."""
+
+    def __init__(self, seed: int, specs: Dict[str, TensorSpec]):
+        self.seed = seed
+        self.specs = specs
+        self._cache: Dict[str, torch.Tensor] = {}
+
+    def __contains__(self, name):
+        return name in self.specs
+
+    def __iter__(self):
+        return iter(self.specs)
+
+    def keys(self):
+        return self.specs.keys()
+
+    def __getitem__(self, name) -> torch.Tensor:
+        if name not in self._cache:
+            self._cache[name] = self.specs[name].generate(self.seed, name)
+        return self._cache[name]
+
+    def shape(self, name):
+        return self.specs[name].shape
+
+    def rows(self, name, a: int, b: int) -> torch.Tensor:
+        if name in self._cache:
+            return self._cache[name][a:b]
+        return self.specs[name].rows(self.seed, name, a, b)
+
+    def take(self, name, index) -> torch.Tensor:
+        """Rows at the given first-dimension indices (in that order)."""
+        idx = np.asarray(index, dtype=np.int64).reshape(-1)
+        if name in self._cache:
+            return self._cache[name][torch.from_numpy(idx)]
+        if len(idx) == 0:
+            return self.rows(name, 0, 0)
+        # regenerate the covering block ranges once, then gather
+        spec = self.specs[name]
+        per = max(1, BLOCK // spec.row_elems)
+        uniq = np.unique(idx // per)
+        spans = []
+        for u in uniq:
+            if spans and spans[-1][1] == u:
+                spans[-1][1] = u + 1
+            else:
+                spans.append([u, u + 1])
+        parts, rowmap, base = [], {}, 0
+        for u0, u1 in spans:
+            a, b = int(u0 * per), int(min(spec.shape[0], u1 * per))
+            parts.append(self.rows(name, a, b))
+            rowmap[(a, b)] = base
+            base += b - a
+        cat = torch.cat(parts) if len(parts) > 1 else parts[0]
+        pos = np.empty_like(idx)
+        starts = np.array([k[0] for k in rowmap], dtype=np.int64)
+        offs = np.array(list(rowmap.values()), dtype=np.int64)
+        j = np.searchsorted(starts, idx, side="right") - 1
+        pos[:] = offs[j] + (idx - starts[j])
+        return cat[torch.from_numpy(pos)]
+
+    def to_device(self, name, device) -> torch.Tensor:
+        if name in self._cache:
+            return self._cache[name].to(device).contiguous()
+        return self.specs[name].to_device(self.seed, name, device)
 
 
 @dataclasses.dataclass
@@ -117,8 +277,8 @@ class Workload:
     prompt_offsets: np.ndarray  # [B+1] uint32
     draft_tokens: np.ndarray   # [B, K] int64
     target_argmax: np.ndarray  # [B, K+1] int64
-    # raw activations (CPU torch tensors)
-    tensors: Dict[str, torch.Tensor]
+    # activations and caches (generated on demand, see Tensors)
+    tensors: Tensors
 
     @property
     def B(self):
@@ -148,7 +308,34 @@ def synthetic_argmax(seed: int, draft: torch.Tensor, vocab: int, p: float) -> to
     return torch.cat([head, bonus], dim=1)
 
 
-def build(name_or_spec, with_tensors: bool = True) -> Workload:
+def _tensor_specs(spec: Spec, R: int, T: int) -> Dict[str, TensorSpec]:
+    std_i = 1.0 / math.sqrt(spec.D_I) if spec.scaled_normal else 1.0
+    std_l = 1.0 / math.sqrt(576.0) if spec.scaled_normal else 1.0
+    lat = torch.float32 if spec.latent_f32 else torch.bfloat16
+    f32 = torch.float32
+    t = {
+        "q_idx": TensorSpec((R, spec.H_I, spec.D_I), "normal", std_i, f32),
+        "w_idx": TensorSpec((R, spec.H_I), "uniform", 1.0, f32),
+        "k_idx": TensorSpec((T, spec.D_I), "normal", std_i, f32),
+        "latent": TensorSpec((T, 576), "normal", std_l, lat),
+        "q_mla": TensorSpec((R, spec.H_Q, 576), "normal", std_l, lat),
+    }
+    if spec.draft_steps:
+        B, W = spec.B, spec.K + 1
+        t.update({
+            "d_k_idx": TensorSpec((T, spec.D_I), "normal", std_i, f32),
+            "d_latent": TensorSpec((T, 576), "normal", std_l, lat),
+            "src_latent": TensorSpec((B, W, 576), "normal", std_l, lat),
+            "src_k_idx": TensorSpec((B, W, spec.D_I), "normal", std_i, f32),
+            "d_q_idx": TensorSpec((B, spec.H_I, spec.D_I), "normal", std_i, f32),
+            "d_w_idx": TensorSpec((B, spec.H_I), "uniform", 1.0, f32),
+        })
+        for j in range(spec.draft_steps):
+            t[f"d_q_mla{j}"] = TensorSpec((B, spec.H_Q, 576), "normal", std_l, lat)
+    return t
+
+
+def build(name_or_spec) -> Workload:
     spec = SPECS[name_or_spec] if isinstance(name_or_spec, str) else name_or_spec
     s = spec.seed
     B, K = spec.B, spec.K
@@ -166,40 +353,13 @@ def build(name_or_spec, with_tensors: bool = True) -> Workload:
     offsets = np.arange(B + 1, dtype=np.uint32)
     draft = integers(s, "draft_tokens", (B, K), 0, spec.vocab)
     argmax = synthetic_argmax(s, draft, spec.vocab, spec.accept_p)
-
-    std_i = 1.0 / math.sqrt(spec.D_I) if spec.scaled_normal else 1.0
-    std_l = 1.0 / math.sqrt(576.0) if spec.scaled_normal else 1.0
-    lat_dtype = torch.float32 if spec.latent_f32 else torch.bfloat16
-    R = len(row_req)
-    tensors: Dict[str, torch.Tensor] = {}
-    if with_tensors:
-        tensors["q_idx"] = normal(s, "q_idx", (R, spec.H_I, spec.D_I), std_i)
-        tensors["w_idx"] = uniform(s, "w_idx", (R, spec.H_I))
-        tensors["k_idx"] = normal(s, "k_idx", (T, spec.D_I), std_i)
-        tensors["latent"] = normal(s, "latent", (T, 576), std_l, lat_dtype)
-        tensors["q_mla"] = normal(s, "q_mla", (R, spec.H_Q, 576), std_l, lat_dtype)
+    tensors = Tensors(s, _tensor_specs(spec, len(row_req), T))
     return Workload(spec, L, r, cap, cache_start, T, row_req, row_pos,
                     prompt.numpy(), offsets, draft.numpy(), argmax.numpy(), tensors)
 
 
-def draft_tensors(w: Workload, with_pool: bool = True) -> Dict[str, torch.Tensor]:
-    """Inputs of the draft layer for the accepted-segment write-back and the
-    shared-index draft loop: a separate draft pool (latent + indexer key), the
-    6-row window of draft-layer KV to write back, and per-step queries."""
-    spec = w.spec
-    s = spec.seed
-    B, W = spec.B, spec.K + 1
-    std_i = 1.0 / math.sqrt(spec.D_I) if spec.scaled_normal else 1.0
-    std_l = 1.0 / math.sqrt(576.0) if spec.scaled_normal else 1.0
-    lat_dtype = torch.float32 if spec.latent_f32 else torch.bfloat16
-    t: Dict[str, torch.Tensor] = {}
-    if with_pool:
-        t["d_k_idx"] = normal(s, "d_k_idx", (w.T, spec.D_I), std_i)
-        t["d_latent"] = normal(s, "d_latent", (w.T, 576), std_l, lat_dtype)
-    t["src_latent"] = normal(s, "src_latent", (B, W, 576), std_l, lat_dtype)
-    t["src_k_idx"] = normal(s, "src_k_idx", (B, W, spec.D_I), std_i)
-    t["d_q_idx"] = normal(s, "d_q_idx", (B, spec.H_I, spec.D_I), std_i)
-    t["d_w_idx"] = uniform(s, "d_w_idx", (B, spec.H_I))
-    for j in range(spec.draft_steps):
-        t[f"d_q_mla{j}"] = normal(s, f"d_q_mla{j}", (B, spec.H_Q, 576), std_l, lat_dtype)
-    return t
+def draft_tensors(w: Workload) -> Tensors:
+    """Inputs of the draft layer (the same on-demand set as the target's): the
+    draft pool (latent + indexer key), the 6-row window of draft-layer KV to
+    write back, and the per-step queries."""
+    return w.tensors

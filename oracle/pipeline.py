@@ -18,7 +18,22 @@ from . import accept, fp8, indexer, merge, mla, share, topk, writeback
 
 
 def _np(x):
+    if hasattr(x, "dtype") and str(x.dtype) == "torch.bfloat16":
+        x = x.float()
     return x.numpy() if hasattr(x, "numpy") else np.asarray(x)
+
+
+def _rows(src, name, a, b):
+    """Rows [a, b) of an input tensor: regenerated on their own when the
+    source can do that (the workload's on-demand tensors), else sliced."""
+    return _np(src.rows(name, a, b)) if hasattr(src, "rows") else _np(src[name][a:b])
+
+
+def _take(src, name, index):
+    """Input rows at the given indices, as float64."""
+    if hasattr(src, "take"):
+        return _np(src.take(name, index)).astype(np.float64)
+    return mla._f64(src[name], list(index))
 
 
 class OracleStep:
@@ -39,15 +54,15 @@ class OracleStep:
     def keys(self, name: str, b: int, upto: int):
         """Dequantized indexer keys of request b, positions 0..upto-1 (float64)."""
         base = int(self.w.cache_start[b])
-        raw = self.t[name] if name in self.t else self.d[name]
-        x = _np(raw[base:base + upto]).astype(np.float32)
+        src = self.t if name in self.t else self.d
+        x = _rows(src, name, base, base + upto).astype(np.float32)
         if not self.fp8:
             return x.astype(np.float64)
         codes, scales = fp8.quantize_block128(x)
         return fp8.decode_e4m3(codes) * scales.astype(np.float64)
 
-    def query(self, raw_q, r):
-        x = _np(raw_q[r]).astype(np.float32)
+    def query(self, src, name, r):
+        x = _rows(src, name, r, r + 1)[0].astype(np.float32)
         if not self.fp8:
             return x.astype(np.float64)
         codes, scales = fp8.quantize_block128(x)          # one scale per head vector
@@ -64,19 +79,28 @@ class OracleStep:
             b = int(w.row_req[r])
             p = int(w.row_pos[r])
             keys = self.keys("k_idx", b, p + 1)
-            out[r] = indexer.indexer_scores_row(self.query(self.t["q_idx"], r), _np(self.t["w_idx"][r]), keys)
+            out[r] = indexer.indexer_scores_row(self.query(self.t, "q_idx", r), _rows(self.t, "w_idx", r, r + 1)[0],
+                                                keys)
         return out
 
     def verify_topk(self, scores):
         return {r: topk.topk_select(s, self.spec.topk) for r, s in scores.items()}
 
     def verify_mla(self, idx_rows, heads=None):
-        """idx_rows: dict row -> selected positions (from the oracle's own top-k)."""
+        """idx_rows: dict row -> selected positions.  The selected latent rows
+        of the row's request are gathered, then attended with the oracle's
+        sparse MLA definition."""
         w = self.w
         res = {}
         for r, idx in idx_rows.items():
-            res.update(mla.sparse_mla(self.t["q_mla"], self.t["latent"], w.cache_start, w.row_req,
-                                      {r: idx}, scale=_scale(), rows=[r], heads=heads))
+            b = int(w.row_req[r])
+            base = int(w.cache_start[b])
+            pos = mla.row_index_list(idx)
+            C = _take(self.t, "latent", [base + s for s in pos]).reshape(len(pos), mla.D_LATENT)
+            q = _rows(self.t, "q_mla", r, r + 1).astype(np.float64)
+            one = mla.sparse_mla(q, C, np.array([0]), np.array([0]), np.arange(len(pos))[None], _scale(),
+                                 heads=heads)
+            res[r] = one[0]
         return res
 
     def accept(self):
@@ -91,11 +115,11 @@ class OracleStep:
     def draft_keys(self, num_accepted, b: int, upto: int):
         """Dequantized draft indexer keys of request b after the write-back."""
         base = int(self.w.cache_start[b])
-        x = _np(self.d["d_k_idx"][base:base + upto]).astype(np.float32).copy()
+        x = _rows(self.d, "d_k_idx", base, base + upto).astype(np.float32).copy()
         W = self.spec.K + 1
         n = int(min(max(num_accepted[b] + 1, 1), W))
         start = int(self.w.L[b])
-        src = _np(self.d["src_k_idx"][b]).astype(np.float32)
+        src = _rows(self.d, "src_k_idx", b, b + 1)[0].astype(np.float32)
         for i in range(n):
             if start + i < upto:
                 x[start + i] = src[i]
@@ -112,9 +136,8 @@ class OracleStep:
         W = self.spec.K + 1
         n = int(min(max(num_accepted[b] + 1, 1), W))
         start = int(self.w.L[b])
-        out = mla._f64(self.d["d_latent"], [base + int(s) for s in positions]).reshape(len(positions), -1)
-        src = _np(self.d["src_latent"][b].float()) if hasattr(self.d["src_latent"], "float") \
-            else _np(self.d["src_latent"][b])
+        out = _take(self.d, "d_latent", [base + int(s) for s in positions]).reshape(len(positions), -1).copy()
+        src = _rows(self.d, "src_latent", b, b + 1)[0].astype(np.float64)
         for j, s in enumerate(positions):
             if start <= s < start + n:
                 out[j] = src[s - start]
@@ -126,7 +149,8 @@ class OracleStep:
         sc, tk = {}, {}
         for b in reqs:
             keys = self.draft_keys(num_accepted, b, int(P[b]) + 1)
-            s = indexer.indexer_scores_row(self.query(self.d["d_q_idx"], b), _np(self.d["d_w_idx"][b]), keys)
+            s = indexer.indexer_scores_row(self.query(self.d, "d_q_idx", b), _rows(self.d, "d_w_idx", b, b + 1)[0],
+                                           keys)
             sc[b] = s
             tk[b] = topk.topk_select(s, self.spec.topk)
         return sc, tk
@@ -135,13 +159,13 @@ class OracleStep:
         """Draft step j attention of each request over the shared set plus the
         positions appended since step 0 ([P1] "阶段 5")."""
         P = self.next_pos(num_accepted)
-        q = self.d[f"d_q_mla{j}"]
         res = {}
         for b in reqs:
             pos = share.shared_step_positions(shared[b], int(P[b]), j)
             C = self.draft_latent_rows(num_accepted, b, pos)
+            q = _rows(self.d, f"d_q_mla{j}", b, b + 1).astype(np.float64)
             # attend over the gathered rows with the same oracle definition
-            one = mla.sparse_mla(mla._f64(q, b)[None], C, np.array([0]), np.array([0]),
+            one = mla.sparse_mla(q, C, np.array([0]), np.array([0]),
                                  np.arange(len(pos))[None], _scale(), heads=heads)
             res[b] = one[0]
         return res

@@ -84,7 +84,7 @@ def test_host_checks_reject_before_launch(native):
     assert lib.mtpsd_sparse_mla_decode(C.byref(m), None) == native.MTPSD_EINVAL
     assert lib.mtpsd_kv_writeback(None, None, None, 1, 6, 7, 128, None, None, None, None, None, None, 10, None,
                                   None, None) == native.MTPSD_EUNSUPPORTED
-    assert lib.mtpsd_topk(None, 10, 1, None, 20, 4, None, None, None, 0, None, None) == native.MTPSD_EINVAL
+    assert lib.mtpsd_topk(None, 10, 1, None, 0, 20, 4, None, None, None, 0, None, None) == native.MTPSD_EINVAL
     assert lib.mtpsd_check_bounded_wait(0, 8, 8, None) == native.MTPSD_EINVAL
     assert lib.mtpsd_check_bounded_wait(2_000_000_000, 8, 8, None) == native.MTPSD_EINVAL
     assert lib.mtpsd_check_bounded_wait(1000, None, 8, None) == native.MTPSD_EINVAL

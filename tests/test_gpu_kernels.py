@@ -239,6 +239,16 @@ def test_indexer_scores_and_topk(mt, H, D, lens, r_per, k, fp8):
         parity.check_scores_row(sc[r, :V], ref[r])
         tolerated += parity.check_topk_row(idx[r], ref[r], k)
     print(f"top-k differences inside the tie band: {tolerated}")
+    # the two halves called separately (score GEMM, then the standalone top-k over row_pos + 1
+    # positions) give exactly the fused call's scores and selection
+    gpos = dev(c["row_pos"], torch.int64)
+    sc2 = mt.indexer_scores(gq, gqs, dev(c["w"]), gk, gks, dev(c["cache_start"]), u32(c["ro"]), gpos, maxv)
+    idx2 = mt.topk(sc2, gpos, maxv, k, row_len_add=1).cpu().numpy()
+    sc2 = sc2.cpu().numpy()
+    for r in range(R):
+        V = int(c["row_pos"][r]) + 1
+        assert np.array_equal(sc2[r, :V].view(np.uint32), sc[r, :V].view(np.uint32))
+    assert np.array_equal(idx2, idx)
 
 
 # ----------------------------------------------------------------------------- sparse MLA
