@@ -132,15 +132,20 @@ typedef struct {
 /* Row stride (floats) of the score matrix for a given max_visible. */
 int64_t mtpsd_scores_ld(int64_t max_visible);
 /* Workspace bytes of mtpsd_indexer_topk: the score matrix (R x mtpsd_scores_ld(max_visible) floats,
- * 256-byte padded) followed by the work plan.  When args->scores is given (16-byte aligned) the scores
- * go there and the workspace needs only mtpsd_indexer_topk_plan_bytes(B, R). */
+ * 256-byte padded), the work plan (mtpsd_indexer_topk_plan_bytes) and, when max_visible exceeds
+ * 40960, the top-k candidate lists (mtpsd_topk_workspace_size, 256-byte padded).  When args->scores
+ * is given (16-byte aligned) the scores go there and the workspace needs only
+ * mtpsd_indexer_topk_aux_bytes(B, R, max_visible, topk) = plan + candidate lists. */
 size_t mtpsd_indexer_topk_workspace_size(int32_t B, int32_t R, int64_t max_visible, int32_t topk);
 size_t mtpsd_indexer_topk_plan_bytes(int32_t B, int32_t R);
+size_t mtpsd_indexer_topk_aux_bytes(int32_t B, int32_t R, int64_t max_visible, int32_t topk);
 int mtpsd_indexer_topk(const mtpsd_indexer_args* args, void* stream);
-/* Kernel launches one mtpsd_indexer_topk call with R > 0 makes on the current device: 3 on the
- * tensor-core path (group plan, FP8 score GEMM, top-k: MTPSD_FP8_E4M3, head_dim 128, 32 or 64 heads,
- * 16-byte aligned q and k_cache, which this count assumes), else 2 (scores, top-k). */
-int32_t mtpsd_indexer_topk_launch_count(int32_t n_heads, int32_t head_dim, int32_t dtype);
+/* Kernel launches one mtpsd_indexer_topk call with R > 0 makes on the current device: the score
+ * launches (2 on the tensor-core path: group plan and FP8 score GEMM, which needs MTPSD_FP8_E4M3,
+ * head_dim 128, 32 or 64 heads and 16-byte aligned q and k_cache, as this count assumes; else 1) plus
+ * those of the top-k (mtpsd_topk_launch_count(max_visible, topk)). */
+int32_t mtpsd_indexer_topk_launch_count(int32_t n_heads, int32_t head_dim, int32_t dtype, int64_t max_visible,
+                                        int32_t topk);
 
 /* The scoring half of mtpsd_indexer_topk, for callers that select (or time the
  * selection) themselves: writes the score matrix args->scores [R, ld] (ld =
@@ -167,7 +172,7 @@ int32_t mtpsd_indexer_scores_launch_count(int32_t n_heads, int32_t head_dim, int
  * process exits.  The caller still passes every input and output.
  * - A call needing more than MTPSD_NOALLOC_SCRATCH_BYTES of scratch
  *   (mtpsd_indexer_topk_workspace_size(B, R, max_visible, topk), about
- *   R * max_visible * 4 bytes; only mtpsd_indexer_topk_plan_bytes(B, R) when
+ *   R * max_visible * 4 bytes; only mtpsd_indexer_topk_aux_bytes(...) when
  *   args->scores is given, since the scores then go to the caller's buffer)
  *   returns MTPSD_EWORKSPACE before any launch.
  * - The first call on a device (the current device) looks up the array's
@@ -183,15 +188,21 @@ int mtpsd_indexer_topk_noalloc(const mtpsd_indexer_args* args, void* stream);
 /* ------------------------------------------------------------------------
  * Standalone per-row top-k over a score matrix (the selection half of the
  * call above, for callers that produce scores themselves).
- *   scores [R, ld] float32 (16-byte aligned rows with ld % 4 == 0 take the
- *   register-resident kernel), row_len [R] int64: row r's valid prefix has
+ *   scores [R, ld] float32, row_len [R] int64: row r's valid prefix has
  *   row_len[r] + row_len_add scores (pass row_pos with row_len_add = 1 for the
  *   indexer's visible lengths), clamped to max_len (flagged
  *   MTPSD_STATUS_INDEX_RANGE when a length exceeds it)
  *   -> out_idx [R, topk] (ascending positions, -1 padded), out_score nullable.
+ * Rows of up to 40960 keys take one CTA each (16-byte aligned rows, ld % 4 == 0).
+ * Longer rows are split: one CTA per 32768-key segment selects that segment's
+ * exact top-k, and merge levels over groups of 32768/topk such lists follow
+ * (one launch per level, mtpsd_topk_launch_count); their candidate lists live
+ * in the workspace (mtpsd_topk_workspace_size, 256-byte aligned; 0 bytes when
+ * max_len <= 40960).  Unaligned score rows take a one-CTA-per-row radix kernel.
  * NaN scores are not supported.
  */
-size_t mtpsd_topk_workspace_size(int32_t R, int32_t topk);
+size_t mtpsd_topk_workspace_size(int32_t R, int64_t max_len, int32_t topk);
+int32_t mtpsd_topk_launch_count(int64_t max_len, int32_t topk);
 int mtpsd_topk(const float* scores, int64_t ld, int32_t R, const int64_t* row_len, int64_t row_len_add,
                int64_t max_len, int32_t topk, int32_t* out_idx, float* out_score, void* workspace,
                size_t workspace_bytes, int32_t* dev_status, void* stream);

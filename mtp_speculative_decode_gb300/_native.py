@@ -61,15 +61,17 @@ SIGNATURES = {
     "mtpsd_scores_ld": (i64, [i64]),
     "mtpsd_indexer_topk_workspace_size": (C.c_size_t, [i32, i32, i64, i32]),
     "mtpsd_indexer_topk_plan_bytes": (C.c_size_t, [i32, i32]),
+    "mtpsd_indexer_topk_aux_bytes": (C.c_size_t, [i32, i32, i64, i32]),
     "mtpsd_indexer_topk": (C.c_int, [C.POINTER(IndexerArgs), vp]),
     "mtpsd_indexer_topk_noalloc": (C.c_int, [C.POINTER(IndexerArgs), vp]),
     "mtpsd_indexer_scores": (C.c_int, [C.POINTER(IndexerArgs), vp]),
     "mtpsd_indexer_scores_launch_count": (i32, [i32, i32, i32]),
-    "mtpsd_topk_workspace_size": (C.c_size_t, [i32, i32]),
+    "mtpsd_topk_workspace_size": (C.c_size_t, [i32, i64, i32]),
+    "mtpsd_topk_launch_count": (i32, [i64, i32]),
     "mtpsd_topk": (C.c_int, [vp, i64, i32, vp, i64, i64, i32, vp, vp, vp, C.c_size_t, vp, vp]),
     "mtpsd_sparse_mla_workspace_size": (C.c_size_t, [i32, i32, i32, i32, i32]),
     "mtpsd_sparse_mla_launch_count": (i32, [i32, i32, i32, i32, i32]),
-    "mtpsd_indexer_topk_launch_count": (i32, [i32, i32, i32]),
+    "mtpsd_indexer_topk_launch_count": (i32, [i32, i32, i32, i64, i32]),
     "mtpsd_sparse_mla_decode": (C.c_int, [C.POINTER(MlaArgs), vp]),
     "mtpsd_accept_greedy": (C.c_int, [vp, vp, i32, i32, i64, vp, vp, vp]),
     "mtpsd_kv_writeback": (C.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp]),

@@ -121,6 +121,14 @@ def indexer_plan_bytes(B, R) -> int:
     return int(lib().mtpsd_indexer_topk_plan_bytes(B, R))
 
 
+def indexer_topk_aux_bytes(B, R, max_visible, topk) -> int:
+    return int(lib().mtpsd_indexer_topk_aux_bytes(B, R, max_visible, topk))
+
+
+def topk_workspace_size(R, max_len, k) -> int:
+    return int(lib().mtpsd_topk_workspace_size(R, max_len, k))
+
+
 def _indexer_args(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets, row_pos, topk, max_visible,
                   topk_idx, topk_score, scores, ws, dev_status):
     fp8 = q.dtype == torch.uint8
@@ -159,7 +167,8 @@ def indexer_topk(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets
     B = cache_start.numel()
     if topk_idx is None:
         topk_idx = torch.empty(R, topk, dtype=torch.int32, device=q.device)
-    nbytes = indexer_plan_bytes(B, R) if scores is not None else indexer_topk_workspace_size(B, R, max_visible, topk)
+    nbytes = indexer_topk_aux_bytes(B, R, max_visible, topk) if scores is not None else \
+        indexer_topk_workspace_size(B, R, max_visible, topk)
     ws = _ws(workspace, nbytes, q.device)
     a = _indexer_args(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets, row_pos, topk, max_visible,
                       topk_idx, topk_score, scores, ws, dev_status)
@@ -182,16 +191,18 @@ def indexer_scores(q, q_scale, weights, k_cache, k_scale, cache_start, row_offse
 
 
 def topk(scores, row_len, max_len: int, k: int, out_idx=None, out_score=None, dev_status=None, stream=None,
-         row_len_add: int = 0):
+         row_len_add: int = 0, workspace=None):
     """Top-k per row; row r's valid prefix has row_len[r] + row_len_add scores."""
     _need(scores, "scores", torch.float32, 2)
     _need(row_len, "row_len", torch.int64, 1)
     R, ld = scores.shape
     if out_idx is None:
         out_idx = torch.empty(R, k, dtype=torch.int32, device=scores.device)
+    nbytes = topk_workspace_size(R, max_len, k)
+    ws = _ws(workspace, nbytes, scores.device) if nbytes else None
     check("mtpsd_topk", lib().mtpsd_topk(
-        _ptr(scores), ld, R, _ptr(row_len), row_len_add, max_len, k, _ptr(out_idx), _ptr(out_score), None, 0,
-        _ptr(dev_status), _stream(stream)))
+        _ptr(scores), ld, R, _ptr(row_len), row_len_add, max_len, k, _ptr(out_idx), _ptr(out_score), _ptr(ws),
+        0 if ws is None else ws.numel(), _ptr(dev_status), _stream(stream)))
     return out_idx
 
 
@@ -201,9 +212,14 @@ def sparse_mla_workspace_size(R, H, n_idx, n_append, dtype) -> int:
     return int(lib().mtpsd_sparse_mla_workspace_size(R, H, n_idx, n_append, dtype))
 
 
-def indexer_topk_launch_count(H, D, dtype) -> int:
+def indexer_topk_launch_count(H, D, dtype, max_visible, topk) -> int:
     """Kernel launches of one indexer_topk call (aligned q and k_cache)."""
-    return int(lib().mtpsd_indexer_topk_launch_count(H, D, dtype))
+    return int(lib().mtpsd_indexer_topk_launch_count(H, D, dtype, max_visible, topk))
+
+
+def topk_launch_count(max_len, k) -> int:
+    """Kernel launches of one topk call (aligned score rows)."""
+    return int(lib().mtpsd_topk_launch_count(max_len, k))
 
 
 def indexer_scores_launch_count(H, D, dtype) -> int:

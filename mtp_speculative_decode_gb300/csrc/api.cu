@@ -71,9 +71,14 @@ int64_t mtpsd_scores_ld(int64_t max_visible) { return (int64_t)align_up((size_t)
 size_t mtpsd_indexer_topk_plan_bytes(int32_t B, int32_t R) { return (B < 0 || R < 0) ? 0 : indexer_tc_plan_bytes(B, R); }
 
 size_t mtpsd_indexer_topk_workspace_size(int32_t B, int32_t R, int64_t max_visible, int32_t topk) {
-  (void)topk;
+  if (B < 0 || R < 0) return 0;
   size_t scores = (size_t)R * (size_t)mtpsd_scores_ld(max_visible) * sizeof(float);
-  return align_up(scores, 256) + indexer_tc_plan_bytes(B, R);
+  return align_up(scores, 256) + indexer_tc_plan_bytes(B, R) + align_up(topk_workspace_bytes(R, max_visible, topk), 256);
+}
+
+size_t mtpsd_indexer_topk_aux_bytes(int32_t B, int32_t R, int64_t max_visible, int32_t topk) {
+  if (B < 0 || R < 0) return 0;
+  return indexer_tc_plan_bytes(B, R) + align_up(topk_workspace_bytes(R, max_visible, topk), 256);
 }
 
 }  // extern "C"
@@ -83,7 +88,7 @@ namespace mtpsd {
 // kernel) into `*scores_out` (args->scores, else the head of the workspace).  need_scores: the call
 // requires a caller score buffer (mtpsd_indexer_scores).
 static int indexer_scores_checked(const mtpsd_indexer_args* a, bool need_scores, bool need_topk,
-                                  cudaStream_t st, float** scores_out) {
+                                  cudaStream_t st, float** scores_out, void** topk_ws, size_t* topk_ws_bytes) {
   if (!a) return fail(MTPSD_EINVAL, "indexer: null args");
   if (a->B < 1 || a->R < 0 || a->n_heads < 1)
     return fail(MTPSD_EINVAL, "indexer: need B >= 1, R >= 0, n_heads >= 1");
@@ -104,9 +109,11 @@ static int indexer_scores_checked(const mtpsd_indexer_args* a, bool need_scores,
   if (!a->q || !a->weights || !a->k_cache || !a->cache_start || !a->row_offsets || !a->row_pos ||
       (need_topk && !a->topk_idx))
     return fail(MTPSD_EINVAL, "indexer: null pointer");
-  // with a caller score buffer the workspace holds only the work plan, else the scores and then the plan
-  size_t need = a->scores ? indexer_tc_plan_bytes(a->B, a->R)
-                          : mtpsd_indexer_topk_workspace_size(a->B, a->R, a->max_visible, a->topk);
+  // the workspace holds the scores (unless the caller gives a buffer), the work plan, and for the top-k
+  // of rows longer than 40960 keys its candidate lists
+  const size_t score_part = a->scores ? 0 : align_up((size_t)a->R * mtpsd_scores_ld(a->max_visible) * sizeof(float), 256);
+  const size_t topk_part = need_topk ? align_up(topk_workspace_bytes(a->R, a->max_visible, a->topk), 256) : 0;
+  size_t need = score_part + indexer_tc_plan_bytes(a->B, a->R) + topk_part;
   if (!a->workspace || a->workspace_bytes < need)
     return fail(MTPSD_EWORKSPACE, "indexer: workspace of %zu bytes needed, %zu given", need, a->workspace_bytes);
   if (!aligned(a->workspace, 256)) return fail(MTPSD_EINVAL, "indexer: workspace must be 256-byte aligned");
@@ -118,9 +125,11 @@ static int indexer_scores_checked(const mtpsd_indexer_args* a, bool need_scores,
   p.q = a->q; p.q_scale = a->q_scale; p.w = a->weights; p.k = a->k_cache; p.k_scale = a->k_scale;
   p.pool = a->pool_tokens; p.cache_start = a->cache_start; p.row_offsets = a->row_offsets; p.row_pos = a->row_pos;
   p.max_visible = a->max_visible; p.scores = scores; p.ld = ld;
-  p.plan_ws = a->scores ? a->workspace : (void*)((char*)a->workspace + align_up((size_t)a->R * ld * sizeof(float), 256));
+  p.plan_ws = (char*)a->workspace + score_part;
   p.status = a->dev_status;
   *scores_out = scores;
+  *topk_ws = (char*)a->workspace + score_part + indexer_tc_plan_bytes(a->B, a->R);
+  *topk_ws_bytes = topk_part;
   return indexer_tc_supported(p) ? launch_indexer_scores_tc(p, st) : launch_indexer_scores(p, st);
 }
 }  // namespace mtpsd
@@ -130,7 +139,9 @@ extern "C" {
 int mtpsd_indexer_scores(const mtpsd_indexer_args* a, void* stream) {
   g_err[0] = 0;
   float* scores = nullptr;
-  return indexer_scores_checked(a, true, false, (cudaStream_t)stream, &scores);
+  void* tws = nullptr;
+  size_t twb = 0;
+  return indexer_scores_checked(a, true, false, (cudaStream_t)stream, &scores, &tws, &twb);
 }
 
 int32_t mtpsd_indexer_scores_launch_count(int32_t n_heads, int32_t head_dim, int32_t dtype) {
@@ -141,37 +152,50 @@ int mtpsd_indexer_topk(const mtpsd_indexer_args* a, void* stream) {
   g_err[0] = 0;
   cudaStream_t st = (cudaStream_t)stream;
   float* scores = nullptr;
-  int rc = indexer_scores_checked(a, false, true, st, &scores);
+  void* tws = nullptr;
+  size_t twb = 0;
+  int rc = indexer_scores_checked(a, false, true, st, &scores, &tws, &twb);
   if (rc || a->R == 0) return rc;
   TopkPlan t;
   t.scores = scores; t.ld = mtpsd_scores_ld(a->max_visible); t.R = a->R; t.row_len = a->row_pos; t.len_add = 1;
   t.max_len = a->max_visible; t.k = a->topk; t.out_idx = a->topk_idx; t.out_score = a->topk_score;
-  t.status = a->dev_status;
+  t.status = a->dev_status; t.ws = tws; t.ws_bytes = twb;
   return launch_topk(t, st);
 }
 
-int32_t mtpsd_indexer_topk_launch_count(int32_t n_heads, int32_t head_dim, int32_t dtype) {
-  return indexer_launch_count(n_heads, head_dim, dtype);
+int32_t mtpsd_indexer_topk_launch_count(int32_t n_heads, int32_t head_dim, int32_t dtype, int64_t max_visible,
+                                        int32_t topk) {
+  if (topk < 1 || topk > 4096) return 0;
+  return indexer_launch_count(n_heads, head_dim, dtype) - 1 + topk_launch_count(max_visible, topk, true);
 }
 
-size_t mtpsd_topk_workspace_size(int32_t R, int32_t topk) {
-  (void)R; (void)topk;
-  return 0;
+size_t mtpsd_topk_workspace_size(int32_t R, int64_t max_len, int32_t topk) {
+  if (R < 0 || topk < 1 || topk > 4096) return 0;
+  return topk_workspace_bytes(R, max_len, topk);
+}
+
+int32_t mtpsd_topk_launch_count(int64_t max_len, int32_t topk) {
+  if (topk < 1 || topk > 4096) return 0;
+  return topk_launch_count(max_len, topk, true);
 }
 
 int mtpsd_topk(const float* scores, int64_t ld, int32_t R, const int64_t* row_len, int64_t row_len_add,
                int64_t max_len, int32_t topk, int32_t* out_idx, float* out_score, void* workspace,
                size_t workspace_bytes, int32_t* dev_status, void* stream) {
   g_err[0] = 0;
-  (void)workspace; (void)workspace_bytes;
   if (R < 0 || topk < 1 || topk > 4096 || max_len < 0 || max_len > 0x7fffffffLL || ld < max_len)
     return fail(MTPSD_EINVAL, "topk: need R >= 0, 1 <= topk <= 4096, 0 <= max_len <= ld");
   if (row_len_add < -0x7fffffffLL || row_len_add > 0x7fffffffLL) return fail(MTPSD_EINVAL, "topk: row_len_add out of range");
   if (R == 0) return MTPSD_OK;
   if (!scores || !row_len || !out_idx) return fail(MTPSD_EINVAL, "topk: null pointer");
+  const size_t need = topk_workspace_bytes(R, max_len, topk);
+  if (need && (!workspace || workspace_bytes < need))
+    return fail(MTPSD_EWORKSPACE, "topk: workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if (need && !aligned(workspace, 256)) return fail(MTPSD_EINVAL, "topk: workspace must be 256-byte aligned");
   TopkPlan t;
   t.scores = scores; t.ld = ld; t.R = R; t.row_len = row_len; t.len_add = row_len_add; t.max_len = max_len;
   t.k = topk; t.out_idx = out_idx; t.out_score = out_score; t.status = dev_status;
+  t.ws = workspace; t.ws_bytes = workspace_bytes;
   return launch_topk(t, (cudaStream_t)stream);
 }
 

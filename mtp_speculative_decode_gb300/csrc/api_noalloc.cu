@@ -52,13 +52,13 @@ extern "C" int mtpsd_indexer_topk_noalloc(const mtpsd_indexer_args* args, void* 
     set_error("indexer_topk_noalloc: null args");
     return MTPSD_EINVAL;
   }
-  // with a caller score buffer only the small work plan lives in the scratch
-  size_t need = args->scores ? mtpsd_indexer_topk_plan_bytes(args->B, args->R)
+  // with a caller score buffer only the work plan and the top-k candidate lists live in the scratch
+  size_t need = args->scores ? mtpsd_indexer_topk_aux_bytes(args->B, args->R, args->max_visible, args->topk)
                              : mtpsd_indexer_topk_workspace_size(args->B, args->R, args->max_visible, args->topk);
   if (need > (size_t)MTPSD_NOALLOC_SCRATCH_BYTES) {
     set_error("indexer_topk_noalloc: this call needs %zu bytes of scratch but the static maximum is %zu bytes "
-              "(R * mtpsd_scores_ld(max_visible) * 4 plus a small tail, or only the tail when args->scores is "
-              "given); pass args->scores or use mtpsd_indexer_topk with a workspace",
+              "(R * mtpsd_scores_ld(max_visible) * 4 plus the plan and top-k lists, or only those when "
+              "args->scores is given); pass args->scores or use mtpsd_indexer_topk with a workspace",
               need, (size_t)MTPSD_NOALLOC_SCRATCH_BYTES);
     return MTPSD_EWORKSPACE;
   }

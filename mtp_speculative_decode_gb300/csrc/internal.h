@@ -48,8 +48,11 @@ int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st);
 struct TopkPlan {
   const float* scores; int64_t ld; int R; const int64_t* row_len; int64_t len_add;
   int64_t max_len; int k; int32_t* out_idx; float* out_score; int32_t* status;
+  void* ws; size_t ws_bytes;   // candidate lists of the split path (rows longer than 40960 keys)
 };
 int launch_topk(const TopkPlan& p, cudaStream_t st);
+size_t topk_workspace_bytes(int R, int64_t max_len, int k);
+int topk_launch_count(int64_t max_len, int k, bool aligned);
 
 // sparse MLA
 struct MlaPlan {

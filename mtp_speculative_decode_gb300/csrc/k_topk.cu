@@ -180,10 +180,58 @@ __global__ void __launch_bounds__(TOPK_THREADS, 1) topk_kernel(TopkPlan p, int64
 // 8198 keys takes 16 keys per thread and a tail of 6, not 20 per thread), and
 // the tail keys, whose positions follow every regular one, are compacted after
 // them.
-template <int KPT, int NTH, bool XT>
-__global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
+//
+// Longer rows are split (MODE 1 and 2, one launch per level).  Level 1 cuts a
+// row into segments of SPLIT_SEG keys, one CTA each, and every CTA selects its
+// segment's exact top-k under the same order (larger key first, ties to the
+// lower position) as a list of k (key, position) entries in position order; a
+// segment with fewer than k keys lists all of them, then -1 positions.  Level
+// l >= 2 merges groups of G = SPLIT_SEG / k consecutive lists of level l-1 the
+// same way.  Every element of a row's top-k is in the top-k of its segment (and
+// of its group) under that order, so every level is exact; the lists of a row
+// stay in position order (segment u's positions precede segment u+1's), so the
+// compaction, which writes in list order, keeps the output ascending.  The level
+// at which a row has one list left writes the row's final output.
+constexpr int SPLIT_SEG = 32768;
+constexpr int SPLIT_KPT = 32;
+constexpr int SPLIT_NTH = 1024;
+
+struct SplitLevel {
+  int level;                     // 1: segments of the score rows; >= 2: merges of the previous lists
+  int G;                         // lists merged per CTA at levels >= 2
+  const uint32_t* in_key;        // previous level's lists, in_stride entries per row
+  const int32_t* in_pos;
+  int64_t in_stride;
+  uint32_t* out_key;             // this level's lists (when not final), out_stride entries per row
+  int32_t* out_pos;
+  int64_t out_stride;
+};
+
+// Shape of a row of V keys at a level: n lists, the last holding last_valid valid entries (every
+// other list holds k); n_prev / prev_last_valid describe level - 1 (0 at level 1).
+__host__ __device__ __forceinline__ void split_shape(int64_t V, int k, int G, int level, int& n, int& last_valid,
+                                                     int& n_prev, int& prev_last_valid) {
+  n = V > 0 ? (int)((V + SPLIT_SEG - 1) / SPLIT_SEG) : 1;
+  const int64_t tail = V - (int64_t)(n - 1) * SPLIT_SEG;
+  last_valid = (int)(tail < k ? (tail > 0 ? tail : 0) : k);
+  n_prev = 0;
+  prev_last_valid = 0;
+  for (int l = 2; l <= level; ++l) {
+    n_prev = n;
+    prev_last_valid = last_valid;
+    const int nn = (n + G - 1) / G;
+    const int m = n - (nn - 1) * G;   // lists in the last group
+    const int cnt = (m - 1) * k + prev_last_valid;
+    last_valid = cnt < k ? cnt : k;
+    n = nn;
+  }
+}
+
+template <int KPT, int NTH, bool XT, int MODE>
+__global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p, SplitLevel sl) {
   griddep_wait();                // the previous kernel's writes are visible from here on
   griddep_launch_dependents();
+  static_assert(MODE == 0 || !XT, "tail keys only for whole rows");
   __shared__ int wsum[2][32];
   __shared__ int warp_sums[32];
   __shared__ int total_s;
@@ -192,34 +240,105 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
   const int r = blockIdx.x;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   constexpr int NW = NTH / 32;
-  int64_t V = p.row_len[r] + p.len_add;
-  if (V > p.max_len) {
-    if (threadIdx.x == 0) flag_status(p.status, MTPSD_STATUS_INDEX_RANGE);
-    V = p.max_len;
+  int64_t Vrow = p.row_len[r] + p.len_add;
+  if (Vrow > p.max_len) {
+    if (threadIdx.x == 0 && (MODE == 0 || (sl.level == 1 && blockIdx.y == 0))) flag_status(p.status, MTPSD_STATUS_INDEX_RANGE);
+    Vrow = p.max_len;
   }
-  if (V < 0) V = 0;
+  if (Vrow < 0) Vrow = 0;
   const int k = p.k;
-  int32_t* out = p.out_idx + (int64_t)r * k;
-  float* outs = p.out_score ? p.out_score + (int64_t)r * k : nullptr;
-  const float* row = p.scores + (int64_t)r * p.ld;
-  if (V <= k) {  // everything visible is selected
-    for (int64_t i = threadIdx.x; i < k; i += blockDim.x) {
-      out[i] = i < V ? (int32_t)i : -1;
-      if (outs) outs[i] = i < V ? row[i] : -INFINITY;
+  // this CTA's keys: V of them, from a score row (MODE 0, 1) or a list of (key, position) (MODE 2)
+  const float* row = nullptr;
+  const uint32_t* krow = nullptr;
+  const int32_t* prow = nullptr;
+  int64_t pos_base = 0, lim = 0;
+  int V;
+  bool fin = true;
+  int32_t* opos = p.out_idx + (int64_t)r * k;                       // final: positions and scores
+  float* oscore = p.out_score ? p.out_score + (int64_t)r * k : nullptr;
+  uint32_t* okey = nullptr;                                         // intermediate: keys and positions
+  if constexpr (MODE == 0) {
+    V = (int)Vrow;
+    row = p.scores + (int64_t)r * p.ld;
+    lim = p.ld;
+  } else {
+    int n, lv, np, plv;
+    split_shape(Vrow, k, sl.G, sl.level, n, lv, np, plv);
+    const int u = blockIdx.y;
+    if (MODE == 2 && np <= 1) return;   // the row was finished at an earlier level
+    if (u >= n) return;
+    fin = n == 1;
+    if constexpr (MODE == 1) {
+      pos_base = (int64_t)u * SPLIT_SEG;
+      V = (int)min((int64_t)SPLIT_SEG, Vrow - pos_base);
+      if (V < 0) V = 0;
+      row = p.scores + (int64_t)r * p.ld + pos_base;
+      lim = p.ld - pos_base;
+    } else {
+      const int m = u < n - 1 ? sl.G : np - (n - 1) * sl.G;   // lists in this group
+      V = u < n - 1 ? sl.G * k : (m - 1) * k + plv;
+      krow = sl.in_key + (int64_t)r * sl.in_stride + (int64_t)u * sl.G * k;
+      prow = sl.in_pos + (int64_t)r * sl.in_stride + (int64_t)u * sl.G * k;
+      lim = (int64_t)m * k;
+    }
+    if (!fin) {
+      okey = sl.out_key + (int64_t)r * sl.out_stride + (int64_t)u * k;
+      opos = sl.out_pos + (int64_t)r * sl.out_stride + (int64_t)u * k;
+      oscore = nullptr;
+    }
+  }
+  auto pos_of = [&](int i) -> int32_t {
+    if constexpr (MODE == 2) return prow[i];
+    else return (int32_t)(pos_base + i);
+  };
+  auto emit = [&](int slot, int i, uint32_t kv) {
+    opos[slot] = pos_of(i);
+    if (okey) okey[slot] = kv;
+    else if (oscore) oscore[slot] = key_float(kv);
+  };
+  if (V <= k) {  // everything is selected
+    for (int i = threadIdx.x; i < k; i += blockDim.x) {
+      if (i < V) {
+        uint32_t kv;
+        if constexpr (MODE == 2) kv = krow[i];
+        else kv = float_key(row[i]);
+        emit(i, i, kv);
+      } else {
+        opos[i] = -1;
+        if (okey) okey[i] = 0u;
+        else if (oscore) oscore[i] = -INFINITY;
+      }
     }
     return;
   }
-  // keys of this thread's positions; 0 (below every finite key) past the row
+  // keys of this thread's entries; 0 (below every finite key) past the end
   const int a = threadIdx.x * KPT;
   uint32_t key[KPT];
+  if constexpr (MODE == 2) {
+    if ((k & 3) == 0) {   // 16-byte aligned lists (k and the row stride are multiples of 4)
 #pragma unroll
-  for (int i = 0; i < KPT; i += 4) {
-    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (a + i < p.ld) f = *(const float4*)(row + a + i);   // ld is a multiple of 4 and rows are 16-byte aligned
-    key[i] = a + i < V ? float_key(f.x) : 0u;
-    key[i + 1] = a + i + 1 < V ? float_key(f.y) : 0u;
-    key[i + 2] = a + i + 2 < V ? float_key(f.z) : 0u;
-    key[i + 3] = a + i + 3 < V ? float_key(f.w) : 0u;
+      for (int i = 0; i < KPT; i += 4) {
+        uint4 f = make_uint4(0u, 0u, 0u, 0u);
+        if (a + i < lim) f = *(const uint4*)(krow + a + i);
+        key[i] = a + i < V ? f.x : 0u;
+        key[i + 1] = a + i + 1 < V ? f.y : 0u;
+        key[i + 2] = a + i + 2 < V ? f.z : 0u;
+        key[i + 3] = a + i + 3 < V ? f.w : 0u;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < KPT; ++i) key[i] = a + i < V ? krow[a + i] : 0u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < KPT; i += 4) {
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (a + i < lim) f = *(const float4*)(row + a + i);   // ld is a multiple of 4 and rows are 16-byte aligned
+      key[i] = a + i < V ? float_key(f.x) : 0u;
+      key[i + 1] = a + i + 1 < V ? float_key(f.y) : 0u;
+      key[i + 2] = a + i + 2 < V ? float_key(f.z) : 0u;
+      key[i + 3] = a + i + 3 < V ? float_key(f.w) : 0u;
+    }
   }
   const int ax = KPT * NTH + threadIdx.x;   // this thread's tail position (XT)
   const bool xv = XT && ax < V;
@@ -344,18 +463,14 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
         --take_eq;
       }
       if (take && out_pos < k) {
-        out[out_pos] = a + i;
-        if (outs) outs[out_pos] = key_float(key[i]);
+        emit(out_pos, a + i, key[i]);
         ++out_pos;
       }
     }
     const int need_eq_x = max(0, need_eq - tot_eq_r);
     const int gx_before = (int)(px & 0xffffu), ex_before = (int)(px >> 16);
     const int x_pos = (int)(tr & 0xffffu) + min(tot_eq_r, need_eq) + gx_before + min(ex_before, need_eq_x);
-    if ((xg || (xe && ex_before < need_eq_x)) && x_pos < k) {
-      out[x_pos] = ax;
-      if (outs) outs[x_pos] = key_float(xkey);
-    }
+    if ((xg || (xe && ex_before < need_eq_x)) && x_pos < k) emit(x_pos, ax, xkey);
     return;
   }
   const int gt_before = block_exclusive_scan(n_gt, warp_sums, &total_s);
@@ -371,8 +486,7 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
       --take_eq;
     }
     if (take && out_pos < k) {
-      out[out_pos] = a + i;
-      if (outs) outs[out_pos] = key_float(key[i]);
+      emit(out_pos, a + i, key[i]);
       ++out_pos;
     }
   }
@@ -380,15 +494,94 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p) {
 
 template <int NTH, bool XT>
 static int launch_topk_reg(const TopkPlan& p, int kpt, cudaStream_t st) {
+  const SplitLevel none = {};
   switch (kpt) {
 #define MTPSD_TOPK_CASE(K) \
-  case K: launch_k(topk_reg_kernel<K, NTH, XT>, p.R, NTH, 0, st, p); break;
+  case K: launch_k(topk_reg_kernel<K, NTH, XT, 0>, p.R, NTH, 0, st, p, none); break;
     MTPSD_TOPK_CASE(4) MTPSD_TOPK_CASE(8) MTPSD_TOPK_CASE(12) MTPSD_TOPK_CASE(16) MTPSD_TOPK_CASE(20)
     MTPSD_TOPK_CASE(24) MTPSD_TOPK_CASE(28) MTPSD_TOPK_CASE(32) MTPSD_TOPK_CASE(36) MTPSD_TOPK_CASE(40)
 #undef MTPSD_TOPK_CASE
     default: return -1;
   }
   return check_launch("topk");
+}
+
+// Levels of the split top-k for rows up to max_len keys: lists per row at each level (the largest
+// row's), until one list is left.  Returns the number of levels (>= 2 when max_len > SPLIT_SEG).
+static int split_levels(int64_t max_len, int k, int* n_at, int max_levels) {
+  const int G = SPLIT_SEG / k;
+  int n = (int)((max_len + SPLIT_SEG - 1) / SPLIT_SEG);
+  if (n < 1) n = 1;
+  int L = 0;
+  n_at[L++] = n;
+  while (n > 1 && L < max_levels) {
+    n = (n + G - 1) / G;
+    n_at[L++] = n;
+  }
+  return L;
+}
+
+static bool split_path(const TopkPlan& p) {
+  const bool aligned = ((uintptr_t)p.scores % 16) == 0 && (p.ld % 4) == 0;
+  return aligned && p.max_len > 40960;
+}
+
+// Workspace of the split top-k: two list buffers per row (levels alternate between them), each list
+// k entries of a uint32 key and an int32 position; row strides are multiples of 4 entries.
+size_t topk_workspace_bytes(int R, int64_t max_len, int k) {
+  if (R <= 0 || k < 1 || max_len <= 40960) return 0;
+  int n_at[8];
+  const int L = split_levels(max_len, k, n_at, 8);
+  if (L < 2) return 0;
+  const int64_t strideA = ((int64_t)n_at[0] * k + 3) & ~3LL;
+  const int64_t strideB = L > 2 ? (((int64_t)n_at[1] * k + 3) & ~3LL) : 0;
+  const size_t a = ((size_t)R * strideA * 8 + 255) / 256 * 256;
+  const size_t b = ((size_t)R * strideB * 8 + 255) / 256 * 256;
+  return a + b;
+}
+
+int topk_launch_count(int64_t max_len, int k, bool aligned) {
+  if (!aligned || max_len <= 40960) return 1;
+  int n_at[8];
+  return split_levels(max_len, k, n_at, 8);
+}
+
+static int launch_topk_split(const TopkPlan& p, cudaStream_t st) {
+  int n_at[8];
+  const int L = split_levels(p.max_len, p.k, n_at, 8);
+  const size_t need = topk_workspace_bytes(p.R, p.max_len, p.k);
+  if (!p.ws || p.ws_bytes < need) {
+    set_error("topk: rows longer than 40960 keys need a workspace of %zu bytes (%zu given)", need, p.ws_bytes);
+    return MTPSD_EWORKSPACE;
+  }
+  const int64_t strideA = ((int64_t)n_at[0] * p.k + 3) & ~3LL;
+  const int64_t strideB = L > 2 ? (((int64_t)n_at[1] * p.k + 3) & ~3LL) : 0;
+  uint32_t* keyA = (uint32_t*)p.ws;
+  int32_t* posA = (int32_t*)(keyA + (size_t)p.R * strideA);
+  char* bbase = (char*)p.ws + ((size_t)p.R * strideA * 8 + 255) / 256 * 256;
+  uint32_t* keyB = (uint32_t*)bbase;
+  int32_t* posB = (int32_t*)(keyB + (size_t)p.R * strideB);
+  SplitLevel sl = {};
+  sl.G = SPLIT_SEG / p.k;
+  for (int l = 1; l <= L; ++l) {
+    // level l writes buffer A when odd, B when even, and reads the other one
+    const bool odd = (l & 1) != 0;
+    sl.level = l;
+    sl.out_key = odd ? keyA : keyB;
+    sl.out_pos = odd ? posA : posB;
+    sl.out_stride = odd ? strideA : strideB;
+    sl.in_key = odd ? keyB : keyA;
+    sl.in_pos = odd ? posB : posA;
+    sl.in_stride = odd ? strideB : strideA;
+    const dim3 grid(p.R, n_at[l - 1]);
+    if (l == 1)
+      launch_k(topk_reg_kernel<SPLIT_KPT, SPLIT_NTH, false, 1>, grid, SPLIT_NTH, 0, st, p, sl);
+    else
+      launch_k(topk_reg_kernel<SPLIT_KPT, SPLIT_NTH, false, 2>, grid, SPLIT_NTH, 0, st, p, sl);
+    const int rc = check_launch("topk_split");
+    if (rc) return rc;
+  }
+  return MTPSD_OK;
 }
 
 int launch_topk(const TopkPlan& p, cudaStream_t st) {
@@ -408,6 +601,8 @@ int launch_topk(const TopkPlan& p, cudaStream_t st) {
     if (nth == 512 && kpt <= 32) return xt ? launch_topk_reg<512, true>(p, kpt, st) : launch_topk_reg<512, false>(p, kpt, st);
     if (nth == 1024 && kpt <= 40) return xt ? launch_topk_reg<1024, true>(p, kpt, st) : launch_topk_reg<1024, false>(p, kpt, st);
   }
+  if (split_path(p)) return launch_topk_split(p, st);
+  // unaligned score rows: one CTA per row, radix passes
   int64_t cache_keys = p.max_len <= TOPK_SMEM_KEYS ? p.max_len : 0;
   size_t smem = (size_t)cache_keys * sizeof(uint32_t);
   if (smem > 48 * 1024)

@@ -102,6 +102,8 @@ class DecodeStep:
         # the indexer's score matrix (read back by the top-k) and its small work plan
         self.scores = torch.empty(R, api.scores_ld(self.max_visible), dtype=torch.float32, device=device)
         self.ws_plan = torch.empty(max(api.indexer_plan_bytes(B, R), 256), dtype=torch.uint8, device=device)
+        self.ws_topk = torch.empty(max(api.topk_workspace_size(R, self.max_visible, spec.topk), 256), dtype=torch.uint8,
+                                   device=device)
         n = api.sparse_mla_workspace_size(R, spec.H_Q, spec.topk, 0, 1 if self.fp8 else 0)
         self.ws_mla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
         # --- draft layer
@@ -144,6 +146,8 @@ class DecodeStep:
                           for _ in range(spec.draft_steps)]
             self.d_scores = torch.empty(B, api.scores_ld(self.d_max_visible), dtype=torch.float32, device=device)
             self.ws_dplan = torch.empty(max(api.indexer_plan_bytes(B, B), 256), dtype=torch.uint8, device=device)
+            self.ws_dtopk = torch.empty(max(api.topk_workspace_size(B, self.d_max_visible, spec.topk), 256),
+                                        dtype=torch.uint8, device=device)
             n = max(api.sparse_mla_workspace_size(B, spec.H_Q, spec.topk, j, 1 if self.fp8 else 0)
                     for j in range(spec.draft_steps))
             self.ws_dmla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
@@ -163,7 +167,7 @@ class DecodeStep:
 
     def verify_topk(self, stream=None):
         api.topk(self.scores, self.row_pos, self.max_visible, self.spec.topk, out_idx=self.topk_idx,
-                 dev_status=self.status, stream=stream, row_len_add=1)
+                 dev_status=self.status, stream=stream, row_len_add=1, workspace=self.ws_topk)
 
     def verify_indexer(self, stream=None):
         self.verify_scores(stream)
@@ -195,7 +199,7 @@ class DecodeStep:
     def draft_topk(self, stream=None):
         """Draft step 0 selection, then the share gather that steps 1.. reuse."""
         api.topk(self.d_scores, self.next_pos, self.d_max_visible, self.spec.topk, out_idx=self.d_topk,
-                 dev_status=self.status, stream=stream, row_len_add=1)
+                 dev_status=self.status, stream=stream, row_len_add=1, workspace=self.ws_dtopk)
         api.topk_share_gather(self.d_topk, self.d_row_offsets, None, self.shared_idx, dev_status=self.status,
                               stream=stream)
 
@@ -232,13 +236,15 @@ class DecodeStep:
         n = 0
         quant = 1 if self.fp8 else 0
         _, H_I, D_I = self.q_idx_raw.shape
-        idx = api.indexer_topk_launch_count(H_I, D_I, N.MTPSD_FP8_E4M3 if self.fp8 else N.MTPSD_F32)
+        dt = N.MTPSD_FP8_E4M3 if self.fp8 else N.MTPSD_F32
+        scores = api.indexer_scores_launch_count(H_I, D_I, dt)
+        k = self.spec.topk
         if self.spec.verify:
-            n += 1 + quant + idx + self._mla_launches(self.spec.topk, 0, self.R)
+            n += 1 + quant + scores + api.topk_launch_count(self.max_visible, k) + self._mla_launches(k, 0, self.R)
         n += 1
         if self.has_draft:
-            n += 1 + quant + idx + 1
-            n += sum(self._mla_launches(self.spec.topk, j, self.B) for j in range(self.spec.draft_steps))
+            n += 1 + quant + scores + api.topk_launch_count(self.d_max_visible, k) + 1
+            n += sum(self._mla_launches(k, j, self.B) for j in range(self.spec.draft_steps))
         return n
 
     def _mla_launches(self, n_idx, n_append, R):

@@ -104,6 +104,10 @@ def test_workspace_queries(native):
     assert lib.mtpsd_scores_ld(8198) % 4 == 0 and lib.mtpsd_scores_ld(8198) >= 8198
     ws = lib.mtpsd_indexer_topk_workspace_size(32, 192, 8198, 2048)
     assert ws >= 192 * 8198 * 4
+    assert lib.mtpsd_topk_workspace_size(192, 40960, 2048) == 0
+    # split path: two list buffers (level 1: 4 lists of 2048, level 2 is final) of 8-byte entries
+    assert lib.mtpsd_topk_workspace_size(10, 100000, 2048) == 10 * 4 * 2048 * 8
+    assert lib.mtpsd_topk_workspace_size(10, 600000, 2048) == 10 * 19 * 2048 * 8 + 10 * 2 * 2048 * 8
     plan = lib.mtpsd_indexer_topk_plan_bytes(32, 192)
     assert 0 < plan < 64 * 1024 and plan % 256 == 0
     # the workspace is the padded score matrix followed by the plan
@@ -118,6 +122,13 @@ def test_launch_count_queries(native):
     for R, n_append in ((192, 0), (32, 3), (1, 0)):
         assert lib.mtpsd_sparse_mla_launch_count(R, 128, 2048, n_append, native.MTPSD_BF16) in (1, 2)
         assert lib.mtpsd_sparse_mla_launch_count(R, 128, 2048, n_append, native.MTPSD_F32) in (1, 2)
-    assert lib.mtpsd_indexer_topk_launch_count(64, 128, native.MTPSD_FP8_E4M3) in (2, 3)
-    assert lib.mtpsd_indexer_topk_launch_count(64, 128, native.MTPSD_F32) == 2
-    assert lib.mtpsd_indexer_topk_launch_count(48, 128, native.MTPSD_FP8_E4M3) == 2   # no tensor-core shape
+    assert lib.mtpsd_indexer_topk_launch_count(64, 128, native.MTPSD_FP8_E4M3, 8198, 2048) in (2, 3)
+    assert lib.mtpsd_indexer_topk_launch_count(64, 128, native.MTPSD_F32, 8198, 2048) == 2
+    assert lib.mtpsd_indexer_topk_launch_count(48, 128, native.MTPSD_FP8_E4M3, 8198, 2048) == 2   # no tensor-core shape
+    # rows past 40960 keys: one launch per split level (32768-key segments, then merges of 16 lists)
+    assert lib.mtpsd_topk_launch_count(40960, 2048) == 1
+    assert lib.mtpsd_topk_launch_count(40961, 2048) == 2
+    assert lib.mtpsd_topk_launch_count(16 * 32768, 2048) == 2
+    assert lib.mtpsd_topk_launch_count(16 * 32768 + 1, 2048) == 3
+    assert lib.mtpsd_topk_launch_count(1 << 20, 4096) == 3            # 32 segments, merges of 8
+    assert lib.mtpsd_indexer_topk_launch_count(48, 128, native.MTPSD_F32, 100000, 2048) == 3
