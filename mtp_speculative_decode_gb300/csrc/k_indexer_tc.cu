@@ -8,20 +8,29 @@
 // so the tensor cores see only FP8 codes and the scales enter the epilogue.
 //
 // Shape of one MMA: M = 128 cached positions (the A operand: a 128 x 128 B
-// key tile, K-major, loaded by TMA with the 128-byte swizzle), N = 128 query
-// columns (2 rows x 64 heads, or 4 rows x 32 heads: the B operand, K-major),
-// K = 128 FP8 values in 4 steps of 32.  Putting the positions on M makes the
-// head sum of the epilogue thread-local: TMEM lane = position, columns =
-// (row, head).  The accumulators rotate through 4 TMEM slots of 128 columns
-// (512 columns) so that the MMAs of the next chunk run while the epilogue
-// drains the previous one.
+// key tile, K-major, loaded by TMA with the 128-byte swizzle), N = 64 * c
+// query columns (c units of 64 (row, head) columns, c <= 4: the B operand,
+// K-major), K = 128 FP8 values in 4 steps of 32.  Putting the positions on M
+// makes the head sum of the epilogue thread-local: TMEM lane = position,
+// columns = (row, head).
 //
-// Roles (320 threads, one persistent CTA per SM):
-//   warps 0-7  epilogue: tcgen05.ld of its 32 lanes x 64 columns, ReLU,
-//              weight, head sum, k_scale, coalesced score store
-//   warp 8     TMA producer: query rows of the current request group and a
-//              6-stage ring of key tiles
-//   warp 9     TMEM allocation and the MMA issue
+// TMEM is a ring of 8 slots of 64 columns; a unit is the 64 columns of one
+// slot: one row of 64 heads, or two rows of 32.  A key tile of a group of n
+// units takes the next n slots of the ring (their MMAs cover up to 4 adjacent
+// slots at once, split where the ring wraps), so a one-row group moves 8 tiles
+// ahead of the epilogue and a six-row group 1.3.
+//
+// Roles (448 threads, one persistent CTA per SM):
+//   warps 0-11  epilogue, 3 warpgroups: unit u is taken by warpgroup u % 3, so
+//               three units drain at once.  Each warp reads its 32 lanes x 64
+//               columns (tcgen05.ld), applies ReLU, the weights (w * q_scale,
+//               paired for fma.rn.f32x2), the head sum and k_scale, and stores
+//               one score per lane and row (coalesced).
+//   warp 12     TMA producer: the group's query rows, a 6-stage ring of key
+//               tiles, and a 16-stage ring of the tiles' key scales (132 floats
+//               from a 4-aligned start, so the copy's first coordinate is
+//               16-byte aligned; the epilogue indexes from the remainder).
+//   warp 13     TMEM allocation and the MMA issue.
 // The producer and MMA roles run with the whole warp (uniform loop state,
 // bounded waits taken by all lanes) and one elected lane issues.
 // Work: the rows of each request are cut into groups of up to 512/H rows
@@ -45,32 +54,40 @@ namespace itc {
 
 constexpr int TILE_M = 128;
 constexpr int KB = 128;                   // bytes per key / query head vector
-constexpr int NSTAGE = 6;
-constexpr int NSLOT = 4;
-constexpr int SLOT_COLS = 128;
+constexpr int NSTAGE = 6;                 // key tiles in flight
+constexpr int NKS = 16;                   // key-scale tiles in flight
+constexpr int KS_BOX = TILE_M + 4;        // key scales per copy (a 4-aligned start)
+constexpr int KS_STRIDE = 640;            // bytes per key-scale slot (128-byte aligned)
+constexpr int NSLOT = 8;                  // TMEM slots
+constexpr int SLOT_COLS = 64;
+constexpr int MAX_CHUNK = 4;              // slots per MMA
 constexpr int Q_ROWS = 512;               // query head vectors held in shared memory
-constexpr int EPI_WARPS = 8;
-constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;
-constexpr int THREADS = 320;
+constexpr int EPI_WG = 3;
+constexpr int EPI_WARPS = 4 * EPI_WG;
+constexpr int PRODUCER_WARP = EPI_WARPS;
+constexpr int MMA_WARP = EPI_WARPS + 1;
+constexpr int THREADS = 32 * (EPI_WARPS + 2);
 constexpr int MAX_GROUP_ROWS = Q_ROWS / 32;
 
 constexpr int OFF_K = 0;
 constexpr int OFF_Q = OFF_K + NSTAGE * TILE_M * KB;      // 98304
-constexpr int OFF_WQ = OFF_Q + Q_ROWS * KB;              // per epilogue warp: [Q_ROWS] float
+constexpr int OFF_KS = OFF_Q + Q_ROWS * KB;              // [NKS][KS_STRIDE]
+constexpr int OFF_WQ = OFF_KS + NKS * KS_STRIDE;         // per epilogue warp: [Q_ROWS] float
 constexpr int OFF_VIS = OFF_WQ + EPI_WARPS * Q_ROWS * 4; // per epilogue warp: [MAX_GROUP_ROWS] int64
 constexpr int OFF_BAR = OFF_VIS + EPI_WARPS * MAX_GROUP_ROWS * 8;
-constexpr int N_BARS = 2 * NSTAGE + 2 + 2 * NSLOT + 1;
+constexpr int NCH = 2 * NSLOT;            // chunk barriers (a chunk holds >= 1 of the <= NSLOT units in flight)
+constexpr int N_BARS = 2 * NSTAGE + 2 + NCH + NSLOT + 2 * NKS + 1;
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;         // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+static_assert((OFF_KS % 128) == 0 && (KS_STRIDE % 128) == 0, "key-scale slots are 128-byte aligned");
+static_assert(KS_BOX * 4 <= KS_STRIDE && (KS_BOX * 4) % 16 == 0, "key-scale box");
 
 constexpr unsigned long long WAIT_LIMIT_NS = mbar::DEFAULT_LIMIT_NS;
 
 struct Params {
   const float* q_scale;
   const float* w;
-  const float* k_scale;
   const int64_t* cache_start;
   const int64_t* row_pos;
   int64_t pool;
@@ -135,15 +152,16 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_byte_addr) {
   return d;
 }
 
-// Instruction descriptor: kind::f8f6f4, A = B = E4M3, D = F32, both K-major,
-// N = 128, M = 128.
-constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+// Instruction descriptor: kind::f8f6f4, A = B = E4M3, D = F32, both K-major, M = 128, N = 64 * c.
+__device__ __forceinline__ uint32_t idesc(int c) {
+  return (1u << 4) | ((uint32_t)(64 * c) >> 3 << 17) | ((128u >> 4) << 24);
+}
 
-__device__ __forceinline__ void mma_fp8(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void mma_fp8(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t id, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(a), "l"(b), "r"(IDESC), "r"(accumulate));
+      "l"(a), "l"(b), "r"(id), "r"(accumulate));
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
@@ -166,6 +184,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// acc.{x,y} += w.{x,y} * (a, b): two float32 FMAs in one instruction (fma.rn.f32x2).
+__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t w, float a, float b) {
+  asm("{\n .reg .b64 t;\n mov.b64 t, {%2, %3};\n fma.rn.f32x2 %0, %1, t, %0;\n}\n"
+      : "+l"(acc) : "l"(w), "f"(a), "f"(b));
+}
+__device__ __forceinline__ float sum2(uint64_t v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return a + b;
+}
 
 // (group, tile) cursor over the flattened work list
 struct Cursor {
@@ -273,6 +302,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const uint32_t* __restrict__
 template <int H>
 __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                 const __grid_constant__ CUtensorMap tmap_q,
+                                                                const __grid_constant__ CUtensorMap tmap_ks,
                                                                 Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -281,15 +311,18 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
   uint64_t* k_empty = bars + NSTAGE;
   uint64_t* q_full = bars + 2 * NSTAGE;
   uint64_t* q_empty = q_full + 1;
-  uint64_t* slot_full = q_full + 2;
-  uint64_t* slot_empty = slot_full + NSLOT;
-  uint64_t* drain = slot_empty + NSLOT;
+  uint64_t* chunk_full = q_full + 2;          // MMA chunk c done: chunk_full[c % NCH], phase c / NCH
+  uint64_t* slot_empty = chunk_full + NCH;
+  uint64_t* ks_full = slot_empty + NSLOT;
+  uint64_t* ks_empty = ks_full + NKS;
+  uint64_t* drain = ks_empty + NKS;
   uint32_t* tmem_slot = (uint32_t*)(sm + OFF_MISC);
   volatile int* abort_flag = (volatile int*)(sm + OFF_MISC + 4);
   // per-warp copies of the group's weights and visible lengths: each epilogue
   // warp fills and reads its own, so only __syncwarp orders them
   float* wq = (float*)(sm + OFF_WQ) + (threadIdx.x >> 5) * Q_ROWS;
   int64_t* vis = (int64_t*)(sm + OFF_VIS) + (threadIdx.x >> 5) * MAX_GROUP_ROWS;
+  constexpr int ROWS_PER_UNIT = SLOT_COLS / H;   // 1 (H = 64) or 2 (H = 32)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // The set-up below touches no global memory, so it overlaps the previous kernel's tail
@@ -301,9 +334,11 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int i = 0; i < NSLOT; ++i) {
-      mbar_init(&slot_full[i], 1);
-      mbar_init(&slot_empty[i], EPI_WARPS);
+    for (int i = 0; i < NCH; ++i) mbar_init(&chunk_full[i], 1);
+    for (int i = 0; i < NSLOT; ++i) mbar_init(&slot_empty[i], 4);   // the four warps of the unit's warpgroup
+    for (int i = 0; i < NKS; ++i) {
+      mbar_init(&ks_full[i], 1);
+      mbar_init(&ks_empty[i], EPI_WARPS);    // every epilogue warp, once per tile
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -318,6 +353,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
   if (warp == PRODUCER_WARP && elect_one()) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_k) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_q) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap_ks) : "memory");
   }
   tc_fence_before();
   __syncthreads();
@@ -358,12 +394,19 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
         cur_g = g;
       }
       const int stage = n_load % NSTAGE, round = n_load / NSTAGE;
+      const int kslot = n_load % NKS, kround = n_load / NKS;
       if (round > 0) ok = __all_sync(0xffffffffu, mbar_wait(&k_empty[stage], (round - 1) & 1, abort_flag, p.status));
+      if (ok && kround > 0)
+        ok = __all_sync(0xffffffffu, mbar_wait(&ks_empty[kslot], (kround - 1) & 1, abort_flag, p.status));
       if (!ok) break;
       const int64_t y = cstart + (int64_t)c.tile * TILE_M;
       if (elect_one()) {
         mbar_expect_tx(&k_full[stage], TILE_M * KB);
         tma_load_2d(saddr(sm + OFF_K + stage * TILE_M * KB), &tmap_k, 0, (int)y, &k_full[stage]);
+        // key scales of the tile from a 4-aligned start (16-byte aligned copy); elements past the pool
+        // read as zero
+        mbar_expect_tx(&ks_full[kslot], KS_BOX * 4);
+        tma_load_2d(saddr(sm + OFF_KS + kslot * KS_STRIDE), &tmap_ks, (int)(y & ~(int64_t)3), 0, &ks_full[kslot]);
       }
       __syncwarp();
       ++n_load;
@@ -374,10 +417,16 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
         const int issued = n_load / NSTAGE + (s < n_load % NSTAGE ? 1 : 0);   // loads of stage s
         if (issued > 0) mbar_wait(&k_full[s], (issued - 1) & 1, &dummy, p.status);
       }
+      for (int s = 0; s < NKS; ++s) {
+        const int issued = n_load / NKS + (s < n_load % NKS ? 1 : 0);
+        if (issued > 0) mbar_wait(&ks_full[s], (issued - 1) & 1, &dummy, p.status);
+      }
       if (gq > 0) mbar_wait(q_full, (gq - 1) & 1, &dummy, p.status);
     }
   } else if (warp == MMA_WARP) {
-    int n_cons = 0, n_chunk = 0, gq = 0, cur_g = -1, nch = 0;
+    int n_cons = 0, gq = 0, cur_g = -1, units = 0;
+    int u = 0;        // running unit (slot use) index
+    int nchunk = 0;   // running MMA chunk index
     bool ok = true;
     Cursor c;
     c.start(p, n_groups, it0);
@@ -392,34 +441,42 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
         if (!ok) break;
         ++gq;
         cur_g = g;
-        nch = (p.g_nrows[g] * H + SLOT_COLS - 1) / SLOT_COLS;
+        units = (p.g_nrows[g] * H + SLOT_COLS - 1) / SLOT_COLS;
       }
       const int stage = n_cons % NSTAGE, round = n_cons / NSTAGE;
+      // Every wait of the tile comes before its first MMA: once about four MMAs are queued, the issuing
+      // warp's memory instructions (these barrier probes included) stall until the queue drains, so
+      // waits between MMA batches would let the tensor pipe run dry once per batch.
       ok = __all_sync(0xffffffffu, mbar_wait(&k_full[stage], round & 1, abort_flag, p.status));
+      for (int v = 0; v < units && ok; ++v) {
+        const int ur = (u + v) / NSLOT;   // previous uses of the unit's slot
+        if (ur > 0)
+          ok = __all_sync(0xffffffffu, mbar_wait(&slot_empty[(u + v) % NSLOT], (ur - 1) & 1, abort_flag, p.status));
+      }
       if (!ok) break;
       tc_fence_after();
       const uint32_t a_base = saddr(sm + OFF_K + stage * TILE_M * KB);
-      for (int ch = 0; ch < nch && ok; ++ch) {
-        const int slot = n_chunk % NSLOT, sround = n_chunk / NSLOT;
-        if (sround > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&slot_empty[slot], (sround - 1) & 1, abort_flag, p.status));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        const uint32_t b_base = saddr(sm + OFF_Q + ch * SLOT_COLS * KB);
-        const uint32_t d = tmem_base + (uint32_t)(slot * SLOT_COLS);
+      for (int v0 = 0; v0 < units; ++nchunk) {
+        // the next up-to-4 units that sit in adjacent slots (the ring does not wrap inside one MMA)
+        const int s0 = (u + v0) % NSLOT;
+        int cnt = units - v0;
+        if (cnt > MAX_CHUNK) cnt = MAX_CHUNK;
+        if (cnt > NSLOT - s0) cnt = NSLOT - s0;
         if (elect_one()) {
+          const uint32_t b_base = saddr(sm + OFF_Q + v0 * SLOT_COLS * KB);
+          const uint32_t d = tmem_base + (uint32_t)(s0 * SLOT_COLS);
+          const uint32_t id = idesc(cnt);
 #pragma unroll
           for (int kk = 0; kk < KB / 32; ++kk)
-            mma_fp8(d, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), kk > 0 ? 1u : 0u);
-          mma_commit(&slot_full[slot]);
+            mma_fp8(d, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), id, kk > 0 ? 1u : 0u);
+          mma_commit(&chunk_full[nchunk % NCH]);
         }
         __syncwarp();
-        ++n_chunk;
+        v0 += cnt;
       }
-      if (!ok) break;
       if (elect_one()) mma_commit(&k_empty[stage]);
       __syncwarp();
+      u += units;
       ++n_cons;
     }
     // all issued MMAs complete before TMEM is released
@@ -429,22 +486,16 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
     mbar_wait(drain, 0, &dummy, p.status);
   } else {
     // ------------------------------------------------------------ epilogue
-    const int wg = warp >> 2;              // which 64 of the slot's 128 columns
+    const int wg = warp >> 2;              // this warpgroup takes units u with u % EPI_WG == wg
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const int pos_in_tile = quarter * 32 + lane;
-    constexpr int rows_per_wg = 64 / H;    // 1 (H = 64) or 2 (H = 32)
-    int n_chunk = 0, cur_g = -1, nrows = 0, row0 = 0, nch = 0, kq_tile = -1;
+    int cur_g = -1, nrows = 0, row0 = 0, units = 0, n_tile = 0, ks_off = 0;
+    int u = 0, nchunk = 0;   // running unit and MMA chunk indices (the MMA warp's chunking, replayed)
     int64_t vmax = 0, cstart = 0;
-    // key scales of this lane's position in the next KQ tiles of the group (loaded KQ tiles ahead:
-    // one tile of work is shorter than a DRAM round trip)
-    constexpr int KQ = 4;
-    float kq[KQ];
-#pragma unroll
-    for (int i = 0; i < KQ; ++i) kq[i] = 0.f;
     bool ok = true;
     Cursor c;
     c.start(p, n_groups, it0);
-    for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups)) {
+    for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups), ++n_tile) {
       const int g = c.g;
       if (g != cur_g) {
         __syncwarp();   // the warp is done with the previous group's copies
@@ -452,7 +503,8 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
         row0 = p.g_row0[g];
         vmax = p.g_vmax[g];
         cstart = p.cache_start[p.g_b[g]];
-        nch = (nrows * H + SLOT_COLS - 1) / SLOT_COLS;
+        ks_off = (int)(cstart & 3);
+        units = (nrows * H + SLOT_COLS - 1) / SLOT_COLS;
         {   // all of the group's (row, head) weights in flight at once
           float wv[Q_ROWS / 32], qv[Q_ROWS / 32];
 #pragma unroll
@@ -469,59 +521,72 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
         for (int i = lane; i < nrows; i += 32) vis[i] = min(p.row_pos[row0 + i] + 1, p.max_visible);
         __syncwarp();
         cur_g = g;
-        kq_tile = -1;
       }
-      // this position's key scale (0 past the group's visible length)
-      auto load_ks = [&](int tile) -> float {
-        const int64_t ss = (int64_t)tile * TILE_M + pos_in_tile;
-        const int64_t pr = cstart + ss;
-        return (ss < vmax && pr >= 0 && pr < p.pool) ? p.k_scale[pr] : 0.f;
-      };
-      if (kq_tile != c.tile) {   // first tile of the group in this CTA: fill the queue
-#pragma unroll
-        for (int i = 0; i < KQ; ++i) kq[i] = load_ks(c.tile + i);
-      }
-      const float ks = kq[0];
-#pragma unroll
-      for (int i = 0; i + 1 < KQ; ++i) kq[i] = kq[i + 1];
-      kq[KQ - 1] = load_ks(c.tile + KQ);
-      kq_tile = c.tile + 1;
+      const int kslot = n_tile % NKS, kround = n_tile / NKS;
+      // every epilogue warp waits for the tile's key scales (so that its release below can never count
+      // toward an earlier use of the slot), reads them if it owns a unit, and releases them
+      ok = __all_sync(0xffffffffu, mbar_wait(&ks_full[kslot], kround & 1, abort_flag, p.status));
+      if (!ok) break;
       const int64_t s = (int64_t)c.tile * TILE_M + pos_in_tile;
-      for (int ch = 0; ch < nch; ++ch) {
-        const int slot = n_chunk % NSLOT, sround = n_chunk / NSLOT;
+      const float ks = (s < vmax) ? ((const float*)(sm + OFF_KS + kslot * KS_STRIDE))[ks_off + pos_in_tile] : 0.f;
+      // chunks of the tile, as the MMA warp forms them: unit v is in chunk nchunk + chunk_of(v)
+      auto chunk_of = [&](int v) -> int {
+        int c = 0;
+#pragma unroll
+        for (int v0 = 0, k = 0; k < NSLOT; ++k) {
+          if (v0 >= units) break;
+          const int s0 = (u + v0) % NSLOT;
+          int cnt = units - v0;
+          if (cnt > MAX_CHUNK) cnt = MAX_CHUNK;
+          if (cnt > NSLOT - s0) cnt = NSLOT - s0;
+          if (v < v0 + cnt) break;
+          v0 += cnt;
+          ++c;
+        }
+        return c;
+      };
+      const int nch_tile = units > 0 ? chunk_of(units - 1) + 1 : 0;
+      // first unit of this tile that belongs to this warpgroup
+      int v = (wg - u % EPI_WG + EPI_WG) % EPI_WG;
+      for (; v < units; v += EPI_WG) {
+        const int uu = u + v;
+        const int slot = uu % NSLOT;
+        const int ch = nchunk + chunk_of(v);
         // warp-uniform outcome: tcgen05.ld below is a warp-collective instruction
-        ok = __all_sync(0xffffffffu, mbar_wait(&slot_full[slot], sround & 1, abort_flag, p.status));
+        ok = __all_sync(0xffffffffu, mbar_wait(&chunk_full[ch % NCH], (ch / NCH) & 1, abort_flag, p.status));
         if (!ok) break;
         tc_fence_after();
-        float v[64];
-        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(slot * SLOT_COLS + wg * 64);
-        tmem_ld32(taddr, v);
-        tmem_ld32(taddr + 32, v + 32);
+        float x[64];
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(slot * SLOT_COLS);
+        tmem_ld32(taddr, x);
+        tmem_ld32(taddr + 32, x + 32);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&slot_empty[slot]);
-        ++n_chunk;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          if (j >= rows_per_wg) break;
-          const int i = ch * (SLOT_COLS / H) + wg * rows_per_wg + j;   // row within the group
+        for (int j = 0; j < ROWS_PER_UNIT; ++j) {
+          const int i = v * ROWS_PER_UNIT + j;   // row within the group
           if (i >= nrows) break;
-          const float4* wr = (const float4*)(wq + i * H);
-          // four independent sums (heads h = 4k + m go to acc[m]) instead of one 64-long chain
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          const int hb = j * H;   // first column of row i within this warp's 64
+          // paired weights of row i: (w q_scale) of heads (2m, 2m+1), two pairs per 16-byte load
+          const ulonglong2* wr = (const ulonglong2*)(wq + i * H);
+          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+          const int hb = j * H;   // first column of row i within the unit
 #pragma unroll
-          for (int h4 = 0; h4 < H / 4; ++h4) {
-            float4 ww = wr[h4];
-            acc[0] = fmaf(ww.x, fmaxf(v[hb + h4 * 4 + 0], 0.f), acc[0]);
-            acc[1] = fmaf(ww.y, fmaxf(v[hb + h4 * 4 + 1], 0.f), acc[1]);
-            acc[2] = fmaf(ww.z, fmaxf(v[hb + h4 * 4 + 2], 0.f), acc[2]);
-            acc[3] = fmaf(ww.w, fmaxf(v[hb + h4 * 4 + 3], 0.f), acc[3]);
+          for (int m = 0; m < H / 4; ++m) {
+            const ulonglong2 ww = wr[m];
+            fma2(acc[(2 * m) & 3], ww.x, fmaxf(x[hb + 4 * m + 0], 0.f), fmaxf(x[hb + 4 * m + 1], 0.f));
+            fma2(acc[(2 * m + 1) & 3], ww.y, fmaxf(x[hb + 4 * m + 2], 0.f), fmaxf(x[hb + 4 * m + 3], 0.f));
           }
-          if (s < vis[i]) p.scores[(int64_t)(row0 + i) * p.ld + s] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * ks;
+          const float sc = (sum2(acc[0]) + sum2(acc[1])) + (sum2(acc[2]) + sum2(acc[3]));
+          if (s < vis[i]) p.scores[(int64_t)(row0 + i) * p.ld + s] = sc * ks;
         }
       }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ks_empty[kslot]);
+      u += units;
+      nchunk += nch_tile;
     }
   }
 
@@ -552,7 +617,7 @@ bool indexer_tc_supported(const IndexerPlan& p) {
   if (env && strcmp(env, "generic") == 0) return false;
   if (p.dtype != MTPSD_FP8_E4M3 || p.D != 128) return false;
   if (p.H != 64 && p.H != 32) return false;
-  if (((uintptr_t)p.k % 16) || ((uintptr_t)p.q % 16)) return false;
+  if (((uintptr_t)p.k % 16) || ((uintptr_t)p.q % 16) || ((uintptr_t)p.k_scale % 16)) return false;
   if (p.pool < 1 || p.pool > 0x7fffffffLL || (int64_t)p.R * p.H > 0x7fffffffLL) return false;
   if (p.max_visible > 0x7fffffffLL - itc::TILE_M) return false;
   if (!p.plan_ws) return false;
@@ -568,8 +633,9 @@ int indexer_launch_count(int H, int D, int dtype) {
 
 int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {
   using namespace itc;
-  CUtensorMap mk, mq;
-  if (!make_map_rows128(&mk, p.k, p.pool, TILE_M) || !make_map_rows128(&mq, p.q, (int64_t)p.R * p.H, (uint32_t)p.H)) {
+  CUtensorMap mk, mq, mks;
+  if (!make_map_rows128(&mk, p.k, p.pool, TILE_M) || !make_map_rows128(&mq, p.q, (int64_t)p.R * p.H, (uint32_t)p.H) ||
+      !make_tma_1d_f32(&mks, p.k_scale, (uint64_t)p.pool, KS_BOX)) {
     set_error("indexer: cuTensorMapEncodeTiled failed");
     return MTPSD_ECUDA;
   }
@@ -588,7 +654,7 @@ int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {
   int rc = check_launch("indexer_tc_plan");
   if (rc) return rc;
   Params kp;
-  kp.q_scale = p.q_scale; kp.w = p.w; kp.k_scale = p.k_scale; kp.cache_start = p.cache_start;
+  kp.q_scale = p.q_scale; kp.w = p.w; kp.cache_start = p.cache_start;
   kp.row_pos = p.row_pos; kp.pool = p.pool; kp.max_visible = p.max_visible; kp.scores = p.scores; kp.ld = p.ld;
   kp.H = p.H; kp.g_b = g_b; kp.g_row0 = g_row0; kp.g_nrows = g_nrows; kp.g_vmax = g_vmax; kp.g_tile0 = g_tile0;
   kp.n_groups = n_groups; kp.status = p.status;
@@ -599,9 +665,9 @@ int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {
     return MTPSD_ECUDA;
   }
   if (p.H == 64)
-    launch_k(indexer_tc_kernel<64>, num_sms(), THREADS, SMEM_BYTES, st, mk, mq, kp);
+    launch_k(indexer_tc_kernel<64>, num_sms(), THREADS, SMEM_BYTES, st, mk, mq, mks, kp);
   else
-    launch_k(indexer_tc_kernel<32>, num_sms(), THREADS, SMEM_BYTES, st, mk, mq, kp);
+    launch_k(indexer_tc_kernel<32>, num_sms(), THREADS, SMEM_BYTES, st, mk, mq, mks, kp);
   return check_launch("indexer_tc");
 }
 

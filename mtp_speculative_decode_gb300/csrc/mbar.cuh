@@ -64,5 +64,15 @@ __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile in
   }
 }
 
+// A non-blocking probe of the phase with the given parity (CTA scope).
+__device__ __forceinline__ bool test_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+  return ok != 0;
+}
+
 }  // namespace mbar
 }  // namespace mtpsd

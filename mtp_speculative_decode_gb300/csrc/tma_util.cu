@@ -39,6 +39,22 @@ bool make_tma_2d(void* map, int dtype_u8_or_bf16, const void* base, uint64_t inn
   return r == CUDA_SUCCESS;
 }
 
+// Float32 vector as a [1, n_elems] tensor map without swizzle (rank 2 with a single row, so the
+// encoding has a stride to check; box of box_elems x 1, box_elems * 4 a multiple of 16 bytes; a copy's
+// start coordinate must be a multiple of 4 elements).  Elements past n_elems read as 0.
+bool make_tma_1d_f32(void* map, const void* base, uint64_t n_elems, uint32_t box_elems) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)n_elems, 1};
+  cuuint64_t strides[1] = {(cuuint64_t)((n_elems * 4 + 15) / 16 * 16)};
+  cuuint32_t box[2] = {box_elems, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn((CUtensorMap*)map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Tensor map for TMA stores from shared memory: rank 2 or 3, bf16 or float32, 128-byte swizzle
 // (the box's inner extent must be 128 bytes).  dims[0] is the contiguous dimension; strides are the
 // byte strides of dims 1.. (multiples of 16).
