@@ -23,9 +23,10 @@
 // Roles (448 threads, one persistent CTA per SM):
 //   warps 0-11  epilogue, 3 warpgroups: unit u is taken by warpgroup u % 3, so
 //               three units drain at once.  Each warp reads its 32 lanes x 64
-//               columns (tcgen05.ld), applies ReLU, the weights (w * q_scale,
-//               paired for fma.rn.f32x2), the head sum and k_scale, and stores
-//               one score per lane and row (coalesced).
+//               columns (tcgen05.ld), applies ReLU and the weights (w * q_scale)
+//               as (x + |x|) * (w q_scale / 2), two FMA-pipe instructions per
+//               value, then the head sum and k_scale, and stores one score per
+//               lane and row (coalesced).
 //   warp 12     TMA producer: the group's query rows, a 6-stage ring of key
 //               tiles, and a 16-stage ring of the tiles' key scales (132 floats
 //               from a 4-aligned start, so the copy's first coordinate is
@@ -184,17 +185,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// acc.{x,y} += w.{x,y} * (a, b): two float32 FMAs in one instruction (fma.rn.f32x2).
-__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t w, float a, float b) {
-  asm("{\n .reg .b64 t;\n mov.b64 t, {%2, %3};\n fma.rn.f32x2 %0, %1, t, %0;\n}\n"
-      : "+l"(acc) : "l"(w), "f"(a), "f"(b));
-}
-__device__ __forceinline__ float sum2(uint64_t v) {
-  float a, b;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-  return a + b;
-}
 
 // (group, tile) cursor over the flattened work list
 struct Cursor {
@@ -514,9 +504,10 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
             wv[k] = in ? p.w[(int64_t)row0 * H + e] : 0.f;
             qv[k] = in ? p.q_scale[(int64_t)row0 * H + e] : 0.f;
           }
+          // halved: the epilogue forms 2 ReLU(x) = x + |x| (exact) on the FMA pipe
 #pragma unroll
           for (int k = 0; k < Q_ROWS / 32; ++k)
-            if (lane + 32 * k < nrows * H) wq[lane + 32 * k] = wv[k] * qv[k];
+            if (lane + 32 * k < nrows * H) wq[lane + 32 * k] = 0.5f * (wv[k] * qv[k]);
         }
         for (int i = lane; i < nrows; i += 32) vis[i] = min(p.row_pos[row0 + i] + 1, p.max_visible);
         __syncwarp();
@@ -568,17 +559,20 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
         for (int j = 0; j < ROWS_PER_UNIT; ++j) {
           const int i = v * ROWS_PER_UNIT + j;   // row within the group
           if (i >= nrows) break;
-          // paired weights of row i: (w q_scale) of heads (2m, 2m+1), two pairs per 16-byte load
-          const ulonglong2* wr = (const ulonglong2*)(wq + i * H);
-          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+          // ReLU(x) w = (x + |x|) (w / 2): an FADD with the free |.| operand modifier and an FFMA, both
+          // on the FMA pipe (x + |x| is 2x or +0 exactly, so the products equal those of max(x, 0) w)
+          const float4* wr = (const float4*)(wq + i * H);
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};   // heads h = 4k + m go to acc[m]
           const int hb = j * H;   // first column of row i within the unit
 #pragma unroll
           for (int m = 0; m < H / 4; ++m) {
-            const ulonglong2 ww = wr[m];
-            fma2(acc[(2 * m) & 3], ww.x, fmaxf(x[hb + 4 * m + 0], 0.f), fmaxf(x[hb + 4 * m + 1], 0.f));
-            fma2(acc[(2 * m + 1) & 3], ww.y, fmaxf(x[hb + 4 * m + 2], 0.f), fmaxf(x[hb + 4 * m + 3], 0.f));
+            const float4 ww = wr[m];
+            acc[0] = fmaf(ww.x, x[hb + 4 * m + 0] + fabsf(x[hb + 4 * m + 0]), acc[0]);
+            acc[1] = fmaf(ww.y, x[hb + 4 * m + 1] + fabsf(x[hb + 4 * m + 1]), acc[1]);
+            acc[2] = fmaf(ww.z, x[hb + 4 * m + 2] + fabsf(x[hb + 4 * m + 2]), acc[2]);
+            acc[3] = fmaf(ww.w, x[hb + 4 * m + 3] + fabsf(x[hb + 4 * m + 3]), acc[3]);
           }
-          const float sc = (sum2(acc[0]) + sum2(acc[1])) + (sum2(acc[2]) + sum2(acc[3]));
+          const float sc = (acc[0] + acc[1]) + (acc[2] + acc[3]);
           if (s < vis[i]) p.scores[(int64_t)(row0 + i) * p.ld + s] = sc * ks;
         }
       }

@@ -43,23 +43,45 @@ __device__ __forceinline__ bool try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same probe, but a thread whose phase is not complete sleeps until it completes or hint_ns pass
+// (the suspend-time hint), instead of returning at once: a waiting warp then takes no issue slots from
+// the warps that work.
+template <bool CLUSTER>
+__device__ __forceinline__ bool try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);
+  uint32_t ok;
+  if constexpr (CLUSTER) {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, "
+        "0, p;\n}\n"
+        : "=r"(ok) : "r"(a), "r"(parity), "r"(hint_ns) : "memory");
+  } else {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(a), "r"(parity), "r"(hint_ns) : "memory");
+  }
+  return ok != 0;
+}
+
+// Longest sleep of one probe: short against the time limit, so the abort flag and the limit are still
+// checked often, and long against any phase of a healthy launch.
+constexpr uint32_t SLEEP_HINT_NS = 20000;
+
 // Waits for the phase; false when it gave up: the limit passed (this thread then sets *abort_flag and
-// flags the status word) or another role of the CTA set *abort_flag first.  Both are checked every 256
-// probes.
+// flags the status word) or another role of the CTA set *abort_flag first.  Both are checked after
+// every sleeping probe.
 template <bool CLUSTER>
 __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
                                      unsigned long long limit_ns) {
   if (try_wait<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (try_wait<CLUSTER>(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
-        *abort_flag = 1;
-        flag_status(status, MTPSD_STATUS_WAIT_TIMEOUT);
-        return false;
-      }
+  for (;;) {
+    if (try_wait_sleep<CLUSTER>(bar, parity, SLEEP_HINT_NS)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      flag_status(status, MTPSD_STATUS_WAIT_TIMEOUT);
+      return false;
     }
   }
 }
