@@ -36,3 +36,74 @@ def accept_greedy(draft: np.ndarray, target_argmax: np.ndarray, magic_draft_id: 
         n_acc[b] = n
         nxt[b] = tgt[b, n]
     return n_acc, nxt
+
+
+def _sample_index(weights: np.ndarray, u: float) -> int:
+    """Inverse-CDF draw: the smallest t with sum_{s <= t} weights[s] > u * sum(weights),
+    sums in float64 in index order.  -1 when the total weight is zero."""
+    w = np.asarray(weights, dtype=np.float64)
+    total = float(np.sum(w))
+    if not total > 0.0:
+        return -1
+    target = float(u) * total
+    run = 0.0
+    for t in range(len(w)):
+        run += w[t]
+        if run > target:
+            return t
+    # rounding left the running sum at or below the target: the last token with weight
+    return int(np.nonzero(w > 0)[0][-1])
+
+
+def accept_stochastic(draft, draft_probs, target_probs, u_accept, u_sample):
+    """Rejection-sampling acceptance of a chain of K drafts ([P2] "接受判定:greedy 与
+    rejection sampling": the draft distribution q and the target distribution p,
+    each draft accepted with probability min(1, p/q); a rejected position draws a
+    token from the corrected distribution instead).  The pages do not print the
+    corrected distribution; the reading adopted is the standard one of
+    speculative sampling, max(0, p - q) normalised, and after K accepted drafts the
+    next token is drawn from p of row K.
+
+    draft [B, K] int64; draft_probs q [B, K, V] float32; target_probs p [B, K+1, V]
+    float32; u_accept [B, K] and u_sample [B] float32 uniforms in [0, 1) (the
+    random numbers are inputs).
+
+    Step i accepts d = draft[b, i] when u_accept[b, i] * q[b, i, d] < p[b, i, d]
+    (the accept test u < p/q without a division).  The product and the comparison
+    are single precision, as in the kernel, since they decide an integer; a draft
+    id outside [0, V) is rejected.  At the first rejected step n the next token is
+    the inverse-CDF draw (u_sample) from r = max(0, p[b,n] - q[b,n]) (single
+    precision differences, float64 sums); if r has no mass, from p[b,n].  After K
+    accepted steps it is the draw from p[b,K].  A distribution with no mass at all
+    gives token 0.
+
+    Returns (num_accepted [B] int32, next_tokens [B] int64).
+    """
+    draft = np.asarray(draft, dtype=np.int64)
+    q = np.asarray(draft_probs, dtype=np.float32)
+    p = np.asarray(target_probs, dtype=np.float32)
+    ua = np.asarray(u_accept, dtype=np.float32)
+    us = np.asarray(u_sample, dtype=np.float32)
+    B, K = draft.shape
+    V = p.shape[2]
+    n_acc = np.zeros(B, dtype=np.int32)
+    nxt = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        n = 0
+        while n < K:
+            d = int(draft[b, n])
+            if not (0 <= d < V):
+                break
+            if not (np.float32(ua[b, n] * q[b, n, d]) < p[b, n, d]):
+                break
+            n += 1
+        if n < K:
+            r = np.maximum(np.float32(0.0), (p[b, n] - q[b, n]).astype(np.float32))
+            t = _sample_index(r, us[b])
+            if t < 0:
+                t = _sample_index(p[b, n], us[b])
+        else:
+            t = _sample_index(p[b, K], us[b])
+        n_acc[b] = n
+        nxt[b] = max(t, 0)
+    return n_acc, nxt

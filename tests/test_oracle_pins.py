@@ -450,3 +450,81 @@ def test_draft_latent_rows_overlay_hand_worked():
     # request 1: accept length 1 -> only position 7; position 8 is the pool row (pool row 28)
     rows = o.draft_latent_rows(n_acc, 1, [8, 7, 3])
     assert rows[:, 0].tolist() == [128, -11, 123]
+
+
+# --------------------------------------------------------------------- stochastic acceptance
+
+def test_accept_stochastic_hand_worked():
+    # row 0: p/q = 0.6/0.25 = 2.4 for draft 1, accepted for every u; row 1: p/q = 0.1/0.7 for draft 1
+    p = np.array([[[0.1, 0.6, 0.2, 0.1], [0.5, 0.1, 0.2, 0.2], [0.0, 0.0, 0.3, 0.7]]], np.float32)
+    q = np.array([[[0.25, 0.25, 0.25, 0.25], [0.1, 0.7, 0.1, 0.1]]], np.float32)
+    d = np.array([[1, 1]])
+    # u = 0.5 rejects row 1 (0.5 * 0.7 >= 0.1); residual max(0, p1 - q1) = [0.4, 0, 0.1, 0.1], mass 0.6
+    n, t = accept.accept_stochastic(d, q, p, np.array([[0.9, 0.5]], np.float32), np.array([0.7], np.float32))
+    assert n.tolist() == [1] and t.tolist() == [2]      # 0.7 * 0.6 = 0.42: cumsum 0.4, 0.4, 0.5 -> token 2
+    n, t = accept.accept_stochastic(d, q, p, np.array([[0.9, 0.5]], np.float32), np.array([0.5], np.float32))
+    assert n.tolist() == [1] and t.tolist() == [0]      # 0.3 < 0.4 -> token 0
+    # u = 0.1 accepts row 1 too (0.1 * 0.7 = 0.07 < 0.1): the next token comes from p2 = [0, 0, 0.3, 0.7]
+    n, t = accept.accept_stochastic(d, q, p, np.array([[0.0, 0.1]], np.float32), np.array([0.5], np.float32))
+    assert n.tolist() == [2] and t.tolist() == [3]      # 0.5 * 1.0 = 0.5: cumsum 0, 0, 0.3, 1.0 -> token 3
+    # a draft outside the vocabulary is rejected; an identical draft and target distribution always accepts
+    n, t = accept.accept_stochastic(np.array([[9, 1]]), q, p, np.array([[0.0, 0.0]], np.float32),
+                                    np.array([0.0], np.float32))
+    # residual of row 0 is max(0, p0 - q0) = [0, 0.35, 0, 0]: all its mass is on token 1
+    assert n.tolist() == [0] and t.tolist() == [1]
+    # p == q accepts whatever u is (u q < q for u < 1)
+    n, _ = accept.accept_stochastic(d, p[:, :2], p, np.array([[0.999, 0.999]], np.float32),
+                                    np.array([0.3], np.float32))
+    assert n.tolist() == [2]
+
+
+def _spec_sampling_trials(p, q, n_trials, seed):
+    """Emitted tokens of n_trials independent one-draft chains (K = 1): the draft
+    is drawn from q by inverse CDF, then the oracle decides."""
+    rng = np.random.default_rng(seed)
+    V = p.shape[-1]
+    cq = np.cumsum(q[0].astype(np.float64))
+    first, second = [], []
+    for _ in range(n_trials):
+        d = int(np.searchsorted(cq, rng.random() * cq[-1], side="right"))
+        d = min(d, V - 1)
+        n, t = accept.accept_stochastic(np.array([[d]]), q[None], p[None],
+                                        rng.random((1, 1)).astype(np.float32),
+                                        rng.random(1).astype(np.float32))
+        if n[0] == 1:
+            first.append(d)
+            second.append(int(t[0]))
+        else:
+            first.append(int(t[0]))
+    return np.array(first), np.array(second)
+
+
+def test_accept_stochastic_emits_the_target_distribution():
+    """The defining property of speculative sampling (no assumption on how the
+    kernel computes it): the first emitted token, accepted draft or corrected
+    draw, is distributed exactly as the target p0, whatever q0 is; and after an
+    accepted draft the bonus token is distributed as p1."""
+    rng = np.random.default_rng(31)
+    V = 6
+    p = rng.dirichlet(np.ones(V), size=2).astype(np.float32)        # rows 0 and 1 of the target
+    q = rng.dirichlet(np.ones(V) * 0.7, size=1).astype(np.float32)  # the draft's row 0
+    N = 60000
+    first, second = _spec_sampling_trials(p, q, N, 7)
+    f1 = np.bincount(first, minlength=V) / N
+    sd = np.sqrt(p[0] * (1 - p[0]) / N)
+    assert np.all(np.abs(f1 - p[0]) < 5 * sd + 1e-4), (f1, p[0])
+    f2 = np.bincount(second, minlength=V) / max(len(second), 1)
+    sd2 = np.sqrt(p[1] * (1 - p[1]) / max(len(second), 1))
+    assert np.all(np.abs(f2 - p[1]) < 5 * sd2 + 1e-4), (f2, p[1])
+    # and the acceptance rate is sum_v min(p0, q0)
+    acc_rate = len(second) / N
+    want = float(np.minimum(p[0], q[0]).sum())
+    assert abs(acc_rate - want) < 5 * np.sqrt(want * (1 - want) / N)
+
+
+def test_accept_stochastic_inverse_cdf_boundaries():
+    w = np.array([0.0, 0.25, 0.0, 0.5, 0.25], np.float32)
+    # u * 1.0 against cumulative 0, .25, .25, .75, 1.0: strictly-greater rule
+    for u, want in [(0.0, 1), (0.2499, 1), (0.25, 3), (0.7499, 3), (0.75, 4), (0.9999, 4)]:
+        assert accept._sample_index(w, u) == want, (u, want)
+    assert accept._sample_index(np.zeros(4, np.float32), 0.5) == -1
