@@ -38,21 +38,39 @@ def accept_greedy(draft: np.ndarray, target_argmax: np.ndarray, magic_draft_id: 
     return n_acc, nxt
 
 
+FIX_SHIFT = 32   # weights are compared at 2^-32 resolution
+
+
+def _fixed_weights(weights) -> list:
+    """floor(w * 2^32) of each single-precision weight, as exact integers."""
+    w = np.asarray(weights, dtype=np.float32).astype(np.float64)   # exact widening
+    return [int(np.floor(x * 2.0 ** FIX_SHIFT)) for x in w.tolist()]
+
+
+def _scaled_floor(u: float, total: int) -> int:
+    """floor(u * total) exactly, for a single-precision u in [0, 1)."""
+    m, e = np.frexp(np.float64(np.float32(u)))     # u = m * 2^e, m in [0.5, 1)
+    mant = int(m * 2 ** 24)                        # the 24-bit significand, exact
+    shift = 24 - int(e)
+    return (mant * total) >> shift if mant else 0
+
+
 def _sample_index(weights: np.ndarray, u: float) -> int:
-    """Inverse-CDF draw: the smallest t with sum_{s <= t} weights[s] > u * sum(weights),
-    sums in float64 in index order.  -1 when the total weight is zero."""
-    w = np.asarray(weights, dtype=np.float64)
-    total = float(np.sum(w))
-    if not total > 0.0:
+    """Inverse-CDF draw: the smallest t with W(t) > floor(u * W(V-1)), where W(t)
+    is the running sum of floor(w * 2^32) over tokens 0..t (exact integers, so
+    the draw does not depend on the order of the additions).  -1 when the total
+    weight is zero."""
+    w = _fixed_weights(weights)
+    total = sum(w)
+    if total == 0:
         return -1
-    target = float(u) * total
-    run = 0.0
-    for t in range(len(w)):
-        run += w[t]
+    target = _scaled_floor(u, total)
+    run = 0
+    for t, x in enumerate(w):
+        run += x
         if run > target:
             return t
-    # rounding left the running sum at or below the target: the last token with weight
-    return int(np.nonzero(w > 0)[0][-1])
+    raise AssertionError("unreachable: target < total")
 
 
 def accept_stochastic(draft, draft_probs, target_probs, u_accept, u_sample):

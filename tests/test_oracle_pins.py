@@ -528,3 +528,20 @@ def test_accept_stochastic_inverse_cdf_boundaries():
     for u, want in [(0.0, 1), (0.2499, 1), (0.25, 3), (0.7499, 3), (0.75, 4), (0.9999, 4)]:
         assert accept._sample_index(w, u) == want, (u, want)
     assert accept._sample_index(np.zeros(4, np.float32), 0.5) == -1
+
+
+def test_accept_stochastic_fixed_point_is_exact():
+    """The threshold floor(u * total) and the weights floor(w * 2^32) equal the
+    exact rational values (fractions.Fraction of the single-precision inputs)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(5)
+    us = np.concatenate([rng.random(200).astype(np.float32),
+                         np.array([0.0, 1e-30, 0.5, 0.99999994, 2.0 ** -24, 0.75], np.float32)])
+    totals = [1, 3, 2 ** 32, 2 ** 40 + 12345, 154880 * (2 ** 32 - 1), 2 ** 63 - 1]
+    for u in us:
+        for tot in totals:
+            want = int(Fraction(float(u)) * tot)   # floor, both non-negative
+            assert accept._scaled_floor(u, tot) == want, (u, tot)
+    ws = np.concatenate([rng.random(200).astype(np.float32), np.array([0.0, 1.0, 2.0 ** -40, 3e-10], np.float32)])
+    got = accept._fixed_weights(ws)
+    assert got == [int(Fraction(float(w)) * 2 ** 32) for w in ws]
