@@ -271,6 +271,29 @@ int mtpsd_accept_greedy(const int64_t* draft, const int64_t* target_argmax, int3
                         void* stream);
 
 /* ------------------------------------------------------------------------
+ * Rejection-sampling acceptance.  [P2] "接受判定:greedy 与 rejection sampling":
+ * draft i is accepted with probability min(1, p/q) (q the draft distribution,
+ * p the target distribution of verify row i); the first rejected position
+ * draws its token from the corrected distribution max(0, p - q) normalised
+ * (the standard speculative-sampling correction; p itself if that has no
+ * mass); after K accepted drafts the next token is drawn from p of row K.
+ *   draft [B, K] int64, draft_probs q [B, K, V] float32,
+ *   target_probs p [B, K+1, V] float32 (probabilities in [0, 1]),
+ *   u_accept [B, K], u_sample [B] float32 uniforms in [0, 1) (the caller draws them)
+ *   -> num_accepted [B] int32 (n_b), next_tokens [B] int64.
+ * Draft i is accepted when u_accept[b,i] * q[b,i,d] < p[b,i,d] (single
+ * precision product); a draft id outside [0, V) is rejected and flagged
+ * MTPSD_STATUS_INDEX_RANGE.  The draw is an exact inverse CDF on fixed-point
+ * weights floor(max(w, 0) * 2^32): the smallest token whose running sum
+ * exceeds floor(u_sample * total), with exact integer sums (a row with no
+ * mass at all gives token 0).  Reads two rows of V per request beyond the K
+ * gathered entries.
+ */
+int mtpsd_accept_stochastic(const int64_t* draft, const float* draft_probs, const float* target_probs,
+                            const float* u_accept, const float* u_sample, int32_t B, int32_t K, int64_t V,
+                            int32_t* num_accepted, int64_t* next_tokens, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * Accepted-segment KV write-back.  [P2] "KV 交账:接受段的搬移与拒绝段的回收"
  * and "draft_extend:把接受段写回草稿层" / "草稿层 KV 的账": only the accepted
  * rows (bonus included: num_accepted[b]+1 rows, at least 1, at most W) of the

@@ -74,6 +74,7 @@ SIGNATURES = {
     "mtpsd_indexer_topk_launch_count": (i32, [i32, i32, i32, i64, i32]),
     "mtpsd_sparse_mla_decode": (C.c_int, [C.POINTER(MlaArgs), vp]),
     "mtpsd_accept_greedy": (C.c_int, [vp, vp, i32, i32, i64, vp, vp, vp]),
+    "mtpsd_accept_stochastic": (C.c_int, [vp, vp, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp]),
     "mtpsd_kv_writeback": (C.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp]),
     "mtpsd_topk_share_gather": (C.c_int, [vp, vp, vp, i32, i32, vp, vp, vp]),
     "mtpsd_check_bounded_wait": (C.c_int, [i64, vp, vp, vp]),

@@ -283,6 +283,31 @@ def accept_greedy(draft, target_argmax, magic_draft_id: int = -1, num_accepted=N
     return num_accepted, next_tokens
 
 
+def accept_stochastic(draft, draft_probs, target_probs, u_accept, u_sample, num_accepted=None, next_tokens=None,
+                      dev_status=None, stream=None):
+    """Rejection-sampling acceptance: draft [B, K] int64, draft_probs [B, K, V] and target_probs [B, K+1, V]
+    float32, u_accept [B, K] and u_sample [B] float32 uniforms."""
+    _need(draft, "draft", torch.int64, 2)
+    _need(draft_probs, "draft_probs", torch.float32, 3)
+    _need(target_probs, "target_probs", torch.float32, 3)
+    _need(u_accept, "u_accept", torch.float32, 2)
+    _need(u_sample, "u_sample", torch.float32, 1)
+    B, K = draft.shape
+    V = target_probs.shape[2]
+    if target_probs.shape != (B, K + 1, V) or draft_probs.shape != (B, K, V) or u_accept.shape != (B, K) \
+            or u_sample.shape != (B,):
+        raise ValueError("shapes must be draft [B,K], draft_probs [B,K,V], target_probs [B,K+1,V], "
+                         "u_accept [B,K], u_sample [B]")
+    if num_accepted is None:
+        num_accepted = torch.empty(B, dtype=torch.int32, device=draft.device)
+    if next_tokens is None:
+        next_tokens = torch.empty(B, dtype=torch.int64, device=draft.device)
+    check("mtpsd_accept_stochastic", lib().mtpsd_accept_stochastic(
+        _ptr(draft), _ptr(draft_probs), _ptr(target_probs), _ptr(u_accept), _ptr(u_sample), B, K, V,
+        _ptr(num_accepted), _ptr(next_tokens), _ptr(dev_status), _stream(stream)))
+    return num_accepted, next_tokens
+
+
 def kv_writeback(src_latent, src_idxk, src_idxs, num_accepted, dst_latent, dst_idxk, dst_idxs, cache_start, dst_pos,
                  next_pos=None, dev_status=None, stream=None):
     bf16 = src_latent.dtype == torch.bfloat16

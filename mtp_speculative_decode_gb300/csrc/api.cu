@@ -248,6 +248,18 @@ int mtpsd_accept_greedy(const int64_t* draft, const int64_t* target_argmax, int3
                               (cudaStream_t)stream);
 }
 
+int mtpsd_accept_stochastic(const int64_t* draft, const float* draft_probs, const float* target_probs,
+                            const float* u_accept, const float* u_sample, int32_t B, int32_t K, int64_t V,
+                            int32_t* num_accepted, int64_t* next_tokens, int32_t* dev_status, void* stream) {
+  g_err[0] = 0;
+  if (B < 0 || K < 0 || V < 1 || V > 0x7fffffffLL) return fail(MTPSD_EINVAL, "accept_stochastic: need B >= 0, K >= 0, 1 <= V < 2^31");
+  if (B == 0) return MTPSD_OK;
+  if ((K > 0 && (!draft || !draft_probs || !u_accept)) || !target_probs || !u_sample || !num_accepted || !next_tokens)
+    return fail(MTPSD_EINVAL, "accept_stochastic: null pointer");
+  return launch_accept_stochastic(draft, draft_probs, target_probs, u_accept, u_sample, B, K, V, num_accepted,
+                                  next_tokens, dev_status, (cudaStream_t)stream);
+}
+
 int mtpsd_kv_writeback(const void* src_latent, const uint8_t* src_idxk, const float* src_idxs, int32_t B, int32_t W,
                        int32_t latent_dtype, int32_t idx_dim, const int32_t* num_accepted, void* dst_latent,
                        uint8_t* dst_idxk, float* dst_idxs, const int64_t* cache_start, const int64_t* dst_pos, int64_t pool_tokens,

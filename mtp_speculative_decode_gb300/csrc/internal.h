@@ -25,6 +25,8 @@ int launch_kv_writeback(const void* src_l, const uint8_t* src_k, const float* sr
                         int lat_bytes, int idx_bytes, const int32_t* n_acc, void* dst_l, uint8_t* dst_k,
                         float* dst_s, const int64_t* cache_start, const int64_t* dst_pos, int64_t pool, int64_t* next_pos,
                         int32_t* status, cudaStream_t st);
+int launch_accept_stochastic(const int64_t* draft, const float* q, const float* p, const float* ua, const float* us,
+                             int B, int K, int64_t V, int32_t* n_acc, int64_t* next, int32_t* status, cudaStream_t st);
 int launch_bounded_wait_check(int64_t limit_ns, int32_t* status, int64_t* out, cudaStream_t st);
 int launch_share_gather(const int32_t* s0, const uint32_t* ro, const int32_t* n_acc, int B, int k,
                         int32_t* out, int32_t* status, cudaStream_t st);

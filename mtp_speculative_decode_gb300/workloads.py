@@ -363,3 +363,24 @@ def draft_tensors(w: Workload) -> Tensors:
     draft pool (latent + indexer key), the 6-row window of draft-layer KV to
     write back, and the per-step queries."""
     return w.tensors
+
+
+def stochastic_inputs(seed: int, B: int, K: int, V: int, temperature: float = 1.0, noise: float = 0.5):
+    """Synthetic inputs of rejection-sampling acceptance: target probabilities
+    p [B, K+1, V] = softmax of N(0, 1) logits / temperature, draft probabilities
+    q [B, K, V] = softmax of the same logits plus N(0, noise^2) (a draft that
+    roughly follows the target), draft tokens drawn from q by inverse CDF with
+    the generator's own uniforms, and the uniforms of the accept tests and of
+    the draws.  Returns numpy arrays (draft, q, p, u_accept, u_sample)."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, _key("stochastic"), B, K, V])))
+    logits = g.standard_normal((B, K + 1, V)) / temperature
+    p = np.exp(logits - logits.max(axis=2, keepdims=True))
+    p /= p.sum(axis=2, keepdims=True)
+    dl = logits[:, :K] + noise * g.standard_normal((B, K, V))
+    q = np.exp(dl - dl.max(axis=2, keepdims=True))
+    q /= q.sum(axis=2, keepdims=True)
+    cq = np.cumsum(q, axis=2)
+    ud = g.random((B, K))
+    draft = np.minimum((cq < (ud * cq[:, :, -1])[:, :, None]).sum(axis=2), V - 1).astype(np.int64)
+    return (draft, q.astype(np.float32), p.astype(np.float32), g.random((B, K)).astype(np.float32),
+            g.random(B).astype(np.float32))

@@ -92,6 +92,28 @@ def test_accept(mt, K):
     assert np.array_equal(n.cpu().numpy(), wn) and np.array_equal(nx.cpu().numpy(), wx)
 
 
+@pytest.mark.parametrize("B,K,V,noise", [(256, 5, 37, 0.5), (300, 1, 1000, 2.0), (64, 0, 500, 0.5),
+                                         (16, 5, 154880, 0.3), (40, 7, 4099, 0.05)])
+def test_accept_stochastic_exact(mt, B, K, V, noise):
+    """Bit-exact against the oracle: accept counts and drawn tokens."""
+    from mtp_speculative_decode_gb300 import workloads
+    draft, q, p, ua, us = workloads.stochastic_inputs(B + K + V, B, K, V, noise=noise)
+    if K > 0 and B > 3:
+        draft[1, 0] = V + 5                   # outside the vocabulary: rejected and flagged
+        p[2, 0] = 0.5 * q[2, 0]               # residual without mass: the draw falls back to p
+        ua[2, 0] = 0.99
+        p[3, K] = 0.0                         # a row with no mass at all (reached if all accepted)
+        q[3] = p[3, :K]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n, nx = mt.accept_stochastic(dev(draft), dev(q), dev(p), dev(ua), dev(us), dev_status=status)
+    wn, wx = oaccept.accept_stochastic(draft, q, p, ua, us)
+    assert np.array_equal(n.cpu().numpy(), wn)
+    assert np.array_equal(nx.cpu().numpy(), wx)
+    if K > 0 and B > 3:
+        assert status.item() & 1, "an out-of-vocabulary draft must be flagged"
+        assert wn[1] == 0 and wn[3] == K
+
+
 # ----------------------------------------------------------------------------- write-back
 
 @pytest.mark.parametrize("lat_dtype", [torch.bfloat16, torch.float32])
