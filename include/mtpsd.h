@@ -82,6 +82,16 @@ int mtpsd_merge_tokens(const int64_t* prompt_tokens, int64_t S, const uint32_t* 
  * prompt_offsets [B+1], out [B+1]. */
 void mtpsd_host_merged_offsets(const uint32_t* prompt_offsets, int32_t B, int32_t K, uint32_t* out);
 
+/* Cross-layer indexer schedule ([P3] "跨层共享的 indexer 调度"), host only: is_full[i] = 1 when
+ * layer i runs its own indexer (full), 0 when it reuses the selection of the most recent full layer
+ * (shared).  From pattern (a string of F and S, one per layer) when given and non-empty; else, when
+ * freq > 0 or offset >= 0, layer i is full when max(i - offset + 1, 0) % freq == 0 (freq 1 and offset
+ * 2 by default: pass freq 0 or offset -1 to take a default); else every layer is full.  The first
+ * layer must be full (MTPSD_EINVAL otherwise).  GLM-5.x's 21 full of 78 layers ([P2] "验证段的逐层算子")
+ * is freq 4, offset 2.  An explicit per-layer list needs no call. */
+int mtpsd_resolve_indexer_types(int32_t n_layers, const char* pattern, int32_t freq, int32_t offset,
+                                int32_t* is_full);
+
 /* ------------------------------------------------------------------------
  * Dynamic FP8 E4M3 quantization with one float32 scale per block of 128
  * contiguous values.  [P3] "Indexer 的结构与计算流程" (q and k quantized to FP8
@@ -327,10 +337,16 @@ int mtpsd_kv_writeback(const void* src_latent, const uint8_t* src_idxk, const fl
  *   segment) -> shared_idx[b, :] = step0_topk[row_offsets[b] + num_accepted[b], :].
  * A local row outside the request's segment is clamped to its last row and
  * flagged MTPSD_STATUS_INDEX_RANGE.
+ * row_pos [R0] int64 and shared_pos [B] int64 (both or neither, nullable):
+ * shared_pos[b] = row_pos of the reused row (-1 for an empty segment), the
+ * position whose selection is shared; a later step appends positions after it.
+ * This serves seed_dsa_topk_from_draft_extend ([P2] "draft_extend:把接受段写回草稿层"):
+ * the selection of the last accepted row of draft_extend seeds the next
+ * round's draft steps.
  */
 int mtpsd_topk_share_gather(const int32_t* step0_topk, const uint32_t* row_offsets,
                             const int32_t* num_accepted, int32_t B, int32_t k, int32_t* shared_idx,
-                            int32_t* dev_status, void* stream);
+                            const int64_t* row_pos, int64_t* shared_pos, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
  * Check of the device-side bounded wait (the source pages have no

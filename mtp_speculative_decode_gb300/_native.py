@@ -57,6 +57,7 @@ class MlaArgs(C.Structure):
 SIGNATURES = {
     "mtpsd_merge_tokens": (C.c_int, [vp, i64, vp, vp, i32, i32, vp, vp, vp]),
     "mtpsd_host_merged_offsets": (None, [vp, i32, i32, vp]),
+    "mtpsd_resolve_indexer_types": (C.c_int, [i32, C.c_char_p, i32, i32, vp]),
     "mtpsd_quantize_fp8_block128": (C.c_int, [vp, i64, vp, vp, vp]),
     "mtpsd_scores_ld": (i64, [i64]),
     "mtpsd_indexer_topk_workspace_size": (C.c_size_t, [i32, i32, i64, i32]),
@@ -76,7 +77,7 @@ SIGNATURES = {
     "mtpsd_accept_greedy": (C.c_int, [vp, vp, i32, i32, i64, vp, vp, vp]),
     "mtpsd_accept_stochastic": (C.c_int, [vp, vp, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp]),
     "mtpsd_kv_writeback": (C.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp]),
-    "mtpsd_topk_share_gather": (C.c_int, [vp, vp, vp, i32, i32, vp, vp, vp]),
+    "mtpsd_topk_share_gather": (C.c_int, [vp, vp, vp, i32, i32, vp, vp, vp, vp, vp]),
     "mtpsd_check_bounded_wait": (C.c_int, [i64, vp, vp, vp]),
     "mtpsd_last_error": (C.c_char_p, []),
     "mtpsd_version": (i32, []),

@@ -91,6 +91,21 @@ def host_merged_offsets(prompt_offsets: np.ndarray, K: int) -> np.ndarray:
     return out
 
 
+def resolve_indexer_types(n_layers: int, explicit=None, pattern=None, freq=None, offset=None):
+    """Per-layer indexer schedule as a list of "full" / "shared" (an explicit list is checked and
+    returned; otherwise the library resolves the pattern or the frequency and offset)."""
+    if explicit is not None and len(explicit) > 0:
+        types = [str(t) for t in explicit]
+        if len(types) != n_layers or any(t not in ("full", "shared") for t in types) or types[0] != "full":
+            raise ValueError("an explicit schedule needs one full/shared entry per layer, the first full")
+        return types
+    out = np.zeros(max(n_layers, 1), dtype=np.int32)
+    check("mtpsd_resolve_indexer_types", lib().mtpsd_resolve_indexer_types(
+        n_layers, pattern.encode() if pattern else None, 0 if freq is None else int(freq),
+        -1 if offset is None else int(offset), out.ctypes.data_as(C.c_void_p)))
+    return ["full" if x else "shared" for x in out[:n_layers]]
+
+
 # --------------------------------------------------------------------------- FP8
 
 def quantize_fp8_block128(x, codes=None, scales=None, stream=None):
@@ -332,7 +347,10 @@ def kv_writeback(src_latent, src_idxk, src_idxs, num_accepted, dst_latent, dst_i
     return next_pos
 
 
-def topk_share_gather(step0_topk, row_offsets, num_accepted=None, shared_idx=None, dev_status=None, stream=None):
+def topk_share_gather(step0_topk, row_offsets, num_accepted=None, shared_idx=None, dev_status=None, stream=None,
+                      row_pos=None, shared_pos=None):
+    """shared_idx[b] = step0_topk[row_offsets[b] + num_accepted[b]] (row 0 without num_accepted); with
+    row_pos, shared_pos[b] receives the position of that row."""
     _need(step0_topk, "step0_topk", torch.int32, 2)
     _need(row_offsets, "row_offsets", torch.uint32, 1)
     if num_accepted is not None:
@@ -341,7 +359,11 @@ def topk_share_gather(step0_topk, row_offsets, num_accepted=None, shared_idx=Non
     k = step0_topk.shape[1]
     if shared_idx is None:
         shared_idx = torch.empty(B, k, dtype=torch.int32, device=step0_topk.device)
+    if row_pos is not None:
+        _need(row_pos, "row_pos", torch.int64, 1)
+        if shared_pos is None:
+            shared_pos = torch.empty(B, dtype=torch.int64, device=step0_topk.device)
     check("mtpsd_topk_share_gather", lib().mtpsd_topk_share_gather(
-        _ptr(step0_topk), _ptr(row_offsets), _ptr(num_accepted), B, k, _ptr(shared_idx), _ptr(dev_status),
-        _stream(stream)))
+        _ptr(step0_topk), _ptr(row_offsets), _ptr(num_accepted), B, k, _ptr(shared_idx), _ptr(row_pos),
+        _ptr(shared_pos if row_pos is not None else None), _ptr(dev_status), _stream(stream)))
     return shared_idx

@@ -56,6 +56,27 @@ void mtpsd_host_merged_offsets(const uint32_t* prompt_offsets, int32_t B, int32_
   for (int32_t i = 0; i <= B; ++i) out[i] = prompt_offsets[i] + (uint32_t)((int64_t)i * K);
 }
 
+int mtpsd_resolve_indexer_types(int32_t n_layers, const char* pattern, int32_t freq, int32_t offset,
+                                int32_t* is_full) {
+  g_err[0] = 0;
+  if (n_layers < 0 || (n_layers > 0 && !is_full)) return fail(MTPSD_EINVAL, "resolve_indexer_types: bad arguments");
+  if (pattern && pattern[0]) {
+    int32_t n = 0;
+    for (const char* c = pattern; *c; ++c, ++n) {
+      if (*c != 'F' && *c != 'S') return fail(MTPSD_EINVAL, "resolve_indexer_types: pattern characters must be F or S");
+      if (n < n_layers) is_full[n] = *c == 'F';
+    }
+    if (n != n_layers) return fail(MTPSD_EINVAL, "resolve_indexer_types: pattern length %d != %d layers", n, n_layers);
+  } else if (freq > 0 || offset >= 0) {
+    const int32_t f = freq > 0 ? freq : 1, o = offset >= 0 ? offset : 2;
+    for (int32_t i = 0; i < n_layers; ++i) is_full[i] = ((i - o + 1 > 0 ? i - o + 1 : 0) % f) == 0;
+  } else {
+    for (int32_t i = 0; i < n_layers; ++i) is_full[i] = 1;
+  }
+  if (n_layers > 0 && !is_full[0]) return fail(MTPSD_EINVAL, "resolve_indexer_types: the first layer must be full");
+  return MTPSD_OK;
+}
+
 int mtpsd_quantize_fp8_block128(const float* x, int64_t n_blocks, uint8_t* codes, float* scales, void* stream) {
   g_err[0] = 0;
   if (n_blocks < 0) return fail(MTPSD_EINVAL, "quantize: n_blocks < 0");
@@ -282,14 +303,18 @@ int mtpsd_kv_writeback(const void* src_latent, const uint8_t* src_idxk, const fl
 }
 
 int mtpsd_topk_share_gather(const int32_t* step0_topk, const uint32_t* row_offsets, const int32_t* num_accepted,
-                            int32_t B, int32_t k, int32_t* shared_idx, int32_t* dev_status, void* stream) {
+                            int32_t B, int32_t k, int32_t* shared_idx, const int64_t* row_pos, int64_t* shared_pos,
+                            int32_t* dev_status, void* stream) {
   g_err[0] = 0;
   if (B < 0 || k < 1) return fail(MTPSD_EINVAL, "topk_share_gather: need B >= 0, k >= 1");
   if (B == 0) return MTPSD_OK;
   if (!step0_topk || !row_offsets || !shared_idx) return fail(MTPSD_EINVAL, "topk_share_gather: null pointer");
+  if ((row_pos == nullptr) != (shared_pos == nullptr))
+    return fail(MTPSD_EINVAL, "topk_share_gather: give row_pos and shared_pos together or neither");
   if ((k & 3) == 0 && (!aligned(step0_topk, 16) || !aligned(shared_idx, 16)))
     return fail(MTPSD_EINVAL, "topk_share_gather: buffers must be 16-byte aligned when k % 4 == 0");
-  return launch_share_gather(step0_topk, row_offsets, num_accepted, B, k, shared_idx, dev_status, (cudaStream_t)stream);
+  return launch_share_gather(step0_topk, row_offsets, num_accepted, B, k, shared_idx, row_pos, shared_pos, dev_status,
+                             (cudaStream_t)stream);
 }
 
 int mtpsd_check_bounded_wait(int64_t limit_ns, int32_t* dev_status, int64_t* result, void* stream) {

@@ -29,7 +29,7 @@ int launch_accept_stochastic(const int64_t* draft, const float* q, const float* 
                              int B, int K, int64_t V, int32_t* n_acc, int64_t* next, int32_t* status, cudaStream_t st);
 int launch_bounded_wait_check(int64_t limit_ns, int32_t* status, int64_t* out, cudaStream_t st);
 int launch_share_gather(const int32_t* s0, const uint32_t* ro, const int32_t* n_acc, int B, int k,
-                        int32_t* out, int32_t* status, cudaStream_t st);
+                        int32_t* out, const int64_t* row_pos, int64_t* shared_pos, int32_t* status, cudaStream_t st);
 
 // indexer scores into a [R, ld] float matrix (positions > row_pos are not written)
 struct IndexerPlan {

@@ -158,6 +158,7 @@ int launch_kv_writeback(const void* src_l, const uint8_t* src_k, const float* sr
 // k-wide row with 16-byte vectors when k % 4 == 0.
 __global__ void share_gather_kernel(const int32_t* __restrict__ s0, const uint32_t* __restrict__ ro,
                                     const int32_t* __restrict__ n_acc, int k, int32_t* __restrict__ out,
+                                    const int64_t* __restrict__ row_pos, int64_t* __restrict__ shared_pos,
                                     int32_t* __restrict__ status) {
   griddep_wait();                // the previous kernel's writes are visible from here on
   griddep_launch_dependents();
@@ -165,6 +166,7 @@ __global__ void share_gather_kernel(const int32_t* __restrict__ s0, const uint32
   int64_t first = ro[b], last = (int64_t)ro[b + 1] - 1;
   if (last < first) {  // empty segment: nothing to share
     for (int j = threadIdx.x; j < k; j += blockDim.x) out[(int64_t)b * k + j] = -1;
+    if (shared_pos && threadIdx.x == 0) shared_pos[b] = -1;
     return;
   }
   int64_t local = n_acc ? n_acc[b] : 0;
@@ -173,6 +175,7 @@ __global__ void share_gather_kernel(const int32_t* __restrict__ s0, const uint32
     if (threadIdx.x == 0) flag_status(status, MTPSD_STATUS_INDEX_RANGE);
     row = local < 0 ? first : last;
   }
+  if (shared_pos && threadIdx.x == 0) shared_pos[b] = row_pos[row];
   if ((k & 3) == 0) {
     const int4* src = (const int4*)(s0 + row * k);
     int4* dst = (int4*)(out + (int64_t)b * k);
@@ -183,8 +186,8 @@ __global__ void share_gather_kernel(const int32_t* __restrict__ s0, const uint32
 }
 
 int launch_share_gather(const int32_t* s0, const uint32_t* ro, const int32_t* n_acc, int B, int k,
-                        int32_t* out, int32_t* status, cudaStream_t st) {
-  launch_k(share_gather_kernel, B, 128, 0, st, s0, ro, n_acc, k, out, status);
+                        int32_t* out, const int64_t* row_pos, int64_t* shared_pos, int32_t* status, cudaStream_t st) {
+  launch_k(share_gather_kernel, B, 128, 0, st, s0, ro, n_acc, k, out, row_pos, shared_pos, status);
   return check_launch("topk_share_gather");
 }
 

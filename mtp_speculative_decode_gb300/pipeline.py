@@ -47,8 +47,14 @@ def _dev(x, device, dtype=None):
 
 
 class DecodeStep:
-    def __init__(self, w: W.Workload, device="cuda", draft: Optional[Dict[str, torch.Tensor]] = None):
+    """One decode step on the GPU.  seeded=True replaces the draft step-0 indexer by draft_extend's attention
+    over the K+1 window rows of the draft layer, whose selection at the last accepted row seeds every draft
+    step of the next round (seed_dsa_topk_from_draft_extend)."""
+
+    def __init__(self, w: W.Workload, device="cuda", draft: Optional[Dict[str, torch.Tensor]] = None,
+                 seeded: bool = False):
         self.w = w
+        self.seeded = seeded
         spec = w.spec
         self.spec = spec
         self.device = device
@@ -151,6 +157,39 @@ class DecodeStep:
             n = max(api.sparse_mla_workspace_size(B, spec.H_Q, spec.topk, j, 1 if self.fp8 else 0)
                     for j in range(spec.draft_steps))
             self.ws_dmla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+            if seeded:
+                self._init_extend(d, device)
+
+    def _init_extend(self, d, device):
+        """Buffers of draft_extend's attention: K+1 rows per request at positions L_b .. L_b + K."""
+        spec, w = self.spec, self.w
+        B, Wn = spec.B, spec.K + 1
+        Rx = B * Wn
+        self.x_row_offsets = _dev_u32(np.arange(0, Rx + 1, Wn), device)
+        self.x_row_pos = _dev((np.repeat(w.L, Wn) + np.tile(np.arange(Wn), B)).astype(np.int64), device, torch.int64)
+        self.x_max_visible = int(w.L.max()) + Wn
+        self.x_q_idx_raw = _gen(d, "x_q_idx", device)
+        self.x_w_idx = _gen(d, "x_w_idx", device)
+        if self.fp8:
+            self.x_q_idx = torch.empty(self.x_q_idx_raw.shape, dtype=torch.uint8, device=device)
+            self.x_q_scale = torch.empty(self.x_q_idx_raw.shape[:2], dtype=torch.float32, device=device)
+        else:
+            self.x_q_idx, self.x_q_scale = self.x_q_idx_raw, None
+        self.x_q_mla = _gen(d, "x_q_mla", device)
+        self.x_scores = torch.empty(Rx, api.scores_ld(self.x_max_visible), dtype=torch.float32, device=device)
+        self.ws_xplan = torch.empty(max(api.indexer_plan_bytes(B, Rx), 256), dtype=torch.uint8, device=device)
+        self.ws_xtopk = torch.empty(max(api.topk_workspace_size(Rx, self.x_max_visible, spec.topk), 256),
+                                    dtype=torch.uint8, device=device)
+        self.x_topk = torch.empty(Rx, spec.topk, dtype=torch.int32, device=device)
+        self.x_out = torch.empty(Rx, spec.H_Q, 512, dtype=self.q_mla.dtype, device=device)
+        self.x_lse = torch.empty(Rx, spec.H_Q, dtype=torch.float32, device=device)
+        n = api.sparse_mla_workspace_size(Rx, spec.H_Q, spec.topk, 0, 1 if self.fp8 else 0)
+        self.ws_xmla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+        self.seed_pos = torch.empty(B, dtype=torch.int64, device=device)
+        n = max(api.sparse_mla_workspace_size(B, spec.H_Q, spec.topk, j + 1, 1 if self.fp8 else 0)
+                for j in range(spec.draft_steps))
+        self.ws_dmla = torch.empty(max(n, 256, self.ws_dmla.numel() if hasattr(self, "ws_dmla") else 0),
+                                   dtype=torch.uint8, device=device)
 
     # ------------------------------------------------------------------ phases
     def merge(self, stream=None):
@@ -213,6 +252,35 @@ class DecodeStep:
                               append_base=self.next_pos if j else None, row_pos_add=j, out=self.d_out[j],
                               lse=self.d_lse[j], workspace=self.ws_dmla, dev_status=self.status, stream=stream)
 
+    def extend_scores(self, stream=None):
+        """draft_extend: FP8 quantization of the window rows' draft indexer queries, then the score GEMM over
+        the written-back draft-layer keys."""
+        if self.fp8:
+            api.quantize_fp8_block128(self.x_q_idx_raw, self.x_q_idx, self.x_q_scale, stream=stream)
+        api.indexer_scores(self.x_q_idx, self.x_q_scale, self.x_w_idx, self.d_k_cache, self.d_k_scale,
+                           self.cache_start, self.x_row_offsets, self.x_row_pos, self.x_max_visible,
+                           scores=self.x_scores, workspace=self.ws_xplan, dev_status=self.status, stream=stream)
+
+    def extend_topk(self, stream=None):
+        """draft_extend's selection per window row, and the seed: the selection of row num_accepted (the last
+        accepted position) with that row's position."""
+        api.topk(self.x_scores, self.x_row_pos, self.x_max_visible, self.spec.topk, out_idx=self.x_topk,
+                 dev_status=self.status, stream=stream, row_len_add=1, workspace=self.ws_xtopk)
+        api.topk_share_gather(self.x_topk, self.x_row_offsets, self.num_accepted, self.shared_idx,
+                              dev_status=self.status, stream=stream, row_pos=self.x_row_pos, shared_pos=self.seed_pos)
+
+    def extend_mla(self, stream=None):
+        api.sparse_mla_decode(self.x_q_mla, self.d_latent, self.cache_start, self.x_row_offsets, self.x_row_pos,
+                              self.x_topk, W.SOFTMAX_SCALE, out=self.x_out, lse=self.x_lse, workspace=self.ws_xmla,
+                              dev_status=self.status, stream=stream)
+
+    def seeded_draft_mla(self, j: int, stream=None):
+        """Draft step j of the next round: the seed plus positions P .. P + j (P = seed position + 1)."""
+        api.sparse_mla_decode(self.d_q_mla[j], self.d_latent, self.cache_start, self.d_row_offsets, self.seed_pos,
+                              self.shared_idx, W.SOFTMAX_SCALE, n_append=j + 1, append_base=self.seed_pos,
+                              row_pos_add=j + 1, out=self.d_out[j], lse=self.d_lse[j], workspace=self.ws_dmla,
+                              dev_status=self.status, stream=stream)
+
     def phases(self):
         """The step as an ordered list of (name, callable(stream)): what step() runs."""
         ph = []
@@ -220,7 +288,12 @@ class DecodeStep:
             ph += [("merge", self.merge), ("verify_scores", self.verify_scores), ("verify_topk", self.verify_topk),
                    ("verify_mla", self.verify_mla)]
         ph.append(("accept", self.accept))
-        if self.has_draft:
+        if self.has_draft and self.seeded:
+            ph += [("writeback", self.writeback), ("extend_scores", self.extend_scores),
+                   ("extend_topk", self.extend_topk), ("extend_mla", self.extend_mla)]
+            ph += [(f"draft_mla{j}", (lambda stream=None, j=j: self.seeded_draft_mla(j, stream)))
+                   for j in range(self.spec.draft_steps)]
+        elif self.has_draft:
             ph += [("writeback", self.writeback), ("draft_scores", self.draft_scores), ("draft_topk", self.draft_topk)]
             ph += [(f"draft_mla{j}", (lambda stream=None, j=j: self.draft_mla(j, stream)))
                    for j in range(self.spec.draft_steps)]
@@ -242,10 +315,121 @@ class DecodeStep:
         if self.spec.verify:
             n += 1 + quant + scores + api.topk_launch_count(self.max_visible, k) + self._mla_launches(k, 0, self.R)
         n += 1
-        if self.has_draft:
+        if self.has_draft and self.seeded:
+            Rx = self.B * (self.K + 1)
+            n += 1 + quant + scores + api.topk_launch_count(self.x_max_visible, k) + 1 + self._mla_launches(k, 0, Rx)
+            n += sum(self._mla_launches(k, j + 1, self.B) for j in range(self.spec.draft_steps))
+        elif self.has_draft:
             n += 1 + quant + scores + api.topk_launch_count(self.d_max_visible, k) + 1
             n += sum(self._mla_launches(k, j, self.B) for j in range(self.spec.draft_steps))
         return n
 
     def _mla_launches(self, n_idx, n_append, R):
         return api.sparse_mla_launch_count(R, self.spec.H_Q, n_idx, n_append, 1 if self.fp8 else 0)
+
+
+class LayeredVerify:
+    """A verify step over several DSA layers with the cross-layer indexer schedule ([P3] "跨层共享的 indexer
+    调度"): a full layer runs its indexer and top-k over its own key cache, a shared layer attends over the
+    selection of the most recent full layer.  Every layer has its own latent cache and queries; the rows are
+    the verify rows of the workload (merged once)."""
+
+    def __init__(self, w: W.Workload, types, device="cuda"):
+        if not types or types[0] != "full":
+            raise ValueError("the first layer must be full")
+        self.w, self.types, self.device = w, list(types), device
+        spec = w.spec
+        self.spec = spec
+        self.fp8 = not spec.latent_f32
+        B, K, R = spec.B, spec.K, w.R
+        self.B, self.K, self.R = B, K, R
+        t = w.tensors
+        self.cache_start = _dev(w.cache_start, device, torch.int64)
+        self.row_pos = _dev(w.row_pos, device, torch.int64)
+        self.row_offsets = _dev_u32(api.host_merged_offsets(w.prompt_offsets, K), device)
+        self.max_visible = int(w.L.max()) + w.r
+        self.prompt_tokens = _dev(w.prompt_tokens, device, torch.int64)
+        self.prompt_offsets = _dev_u32(w.prompt_offsets, device)
+        self.draft_tokens = _dev(w.draft_tokens, device, torch.int64)
+        self.merged_tokens = torch.empty(w.prompt_tokens.shape[0] + B * K, dtype=torch.int64, device=device)
+        self.merged_offsets = torch.empty(B + 1, dtype=torch.uint32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.scores = torch.empty(R, api.scores_ld(self.max_visible), dtype=torch.float32, device=device)
+        self.ws_plan = torch.empty(max(api.indexer_plan_bytes(B, R), 256), dtype=torch.uint8, device=device)
+        self.ws_topk = torch.empty(max(api.topk_workspace_size(R, self.max_visible, spec.topk), 256),
+                                   dtype=torch.uint8, device=device)
+        n = api.sparse_mla_workspace_size(R, spec.H_Q, spec.topk, 0, 1 if self.fp8 else 0)
+        self.ws_mla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+        self.layers = []
+        src = -1
+        for l, typ in enumerate(self.types):
+            L = {"type": typ}
+            L["latent"] = _gen(t, W.layer_name("latent", l), device)
+            L["q_mla"] = _gen(t, W.layer_name("q_mla", l), device)
+            if typ == "full":
+                src = l
+                kr = _gen(t, W.layer_name("k_idx", l), device)
+                if self.fp8:
+                    L["k_cache"], ks = api.quantize_fp8_block128(kr)
+                    L["k_scale"] = ks.reshape(-1).contiguous()
+                else:
+                    L["k_cache"], L["k_scale"] = kr, None
+                L["q_idx_raw"] = _gen(t, W.layer_name("q_idx", l), device)
+                L["w_idx"] = _gen(t, W.layer_name("w_idx", l), device)
+                if self.fp8:
+                    L["q_idx"] = torch.empty(L["q_idx_raw"].shape, dtype=torch.uint8, device=device)
+                    L["q_scale"] = torch.empty(L["q_idx_raw"].shape[:2], dtype=torch.float32, device=device)
+                else:
+                    L["q_idx"], L["q_scale"] = L["q_idx_raw"], None
+                L["topk"] = torch.empty(R, spec.topk, dtype=torch.int32, device=device)
+            L["src"] = src
+            L["out"] = torch.empty(R, spec.H_Q, 512, dtype=L["q_mla"].dtype, device=device)
+            L["lse"] = torch.empty(R, spec.H_Q, dtype=torch.float32, device=device)
+            self.layers.append(L)
+
+    def merge(self, stream=None):
+        api.merge_tokens(self.prompt_tokens, self.prompt_offsets, self.draft_tokens, self.merged_tokens,
+                         self.merged_offsets, stream=stream)
+
+    def scores_of(self, l, stream=None):
+        L = self.layers[l]
+        if self.fp8:
+            api.quantize_fp8_block128(L["q_idx_raw"], L["q_idx"], L["q_scale"], stream=stream)
+        api.indexer_scores(L["q_idx"], L["q_scale"], L["w_idx"], L["k_cache"], L["k_scale"], self.cache_start,
+                           self.row_offsets, self.row_pos, self.max_visible, scores=self.scores,
+                           workspace=self.ws_plan, dev_status=self.status, stream=stream)
+
+    def topk_of(self, l, stream=None):
+        api.topk(self.scores, self.row_pos, self.max_visible, self.spec.topk, out_idx=self.layers[l]["topk"],
+                 dev_status=self.status, stream=stream, row_len_add=1, workspace=self.ws_topk)
+
+    def mla_of(self, l, stream=None):
+        L = self.layers[l]
+        api.sparse_mla_decode(L["q_mla"], L["latent"], self.cache_start, self.row_offsets, self.row_pos,
+                              self.layers[L["src"]]["topk"], W.SOFTMAX_SCALE, out=L["out"], lse=L["lse"],
+                              workspace=self.ws_mla, dev_status=self.status, stream=stream)
+
+    def phases(self):
+        ph = [("merge", self.merge)]
+        for l, L in enumerate(self.layers):
+            if L["type"] == "full":
+                ph += [(f"L{l}_scores", (lambda stream=None, l=l: self.scores_of(l, stream))),
+                       (f"L{l}_topk", (lambda stream=None, l=l: self.topk_of(l, stream)))]
+            ph.append((f"L{l}_mla", (lambda stream=None, l=l: self.mla_of(l, stream))))
+        return ph
+
+    def step(self, stream=None):
+        for _, fn in self.phases():
+            fn(stream)
+
+    def launches_per_step(self) -> int:
+        _, H_I, D_I = self.layers[0]["q_idx_raw"].shape
+        dt = N.MTPSD_FP8_E4M3 if self.fp8 else N.MTPSD_F32
+        k = self.spec.topk
+        n = 1
+        for L in self.layers:
+            if L["type"] == "full":
+                n += (1 if self.fp8 else 0) + api.indexer_scores_launch_count(H_I, D_I, dt) + \
+                    api.topk_launch_count(self.max_visible, k)
+            n += api.sparse_mla_launch_count(self.R, self.spec.H_Q, k, 0, 1 if self.fp8 else 0)
+        return n

@@ -384,3 +384,34 @@ def stochastic_inputs(seed: int, B: int, K: int, V: int, temperature: float = 1.
     draft = np.minimum((cq < (ud * cq[:, :, -1])[:, :, None]).sum(axis=2), V - 1).astype(np.int64)
     return (draft, q.astype(np.float32), p.astype(np.float32), g.random((B, K)).astype(np.float32),
             g.random(B).astype(np.float32))
+
+
+def layer_name(name: str, layer: int) -> str:
+    """Name of a per-layer input: the first layer keeps the plain name."""
+    return name if layer == 0 else f"{name}@{layer}"
+
+
+def add_layers(w: Workload, n_layers: int) -> Workload:
+    """Inputs of layers 1..n_layers-1 of a multi-layer verify (the same shapes as
+    layer 0, their own streams): indexer queries, weights and keys, latent pool
+    and MLA queries."""
+    for l in range(1, n_layers):
+        for base in ("q_idx", "w_idx", "k_idx", "latent", "q_mla"):
+            w.tensors.specs[layer_name(base, l)] = w.tensors.specs[base]
+    return w
+
+
+def add_draft_extend(w: Workload) -> Workload:
+    """Inputs of draft_extend's attention over the window rows in the draft layer:
+    indexer queries and weights and MLA queries of each of the K+1 rows."""
+    spec = w.spec
+    B, W = spec.B, spec.K + 1
+    std_i = 1.0 / math.sqrt(spec.D_I) if spec.scaled_normal else 1.0
+    std_l = 1.0 / math.sqrt(576.0) if spec.scaled_normal else 1.0
+    lat = torch.float32 if spec.latent_f32 else torch.bfloat16
+    w.tensors.specs.update({
+        "x_q_idx": TensorSpec((B * W, spec.H_I, spec.D_I), "normal", std_i, torch.float32),
+        "x_w_idx": TensorSpec((B * W, spec.H_I), "uniform", 1.0, torch.float32),
+        "x_q_mla": TensorSpec((B * W, spec.H_Q, 576), "normal", std_l, lat),
+    })
+    return w

@@ -42,9 +42,9 @@ FIX_SHIFT = 32   # weights are compared at 2^-32 resolution
 
 
 def _fixed_weights(weights) -> list:
-    """floor(w * 2^32) of each single-precision weight, as exact integers."""
+    """floor(max(w, 0) * 2^32) of each single-precision weight, as exact integers."""
     w = np.asarray(weights, dtype=np.float32).astype(np.float64)   # exact widening
-    return [int(np.floor(x * 2.0 ** FIX_SHIFT)) for x in w.tolist()]
+    return [int(np.floor(max(x, 0.0) * 2.0 ** FIX_SHIFT)) for x in w.tolist()]
 
 
 def _scaled_floor(u: float, total: int) -> int:

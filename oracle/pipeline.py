@@ -72,21 +72,21 @@ class OracleStep:
     def merge(self):
         return merge.merge_tokens(self.w.prompt_tokens, self.w.prompt_offsets, self.w.draft_tokens)
 
-    def verify_scores(self, rows):
+    def verify_scores(self, rows, layer: int = 0):
         w = self.w
         out = {}
         for r in rows:
             b = int(w.row_req[r])
             p = int(w.row_pos[r])
-            keys = self.keys("k_idx", b, p + 1)
-            out[r] = indexer.indexer_scores_row(self.query(self.t, "q_idx", r), _rows(self.t, "w_idx", r, r + 1)[0],
-                                                keys)
+            keys = self.keys(_ln("k_idx", layer), b, p + 1)
+            out[r] = indexer.indexer_scores_row(self.query(self.t, _ln("q_idx", layer), r),
+                                                _rows(self.t, _ln("w_idx", layer), r, r + 1)[0], keys)
         return out
 
     def verify_topk(self, scores):
         return {r: topk.topk_select(s, self.spec.topk) for r, s in scores.items()}
 
-    def verify_mla(self, idx_rows, heads=None):
+    def verify_mla(self, idx_rows, heads=None, layer: int = 0):
         """idx_rows: dict row -> selected positions.  The selected latent rows
         of the row's request are gathered, then attended with the oracle's
         sparse MLA definition."""
@@ -96,8 +96,8 @@ class OracleStep:
             b = int(w.row_req[r])
             base = int(w.cache_start[b])
             pos = mla.row_index_list(idx)
-            C = _take(self.t, "latent", [base + s for s in pos]).reshape(len(pos), mla.D_LATENT)
-            q = _rows(self.t, "q_mla", r, r + 1).astype(np.float64)
+            C = _take(self.t, _ln("latent", layer), [base + s for s in pos]).reshape(len(pos), mla.D_LATENT)
+            q = _rows(self.t, _ln("q_mla", layer), r, r + 1).astype(np.float64)
             one = mla.sparse_mla(q, C, np.array([0]), np.array([0]), np.arange(len(pos))[None], _scale(),
                                  heads=heads)
             res[r] = one[0]
@@ -169,6 +169,68 @@ class OracleStep:
                                  np.arange(len(pos))[None], _scale(), heads=heads)
             res[b] = one[0]
         return res
+
+
+    # ------------------------------------------------------------ cross-layer and cross-phase reuse
+    def layered_verify(self, types, rows, heads=None):
+        """A verify step over len(types) layers with the full/shared schedule
+        ([P3] "跨层共享的 indexer 调度"): a full layer runs its own indexer and
+        top-k, a shared layer attends over the selection of the most recent full
+        layer.  Returns ({layer: {row: selection}}, {layer: {row: (o, lse)}})."""
+        src = share.source_layers(types)
+        sel, out = {}, {}
+        for l, t in enumerate(types):
+            if t == "full":
+                sel[l] = self.verify_topk(self.verify_scores(rows, layer=l))
+            out[l] = self.verify_mla(sel[src[l]], heads=heads, layer=l)
+        return sel, out
+
+    def extend_rows(self, b: int):
+        W = self.spec.K + 1
+        return list(range(b * W, (b + 1) * W))
+
+    def draft_extend(self, num_accepted, reqs, heads=None, selections=None):
+        """draft_extend's attention in the draft layer after the write-back: each
+        of the K+1 window rows of request b sits at position L_b + i and runs the
+        indexer, the top-k and sparse MLA over the written-back caches (over
+        selections[(b, i)] instead of its own top-k where given).
+        Returns (scores {(b,i)}, selection {(b,i)}, outputs {(b,i)})."""
+        W = self.spec.K + 1
+        sc, tk, out = {}, {}, {}
+        for b in reqs:
+            L = int(self.w.L[b])
+            for i in range(W):
+                x = b * W + i
+                keys = self.draft_keys(num_accepted, b, L + i + 1)
+                s = indexer.indexer_scores_row(self.query(self.d, "x_q_idx", x), _rows(self.d, "x_w_idx", x, x + 1)[0],
+                                               keys)
+                sc[(b, i)] = s
+                tk[(b, i)] = topk.topk_select(s, self.spec.topk)
+                chosen = tk[(b, i)] if selections is None or (b, i) not in selections else selections[(b, i)]
+                pos = mla.row_index_list(chosen)
+                C = self.draft_latent_rows(num_accepted, b, pos)
+                q = _rows(self.d, "x_q_mla", x, x + 1).astype(np.float64)
+                out[(b, i)] = mla.sparse_mla(q, C, np.array([0]), np.array([0]), np.arange(len(pos))[None],
+                                             _scale(), heads=heads)[0]
+        return sc, tk, out
+
+    def seeded_draft_mla(self, num_accepted, seed, j: int, reqs, heads=None):
+        """Draft step j of the next round with the selection seeded by draft_extend
+        (seed_dsa_topk_from_draft_extend): the seed (the last accepted row's
+        selection, position P_b - 1) plus the positions P_b .. P_b + j."""
+        P = self.next_pos(num_accepted)
+        res = {}
+        for b in reqs:
+            pos = share.seeded_step_positions(seed[b], int(P[b])) + [int(P[b]) + 1 + i for i in range(j)]
+            C = self.draft_latent_rows(num_accepted, b, pos)
+            q = _rows(self.d, f"d_q_mla{j}", b, b + 1).astype(np.float64)
+            res[b] = mla.sparse_mla(q, C, np.array([0]), np.array([0]), np.arange(len(pos))[None], _scale(),
+                                    heads=heads)[0]
+        return res
+
+
+def _ln(name: str, layer: int) -> str:
+    return name if layer == 0 else f"{name}@{layer}"
 
 
 def _scale():

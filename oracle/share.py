@@ -37,3 +37,54 @@ def shared_step_positions(shared_row: np.ndarray, P_b: int, j: int):
     """Positions attended at draft step j: the shared set plus P_b+1..P_b+j."""
     sel = [int(s) for s in np.asarray(shared_row).tolist() if int(s) >= 0]
     return sel + [P_b + 1 + i for i in range(j)]
+
+
+# --------------------------------------------------------------------- cross-layer sharing
+
+def resolve_indexer_types(n_layers: int, explicit=None, pattern=None, freq=None, offset=None):
+    """Per-layer indexer schedule, 'full' or 'shared' ([P3] "跨层共享的 indexer 调度"):
+    an explicit per-layer list first; else a pattern string where F is full and
+    S shared; else, when a frequency or an offset is given, layer i is full when
+    max(i - offset + 1, 0) % freq == 0 (freq 1 and offset 2 by default); with no
+    schedule information every layer is full.  The first layer must be full,
+    since no earlier selection exists for it to reuse."""
+    if explicit is not None and len(explicit) > 0:
+        types = [str(t) for t in explicit]
+    elif pattern:
+        types = ["full" if c == "F" else "shared" if c == "S" else "?" for c in pattern]
+        if "?" in types:
+            raise ValueError("pattern characters must be F or S")
+    elif freq is not None or offset is not None:
+        f = 1 if freq is None else int(freq)
+        o = 2 if offset is None else int(offset)
+        types = ["full" if max(i - o + 1, 0) % f == 0 else "shared" for i in range(n_layers)]
+    else:
+        types = ["full"] * n_layers
+    if len(types) != n_layers:
+        raise ValueError("schedule length must equal the layer count")
+    if any(t not in ("full", "shared") for t in types):
+        raise ValueError("schedule entries must be full or shared")
+    if n_layers > 0 and types[0] != "full":
+        raise ValueError("the first layer must be full")
+    return types
+
+
+def source_layers(types):
+    """For each layer, the layer whose indexer selection it attends over: itself
+    when full, else the most recent full layer before it."""
+    src, last = [], -1
+    for i, t in enumerate(types):
+        if t == "full":
+            last = i
+        src.append(last)
+    return src
+
+
+def seeded_step_positions(seed_row, P_b: int):
+    """Positions attended at the first draft step of the next round when the
+    draft indexer's selection is seeded by draft_extend ([P2] "draft_extend:把接受段写回草稿层",
+    seed_dsa_topk_from_draft_extend): the selection of the last accepted row,
+    which sits at position P_b - 1, plus the step's own position P_b (its key is
+    written before attention and it lies past every seeded position)."""
+    sel = [int(s) for s in np.asarray(seed_row).tolist() if int(s) >= 0]
+    return sel + [P_b]

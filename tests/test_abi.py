@@ -132,3 +132,16 @@ def test_launch_count_queries(native):
     assert lib.mtpsd_topk_launch_count(16 * 32768 + 1, 2048) == 3
     assert lib.mtpsd_topk_launch_count(1 << 20, 4096) == 3            # 32 segments, merges of 8
     assert lib.mtpsd_indexer_topk_launch_count(48, 128, native.MTPSD_F32, 100000, 2048) == 3
+
+
+def test_indexer_schedule_matches_the_oracle(native):
+    from mtp_speculative_decode_gb300 import api
+    from oracle import share
+    cases = [dict(n_layers=78, freq=4, offset=2), dict(n_layers=3), dict(n_layers=4, pattern="FSSF"),
+             dict(n_layers=5, freq=1), dict(n_layers=6, freq=2, offset=1), dict(n_layers=9, offset=4),
+             dict(n_layers=7, freq=3), dict(n_layers=0)]
+    for c in cases:
+        assert api.resolve_indexer_types(**c) == share.resolve_indexer_types(**c), c
+    for bad in (dict(n_layers=3, pattern="SFF"), dict(n_layers=3, pattern="FX"), dict(n_layers=2, pattern="FFF")):
+        with pytest.raises(Exception):
+            api.resolve_indexer_types(**bad)

@@ -166,6 +166,12 @@ def test_share_gather(mt):
     assert np.array_equal(got, oshare.topk_share_gather(s0, ro, nacc))
     got0 = mt.topk_share_gather(dev(s0), u32(ro), None).cpu().numpy()
     assert np.array_equal(got0, oshare.topk_share_gather(s0, ro, None))
+    # the position of the reused row comes back with it
+    rpos = rng.integers(0, 10 ** 6, int(ro[-1])).astype(np.int64)
+    spos = torch.empty(B, dtype=torch.int64, device="cuda")
+    got1 = mt.topk_share_gather(dev(s0), u32(ro), dev(nacc), row_pos=dev(rpos), shared_pos=spos).cpu().numpy()
+    assert np.array_equal(got1, oshare.topk_share_gather(s0, ro, nacc))
+    assert np.array_equal(spos.cpu().numpy(), rpos[ro[:-1].astype(np.int64) + nacc])
     # a local row beyond the segment is clamped to its last row and flagged
     bad = nacc.copy()
     bad[3] = lens[3] + 2

@@ -108,3 +108,95 @@ def test_long_context_full_size(mods):
 @pytest.mark.slow
 def test_decode_step_full_size(mods):
     run_case(mods, "decode", n_rows=10, n_reqs=6, heads=range(0, 128, 8))
+
+
+# ----------------------------------------------------------------------------- cross-layer and cross-phase reuse
+
+def run_layered(mods, name, types, n_rows, heads=None):
+    """A multi-layer verify with the full/shared indexer schedule against the oracle."""
+    pipeline, W, OracleStep = mods
+    w = W.add_layers(W.build(name), len(types))
+    g = pipeline.LayeredVerify(w, types, "cuda")
+    g.step()
+    torch.cuda.synchronize()
+    assert g.status.item() == 0, f"device status {g.status.item()}"
+    o = OracleStep(w)
+    k = w.spec.topk
+    tol = parity.ATT_TOL_F32 if w.spec.latent_f32 else parity.ATT_TOL_BF16
+    rows = _sample(w.R, n_rows, 3)
+    used, errs, ties = {}, [], 0
+    for l, typ in enumerate(types):
+        L = g.layers[l]
+        if typ == "full":
+            sc = o.verify_scores(rows, layer=l)
+            tk = o.verify_topk(sc)
+            gi = L["topk"].cpu().numpy()
+            diffs = {r: parity.check_topk_row(gi[r], sc[r], k) for r in rows}
+            ties += sum(diffs.values())
+            used[l] = {r: (gi[r] if diffs[r] else tk[r]) for r in rows}
+        ref = o.verify_mla(used[L["src"]], heads=heads, layer=l)
+        go = L["out"].float().cpu().numpy()
+        for r in rows:
+            gr = go[r] if heads is None else go[r][list(heads)]
+            errs.append(parity.check_attention_row(gr, ref[r][0], tol))
+    print(name, types, {"tie_diffs": ties, "att_err": max(errs)})
+
+
+def test_layered_verify_tiny(mods):
+    run_layered(mods, "tiny", ["full", "shared", "full", "shared"], n_rows=10 ** 6)
+
+
+@pytest.mark.slow
+def test_layered_verify_full_size(mods):
+    run_layered(mods, "verify", ["full", "shared", "shared", "shared"], n_rows=12, heads=range(0, 128, 16))
+
+
+def run_seeded(mods, name, n_reqs, heads=None):
+    """draft_extend's attention over the window rows, the seed gathered at the last accepted row, and the
+    next round's draft steps over the seed plus the new positions, against the oracle."""
+    pipeline, W, OracleStep = mods
+    w = W.add_draft_extend(W.build(name))
+    d = W.draft_tensors(w)
+    g = pipeline.DecodeStep(w, "cuda", d, seeded=True)
+    g.step()
+    torch.cuda.synchronize()
+    assert g.status.item() == 0, f"device status {g.status.item()}"
+    o = OracleStep(w, d)
+    k, Wn = w.spec.topk, w.spec.K + 1
+    tol = parity.ATT_TOL_F32 if w.spec.latent_f32 else parity.ATT_TOL_BF16
+    n_acc, _ = o.accept()
+    assert np.array_equal(g.num_accepted.cpu().numpy(), n_acc)
+    reqs = _sample(w.B, n_reqs, 4)
+    gx = g.x_topk.cpu().numpy()
+    sc, tk, _ = o.draft_extend(n_acc, reqs, heads=heads)
+    diffs = {(b, i): parity.check_topk_row(gx[b * Wn + i], sc[(b, i)], k) for b in reqs for i in range(Wn)}
+    chosen = {key: (gx[key[0] * Wn + key[1]] if diffs[key] else tk[key]) for key in diffs}
+    _, _, ref = o.draft_extend(n_acc, reqs, heads=heads, selections=chosen)
+    gxo = g.x_out.float().cpu().numpy()
+    errs = []
+    for (b, i), (o_ref, _) in ref.items():
+        gr = gxo[b * Wn + i] if heads is None else gxo[b * Wn + i][list(heads)]
+        errs.append(parity.check_attention_row(gr, o_ref, tol))
+    # the seed is the selection of row num_accepted, at position L + num_accepted (exact)
+    gs = g.shared_idx.cpu().numpy()
+    gsp = g.seed_pos.cpu().numpy()
+    for b in range(w.B):
+        assert np.array_equal(gs[b], gx[b * Wn + n_acc[b]])
+        assert gsp[b] == w.L[b] + n_acc[b]
+    seed = {b: chosen[(b, int(n_acc[b]))] for b in reqs}
+    for j in range(w.spec.draft_steps):
+        ref = o.seeded_draft_mla(n_acc, seed, j, reqs, heads=heads)
+        go = g.d_out[j].float().cpu().numpy()
+        for b in reqs:
+            gr = go[b] if heads is None else go[b][list(heads)]
+            errs.append(parity.check_attention_row(gr, ref[b][0], tol))
+    print(name, "seeded", {"tie_diffs": sum(diffs.values()), "att_err": max(errs)})
+
+
+def test_seeded_draft_tiny(mods):
+    run_seeded(mods, "tiny", n_reqs=10 ** 6)
+
+
+@pytest.mark.slow
+def test_seeded_draft_full_size(mods):
+    run_seeded(mods, "draft", n_reqs=4, heads=range(0, 128, 16))

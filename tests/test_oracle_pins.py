@@ -545,3 +545,47 @@ def test_accept_stochastic_fixed_point_is_exact():
     ws = np.concatenate([rng.random(200).astype(np.float32), np.array([0.0, 1.0, 2.0 ** -40, 3e-10], np.float32)])
     got = accept._fixed_weights(ws)
     assert got == [int(Fraction(float(w)) * 2 ** 32) for w in ws]
+
+
+# --------------------------------------------------------------------- cross-layer sharing
+
+def test_indexer_schedule_reproduces_the_pages_counts():
+    """GLM-5.3's verify step runs the indexer in 21 full layers of 78 and shares it in
+    57 ([P2] "验证段的逐层算子"); the automatic rule with frequency 4 and offset 2 gives
+    exactly that, with layers 0 and 1 full, then every fourth."""
+    t = share.resolve_indexer_types(78, freq=4, offset=2)
+    assert t.count("full") == 21 and t.count("shared") == 57
+    full = [i for i, x in enumerate(t) if x == "full"]
+    assert full[:4] == [0, 1, 5, 9] and full[-1] == 77
+
+
+def test_indexer_schedule_sources_and_rules():
+    assert share.resolve_indexer_types(3) == ["full"] * 3                      # no information
+    assert share.resolve_indexer_types(4, pattern="FSSF") == ["full", "shared", "shared", "full"]
+    assert share.resolve_indexer_types(2, explicit=["full", "shared"], pattern="FF") == ["full", "shared"]
+    assert share.resolve_indexer_types(5, freq=1) == ["full"] * 5              # every layer with frequency 1
+    assert share.resolve_indexer_types(6, freq=2, offset=1) == ["full", "shared", "full", "shared", "full", "shared"]
+    with pytest.raises(ValueError):
+        share.resolve_indexer_types(3, pattern="SFF")                          # first must be full
+    with pytest.raises(ValueError):
+        share.resolve_indexer_types(3, pattern="FX")
+    assert share.source_layers(["full", "shared", "shared", "full", "shared"]) == [0, 0, 0, 3, 3]
+
+
+def test_seeded_step_positions():
+    assert share.seeded_step_positions(np.array([3, 1, -1, 7]), 12) == [3, 1, 7, 12]
+
+
+def test_seeded_steps_equal_rerun_when_context_below_k():
+    """With a context shorter than k the seed (the selection at P - 1) holds every
+    position up to P - 1, so the seeded step at P attends exactly what rerunning
+    the indexer at P would select: every position 0..P."""
+    rng = np.random.default_rng(12)
+    H, D, P, k = 2, 16, 40, 64
+    keys = rng.normal(size=(P + 4, D))
+    seed = topk.topk_select(indexer.indexer_scores(rng.normal(size=(1, H, D)), None, np.ones((1, H)), keys, None,
+                                                   np.array([0]), np.array([0]), np.array([P - 1]),
+                                                   fp8=False)[0], k)
+    rerun = topk.topk_select(indexer.indexer_scores(rng.normal(size=(1, H, D)), None, np.ones((1, H)), keys, None,
+                                                    np.array([0]), np.array([0]), np.array([P]), fp8=False)[0], k)
+    assert sorted(share.seeded_step_positions(seed, P)) == sorted(int(x) for x in rerun if x >= 0)
