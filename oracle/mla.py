@@ -77,3 +77,46 @@ def sparse_mla(q, latent, cache_start, row_req, idx, scale, n_append=0,
         lse = m[:, 0] + np.log(ssum)
         out[r] = (o, lse)
     return out
+
+
+# --------------------------------------------------------------------- FP8 latent cache
+
+FP8_DS_MLA_BYTES = 656   # per token: 512 E4M3 codes + 4 float32 scales + 64 bf16 rope values
+
+
+def pack_fp8_ds_mla(latent) -> np.ndarray:
+    """The 656-byte token layout of the FP8 latent cache ([P2] "草稿层 KV 的账":
+    656 bytes per token per layer, the fp8_ds_mla layout; the page gives only
+    the total).  Reading adopted: bytes 0..511 the E4M3 codes of latent values
+    0..511 in four blocks of 128 (value = code * scale of its block, the
+    indexer's block-128 quantizer: scale = amax/448, round to nearest even,
+    saturating), bytes 512..527 the four float32 scales, bytes 528..655 the 64
+    rope values 512..575 as bf16 (round to nearest even from float32).
+
+    latent [T, 576] (float32 values or a CPU torch tensor) -> uint8 [T, 656]."""
+    from .fp8 import quantize_block128
+    x = np.asarray(latent.float() if hasattr(latent, "float") else latent, dtype=np.float32)
+    T = x.shape[0]
+    codes, scales = quantize_block128(x[:, :512])             # [T, 512] uint8, [T, 4] float32
+    rope = x[:, 512:576]
+    bits = rope.view(np.uint32).astype(np.uint64)
+    # bf16 by round to nearest even: add 0x7fff plus the lowest kept bit, keep the high half
+    rbits = ((bits + 0x7FFF + ((bits >> 16) & 1)) >> 16).astype(np.uint16)
+    out = np.empty((T, FP8_DS_MLA_BYTES), dtype=np.uint8)
+    out[:, :512] = codes
+    out[:, 512:528] = np.ascontiguousarray(scales, dtype=np.float32).view(np.uint8).reshape(T, 16)
+    out[:, 528:656] = np.ascontiguousarray(rbits).view(np.uint8).reshape(T, 128)
+    return out
+
+
+def unpack_fp8_ds_mla(packed) -> np.ndarray:
+    """uint8 [T, 656] -> float64 [T, 576]: code * scale for 0..511 (exact in
+    float64), the bf16 rope values for 512..575."""
+    from .fp8 import decode_e4m3
+    pk = np.ascontiguousarray(np.asarray(packed, dtype=np.uint8))
+    T = pk.shape[0]
+    codes = pk[:, :512]
+    scales = pk[:, 512:528].copy().view(np.float32).reshape(T, 4).astype(np.float64)
+    vals = decode_e4m3(codes).reshape(T, 4, 128) * scales[:, :, None]
+    rope = (pk[:, 528:656].copy().view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.concatenate([vals.reshape(T, 512), rope.reshape(T, 64)], axis=1)

@@ -589,3 +589,39 @@ def test_seeded_steps_equal_rerun_when_context_below_k():
     rerun = topk.topk_select(indexer.indexer_scores(rng.normal(size=(1, H, D)), None, np.ones((1, H)), keys, None,
                                                     np.array([0]), np.array([0]), np.array([P]), fp8=False)[0], k)
     assert sorted(share.seeded_step_positions(seed, P)) == sorted(int(x) for x in rerun if x >= 0)
+
+
+# --------------------------------------------------------------------- FP8 latent cache (656 B per token)
+
+def test_fp8_ds_mla_hand_worked_token():
+    """One token by hand: latent values 0..511 are block constants c_k (so each
+    block's codes are all 448 with scale |c_k|/448, i.e. code 0x7E or 0xFE), the
+    rope values are exact bf16 numbers."""
+    c = [1.0, -2.5, 448.0, 0.0]
+    x = np.zeros((1, 576), np.float32)
+    for k in range(4):
+        x[0, 128 * k:128 * (k + 1)] = c[k]
+    x[0, 512:] = np.arange(64, dtype=np.float32) * 0.5 - 7.0
+    pk = mla.pack_fp8_ds_mla(x)
+    assert pk.shape == (1, 656) and mla.FP8_DS_MLA_BYTES == 512 + 16 + 128 == 656
+    assert set(pk[0, 0:128].tolist()) == {0x7E} and set(pk[0, 128:256].tolist()) == {0xFE}
+    assert set(pk[0, 256:384].tolist()) == {0x7E} and set(pk[0, 384:512].tolist()) == {0x00}
+    assert pk[0, 512:528].view(np.float32).tolist() == [np.float32(1.0 / 448), np.float32(2.5 / 448), 1.0, 1.0]
+    un = mla.unpack_fp8_ds_mla(pk)[0]
+    assert np.allclose(un[:512], np.repeat(c, 128), rtol=2 ** -22, atol=0)   # 448 * (c/448) rounded once
+    assert np.array_equal(un[512:], x[0, 512:].astype(np.float64))
+
+
+def test_fp8_ds_mla_round_trip_and_rope_rounding():
+    rng = np.random.default_rng(13)
+    x = rng.normal(size=(200, 576)).astype(np.float32)
+    un = mla.unpack_fp8_ds_mla(mla.pack_fp8_ds_mla(x))
+    # E4M3 keeps 3 mantissa bits: |error| <= 2^-4 |x| for normal codes, plus half the smallest
+    # subnormal step of the block (2^-10 * scale)
+    blk = np.abs(x[:, :512]).reshape(200, 4, 128).max(axis=2) / 448.0
+    bound = 2.0 ** -4 * np.abs(x[:, :512]) + 2.0 ** -10 * np.repeat(blk, 128, axis=1) + 1e-30
+    assert np.all(np.abs(un[:, :512] - x[:, :512]) <= bound)
+    # rope: bf16 of each value, against torch's round-to-nearest-even cast
+    import torch
+    want = torch.from_numpy(x[:, 512:]).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(un[:, 512:], want)
