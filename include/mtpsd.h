@@ -56,6 +56,8 @@ extern "C" {
 #define MTPSD_F32 0
 #define MTPSD_BF16 1
 #define MTPSD_FP8_E4M3 2
+#define MTPSD_FP8_DS_MLA 3  /* latent cache rows of 656 bytes: 512 E4M3 codes (four blocks of 128), the four
+                               float32 block scales, the 64 rope values as bf16 ([P2] "草稿层 KV 的账") */
 
 /* bits ORed into *dev_status */
 #define MTPSD_STATUS_INDEX_RANGE 1   /* a selected index outside 0..row_pos (skipped) */
@@ -102,6 +104,16 @@ int mtpsd_resolve_indexer_types(int32_t n_layers, const char* pattern, int32_t f
  */
 int mtpsd_quantize_fp8_block128(const float* x, int64_t n_blocks, uint8_t* codes, float* scales,
                                 void* stream);
+
+/* ------------------------------------------------------------------------
+ * FP8 latent cache rows.  [P2] "草稿层 KV 的账" (656 bytes per token per layer, the
+ * fp8_ds_mla layout): latent [T, 576] (MTPSD_BF16 or MTPSD_F32) -> packed
+ * [T, 656] uint8: bytes 0..511 the E4M3 codes of values 0..511 in four blocks of
+ * 128 (the block-128 quantizer above), bytes 512..527 the four float32 scales,
+ * bytes 528..655 the 64 rope values 512..575 as bf16 (round to nearest even).
+ * latent 16-byte aligned; packed 16-byte aligned.
+ */
+int mtpsd_pack_latent_fp8(const void* latent, int32_t dtype, int64_t T, uint8_t* packed, void* stream);
 
 /* ------------------------------------------------------------------------
  * Lightning-indexer scores and per-row top-k in one call.
@@ -239,7 +251,8 @@ typedef struct {
   int32_t d_v;             /* 512 */
   int32_t n_idx;           /* selected entries per row (row stride of idx) */
   int32_t n_append;        /* appended positions per row (0 = none) */
-  int32_t dtype;           /* MTPSD_BF16 or MTPSD_F32: q, latent and out */
+  int32_t dtype;           /* MTPSD_BF16 or MTPSD_F32: q, latent and out; MTPSD_FP8_DS_MLA: bf16 q and out,
+                              latent rows of 656 bytes (the FP8 cache; dequantized tile by tile in shared memory) */
   float softmax_scale;
   int64_t row_pos_add;     /* added to row_pos[r] (draft step j of a shared loop passes j) */
   const void* q;           /* [R, H, d_latent] */
@@ -310,7 +323,8 @@ int mtpsd_accept_stochastic(const int64_t* draft, const float* draft_probs, cons
  * W-row window are copied, byte for byte, to positions dst_pos[b] + i of
  * request b (pool rows cache_start[b] + dst_pos[b] + i); rejected rows are not
  * written.  Both caches of the layer move together.
- *   src_latent [B, W, 576] (latent_dtype: MTPSD_BF16 or MTPSD_F32)
+ *   src_latent [B, W, 576] (latent_dtype: MTPSD_BF16 or MTPSD_F32), or [B, W, 656] packed
+ *   bytes (MTPSD_FP8_DS_MLA)
  *   src_idxk [B, W, idx_dim] uint8, src_idxs [B, W] float32
  *   dst_latent [pool_tokens, 576], dst_idxk [pool_tokens, idx_dim], dst_idxs [pool_tokens]
  *   cache_start [B], dst_pos [B] int64

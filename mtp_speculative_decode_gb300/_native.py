@@ -20,6 +20,7 @@ MTPSD_EWORKSPACE = -4
 MTPSD_F32 = 0
 MTPSD_BF16 = 1
 MTPSD_FP8_E4M3 = 2
+MTPSD_FP8_DS_MLA = 3
 
 NOALLOC_SCRATCH_BYTES = 16 << 20   # MTPSD_NOALLOC_SCRATCH_BYTES
 
@@ -59,6 +60,7 @@ SIGNATURES = {
     "mtpsd_host_merged_offsets": (None, [vp, i32, i32, vp]),
     "mtpsd_resolve_indexer_types": (C.c_int, [i32, C.c_char_p, i32, i32, vp]),
     "mtpsd_quantize_fp8_block128": (C.c_int, [vp, i64, vp, vp, vp]),
+    "mtpsd_pack_latent_fp8": (C.c_int, [vp, i32, i64, vp, vp]),
     "mtpsd_scores_ld": (i64, [i64]),
     "mtpsd_indexer_topk_workspace_size": (C.c_size_t, [i32, i32, i64, i32]),
     "mtpsd_indexer_topk_plan_bytes": (C.c_size_t, [i32, i32]),

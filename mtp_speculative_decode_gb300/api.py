@@ -91,6 +91,20 @@ def host_merged_offsets(prompt_offsets: np.ndarray, K: int) -> np.ndarray:
     return out
 
 
+def pack_latent_fp8(latent, packed=None, stream=None):
+    """latent [T, 576] bf16 or float32 -> the FP8 latent cache rows [T, 656] uint8."""
+    f32 = latent.dtype == torch.float32
+    _need(latent, "latent", torch.float32 if f32 else torch.bfloat16, 2)
+    if latent.shape[1] != 576:
+        raise ValueError("latent rows must have 576 values")
+    T = latent.shape[0]
+    if packed is None:
+        packed = torch.empty(T, 656, dtype=torch.uint8, device=latent.device)
+    check("mtpsd_pack_latent_fp8", lib().mtpsd_pack_latent_fp8(
+        _ptr(latent), N.MTPSD_F32 if f32 else N.MTPSD_BF16, T, _ptr(packed), _stream(stream)))
+    return packed
+
+
 def resolve_indexer_types(n_layers: int, explicit=None, pattern=None, freq=None, offset=None):
     """Per-layer indexer schedule as a list of "full" / "shared" (an explicit list is checked and
     returned; otherwise the library resolves the pattern or the frequency and offset)."""
@@ -252,7 +266,13 @@ def sparse_mla_decode(q, latent, cache_start, row_offsets, row_pos, idx, softmax
                       workspace=None, dev_status=None, stream=None):
     bf16 = q.dtype == torch.bfloat16
     _need(q, "q", torch.bfloat16 if bf16 else torch.float32, 3)
-    _need(latent, "latent", q.dtype, 2)
+    fp8kv = latent.dtype == torch.uint8     # the packed FP8 latent cache (656-byte rows)
+    if fp8kv:
+        _need(latent, "latent", torch.uint8, 2)
+        if not bf16 or latent.shape[1] != 656:
+            raise ValueError("an FP8 latent cache needs bf16 queries and 656-byte rows")
+    else:
+        _need(latent, "latent", q.dtype, 2)
     _need(cache_start, "cache_start", torch.int64, 1)
     _need(row_offsets, "row_offsets", torch.uint32, 1)
     _need(row_pos, "row_pos", torch.int64, 1)
@@ -260,7 +280,7 @@ def sparse_mla_decode(q, latent, cache_start, row_offsets, row_pos, idx, softmax
     if append_base is not None:
         _need(append_base, "append_base", torch.int64, 1)
     R, H, DL = q.shape
-    dt = N.MTPSD_BF16 if bf16 else N.MTPSD_F32
+    dt = N.MTPSD_FP8_DS_MLA if fp8kv else (N.MTPSD_BF16 if bf16 else N.MTPSD_F32)
     if out is None:
         out = torch.empty(R, H, 512, dtype=q.dtype, device=q.device)
     nbytes = sparse_mla_workspace_size(R, H, idx.shape[1], n_append, dt)
@@ -326,7 +346,8 @@ def accept_stochastic(draft, draft_probs, target_probs, u_accept, u_sample, num_
 def kv_writeback(src_latent, src_idxk, src_idxs, num_accepted, dst_latent, dst_idxk, dst_idxs, cache_start, dst_pos,
                  next_pos=None, dev_status=None, stream=None):
     bf16 = src_latent.dtype == torch.bfloat16
-    _need(src_latent, "src_latent", torch.bfloat16 if bf16 else torch.float32, 3)
+    fp8kv = src_latent.dtype == torch.uint8   # packed FP8 latent rows (656 bytes)
+    _need(src_latent, "src_latent", src_latent.dtype if fp8kv else (torch.bfloat16 if bf16 else torch.float32), 3)
     _need(dst_latent, "dst_latent", src_latent.dtype, 2)
     _need(num_accepted, "num_accepted", torch.int32, 1)
     _need(cache_start, "cache_start", torch.int64, 1)
@@ -341,7 +362,8 @@ def kv_writeback(src_latent, src_idxk, src_idxs, num_accepted, dst_latent, dst_i
         _need(src_idxs, "src_idxs", torch.float32)
         _need(dst_idxs, "dst_idxs", torch.float32)
     check("mtpsd_kv_writeback", lib().mtpsd_kv_writeback(
-        _ptr(src_latent), _ptr(src_idxk), _ptr(src_idxs), B, W, N.MTPSD_BF16 if bf16 else N.MTPSD_F32, idx_dim,
+        _ptr(src_latent), _ptr(src_idxk), _ptr(src_idxs), B, W,
+        N.MTPSD_FP8_DS_MLA if fp8kv else (N.MTPSD_BF16 if bf16 else N.MTPSD_F32), idx_dim,
         _ptr(num_accepted), _ptr(dst_latent), _ptr(dst_idxk), _ptr(dst_idxs), _ptr(cache_start), _ptr(dst_pos),
         dst_latent.shape[0], _ptr(next_pos), _ptr(dev_status), _stream(stream)))
     return next_pos

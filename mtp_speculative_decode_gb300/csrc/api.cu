@@ -87,6 +87,16 @@ int mtpsd_quantize_fp8_block128(const float* x, int64_t n_blocks, uint8_t* codes
   return launch_quantize_fp8(x, n_blocks, codes, scales, (cudaStream_t)stream);
 }
 
+int mtpsd_pack_latent_fp8(const void* latent, int32_t dtype, int64_t T, uint8_t* packed, void* stream) {
+  g_err[0] = 0;
+  if (T < 0) return fail(MTPSD_EINVAL, "pack_latent_fp8: T < 0");
+  if (dtype != MTPSD_BF16 && dtype != MTPSD_F32) return fail(MTPSD_EUNSUPPORTED, "pack_latent_fp8: dtype must be MTPSD_BF16 or MTPSD_F32");
+  if (T == 0) return MTPSD_OK;
+  if (!latent || !packed) return fail(MTPSD_EINVAL, "pack_latent_fp8: null pointer");
+  if (!aligned(latent, 16) || !aligned(packed, 16)) return fail(MTPSD_EINVAL, "pack_latent_fp8: buffers must be 16-byte aligned");
+  return launch_pack_latent_fp8(latent, dtype == MTPSD_F32, T, packed, (cudaStream_t)stream);
+}
+
 int64_t mtpsd_scores_ld(int64_t max_visible) { return (int64_t)align_up((size_t)(max_visible > 0 ? max_visible : 1), 4); }
 
 size_t mtpsd_indexer_topk_plan_bytes(int32_t B, int32_t R) { return (B < 0 || R < 0) ? 0 : indexer_tc_plan_bytes(B, R); }
@@ -238,16 +248,16 @@ int mtpsd_sparse_mla_decode(const mtpsd_mla_args* a, void* stream) {
   if (a->d_latent != 576 || a->d_v != 512)
     return fail(MTPSD_EUNSUPPORTED, "sparse_mla_decode: d_latent must be 576 and d_v 512");
   if ((int64_t)a->n_idx + a->n_append > 65536) return fail(MTPSD_EUNSUPPORTED, "sparse_mla_decode: more than 65536 positions per row");
-  if (a->dtype == MTPSD_BF16) {
+  if (a->dtype == MTPSD_BF16 || a->dtype == MTPSD_FP8_DS_MLA) {
     if (a->n_heads % 16) return fail(MTPSD_EUNSUPPORTED, "sparse_mla_decode: bf16 needs n_heads % 16 == 0");
   } else if (a->dtype != MTPSD_F32) {
-    return fail(MTPSD_EUNSUPPORTED, "sparse_mla_decode: dtype must be MTPSD_BF16 or MTPSD_F32");
+    return fail(MTPSD_EUNSUPPORTED, "sparse_mla_decode: dtype must be MTPSD_BF16, MTPSD_FP8_DS_MLA or MTPSD_F32");
   }
   if (a->n_append > 0 && !a->append_base) return fail(MTPSD_EINVAL, "sparse_mla_decode: n_append > 0 needs append_base");
   if (a->R == 0) return MTPSD_OK;
   if (!a->q || !a->latent || !a->cache_start || !a->row_offsets || !a->row_pos || !a->out || (a->n_idx > 0 && !a->idx))
     return fail(MTPSD_EINVAL, "sparse_mla_decode: null pointer");
-  if (a->dtype == MTPSD_BF16 && (!aligned(a->q, 16) || !aligned(a->latent, 16) || !aligned(a->out, 4)))
+  if (a->dtype != MTPSD_F32 && (!aligned(a->q, 16) || !aligned(a->latent, 16) || !aligned(a->out, 4)))
     return fail(MTPSD_EINVAL, "sparse_mla_decode: q and latent must be 16-byte aligned");
   MlaPlan p;
   p.B = a->B; p.R = a->R; p.H = a->n_heads; p.d_latent = a->d_latent; p.d_v = a->d_v; p.n_idx = a->n_idx;
@@ -290,7 +300,8 @@ int mtpsd_kv_writeback(const void* src_latent, const uint8_t* src_idxk, const fl
   int lat_bytes;
   if (latent_dtype == MTPSD_BF16) lat_bytes = 576 * 2;
   else if (latent_dtype == MTPSD_F32) lat_bytes = 576 * 4;
-  else return fail(MTPSD_EUNSUPPORTED, "kv_writeback: latent dtype must be MTPSD_BF16 or MTPSD_F32");
+  else if (latent_dtype == MTPSD_FP8_DS_MLA) lat_bytes = 656;
+  else return fail(MTPSD_EUNSUPPORTED, "kv_writeback: latent dtype must be MTPSD_BF16, MTPSD_F32 or MTPSD_FP8_DS_MLA");
   if (idx_dim != 0 && idx_dim % 16) return fail(MTPSD_EUNSUPPORTED, "kv_writeback: idx_dim must be a multiple of 16");
   if (B == 0) return MTPSD_OK;
   if (!src_latent || !dst_latent || !num_accepted || !cache_start || !dst_pos) return fail(MTPSD_EINVAL, "kv_writeback: null pointer");

@@ -19,6 +19,7 @@ bool make_tma_1d_f32(void* map, const void* base, uint64_t n_elems, uint32_t box
 int launch_merge_tokens(const int64_t* prompt, int64_t S, const uint32_t* po, const int64_t* draft,
                         int B, int K, int64_t* out, uint32_t* mo, cudaStream_t st);
 int launch_quantize_fp8(const float* x, int64_t n_blocks, uint8_t* codes, float* scales, cudaStream_t st);
+int launch_pack_latent_fp8(const void* latent, bool f32_in, int64_t T, uint8_t* out, cudaStream_t st);
 int launch_accept_greedy(const int64_t* draft, const int64_t* tgt, int B, int K, int64_t magic,
                          int32_t* n_acc, int64_t* next, cudaStream_t st);
 int launch_kv_writeback(const void* src_l, const uint8_t* src_k, const float* src_s, int B, int W,

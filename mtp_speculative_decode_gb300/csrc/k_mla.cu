@@ -17,6 +17,8 @@
 // mla_combine_kernel merges with their log-sum-exp weights.
 // float32 path (sparse_mla_f32_kernel): CUDA cores, one CTA per (row, head).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -87,19 +89,51 @@ struct MlaSplit {
   int64_t per_split;   // positions per split (multiple of MLA_NT)
 };
 
-// Shared memory layout of the bf16 kernel.
-struct MlaSmem {
+// Shared memory layout of the bf16 kernel (FP8KV adds the staging tiles of the packed rows).
+constexpr int MLA_FP8_ROW = 656;          // packed FP8 latent row: 512 codes, 4 float32 scales, 64 bf16 rope
+template <bool FP8KV>
+struct MlaSmemT {
   static constexpr int Q = 0;                                     // [64][ROWB]
   static constexpr int C = Q + MLA_HG * MLA_ROWB;                 // [2][32][ROWB]
   static constexpr int P = C + 2 * MLA_NT * MLA_ROWB;             // [64][PROWB]
   static constexpr int RED = P + MLA_HG * MLA_PROWB;              // [2][64] float
   static constexpr int LSUM = RED + 2 * MLA_HG * 4;               // [2][64] float
   static constexpr int ROWS = LSUM + 2 * MLA_HG * 4;              // [MAX_SPLIT] int64
-  static constexpr int BYTES = ROWS + MLA_MAX_SPLIT * 8;
+  static constexpr int STG = ROWS + MLA_MAX_SPLIT * 8;            // FP8KV: [2][32][656] packed rows
+  static constexpr int BYTES = STG + (FP8KV ? 2 * MLA_NT * MLA_FP8_ROW : 0);
 };
+using MlaSmem = MlaSmemT<false>;
 
+// One tile of packed FP8 rows (staging) -> bf16 rows of the compute tile: value = code * block scale
+// (E4M3 -> f16 is exact; the product is formed in float32 and rounded to bf16), rope copied.
+__device__ __forceinline__ void mla_dequant_tile(const uint8_t* stg, uint8_t* c) {
+  for (int w = threadIdx.x; w < MLA_NT * 64; w += blockDim.x) {   // 64 groups of 8 codes per row
+    const int i = w >> 6, grp = w & 63;
+    const uint8_t* src = stg + i * MLA_FP8_ROW;
+    const uint2 codes = *(const uint2*)(src + grp * 8);
+    const float sc = *(const float*)(src + 512 + (grp >> 4) * 4);
+    uint32_t outw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t word = e < 2 ? codes.x : codes.y;
+      const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((word >> (16 * (e & 1))) & 0xffffu);
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+      const float2 f = __half22float2(*(const __half2*)&hr);
+      const __nv_bfloat162 bv = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+      outw[e] = *(const uint32_t*)&bv;
+    }
+    *(uint4*)(c + i * MLA_ROWB + grp * 16) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+  }
+  for (int w = threadIdx.x; w < MLA_NT * 8; w += blockDim.x) {    // rope: 8 chunks of 16 bytes per row
+    const int i = w >> 3, ch = w & 7;
+    *(uint4*)(c + i * MLA_ROWB + 1024 + ch * 16) = *(const uint4*)(stg + i * MLA_FP8_ROW + 528 + ch * 16);
+  }
+}
+
+template <bool FP8KV>
 __global__ void __launch_bounds__(256, 1) sparse_mla_bf16_kernel(MlaPlan p, MlaSplit sp, float* __restrict__ part_o,
                                                                   float* __restrict__ part_ml) {
+  using MlaSmem = MlaSmemT<FP8KV>;
   griddep_wait();                // the previous kernel's writes are visible from here on
   griddep_launch_dependents();
   extern __shared__ __align__(128) uint8_t sm[];
@@ -138,11 +172,21 @@ __global__ void __launch_bounds__(256, 1) sparse_mla_bf16_kernel(MlaPlan p, MlaS
 
   const __nv_bfloat16* lat = (const __nv_bfloat16*)p.latent;
   auto gather = [&](int tile, int buf) {
-    for (int c = tid; c < MLA_NT * (MLA_DL / 8); c += blockDim.x) {
-      int i = c / (MLA_DL / 8), ch = c % (MLA_DL / 8);
-      int64_t row = rows_s[(int64_t)tile * MLA_NT + i];
-      const void* src = row >= 0 ? (const void*)(lat + row * MLA_DL + ch * 8) : (const void*)lat;
-      cp_async16(smem_u32(sm + MlaSmem::C + (buf * MLA_NT + i) * MLA_ROWB + ch * 16), src, row >= 0);
+    if constexpr (FP8KV) {   // packed rows into the staging tile (invalid rows zero-filled: scale 0)
+      const uint8_t* lat8 = (const uint8_t*)p.latent;
+      for (int c = tid; c < MLA_NT * (MLA_FP8_ROW / 16); c += blockDim.x) {
+        int i = c / (MLA_FP8_ROW / 16), ch = c % (MLA_FP8_ROW / 16);
+        int64_t row = rows_s[(int64_t)tile * MLA_NT + i];
+        const void* src = row >= 0 ? (const void*)(lat8 + row * MLA_FP8_ROW + ch * 16) : (const void*)lat8;
+        cp_async16(smem_u32(sm + MlaSmem::STG + (buf * MLA_NT + i) * MLA_FP8_ROW + ch * 16), src, row >= 0);
+      }
+    } else {
+      for (int c = tid; c < MLA_NT * (MLA_DL / 8); c += blockDim.x) {
+        int i = c / (MLA_DL / 8), ch = c % (MLA_DL / 8);
+        int64_t row = rows_s[(int64_t)tile * MLA_NT + i];
+        const void* src = row >= 0 ? (const void*)(lat + row * MLA_DL + ch * 8) : (const void*)lat;
+        cp_async16(smem_u32(sm + MlaSmem::C + (buf * MLA_NT + i) * MLA_ROWB + ch * 16), src, row >= 0);
+      }
     }
     cp_async_commit();
   };
@@ -164,6 +208,10 @@ __global__ void __launch_bounds__(256, 1) sparse_mla_bf16_kernel(MlaPlan p, MlaS
       cp_async_wait<0>();
     }
     __syncthreads();
+    if constexpr (FP8KV) {
+      mla_dequant_tile(sm + MlaSmem::STG + buf * MLA_NT * MLA_FP8_ROW, sm + MlaSmem::C + buf * MLA_NT * MLA_ROWB);
+      __syncthreads();
+    }
 
     // ---- S = Q_blk(16 heads) . C_half(16 positions)^T over 576
     float s[2][4];
@@ -480,7 +528,7 @@ __global__ void __launch_bounds__(256) sparse_mla_f32_kernel(MlaPlan p, MlaSplit
 static MlaSplit choose_split(int R, int H, int n_idx, int n_append, int dtype) {
   int64_t total = (int64_t)n_idx + n_append;
   MlaSplit sp;
-  int64_t ctas = (int64_t)R * (dtype == MTPSD_BF16 ? ceil_div(H, MLA_HG) : H);
+  int64_t ctas = (int64_t)R * (dtype != MTPSD_F32 ? ceil_div(H, MLA_HG) : H);
   int64_t want = ctas >= 2 * num_sms() ? 1 : ceil_div(2 * num_sms(), ctas);
   int64_t by_len = ceil_div(total, 256);
   int64_t ns = want < by_len ? want : by_len;
@@ -550,14 +598,19 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
     }
     return MTPSD_OK;
   }
-  if (p.dtype == MTPSD_BF16) {
-    static std::atomic<uint64_t> attr{0};
-    if (!set_smem_limit_once(sparse_mla_bf16_kernel, MlaSmem::BYTES, attr)) {
+  if (p.dtype == MTPSD_BF16 || p.dtype == MTPSD_FP8_DS_MLA) {
+    const bool fp8kv = p.dtype == MTPSD_FP8_DS_MLA;
+    static std::atomic<uint64_t> attr{0}, attr8{0};
+    if (!(fp8kv ? set_smem_limit_once(sparse_mla_bf16_kernel<true>, MlaSmemT<true>::BYTES, attr8)
+                : set_smem_limit_once(sparse_mla_bf16_kernel<false>, MlaSmem::BYTES, attr))) {
       set_error("sparse_mla_bf16: cudaFuncSetAttribute failed");
       return MTPSD_ECUDA;
     }
     dim3 grid(p.R, (unsigned)ceil_div(p.H, MLA_HG), sp.n_splits);
-    launch_k(sparse_mla_bf16_kernel, grid, 256, MlaSmem::BYTES, st, p, sp, part_o, part_ml);
+    if (fp8kv)
+      launch_k(sparse_mla_bf16_kernel<true>, grid, 256, MlaSmemT<true>::BYTES, st, p, sp, part_o, part_ml);
+    else
+      launch_k(sparse_mla_bf16_kernel<false>, grid, 256, MlaSmem::BYTES, st, p, sp, part_o, part_ml);
     int rc = check_launch("sparse_mla_bf16");
     if (rc) return rc;
     if (sp.n_splits > 1) {

@@ -1,6 +1,7 @@
 // Small fused kernels of the MTP decode step: ragged merge, FP8 block-128
 // quantization, greedy acceptance, accepted-segment KV write-back and the
 // step-0 top-k share gather.  All are HBM/latency bound; each is one launch.
+#include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -80,6 +81,63 @@ int launch_quantize_fp8(const float* x, int64_t n_blocks, uint8_t* codes, float*
   if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
   launch_k(quantize_fp8_kernel, (int)blocks, 256, 0, st, (const float4*)x, n_blocks, (uint32_t*)codes, scales);
   return check_launch("quantize_fp8_block128");
+}
+
+// ---------------------------------------------------------------------------
+// FP8 latent cache rows ([P2] "草稿层 KV 的账": 656 bytes per token).  One warp
+// per token: the 512 latent values in four blocks of 128, each quantized like
+// the indexer keys (amax/448 scale, IEEE division, saturating RNE E4M3), the
+// four float32 scales, then the 64 rope values as bf16.
+template <bool F32IN>
+__global__ void pack_latent_fp8_kernel(const void* __restrict__ latent, int64_t T, uint8_t* __restrict__ out) {
+  griddep_wait();                // the previous kernel's writes are visible from here on
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = warp; t < T; t += nwarps) {
+    uint8_t* o = out + t * 656;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float v[4];
+      if constexpr (F32IN) {
+        const float4 f = *(const float4*)((const float*)latent + t * 576 + 128 * k + 4 * lane);
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+      } else {
+        const uint2 u = *(const uint2*)((const __nv_bfloat16*)latent + t * 576 + 128 * k + 4 * lane);
+        v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xffff0000u);
+        v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xffff0000u);
+      }
+      float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+      for (int sh = 16; sh; sh >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, sh));
+      const float scale = m > 0.f ? __fdiv_rn(m, 448.0f) : 1.0f;
+      uint32_t c = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        c |= (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(v[e], scale), __NV_SATFINITE, __NV_E4M3) << (8 * e);
+      *(uint32_t*)(o + 128 * k + 4 * lane) = c;
+      if (lane == 0) *(float*)(o + 512 + 4 * k) = scale;
+    }
+    uint32_t r;   // rope values 2 lane, 2 lane + 1 as bf16
+    if constexpr (F32IN) {
+      const float2 f = *(const float2*)((const float*)latent + t * 576 + 512 + 2 * lane);
+      __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+      r = *(uint32_t*)&b;
+    } else {
+      r = *(const uint32_t*)((const __nv_bfloat16*)latent + t * 576 + 512 + 2 * lane);
+    }
+    *(uint32_t*)(o + 528 + 4 * lane) = r;
+  }
+}
+
+int launch_pack_latent_fp8(const void* latent, bool f32_in, int64_t T, uint8_t* out, cudaStream_t st) {
+  if (T == 0) return MTPSD_OK;
+  int64_t blocks = (T * 32 + 255) / 256;
+  if (blocks > 16 * num_sms()) blocks = 16 * num_sms();
+  if (f32_in) launch_k(pack_latent_fp8_kernel<true>, (int)blocks, 256, 0, st, latent, T, out);
+  else launch_k(pack_latent_fp8_kernel<false>, (int)blocks, 256, 0, st, latent, T, out);
+  return check_launch("pack_latent_fp8");
 }
 
 // ---------------------------------------------------------------------------

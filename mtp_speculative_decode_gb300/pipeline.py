@@ -52,9 +52,10 @@ class DecodeStep:
     step of the next round (seed_dsa_topk_from_draft_extend)."""
 
     def __init__(self, w: W.Workload, device="cuda", draft: Optional[Dict[str, torch.Tensor]] = None,
-                 seeded: bool = False):
+                 seeded: bool = False, latent_fp8: bool = False):
         self.w = w
         self.seeded = seeded
+        self.latent_fp8 = latent_fp8   # latent caches as 656-byte FP8 rows ([P2] "草稿层 KV 的账")
         spec = w.spec
         self.spec = spec
         self.device = device
@@ -64,7 +65,7 @@ class DecodeStep:
         t = w.tensors
         # --- resident caches (target layer)
         self.cache_start = _dev(w.cache_start, device, torch.int64)
-        self.latent = _gen(t, "latent", device)
+        self.latent = self._latent(_gen(t, "latent", device))
         if self.fp8:
             k_raw = _gen(t, "k_idx", device)
             self.k_cache, k_scale = api.quantize_fp8_block128(k_raw)
@@ -101,6 +102,8 @@ class DecodeStep:
             self.q_idx, self.q_scale = self.q_idx_raw, None
         self.topk_idx = torch.empty(R, spec.topk, dtype=torch.int32, device=device)
         self.out = torch.empty(R, spec.H_Q, 512, dtype=self.q_mla.dtype, device=device)
+        mla_dt = N.MTPSD_FP8_DS_MLA if latent_fp8 else (1 if self.fp8 else 0)
+        self.mla_dtype = mla_dt
         self.lse = torch.empty(R, spec.H_Q, dtype=torch.float32, device=device)
         self.num_accepted = torch.empty(B, dtype=torch.int32, device=device)
         self.next_tokens = torch.empty(B, dtype=torch.int64, device=device)
@@ -110,13 +113,13 @@ class DecodeStep:
         self.ws_plan = torch.empty(max(api.indexer_plan_bytes(B, R), 256), dtype=torch.uint8, device=device)
         self.ws_topk = torch.empty(max(api.topk_workspace_size(R, self.max_visible, spec.topk), 256), dtype=torch.uint8,
                                    device=device)
-        n = api.sparse_mla_workspace_size(R, spec.H_Q, spec.topk, 0, 1 if self.fp8 else 0)
+        n = api.sparse_mla_workspace_size(R, spec.H_Q, spec.topk, 0, self.mla_dtype)
         self.ws_mla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
         # --- draft layer
         self.has_draft = spec.draft_steps > 0
         if self.has_draft:
             d = draft if draft is not None else W.draft_tensors(w)
-            self.d_latent = _gen(d, "d_latent", device)
+            self.d_latent = self._latent(_gen(d, "d_latent", device))
             if self.fp8:
                 kr = _gen(d, "d_k_idx", device)
                 self.d_k_cache, ks = api.quantize_fp8_block128(kr)
@@ -131,7 +134,9 @@ class DecodeStep:
                 self.d_k_scale = None
                 self.src_idxk = _gen(d, "src_k_idx", device).view(torch.uint8)
                 self.src_idxs = None
-            self.src_latent = _gen(d, "src_latent", device)
+            src = _gen(d, "src_latent", device)
+            self.src_latent = self._latent(src.reshape(-1, 576)).reshape(src.shape[0], src.shape[1], -1) \
+                if latent_fp8 else src
             self.dst_pos = _dev(w.L, device, torch.int64)    # accepted segment starts at L_b
             self.next_pos = torch.empty(B, dtype=torch.int64, device=device)
             self.d_q_idx_raw = _gen(d, "d_q_idx", device)
@@ -154,11 +159,15 @@ class DecodeStep:
             self.ws_dplan = torch.empty(max(api.indexer_plan_bytes(B, B), 256), dtype=torch.uint8, device=device)
             self.ws_dtopk = torch.empty(max(api.topk_workspace_size(B, self.d_max_visible, spec.topk), 256),
                                         dtype=torch.uint8, device=device)
-            n = max(api.sparse_mla_workspace_size(B, spec.H_Q, spec.topk, j, 1 if self.fp8 else 0)
+            n = max(api.sparse_mla_workspace_size(B, spec.H_Q, spec.topk, j, self.mla_dtype)
                     for j in range(spec.draft_steps))
             self.ws_dmla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
             if seeded:
                 self._init_extend(d, device)
+
+    def _latent(self, x):
+        """A latent pool as the step stores it: as generated, or packed into FP8 rows."""
+        return api.pack_latent_fp8(x) if self.latent_fp8 else x
 
     def _init_extend(self, d, device):
         """Buffers of draft_extend's attention: K+1 rows per request at positions L_b .. L_b + K."""
@@ -183,10 +192,10 @@ class DecodeStep:
         self.x_topk = torch.empty(Rx, spec.topk, dtype=torch.int32, device=device)
         self.x_out = torch.empty(Rx, spec.H_Q, 512, dtype=self.q_mla.dtype, device=device)
         self.x_lse = torch.empty(Rx, spec.H_Q, dtype=torch.float32, device=device)
-        n = api.sparse_mla_workspace_size(Rx, spec.H_Q, spec.topk, 0, 1 if self.fp8 else 0)
+        n = api.sparse_mla_workspace_size(Rx, spec.H_Q, spec.topk, 0, self.mla_dtype)
         self.ws_xmla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
         self.seed_pos = torch.empty(B, dtype=torch.int64, device=device)
-        n = max(api.sparse_mla_workspace_size(B, spec.H_Q, spec.topk, j + 1, 1 if self.fp8 else 0)
+        n = max(api.sparse_mla_workspace_size(B, spec.H_Q, spec.topk, j + 1, self.mla_dtype)
                 for j in range(spec.draft_steps))
         self.ws_dmla = torch.empty(max(n, 256, self.ws_dmla.numel() if hasattr(self, "ws_dmla") else 0),
                                    dtype=torch.uint8, device=device)
@@ -325,7 +334,7 @@ class DecodeStep:
         return n
 
     def _mla_launches(self, n_idx, n_append, R):
-        return api.sparse_mla_launch_count(R, self.spec.H_Q, n_idx, n_append, 1 if self.fp8 else 0)
+        return api.sparse_mla_launch_count(R, self.spec.H_Q, n_idx, n_append, self.mla_dtype)
 
 
 class LayeredVerify:

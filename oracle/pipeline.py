@@ -42,8 +42,9 @@ class OracleStep:
     `t` holds the raw inputs of the target layer (q_idx, w_idx, k_idx, latent,
     q_mla) and `d` those of the draft layer."""
 
-    def __init__(self, w, d=None):
+    def __init__(self, w, d=None, latent_fp8: bool = False):
         self.w = w
+        self.latent_fp8 = latent_fp8   # latent rows stored as 656-byte FP8 rows (mla.pack_fp8_ds_mla)
         self.spec = w.spec
         self.fp8 = not w.spec.latent_f32
         self.t = w.tensors
@@ -51,6 +52,13 @@ class OracleStep:
         self._kq = {}      # cached per-request quantized keys: (pool name, b) -> (codes, scales)
 
     # ------------------------------------------------------------ helpers
+    def lat(self, rows):
+        """Latent rows (float64) as the cache holds them: exact, or through the FP8 row layout."""
+        rows = np.asarray(rows, dtype=np.float64)
+        if not self.latent_fp8:
+            return rows
+        return mla.unpack_fp8_ds_mla(mla.pack_fp8_ds_mla(rows.astype(np.float32)))
+
     def keys(self, name: str, b: int, upto: int):
         """Dequantized indexer keys of request b, positions 0..upto-1 (float64)."""
         base = int(self.w.cache_start[b])
@@ -96,7 +104,7 @@ class OracleStep:
             b = int(w.row_req[r])
             base = int(w.cache_start[b])
             pos = mla.row_index_list(idx)
-            C = _take(self.t, _ln("latent", layer), [base + s for s in pos]).reshape(len(pos), mla.D_LATENT)
+            C = self.lat(_take(self.t, _ln("latent", layer), [base + s for s in pos]).reshape(len(pos), mla.D_LATENT))
             q = _rows(self.t, _ln("q_mla", layer), r, r + 1).astype(np.float64)
             one = mla.sparse_mla(q, C, np.array([0]), np.array([0]), np.arange(len(pos))[None], _scale(),
                                  heads=heads)
@@ -141,7 +149,7 @@ class OracleStep:
         for j, s in enumerate(positions):
             if start <= s < start + n:
                 out[j] = src[s - start]
-        return out
+        return self.lat(out)
 
     def draft_step0(self, num_accepted, reqs):
         """Step-0 indexer scores and top-k of the draft row of each request."""

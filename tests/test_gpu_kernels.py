@@ -334,6 +334,68 @@ def test_sparse_mla(mt, H, lens, n_idx, dtype):
     print(f"worst relative L2 error {worst:.2e}")
 
 
+# ----------------------------------------------------------------------------- FP8 latent cache
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_pack_latent_fp8_bit_exact(mt, dtype):
+    g = torch.Generator().manual_seed(17)
+    x = torch.randn(1500, 576, generator=g).to(dtype)
+    x[3] = 0
+    x[4, :128] = 0                                   # a block without mass: scale 1
+    x[5] *= 1e3
+    got = mt.pack_latent_fp8(dev(x)).cpu().numpy()
+    want = omla.pack_fp8_ds_mla(x.float().numpy())
+    assert got.tobytes() == want.tobytes()
+
+
+@pytest.mark.parametrize("H,lens,n_idx,n_append", [
+    (128, [300, 2100, 50], 512, 0),
+    (128, [9000], 2048, 0),                           # several splits, merged
+    (64, [700, 40], 256, 3),                          # appended positions, a row shorter than n_idx
+    (128, [5000, 64], 2048, 1),
+])
+def test_sparse_mla_fp8_latent(mt, H, lens, n_idx, n_append):
+    """Sparse MLA over the 656-byte FP8 latent rows against the oracle over their exact dequantization."""
+    c = _mla_case(H, lens, n_idx, torch.bfloat16, seed=H + n_idx + 5)
+    R = len(c["row_req"])
+    scale = 1.0 / math.sqrt(576.0)
+    packed = mt.pack_latent_fp8(dev(c["latent"]))
+    lat_deq = omla.unpack_fp8_ds_mla(omla.pack_fp8_ds_mla(c["latent"].float().numpy()))
+    base = c["row_pos"].astype(np.int64) - n_append
+    idx = c["idx"].copy()
+    idx[idx > base[:, None]] = -1                     # the selection sees positions up to base
+    lse = torch.empty(R, H, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = mt.sparse_mla_decode(dev(c["q"]), packed, dev(c["cache_start"]), u32(c["ro"]), dev(base, torch.int64),
+                               dev(idx), scale, n_append=n_append, append_base=dev(base, torch.int64) if n_append else None,
+                               row_pos_add=n_append, lse=lse, dev_status=status)
+    assert status.item() == 0
+    ref = omla.sparse_mla(c["q"], lat_deq, c["cache_start"], c["row_req"], idx, scale, n_append=n_append,
+                          append_base=base if n_append else None)
+    o = out.float().cpu().numpy()
+    ls = lse.cpu().numpy()
+    worst = 0.0
+    for r in range(R):
+        worst = max(worst, parity.check_attention_row(o[r], ref[r][0], parity.ATT_TOL_BF16))
+        assert np.max(np.abs(ls[r] - ref[r][1])) <= 2e-3 * max(1.0, np.max(np.abs(ref[r][1])))
+    print(f"worst relative L2 error {worst:.2e}")
+
+
+def test_writeback_fp8_latent_rows(mt):
+    rng = np.random.default_rng(8)
+    B, Wn, T = 20, 6, 2000
+    src = rng.integers(0, 256, (B, Wn, 656), dtype=np.uint8)
+    dst = rng.integers(0, 256, (T, 656), dtype=np.uint8)
+    n_acc = rng.integers(0, Wn, B).astype(np.int32)
+    start = (np.arange(B) * 90).astype(np.int64)
+    g_dst = dev(dst)
+    mt.kv_writeback(dev(src), None, None, dev(n_acc), g_dst, None, None, dev(np.zeros(B, np.int64)), dev(start))
+    want = owb.kv_writeback(src, np.zeros((B, Wn, 16), np.uint8), np.zeros((B, Wn), np.float32),
+                            np.minimum(n_acc + 1, Wn), dst, np.zeros((T, 16), np.uint8), np.zeros(T, np.float32),
+                            start)[0]
+    assert g_dst.cpu().numpy().tobytes() == want.tobytes()
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_sparse_mla_append_and_edges(mt, dtype):
     """Shared-index draft steps (appended positions), -1 padding, empty rows and

@@ -25,15 +25,15 @@ def _sample(n, k, seed):
     return sorted(set([0, n - 1] + list(rng.choice(n, size=min(n, k), replace=False))))
 
 
-def run_case(mods, name, n_rows, n_reqs, heads=None):
+def run_case(mods, name, n_rows, n_reqs, heads=None, latent_fp8=False):
     pipeline, W, OracleStep = mods
     w = W.build(name)
     d = W.draft_tensors(w) if w.spec.draft_steps else None
-    g = pipeline.DecodeStep(w, "cuda", d)
+    g = pipeline.DecodeStep(w, "cuda", d, latent_fp8=latent_fp8)
     g.step()
     torch.cuda.synchronize()
     assert g.status.item() == 0, f"device status {g.status.item()}"
-    o = OracleStep(w, d)
+    o = OracleStep(w, d, latent_fp8=latent_fp8)
     spec = w.spec
     tol = parity.ATT_TOL_F32 if spec.latent_f32 else parity.ATT_TOL_BF16
     report = {}
@@ -103,6 +103,17 @@ def test_draft_loop_full_size(mods):
 @pytest.mark.slow
 def test_long_context_full_size(mods):
     run_case(mods, "long", n_rows=4, n_reqs=0)
+
+
+@pytest.mark.slow
+def test_draft_loop_fp8_latent(mods):
+    """The draft loop (write-back, step-0 indexer, four shared-index MLA steps) over 656-byte FP8 latent rows."""
+    run_case(mods, "draft", n_rows=0, n_reqs=6, heads=range(0, 128, 16), latent_fp8=True)
+
+
+@pytest.mark.slow
+def test_verify_fp8_latent(mods):
+    run_case(mods, "verify", n_rows=12, n_reqs=4, heads=range(0, 128, 16), latent_fp8=True)
 
 
 @pytest.mark.slow
