@@ -13,7 +13,10 @@ caches, and the 4-step shared-index draft loop (indexer + top-k at step 0,
 sparse MLA at every step).  ``value`` is verify rows per second of whole
 steps.  The same line carries, under ``configs``, the verify (32 x 8192),
 draft-loop (64 x 32768, draft rows/s) and long-context (8 requests up to 1M)
-workloads, each with its own timing and roofline.
+workloads, the draft loop over the FP8 latent cache and with draft_extend
+seeding, a 4-layer verify with the cross-layer indexer schedule, and
+rejection-sampling acceptance over a 154880-token vocabulary, each with its
+own timing and roofline.
 
 Inputs are resident in HBM; L2 is flushed (a 512 MB write) before every timed
 step; every step is timed with CUDA events on its stream: a first pass times
@@ -45,7 +48,8 @@ if ROOT not in sys.path:
 
 METRIC = "MTP verify rows/s (DSA indexer+top-k+sparse MLA); % HBM roofline on 1 GB300"
 DEFAULT = "decode"
-SUBS = ("verify", "draft", "long")
+BASE = ("tiny", "verify", "draft", "long", "decode")      # workloads of workloads.build (headline candidates)
+SUBS = ("verify", "draft", "long", "draft_fp8", "draft_seeded", "verify_layered", "accept_stochastic")
 DESC = {
     "tiny": "2 requests (contexts 100, 300), 4 verify rows each, 8 query heads, float32 latent, float32 4x64 "
             "indexer, top-k 32, 4 shared-index draft steps",
@@ -61,6 +65,15 @@ DESC = {
               "log-uniform in [1024, 131072]; merge of 1 + 5 tokens, 6-row verify (FP8 64x128 indexer, top-2048, "
               "sparse MLA over 128 heads of the 576-d bf16 latent), greedy acceptance (mean accept length about "
               "2.76), draft-layer write-back, 4 shared-index draft steps",
+    "draft_fp8": "the draft loop (64 requests x 32768 context) over the FP8 latent cache: 656-byte rows "
+                 "(512 E4M3 + 4 float32 scales + 64 bf16 rope) instead of 1152-byte bf16 rows",
+    "draft_seeded": "the draft loop (64 requests x 32768) with seed_dsa_topk_from_draft_extend: draft_extend's "
+                    "attention over the 6 window rows (indexer, top-2048, sparse MLA), its selection at the last "
+                    "accepted row seeds all 4 draft steps (no step-0 indexer)",
+    "verify_layered": "verify (32 requests x 8192, 6 rows) over 4 DSA layers with the cross-layer indexer "
+                      "schedule full, shared, shared, shared: one indexer + top-k, four sparse MLA",
+    "accept_stochastic": "rejection-sampling acceptance: 128 requests x 5 drafts over the 154880-token "
+                         "vocabulary (synthetic softmax rows), draw from the residual of the first rejected row",
 }
 
 
@@ -70,7 +83,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=list(DESC), default=DEFAULT)
+    ap.add_argument("--config", choices=[c for c in DESC if c not in SUBS or c in BASE], default=DEFAULT)
     ap.add_argument("--no-sub", action="store_true", help="only the chosen workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -258,26 +271,58 @@ def work_model(g, w):
     import numpy as np
 
     from mtp_speculative_decode_gb300 import roofline
+    if w is None:   # rejection-sampling acceptance
+        n_acc = g.num_accepted.cpu().numpy()
+        return {"accept_stochastic": {"rows": g.B, "flops": 0.0,
+                                      "bytes": roofline.accept_stochastic_bytes(g.B, g.K, g.V, n_acc)}}
     spec = w.spec
     m = {}
+    if hasattr(g, "layers"):   # layered verify: per full layer the indexer, per layer the MLA
+        vis_row = w.row_pos + 1
+        vis_req = w.L + w.r
+        for l, L in enumerate(g.layers):
+            if L["type"] == "full":
+                m[f"L{l}_scores"] = {"rows": w.R, "bytes": roofline.indexer_bytes(vis_req, w.R, spec.H_I, spec.D_I),
+                                     "flops": roofline.indexer_flops(vis_row, spec.H_I, spec.D_I), "dtype": "fp8"}
+                m[f"L{l}_topk"] = {"bytes": int(np.sum(vis_row)) * 8, "flops": 0.0}
+            sel = g.layers[L["src"]]["topk"].cpu().numpy()
+            union = [len(np.unique(sel[b * w.r:(b + 1) * w.r][sel[b * w.r:(b + 1) * w.r] >= 0])) for b in range(w.B)]
+            m[f"L{l}_mla"] = {"rows": w.R, "bytes": roofline.mla_bytes(union, w.R, spec.H_Q, spec.topk),
+                              "flops": roofline.mla_flops((sel >= 0).sum(axis=1), spec.H_Q), "dtype": "bf16"}
+        return m
+    row_bytes = roofline.FP8_LATENT_ROW_BYTES if getattr(g, "latent_fp8", False) else roofline.LATENT_ROW_BYTES
     if spec.verify:
         vis_row = w.row_pos + 1
         vis_req = w.L + w.r
-        m["verify_scores"] = {"bytes": roofline.indexer_bytes(vis_req, w.R, spec.H_I, spec.D_I),
+        m["verify_scores"] = {"rows": w.R, "bytes": roofline.indexer_bytes(vis_req, w.R, spec.H_I, spec.D_I),
                               "flops": roofline.indexer_flops(vis_row, spec.H_I, spec.D_I), "dtype": "fp8"}
         m["verify_topk"] = {"bytes": int(np.sum(vis_row)) * 8, "flops": 0.0}
         sel = g.topk_idx.cpu().numpy()
         union = [len(np.unique(sel[b * w.r:(b + 1) * w.r][sel[b * w.r:(b + 1) * w.r] >= 0])) for b in range(w.B)]
-        m["verify_mla"] = {"bytes": roofline.mla_bytes(union, w.R, spec.H_Q, spec.topk),
+        m["verify_mla"] = {"rows": w.R, "bytes": roofline.mla_bytes(union, w.R, spec.H_Q, spec.topk, row_bytes),
                            "flops": roofline.mla_flops((sel >= 0).sum(axis=1), spec.H_Q), "dtype": "bf16"}
-    if spec.draft_steps:
+    if spec.draft_steps and getattr(g, "seeded", False):
+        Wn = spec.K + 1
+        vis = (np.repeat(w.L, Wn) + np.tile(np.arange(Wn), w.B) + 1)
+        m["extend_scores"] = {"rows": w.B * Wn, "bytes": roofline.indexer_bytes(w.L + Wn, w.B * Wn, spec.H_I, spec.D_I),
+                              "flops": roofline.indexer_flops(vis, spec.H_I, spec.D_I), "dtype": "fp8"}
+        m["extend_topk"] = {"bytes": int(np.sum(vis)) * 8, "flops": 0.0}
+        xs = g.x_topk.cpu().numpy()
+        union = [len(np.unique(xs[b * Wn:(b + 1) * Wn][xs[b * Wn:(b + 1) * Wn] >= 0])) for b in range(w.B)]
+        m["extend_mla"] = {"rows": w.B * Wn, "bytes": roofline.mla_bytes(union, w.B * Wn, spec.H_Q, spec.topk, row_bytes),
+                           "flops": roofline.mla_flops((xs >= 0).sum(axis=1), spec.H_Q), "dtype": "bf16"}
+        n_sel = (g.shared_idx.cpu().numpy() >= 0).sum(axis=1)
+        for j in range(spec.draft_steps):
+            m[f"draft_mla{j}"] = {"rows": w.B, "bytes": roofline.mla_bytes(n_sel + j + 1, w.B, spec.H_Q, spec.topk, row_bytes),
+                                  "flops": roofline.mla_flops(n_sel + j + 1, spec.H_Q), "dtype": "bf16"}
+    elif spec.draft_steps:
         P = g.next_pos.cpu().numpy()
-        m["draft_scores"] = {"bytes": roofline.indexer_bytes(P + 1, w.B, spec.H_I, spec.D_I),
+        m["draft_scores"] = {"rows": w.B, "bytes": roofline.indexer_bytes(P + 1, w.B, spec.H_I, spec.D_I),
                              "flops": roofline.indexer_flops(P + 1, spec.H_I, spec.D_I), "dtype": "fp8"}
         m["draft_topk"] = {"bytes": int(np.sum(P + 1)) * 8, "flops": 0.0}
         n_sel = (g.shared_idx.cpu().numpy() >= 0).sum(axis=1)
         for j in range(spec.draft_steps):
-            m[f"draft_mla{j}"] = {"bytes": roofline.mla_bytes(n_sel + j, w.B, spec.H_Q, spec.topk),
+            m[f"draft_mla{j}"] = {"rows": w.B, "bytes": roofline.mla_bytes(n_sel + j, w.B, spec.H_Q, spec.topk, row_bytes),
                                   "flops": roofline.mla_flops(n_sel + j, spec.H_Q), "dtype": "bf16"}
     return m
 
@@ -314,8 +359,21 @@ def measure(config, a, world, local, e2e: bool, clocks_on: bool):
     dev = f"cuda:{local}"
     stream = torch.cuda.current_stream()
     t_build = time.perf_counter()
-    w = W.build(config)
-    g = pipeline.DecodeStep(w, dev, W.draft_tensors(w))
+    if config == "draft_fp8":
+        w = W.build("draft")
+        g = pipeline.DecodeStep(w, dev, W.draft_tensors(w), latent_fp8=True)
+    elif config == "draft_seeded":
+        w = W.add_draft_extend(W.build("draft"))
+        g = pipeline.DecodeStep(w, dev, W.draft_tensors(w), seeded=True)
+    elif config == "verify_layered":
+        w = W.add_layers(W.build("verify"), 4)
+        g = pipeline.LayeredVerify(w, ["full", "shared", "shared", "shared"], dev)
+    elif config == "accept_stochastic":
+        w = None
+        g = pipeline.StochasticAccept(128, 5, 154880, dev)
+    else:
+        w = W.build(config)
+        g = pipeline.DecodeStep(w, dev, W.draft_tensors(w))
     torch.cuda.synchronize()
     t_build = time.perf_counter() - t_build
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -365,9 +423,24 @@ def measure(config, a, world, local, e2e: bool, clocks_on: bool):
 
     pk = peaks()
     model = work_model(g, w)
-    spec = w.spec
     res = {"workload": DESC[config], "name": config, "ms_per_step": ms_step, "phases_ms": phase_ms,
            "build_s": t_build, "launches_per_step": g.launches_per_step(), "clocks": clk}
+    if w is None:
+        res["metric"] = "requests/s (acceptance of 5 drafts per request)"
+        res["value"] = world * g.B / (ms_step / 1e3)
+        res["unit"] = "requests/s"
+        res["mean_accept_length"] = float(g.num_accepted.float().mean().item()) + 1.0
+        res["roofline"] = {n: kernel_roofline(m, phase_ms[n], pk) for n, m in model.items()}
+        res["_g"], res["_w"], res["_model"], res["_flush"] = g, w, model, flush
+        return res
+    spec = w.spec
+    if config == "verify_layered":
+        res["metric"] = "verify rows/s (whole steps, 4 layers)"
+        res["value"] = world * w.R / (ms_step / 1e3)
+        res["unit"] = "rows/s"
+        res["roofline"] = {n: kernel_roofline(m, phase_ms[n], pk) for n, m in model.items() if n in phase_ms}
+        res["_g"], res["_w"], res["_model"], res["_flush"] = g, w, model, flush
+        return res
     if spec.verify:
         res["metric"] = "verify rows/s (whole steps)"
         res["value"] = world * w.R / (ms_step / 1e3)
@@ -386,10 +459,11 @@ def measure(config, a, world, local, e2e: bool, clocks_on: bool):
                                             "verify indexer + top-k + sparse MLA: (indexer + MLA algorithmic "
                                             "bytes) / (scores + top-k + MLA time)")
     if spec.draft_steps:
-        dn = ["draft_scores", "draft_topk"] + [f"draft_mla{j}" for j in range(spec.draft_steps)]
+        dn = (["extend_scores", "extend_topk", "extend_mla"] if getattr(g, "seeded", False) else
+              ["draft_scores", "draft_topk"]) + [f"draft_mla{j}" for j in range(spec.draft_steps)]
         roof["draft_path"] = path_roofline(model, phase_ms, dn, pk,
-                                           "draft loop: (step-0 indexer + 4 MLA algorithmic bytes) / "
-                                           "(step-0 scores + top-k + 4 MLA time)")
+                                           "draft loop: (indexer + MLA algorithmic bytes) / (its scores + "
+                                           "top-k + MLA time)")
     rec = profile_record("indexer_tc_kernel")
     roof["indexer_tensor_pipe_ncu"] = None if rec is None else {
         k: rec[k] for k in ("tensor_pipe_active_pct", "workload", "capture") if k in rec}
@@ -407,18 +481,18 @@ def headline_roofline(res, pk):
     model = res["_model"]
     cand = [n for n in model if n in phase_ms and (n.endswith("mla0") or n.endswith("mla") or n.endswith("scores"))]
     # draft MLA steps are separate launches of one kernel: compare the kernels' largest single launch
-    top = max(cand, key=lambda n: phase_ms[n])
+    top = max(cand or [n for n in model if n in phase_ms], key=lambda n: phase_ms[n])
     mdl, ms = model[top], phase_ms[top]
     tpeak = pk["bf16"] * (2.0 if mdl.get("dtype") == "fp8" else 1.0)
     t_hbm = mdl["bytes"] / (pk["hbm"] * 1e9)
     t_tc = mdl["flops"] / (tpeak * 1e12)
-    kern = "sparse_mla_tc_kernel" if "mla" in top else "indexer_tc_kernel"
+    kern = ("sparse_mla_tc_kernel" if "mla" in top else "indexer_tc_kernel" if "scores" in top
+            else "accept_stochastic_kernel")
     rec = profile_record(kern)
     traffic = None
-    if rec and rec.get("dram_bytes_per_unit") and rec.get("unit"):
-        units = {"row": (res["_w"].R if top.startswith("verify") else res["_w"].B)}.get(rec["unit"])
-        if units:
-            traffic = rec["dram_bytes_per_unit"] * units
+    if rec and rec.get("dram_bytes") and rec.get("algorithmic_bytes"):
+        # the captured launch's DRAM bytes per algorithmic byte, applied to this launch's algorithmic bytes
+        traffic = rec["dram_bytes"] / rec["algorithmic_bytes"] * mdl["bytes"]
     if t_tc >= t_hbm:
         achieved = mdl["flops"] / (ms / 1e3) / 1e12
         out = {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s", "frac": achieved / tpeak,

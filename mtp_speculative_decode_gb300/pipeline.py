@@ -442,3 +442,29 @@ class LayeredVerify:
                     api.topk_launch_count(self.max_visible, k)
             n += api.sparse_mla_launch_count(self.R, self.spec.H_Q, k, 0, 1 if self.fp8 else 0)
         return n
+
+
+class StochasticAccept:
+    """Rejection-sampling acceptance over a vocabulary-sized batch ([P2] the acceptance rule of speculative
+    sampling): draft tokens and their draft probabilities q, target probabilities p of the K+1 rows, and the
+    uniforms of the accept tests and of the draw, all resident on the device."""
+
+    def __init__(self, B: int, K: int, V: int, device="cuda", seed: int = 7):
+        self.B, self.K, self.V = B, K, V
+        self.draft, self.q, self.p, self.u_accept, self.u_sample = W.stochastic_inputs_device(seed, B, K, V, device)
+        self.num_accepted = torch.empty(B, dtype=torch.int32, device=device)
+        self.next_tokens = torch.empty(B, dtype=torch.int64, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def accept(self, stream=None):
+        api.accept_stochastic(self.draft, self.q, self.p, self.u_accept, self.u_sample, self.num_accepted,
+                              self.next_tokens, dev_status=self.status, stream=stream)
+
+    def phases(self):
+        return [("accept_stochastic", self.accept)]
+
+    def step(self, stream=None):
+        self.accept(stream)
+
+    def launches_per_step(self) -> int:
+        return 1

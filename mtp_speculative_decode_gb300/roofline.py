@@ -33,8 +33,20 @@ def indexer_flops(visible_per_row, H_I, D_I):
     return 2.0 * H_I * D_I * float(np.sum(visible_per_row))
 
 
-def mla_bytes(union_rows_per_request, R, H_Q, k):
-    return int(np.sum(union_rows_per_request)) * LATENT_ROW_BYTES + R * H_Q * (576 + 512) * 2 + R * k * 4
+FP8_LATENT_ROW_BYTES = 656   # 512 E4M3 codes + 4 float32 scales + 64 bf16 rope values
+
+
+def mla_bytes(union_rows_per_request, R, H_Q, k, row_bytes=LATENT_ROW_BYTES):
+    return int(np.sum(union_rows_per_request)) * row_bytes + R * H_Q * (576 + 512) * 2 + R * k * 4
+
+
+def accept_stochastic_bytes(B, K, V, n_accepted):
+    """The K gathered (q, p) pairs and draft ids per request, the uniforms, and the two rows of V
+    probabilities the draw scans (residual: p and q of the rejected row; p of row K after full
+    acceptance, one row)."""
+    n_accepted = np.asarray(n_accepted)
+    rows = np.where(n_accepted < K, 2, 1)
+    return int(B * K * (8 + 8 + 4) + B * 4 + int(np.sum(rows)) * V * 4 + B * 12)
 
 
 def mla_flops(selected_per_row, H_Q):

@@ -386,6 +386,24 @@ def stochastic_inputs(seed: int, B: int, K: int, V: int, temperature: float = 1.
             g.random(B).astype(np.float32))
 
 
+def stochastic_inputs_device(seed: int, B: int, K: int, V: int, device, temperature: float = 1.0,
+                             noise: float = 0.5):
+    """The recipe of stochastic_inputs drawn on the device with torch's seeded
+    CUDA generator (for vocabulary-sized batches whose host generation would
+    take longer than the timing; not bit-identical to the host draw).  Draft
+    tokens are drawn from q with torch.multinomial.  Returns device tensors
+    (draft, q, p, u_accept, u_sample)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + _key("stochastic") % 1000003)
+    logits = torch.randn(B, K + 1, V, generator=g, device=device) / temperature
+    p = torch.softmax(logits, dim=2)
+    q = torch.softmax(logits[:, :K] + noise * torch.randn(B, K, V, generator=g, device=device), dim=2)
+    draft = torch.multinomial(q.reshape(B * K, V), 1, generator=g).reshape(B, K).to(torch.int64)
+    return (draft, q.contiguous(), p.contiguous(), torch.rand(B, K, generator=g, device=device),
+            torch.rand(B, generator=g, device=device))
+
+
 def layer_name(name: str, layer: int) -> str:
     """Name of a per-layer input: the first layer keeps the plain name."""
     return name if layer == 0 else f"{name}@{layer}"
