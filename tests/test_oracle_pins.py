@@ -625,3 +625,100 @@ def test_fp8_ds_mla_round_trip_and_rope_rounding():
     import torch
     want = torch.from_numpy(x[:, 512:]).to(torch.bfloat16).double().numpy()
     assert np.array_equal(un[:, 512:], want)
+
+
+# --------------------------------------------------------------------- the composed step against dense attention
+
+def _composed_step():
+    """A hand-built two-request step with k above every context, so that each
+    top-k takes every visible position and each attention of the composed
+    oracle step must equal textbook dense attention over the rows the readings
+    name: contexts L = [6, 9], K = 2 (window W = 3), float32 inputs, and the
+    draft-layer pool with the accepted window rows overlaid at L .. L + n - 1."""
+    import types
+
+    from oracle.pipeline import OracleStep
+    rng = np.random.default_rng(31)
+    B, K, W, H_I, D_I, H_Q = 2, 2, 3, 2, 8, 2
+    L = np.array([6, 9])
+    cap = L + W + 6
+    cache_start = np.concatenate([[0], np.cumsum(cap)[:-1]])
+    T = int(cap.sum())
+    R = B * W
+    spec = types.SimpleNamespace(K=K, topk=64, latent_f32=True, draft_steps=3)
+    row_req = np.repeat(np.arange(B), W)
+    row_pos = np.repeat(L, W) + np.tile(np.arange(W), B)
+    f = lambda *s: torch.from_numpy(rng.normal(size=s).astype(np.float32))
+    u = lambda *s: torch.from_numpy(rng.uniform(0.1, 1.0, size=s).astype(np.float32))
+    t = {"q_idx": f(R, H_I, D_I), "w_idx": u(R, H_I), "k_idx": f(T, D_I), "latent": f(T, 576),
+         "q_mla": f(R, H_Q, 576)}
+    for l in (1, 2):
+        for n, v in (("q_idx", f(R, H_I, D_I)), ("w_idx", u(R, H_I)), ("k_idx", f(T, D_I)), ("latent", f(T, 576)),
+                     ("q_mla", f(R, H_Q, 576))):
+            t[f"{n}@{l}"] = v
+    d = {"d_k_idx": f(T, D_I), "d_latent": f(T, 576), "src_k_idx": f(B, W, D_I), "src_latent": f(B, W, 576),
+         "d_q_idx": f(B, H_I, D_I), "d_w_idx": u(B, H_I), "x_q_idx": f(R, H_I, D_I), "x_w_idx": u(R, H_I),
+         "x_q_mla": f(R, H_Q, 576)}
+    for j in range(spec.draft_steps):
+        d[f"d_q_mla{j}"] = f(B, H_Q, 576)
+    w = types.SimpleNamespace(spec=spec, L=L, cache_start=cache_start, row_req=row_req, row_pos=row_pos, tensors=t)
+    return OracleStep(w, d), w, t, d
+
+
+def _draft_rows_after_writeback(w, d, b, n_acc, upto):
+    """Draft latent rows 0..upto-1 of request b, the first n_acc + 1 window rows written at L_b."""
+    base = int(w.cache_start[b])
+    rows = d["d_latent"][base:base + upto].double().numpy().copy()
+    for i in range(n_acc + 1):
+        if w.L[b] + i < upto:
+            rows[w.L[b] + i] = d["src_latent"][b, i].double().numpy()
+    return rows
+
+
+def test_composed_verify_and_layers_equal_dense_attention():
+    o, w, t, _ = _composed_step()
+    scale = 1.0 / math.sqrt(576.0)
+    rows = list(range(len(w.row_pos)))
+    out = o.verify_mla(o.verify_topk(o.verify_scores(rows)))
+    for r in rows:
+        base = int(w.cache_start[w.row_req[r]])
+        ref = _dense_attention(t["q_mla"][r].double().numpy(),
+                               t["latent"][base:base + w.row_pos[r] + 1].double().numpy(), scale)
+        assert np.allclose(out[r][0], ref[0], rtol=1e-10, atol=1e-12) and np.allclose(out[r][1], ref[1], rtol=1e-12)
+    # full, shared, full: every layer attends its own latent rows 0..p
+    _, lo = o.layered_verify(["full", "shared", "full"], rows)
+    for l in range(3):
+        lat = t["latent"] if l == 0 else t[f"latent@{l}"]
+        qm = t["q_mla"] if l == 0 else t[f"q_mla@{l}"]
+        for r in rows:
+            base = int(w.cache_start[w.row_req[r]])
+            ref = _dense_attention(qm[r].double().numpy(), lat[base:base + w.row_pos[r] + 1].double().numpy(), scale)
+            assert np.allclose(lo[l][r][0], ref[0], rtol=1e-10, atol=1e-12)
+
+
+def test_composed_draft_loop_extend_and_seed_equal_dense_attention():
+    """Draft step j at P + j = L + n_acc + 1 + j attends rows 0..P+j; draft_extend's
+    window row i attends rows 0..L+i; the seeded step j of the next round (seed =
+    draft_extend's selection at window row n_acc, position P - 1) attends rows
+    0..P+j too: all over the written-back draft pool."""
+    o, w, _, d = _composed_step()
+    scale = 1.0 / math.sqrt(576.0)
+    n_acc = np.array([1, 0])
+    P = [int(w.L[b]) + int(n_acc[b]) + 1 for b in range(2)]
+    _, shared = o.draft_step0(n_acc, [0, 1])
+    _, sel, xo = o.draft_extend(n_acc, [0, 1])
+    seed = {b: sel[(b, int(n_acc[b]))] for b in range(2)}
+    for j in range(3):
+        dm = o.draft_mla(n_acc, shared, j, [0, 1])
+        sm = o.seeded_draft_mla(n_acc, seed, j, [0, 1])
+        for b in range(2):
+            rows = _draft_rows_after_writeback(w, d, b, int(n_acc[b]), P[b] + j + 1)
+            ref = _dense_attention(d[f"d_q_mla{j}"][b].double().numpy(), rows, scale)
+            assert np.allclose(dm[b][0], ref[0], rtol=1e-10, atol=1e-12), (j, b)
+            assert np.allclose(sm[b][0], ref[0], rtol=1e-10, atol=1e-12), (j, b)
+            assert np.allclose(sm[b][1], ref[1], rtol=1e-12)
+    for b in range(2):
+        for i in range(3):
+            rows = _draft_rows_after_writeback(w, d, b, int(n_acc[b]), int(w.L[b]) + i + 1)
+            ref = _dense_attention(d["x_q_mla"][b * 3 + i].double().numpy(), rows, scale)
+            assert np.allclose(xo[(b, i)][0], ref[0], rtol=1e-10, atol=1e-12), (b, i)
