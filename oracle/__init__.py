@@ -29,4 +29,14 @@ Pinning (what each function is checked against, other than itself) lives in
 * writeback.kv_writeback — pinned (byte-level cases)
 * share.topk_share_gather / shared_index_list — pinned (equals rerunning the
   indexer when the context is shorter than k)
+* accept.accept_stochastic — pinned (hand-worked chains, the emitted
+  distribution equals the target's, exact fixed-point draw)
+* share.resolve_indexer_types / source_layers / seeded_step_positions —
+  pinned (the pages' layer counts, hand-worked schedules and positions)
+* mla.pack_fp8_ds_mla / unpack_fp8_ds_mla — pinned (hand-worked token, round
+  trip)
+* paged.slot_of / assign_cache_locs / gather_positions / kv_move_accepted /
+  kv_writeback_slots — pinned (hand-worked block tables, a paged pool built
+  page by page reads back the contiguous cache, a swap that an in-place copy
+  gets wrong, the contiguous write-back as a special case)
 """

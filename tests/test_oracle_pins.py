@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import accept, fp8, indexer, merge, mla, share, topk, writeback
+from oracle import accept, fp8, indexer, merge, mla, paged, share, topk, writeback
 
 
 # --------------------------------------------------------------------- FP8 codec
@@ -722,3 +722,110 @@ def test_composed_draft_loop_extend_and_seed_equal_dense_attention():
             rows = _draft_rows_after_writeback(w, d, b, int(n_acc[b]), int(w.L[b]) + i + 1)
             ref = _dense_attention(d["x_q_mla"][b * 3 + i].double().numpy(), rows, scale)
             assert np.allclose(xo[(b, i)][0], ref[0], rtol=1e-10, atol=1e-12), (b, i)
+
+
+# --------------------------------------------------------------------- paged / slotted KV
+
+# page size 4; request 0 owns pages 2, 0, 5 (positions 0..11), request 1 pages 1, 3 and no third page
+_BT = np.array([[2, 0, 5], [1, 3, -1]], dtype=np.int32)
+
+
+def test_slot_of_hand_worked():
+    assert paged.slot_of(_BT, 4, 0, 0) == 8        # page 2, offset 0
+    assert paged.slot_of(_BT, 4, 0, 5) == 1        # page 0, offset 1
+    assert paged.slot_of(_BT, 4, 0, 11) == 23      # page 5, offset 3
+    assert paged.slot_of(_BT, 4, 1, 2) == 6        # page 1, offset 2
+    assert paged.slot_of(_BT, 4, 1, 7) == 15       # page 3, offset 3
+    assert paged.slot_of(_BT, 4, 1, 9) == -1       # no page
+    assert paged.slot_of(_BT, 4, 1, -1) == -1
+
+
+def test_slot_of_page_size_one_is_the_token_table():
+    req_to_token = np.array([[7, 3, 9, 0], [1, 2, 8, 5]], dtype=np.int32)
+    for b in range(2):
+        for s in range(4):
+            assert paged.slot_of(req_to_token, 1, b, s) == req_to_token[b, s]
+
+
+def test_assign_cache_locs_hand_worked():
+    out = paged.assign_cache_locs(_BT, 4, [3, 1], 3)
+    assert out.dtype == np.int64
+    assert out.tolist() == [[11, 0, 1], [5, 6, 7]]   # request 0 crosses from page 2 into page 0
+
+
+def test_paged_pool_built_page_by_page_reads_back_the_contiguous_cache():
+    """A pool filled one page at a time from each request's page list (no slot
+    arithmetic) holds, at slot_of(b, s), position s of the contiguous cache."""
+    rng = np.random.default_rng(5)
+    P, lengths = 8, [21, 8, 3]
+    pages_needed = [(n + P - 1) // P for n in lengths]
+    perm = rng.permutation(sum(pages_needed) + 2)        # pages handed out in a random order
+    bt = np.full((3, max(pages_needed)), -1, dtype=np.int32)
+    pool = np.full((len(perm) * P, 6), np.nan)
+    cont = [rng.standard_normal((n, 6)) for n in lengths]
+    k = 0
+    for b, n in enumerate(lengths):
+        for j in range(pages_needed[b]):
+            page = int(perm[k]); k += 1
+            bt[b, j] = page
+            chunk = cont[b][j * P:(j + 1) * P]
+            pool[page * P: page * P + len(chunk)] = chunk
+    for b, n in enumerate(lengths):
+        got = paged.gather_positions(pool, bt, P, b, range(n))
+        assert np.array_equal(got, cont[b])
+        got = paged.gather_positions(pool, bt, P, b, [n - 1, 0])
+        assert np.array_equal(got, cont[b][[n - 1, 0]])
+
+
+def test_kv_move_accepted_is_a_move_not_an_in_place_copy():
+    """Window slots 10..13; the accepted rows are columns 1 and 0 (a swap):
+    slot 10 receives slot 11's old bytes and slot 11 slot 10's old bytes.
+    A copy done in place, in order, would leave both slots equal."""
+    lat = np.arange(16 * 3, dtype=np.float32).reshape(16, 3)
+    key = np.arange(16 * 2, dtype=np.uint8).reshape(16, 2)
+    sc = np.arange(16, dtype=np.float32)
+    loc = np.array([[10, 11, 12, 13]], dtype=np.int64)
+    out = paged.kv_move_accepted([lat, key, sc], loc, np.array([[1, 0, -1, -1]]), [2])
+    for before, after in zip([lat, key, sc], out):
+        assert np.array_equal(after[10], before[11]) and np.array_equal(after[11], before[10])
+        rest = [t for t in range(16) if t not in (10, 11)]
+        assert np.array_equal(after[rest], before[rest])
+
+
+def test_kv_move_accepted_hand_worked_shift_and_chain():
+    lat = np.arange(20, dtype=np.float64).reshape(10, 2)
+    loc = np.array([[2, 3, 4, 5], [6, 7, 8, 9]], dtype=np.int64)
+    # request 0 keeps columns 1 and 3 (slots 3, 5) -> slots 2, 3; request 1 is a chain of 3
+    (after,) = paged.kv_move_accepted([lat], loc, np.array([[1, 3, 0, 0], [0, 1, 2, 0]]), [2, 3])
+    assert after[2].tolist() == lat[3].tolist() and after[3].tolist() == lat[5].tolist()
+    assert np.array_equal(after[4:], lat[4:]) and np.array_equal(after[:2], lat[:2])
+    # a chain (accept_index = 0, 1, 2, ...) moves nothing
+    (same,) = paged.kv_move_accepted([lat], loc, np.tile(np.arange(4), (2, 1)), [4, 4])
+    assert np.array_equal(same, lat)
+
+
+def test_kv_writeback_slots_contiguous_special_case():
+    """With dst_slots[b, i] = dst_start[b] + i the write-back by slot is the
+    contiguous write-back."""
+    rng = np.random.default_rng(9)
+    B, Wn, T = 3, 4, 40
+    sl = rng.standard_normal((B, Wn, 5)); sk = rng.integers(0, 256, (B, Wn, 7), dtype=np.uint8)
+    ss = rng.standard_normal((B, Wn)).astype(np.float32)
+    dl = rng.standard_normal((T, 5)); dk = rng.integers(0, 256, (T, 7), dtype=np.uint8)
+    ds = rng.standard_normal(T).astype(np.float32)
+    acc, start = [1, 4, 2], [0, 17, 30]
+    slots = np.array([[start[b] + i for i in range(Wn)] for b in range(B)], dtype=np.int64)
+    a = paged.kv_writeback_slots(sl, sk, ss, acc, dl, dk, ds, slots)
+    e = writeback.kv_writeback(sl, sk, ss, acc, dl, dk, ds, start)
+    for x, y in zip(a, e):
+        assert np.array_equal(x, y)
+    # scattered slots: row i lands where the plan says, nothing else changes
+    slots = np.array([[39, 0, 5, 6], [12, 2, 31, 8], [20, 21, 1, 3]], dtype=np.int64)
+    l2, k2, s2 = paged.kv_writeback_slots(sl, sk, ss, acc, dl, dk, ds, slots)
+    touched = {int(slots[b, i]) for b in range(B) for i in range(acc[b])}
+    for b in range(B):
+        for i in range(acc[b]):
+            t = int(slots[b, i])
+            assert np.array_equal(l2[t], sl[b, i]) and np.array_equal(k2[t], sk[b, i]) and s2[t] == ss[b, i]
+    rest = [t for t in range(T) if t not in touched]
+    assert np.array_equal(l2[rest], dl[rest]) and np.array_equal(k2[rest], dk[rest])
