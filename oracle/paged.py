@@ -13,8 +13,8 @@ The same section speaks of page_size > 1 (pages of consecutive slots).
 Reading adopted: a block table per request, block_table[b][j] = the pool page
 holding positions j*page_size .. (j+1)*page_size - 1 of request b, so that
 position s lives in slot block_table[b][s // page_size] * page_size +
-s % page_size; page_size 1 is the token table itself.  A negative page entry
-means no page.
+s % page_size; page_size 1 is the token table itself.  A negative page entry,
+or a position past the table's width, means no slot.
 
 [P2] section "KV 交账:接受段的搬移与拒绝段的回收": fill_front_out_cache_loc
 takes the first accept_len slots of the window (the target slots),
@@ -29,9 +29,9 @@ import numpy as np
 
 
 def slot_of(block_table, page_size: int, b: int, s: int) -> int:
-    """Pool slot of position s of request b, or -1 when its page entry is
-    negative or s is negative."""
-    if s < 0:
+    """Pool slot of position s of request b, or -1 when s is negative, lies
+    past the table's width, or its page entry is negative."""
+    if s < 0 or s // page_size >= len(block_table[b]):
         return -1
     page = int(block_table[b][s // page_size])
     if page < 0:

@@ -738,6 +738,7 @@ def test_slot_of_hand_worked():
     assert paged.slot_of(_BT, 4, 1, 7) == 15       # page 3, offset 3
     assert paged.slot_of(_BT, 4, 1, 9) == -1       # no page
     assert paged.slot_of(_BT, 4, 1, -1) == -1
+    assert paged.slot_of(_BT, 4, 0, 12) == -1      # past the table's three pages
 
 
 def test_slot_of_page_size_one_is_the_token_table():
