@@ -49,7 +49,7 @@ if ROOT not in sys.path:
 METRIC = "MTP verify rows/s (DSA indexer+top-k+sparse MLA); % HBM roofline on 1 GB300"
 DEFAULT = "decode"
 BASE = ("tiny", "verify", "draft", "long", "decode")      # workloads of workloads.build (headline candidates)
-SUBS = ("verify", "draft", "long", "draft_fp8", "draft_seeded", "verify_layered", "accept_stochastic")
+SUBS = ("verify", "draft", "long", "draft_fp8", "draft_seeded", "verify_layered", "verify_paged", "accept_stochastic")
 DESC = {
     "tiny": "2 requests (contexts 100, 300), 4 verify rows each, 8 query heads, float32 latent, float32 4x64 "
             "indexer, top-k 32, 4 shared-index draft steps",
@@ -72,6 +72,9 @@ DESC = {
                     "accepted row seeds all 4 draft steps (no step-0 indexer)",
     "verify_layered": "verify (32 requests x 8192, 6 rows) over 4 DSA layers with the cross-layer indexer "
                       "schedule full, shared, shared, shared: one indexer + top-k, four sparse MLA",
+    "verify_paged": "the verify workload (32 requests x 8192, 6 rows, write-back, 4-step shared-index draft loop) "
+                    "over paged caches: pages of 64 tokens in shuffled order, one block table shared by the target "
+                    "and draft layers; adds the window's slot plan and the accepted-KV move, and writes back by slot",
     "accept_stochastic": "rejection-sampling acceptance: 128 requests x 5 drafts over the 154880-token "
                          "vocabulary (synthetic softmax rows), draw from the residual of the first rejected row",
 }
@@ -85,6 +88,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=[c for c in DESC if c not in SUBS or c in BASE], default=DEFAULT)
     ap.add_argument("--no-sub", action="store_true", help="only the chosen workload")
+    ap.add_argument("--subs", default="", help="comma-separated sub-workloads to run (default: all)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-sample", type=float, default=0.0, help=argparse.SUPPRESS)
@@ -368,6 +372,9 @@ def measure(config, a, world, local, e2e: bool, clocks_on: bool):
     elif config == "verify_layered":
         w = W.add_layers(W.build("verify"), 4)
         g = pipeline.LayeredVerify(w, ["full", "shared", "shared", "shared"], dev)
+    elif config == "verify_paged":
+        w = W.build("verify")
+        g = pipeline.DecodeStep(w, dev, W.draft_tensors(w), page_size=64)
     elif config == "accept_stochastic":
         w = None
         g = pipeline.StochasticAccept(128, 5, 154880, dev)
@@ -583,7 +590,10 @@ def run_ours(a, world, rank, local):
     torch.cuda.empty_cache()
     subs = {}
     if not a.no_sub and a.config == DEFAULT:
-        for name in SUBS:
+        names = [n for n in a.subs.split(",") if n] or list(SUBS)
+        for name in names:
+            if name not in SUBS:
+                raise SystemExit(f"unknown sub-workload {name}")
             r = measure(name, a, world, local, e2e=False, clocks_on=True)
             r["roofline_headline"] = headline_roofline(r, pk)
             for k in ("_g", "_w", "_model", "_flush"):

@@ -343,6 +343,77 @@ int mtpsd_kv_writeback(const void* src_latent, const uint8_t* src_idxk, const fl
                        int64_t pool_tokens, int64_t* next_pos, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Paged (slotted) KV caches.  [P2] "输入准备:prepare_for_draft": the caches
+ * are pools of token slots and each request reaches its positions through a
+ * token table (req_to_token; page_size > 1 groups consecutive slots into
+ * pages).  Here a request's table is one row of a block table:
+ *   block_table [B, bt_stride] int32 (device): page ids, -1 = no page;
+ *   position s of request b lives in pool slot
+ *     block_table[b, s / page_size] * page_size + s % page_size,
+ *   and has no slot when s < 0, s / page_size >= bt_stride or the entry is
+ *   negative.  page_size 1 is the token table itself.
+ * The slots of different requests are disjoint (a slot belongs to one request).
+ */
+typedef struct {
+  const int32_t* block_table;  /* [B, bt_stride] page ids (device) */
+  int32_t bt_stride;           /* entries per request (>= 1) */
+  int32_t page_size;           /* tokens per page: a power of two, 1 .. 65536 */
+} mtpsd_paged_kv;
+
+/* The window's slot plan (assign_draft_cache_locs in [P2] "输入准备:prepare_for_draft"):
+ *   out_cache_loc[b, j] = slot of position start_pos[b] + j, j < W (int64 [B, W]), or -1
+ *   when that position has no slot (flagged MTPSD_STATUS_ROW_RANGE).
+ * start_pos [B] int64 (the committed length: the window follows it). */
+int mtpsd_assign_cache_locs(const mtpsd_paged_kv* paged, int32_t B, const int64_t* start_pos, int32_t W,
+                            int64_t* out_cache_loc, int32_t* dev_status, void* stream);
+
+/* The accepted-KV move (move_kv_cache over fill_front_out_cache_loc /
+ * fill_accept_out_cache_loc, [P2] "KV 交账:接受段的搬移与拒绝段的回收"):
+ * for i < accept_len = num_accepted[b] + 1 (the bonus row included; clamped
+ * to [0, W]), row i of request b moves from window slot
+ * out_cache_loc[b, accept_index[b, i]] to the front slot out_cache_loc[b, i],
+ * in every cache of the layer at once.  It is a move: each destination
+ * receives what its source held before the call, whatever the overlap of the
+ * two slot lists of a request (rows whose source is their destination are
+ * left alone; a chain of drafts, accept_index[b, i] = i, moves nothing).
+ *   latent [pool_tokens, 576] (latent_dtype MTPSD_BF16 / MTPSD_F32) or [pool_tokens, 656]
+ *   bytes (MTPSD_FP8_DS_MLA); idxk [pool_tokens, idx_dim] uint8 (idx_dim a multiple of 16,
+ *   0 = none, idxk may then be NULL); idxs [pool_tokens] float32 or NULL.
+ *   out_cache_loc [B, W] int64, accept_index [B, W] int32 (window columns), num_accepted [B] int32.
+ * A window column outside [0, W) is skipped and flagged MTPSD_STATUS_INDEX_RANGE; a slot
+ * outside the pool is skipped and flagged MTPSD_STATUS_WRITE_RANGE.  W <= 16. */
+int mtpsd_kv_move_accepted(void* latent, int32_t latent_dtype, uint8_t* idxk, int32_t idx_dim, float* idxs,
+                           int64_t pool_tokens, const int64_t* out_cache_loc, const int32_t* accept_index,
+                           const int32_t* num_accepted, int32_t B, int32_t W, int32_t* dev_status, void* stream);
+
+/* mtpsd_kv_writeback by slot: the accepted rows (num_accepted[b] + 1, at
+ * least 1, at most W) of request b's window go to pool slots
+ * dst_slots[b, 0 ..] (int64 [B, W], the window slots planned by
+ * mtpsd_assign_cache_locs: the token table is shared by the layers, each
+ * layer has its own pools); rejected rows are not written.  dst_pos [B]
+ * int64 and next_pos [B] int64 (both or neither, nullable): next_pos[b] =
+ * dst_pos[b] + the rows written, the position of the next draft row when
+ * dst_pos is the window's first position.  Other arguments as
+ * mtpsd_kv_writeback; a slot outside the pool is skipped and flagged
+ * MTPSD_STATUS_WRITE_RANGE. */
+int mtpsd_kv_writeback_slots(const void* src_latent, const uint8_t* src_idxk, const float* src_idxs,
+                             int32_t B, int32_t W, int32_t latent_dtype, int32_t idx_dim,
+                             const int32_t* num_accepted, void* dst_latent, uint8_t* dst_idxk,
+                             float* dst_idxs, const int64_t* dst_slots, int64_t pool_tokens,
+                             const int64_t* dst_pos, int64_t* next_pos, int32_t* dev_status, void* stream);
+
+/* mtpsd_indexer_topk, mtpsd_indexer_scores and mtpsd_sparse_mla_decode over
+ * paged caches: position s of request b is read from the slot the block
+ * table gives (args->cache_start is ignored and may be NULL); a visible
+ * position without a slot reads as zero keys (score 0 x its scale: 0) in the
+ * indexer and is skipped in the attention, both flagged
+ * MTPSD_STATUS_ROW_RANGE.  Everything else is as the contiguous calls,
+ * including workspaces and launch counts.  paged NULL = the contiguous call. */
+int mtpsd_indexer_topk_paged(const mtpsd_indexer_args* args, const mtpsd_paged_kv* paged, void* stream);
+int mtpsd_indexer_scores_paged(const mtpsd_indexer_args* args, const mtpsd_paged_kv* paged, void* stream);
+int mtpsd_sparse_mla_decode_paged(const mtpsd_mla_args* args, const mtpsd_paged_kv* paged, void* stream);
+
+/* ------------------------------------------------------------------------
  * index_share_for_mtp_iteration gather.  [P1] "阶段 5:Draft 后续步骤(复用
  * top-k)" (gather_accepted_hidden_states over step0_topk at num_accepted);
  * [P2] "索引器复用的收益与边界" (compact_topk_indices: one row per request).

@@ -54,6 +54,10 @@ class MlaArgs(C.Structure):
     ]
 
 
+class PagedKV(C.Structure):
+    _fields_ = [("block_table", vp), ("bt_stride", i32), ("page_size", i32)]
+
+
 # name -> (restype, argtypes); every symbol include/mtpsd.h declares
 SIGNATURES = {
     "mtpsd_merge_tokens": (C.c_int, [vp, i64, vp, vp, i32, i32, vp, vp, vp]),
@@ -79,6 +83,12 @@ SIGNATURES = {
     "mtpsd_accept_greedy": (C.c_int, [vp, vp, i32, i32, i64, vp, vp, vp]),
     "mtpsd_accept_stochastic": (C.c_int, [vp, vp, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp]),
     "mtpsd_kv_writeback": (C.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp]),
+    "mtpsd_assign_cache_locs": (C.c_int, [C.POINTER(PagedKV), i32, vp, i32, vp, vp, vp]),
+    "mtpsd_kv_move_accepted": (C.c_int, [vp, i32, vp, i32, vp, i64, vp, vp, vp, i32, i32, vp, vp]),
+    "mtpsd_kv_writeback_slots": (C.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp]),
+    "mtpsd_indexer_topk_paged": (C.c_int, [C.POINTER(IndexerArgs), C.POINTER(PagedKV), vp]),
+    "mtpsd_indexer_scores_paged": (C.c_int, [C.POINTER(IndexerArgs), C.POINTER(PagedKV), vp]),
+    "mtpsd_sparse_mla_decode_paged": (C.c_int, [C.POINTER(MlaArgs), C.POINTER(PagedKV), vp]),
     "mtpsd_topk_share_gather": (C.c_int, [vp, vp, vp, i32, i32, vp, vp, vp, vp, vp]),
     "mtpsd_check_bounded_wait": (C.c_int, [i64, vp, vp, vp]),
     "mtpsd_last_error": (C.c_char_p, []),

@@ -62,6 +62,19 @@ def _ws(workspace: Optional[torch.Tensor], nbytes: int, device) -> torch.Tensor:
     return _default_ws[key].get(nbytes)
 
 
+def _paged(paged):
+    """(block_table [B, n] int32 CUDA tensor, page_size) -> a PagedKV (None stays None)."""
+    if paged is None:
+        return None
+    bt, page_size = paged
+    _need(bt, "block_table", torch.int32, 2)
+    return N.PagedKV(block_table=bt.data_ptr(), bt_stride=bt.shape[1], page_size=int(page_size))
+
+
+def _byref(x):
+    return None if x is None else C.byref(x)
+
+
 # --------------------------------------------------------------------------- merge
 
 def merge_tokens(prompt_tokens, prompt_offsets, draft_tokens, merged_tokens=None, merged_offsets=None,
@@ -164,7 +177,8 @@ def _indexer_args(q, q_scale, weights, k_cache, k_scale, cache_start, row_offset
     _need(q, "q", torch.uint8 if fp8 else torch.float32, 3)
     _need(k_cache, "k_cache", q.dtype, 2)
     _need(weights, "weights", torch.float32, 2)
-    _need(cache_start, "cache_start", torch.int64, 1)
+    if cache_start is not None:
+        _need(cache_start, "cache_start", torch.int64, 1)
     _need(row_offsets, "row_offsets", torch.uint32, 1)
     _need(row_pos, "row_pos", torch.int64, 1)
     if fp8:
@@ -175,12 +189,13 @@ def _indexer_args(q, q_scale, weights, k_cache, k_scale, cache_start, row_offset
         if scores.shape[0] != q.shape[0] or scores.shape[1] != scores_ld(max_visible):
             raise ValueError("scores must be [R, scores_ld(max_visible)]")
     R, H, D = q.shape
-    return N.IndexerArgs(B=cache_start.numel(), R=R, n_heads=H, head_dim=D, topk=topk,
+    return N.IndexerArgs(B=row_offsets.numel() - 1, R=R, n_heads=H, head_dim=D, topk=topk,
                          dtype=N.MTPSD_FP8_E4M3 if fp8 else N.MTPSD_F32,
                          q=q.data_ptr(), q_scale=q_scale.data_ptr() if fp8 else None,
                          weights=weights.data_ptr(), k_cache=k_cache.data_ptr(),
                          k_scale=k_scale.data_ptr() if fp8 else None, pool_tokens=k_cache.shape[0],
-                         cache_start=cache_start.data_ptr(), row_offsets=row_offsets.data_ptr(),
+                         cache_start=None if cache_start is None else cache_start.data_ptr(),
+                         row_offsets=row_offsets.data_ptr(),
                          row_pos=row_pos.data_ptr(), max_visible=max_visible,
                          topk_idx=None if topk_idx is None else topk_idx.data_ptr(),
                          topk_score=None if topk_score is None else topk_score.data_ptr(),
@@ -191,9 +206,11 @@ def _indexer_args(q, q_scale, weights, k_cache, k_scale, cache_start, row_offset
 
 def indexer_topk(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets, row_pos, topk: int,
                  max_visible: int, topk_idx=None, topk_score=None, scores=None, workspace=None,
-                 dev_status=None, stream=None):
+                 dev_status=None, stream=None, paged=None):
+    """paged = (block_table [B, n] int32, page_size) reads the caches through the block table
+    (cache_start is then ignored and may be None)."""
     R = q.shape[0]
-    B = cache_start.numel()
+    B = row_offsets.numel() - 1
     if topk_idx is None:
         topk_idx = torch.empty(R, topk, dtype=torch.int32, device=q.device)
     nbytes = indexer_topk_aux_bytes(B, R, max_visible, topk) if scores is not None else \
@@ -201,21 +218,29 @@ def indexer_topk(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets
     ws = _ws(workspace, nbytes, q.device)
     a = _indexer_args(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets, row_pos, topk, max_visible,
                       topk_idx, topk_score, scores, ws, dev_status)
-    check("mtpsd_indexer_topk", lib().mtpsd_indexer_topk(C.byref(a), _stream(stream)))
+    if paged is None:
+        check("mtpsd_indexer_topk", lib().mtpsd_indexer_topk(C.byref(a), _stream(stream)))
+    else:
+        check("mtpsd_indexer_topk_paged", lib().mtpsd_indexer_topk_paged(C.byref(a), _byref(_paged(paged)),
+                                                                           _stream(stream)))
     return topk_idx
 
 
 def indexer_scores(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets, row_pos, max_visible: int,
-                   scores=None, workspace=None, dev_status=None, stream=None):
+                   scores=None, workspace=None, dev_status=None, stream=None, paged=None):
     """The score matrix [R, scores_ld(max_visible)] alone (row r valid up to row_pos[r])."""
     R = q.shape[0]
-    B = cache_start.numel()
+    B = row_offsets.numel() - 1
     if scores is None:
         scores = torch.empty(R, scores_ld(max_visible), dtype=torch.float32, device=q.device)
     ws = _ws(workspace, indexer_plan_bytes(B, R), q.device)
     a = _indexer_args(q, q_scale, weights, k_cache, k_scale, cache_start, row_offsets, row_pos, 1, max_visible,
                       None, None, scores, ws, dev_status)
-    check("mtpsd_indexer_scores", lib().mtpsd_indexer_scores(C.byref(a), _stream(stream)))
+    if paged is None:
+        check("mtpsd_indexer_scores", lib().mtpsd_indexer_scores(C.byref(a), _stream(stream)))
+    else:
+        check("mtpsd_indexer_scores_paged", lib().mtpsd_indexer_scores_paged(C.byref(a), _byref(_paged(paged)),
+                                                                             _stream(stream)))
     return scores
 
 
@@ -263,7 +288,9 @@ def sparse_mla_launch_count(R, H, n_idx, n_append, dtype) -> int:
 
 def sparse_mla_decode(q, latent, cache_start, row_offsets, row_pos, idx, softmax_scale: float,
                       n_append: int = 0, append_base=None, row_pos_add: int = 0, out=None, lse=None,
-                      workspace=None, dev_status=None, stream=None):
+                      workspace=None, dev_status=None, stream=None, paged=None):
+    """paged = (block_table [B, n] int32, page_size) gathers through the block table (cache_start is
+    then ignored and may be None)."""
     bf16 = q.dtype == torch.bfloat16
     _need(q, "q", torch.bfloat16 if bf16 else torch.float32, 3)
     fp8kv = latent.dtype == torch.uint8     # the packed FP8 latent cache (656-byte rows)
@@ -273,7 +300,8 @@ def sparse_mla_decode(q, latent, cache_start, row_offsets, row_pos, idx, softmax
             raise ValueError("an FP8 latent cache needs bf16 queries and 656-byte rows")
     else:
         _need(latent, "latent", q.dtype, 2)
-    _need(cache_start, "cache_start", torch.int64, 1)
+    if cache_start is not None:
+        _need(cache_start, "cache_start", torch.int64, 1)
     _need(row_offsets, "row_offsets", torch.uint32, 1)
     _need(row_pos, "row_pos", torch.int64, 1)
     _need(idx, "idx", torch.int32, 2)
@@ -285,17 +313,21 @@ def sparse_mla_decode(q, latent, cache_start, row_offsets, row_pos, idx, softmax
         out = torch.empty(R, H, 512, dtype=q.dtype, device=q.device)
     nbytes = sparse_mla_workspace_size(R, H, idx.shape[1], n_append, dt)
     ws = _ws(workspace, nbytes, q.device) if nbytes else workspace
-    a = N.MlaArgs(B=cache_start.numel(), R=R, n_heads=H, d_latent=DL, d_v=512, n_idx=idx.shape[1],
+    a = N.MlaArgs(B=row_offsets.numel() - 1, R=R, n_heads=H, d_latent=DL, d_v=512, n_idx=idx.shape[1],
                   n_append=n_append, dtype=dt, softmax_scale=softmax_scale, row_pos_add=row_pos_add,
                   q=q.data_ptr(), latent=latent.data_ptr(), pool_tokens=latent.shape[0],
-                  cache_start=cache_start.data_ptr(), row_offsets=row_offsets.data_ptr(),
-                  row_pos=row_pos.data_ptr(), idx=idx.data_ptr(),
+                  cache_start=None if cache_start is None else cache_start.data_ptr(),
+                  row_offsets=row_offsets.data_ptr(), row_pos=row_pos.data_ptr(), idx=idx.data_ptr(),
                   append_base=None if append_base is None else append_base.data_ptr(),
                   out=out.data_ptr(), lse=None if lse is None else lse.data_ptr(),
                   workspace=None if ws is None else ws.data_ptr(),
                   workspace_bytes=0 if ws is None else ws.numel(),
                   dev_status=None if dev_status is None else dev_status.data_ptr())
-    check("mtpsd_sparse_mla_decode", lib().mtpsd_sparse_mla_decode(C.byref(a), _stream(stream)))
+    if paged is None:
+        check("mtpsd_sparse_mla_decode", lib().mtpsd_sparse_mla_decode(C.byref(a), _stream(stream)))
+    else:
+        check("mtpsd_sparse_mla_decode_paged", lib().mtpsd_sparse_mla_decode_paged(
+            C.byref(a), _byref(_paged(paged)), _stream(stream)))
     return out
 
 
@@ -389,3 +421,67 @@ def topk_share_gather(step0_topk, row_offsets, num_accepted=None, shared_idx=Non
         _ptr(step0_topk), _ptr(row_offsets), _ptr(num_accepted), B, k, _ptr(shared_idx), _ptr(row_pos),
         _ptr(shared_pos if row_pos is not None else None), _ptr(dev_status), _stream(stream)))
     return shared_idx
+
+
+# --------------------------------------------------------------------------- paged caches
+
+def _latent_dtype(t):
+    if t.dtype == torch.uint8:
+        return N.MTPSD_FP8_DS_MLA
+    return N.MTPSD_BF16 if t.dtype == torch.bfloat16 else N.MTPSD_F32
+
+
+def assign_cache_locs(block_table, page_size: int, start_pos, W: int, out_cache_loc=None, dev_status=None,
+                      stream=None):
+    """out_cache_loc [B, W] int64: the slots of positions start_pos[b] + j (j < W), -1 where none."""
+    _need(start_pos, "start_pos", torch.int64, 1)
+    B = start_pos.numel()
+    if out_cache_loc is None:
+        out_cache_loc = torch.empty(B, W, dtype=torch.int64, device=start_pos.device)
+    pk = _paged((block_table, page_size))
+    check("mtpsd_assign_cache_locs", lib().mtpsd_assign_cache_locs(
+        C.byref(pk), B, _ptr(start_pos), W, _ptr(out_cache_loc), _ptr(dev_status), _stream(stream)))
+    return out_cache_loc
+
+
+def kv_move_accepted(latent, idxk, idxs, out_cache_loc, accept_index, num_accepted, dev_status=None, stream=None):
+    """Moves the accepted rows' KV (window slots out_cache_loc[b, accept_index[b, i]]) to the front slots
+    out_cache_loc[b, i], i < num_accepted[b] + 1, in every cache of the layer (in place)."""
+    _need(latent, "latent", latent.dtype, 2)
+    _need(out_cache_loc, "out_cache_loc", torch.int64, 2)
+    _need(accept_index, "accept_index", torch.int32, 2)
+    _need(num_accepted, "num_accepted", torch.int32, 1)
+    B, W = out_cache_loc.shape
+    idx_dim = 0
+    if idxk is not None:
+        _need(idxk, "idxk", torch.uint8, 2)
+        idx_dim = idxk.shape[1]
+    if idxs is not None:
+        _need(idxs, "idxs", torch.float32, 1)
+    check("mtpsd_kv_move_accepted", lib().mtpsd_kv_move_accepted(
+        _ptr(latent), _latent_dtype(latent), _ptr(idxk), idx_dim, _ptr(idxs), latent.shape[0],
+        _ptr(out_cache_loc), _ptr(accept_index), _ptr(num_accepted), B, W, _ptr(dev_status), _stream(stream)))
+
+
+def kv_writeback_slots(src_latent, src_idxk, src_idxs, num_accepted, dst_latent, dst_idxk, dst_idxs, dst_slots,
+                       dst_pos=None, next_pos=None, dev_status=None, stream=None):
+    """The accepted rows (num_accepted + 1, clamped to [1, W]) of each window to pool slots dst_slots [B, W];
+    with dst_pos, next_pos[b] = dst_pos[b] + the rows written."""
+    _need(src_latent, "src_latent", src_latent.dtype, 3)
+    _need(dst_latent, "dst_latent", src_latent.dtype, 2)
+    _need(num_accepted, "num_accepted", torch.int32, 1)
+    _need(dst_slots, "dst_slots", torch.int64, 2)
+    B, W, _ = src_latent.shape
+    idx_dim = 0
+    if src_idxk is not None:
+        _need(src_idxk, "src_idxk", torch.uint8, 3)
+        _need(dst_idxk, "dst_idxk", torch.uint8, 2)
+        idx_dim = src_idxk.shape[2]
+    if src_idxs is not None:
+        _need(src_idxs, "src_idxs", torch.float32)
+        _need(dst_idxs, "dst_idxs", torch.float32)
+    check("mtpsd_kv_writeback_slots", lib().mtpsd_kv_writeback_slots(
+        _ptr(src_latent), _ptr(src_idxk), _ptr(src_idxs), B, W, _latent_dtype(src_latent), idx_dim,
+        _ptr(num_accepted), _ptr(dst_latent), _ptr(dst_idxk), _ptr(dst_idxs), _ptr(dst_slots), dst_latent.shape[0],
+        _ptr(dst_pos), _ptr(next_pos), _ptr(dev_status), _stream(stream)))
+    return next_pos

@@ -29,6 +29,19 @@ static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Checks a paged-cache descriptor (NULL: contiguous caches) and converts it.
+static int check_paged(const mtpsd_paged_kv* pk, Paging* out, const char* who) {
+  *out = Paging();
+  if (!pk) return MTPSD_OK;
+  if (!pk->block_table || pk->bt_stride < 1) return fail(MTPSD_EINVAL, "%s: paged caches need block_table and bt_stride >= 1", who);
+  const int32_t ps = pk->page_size;
+  if (ps < 1 || ps > 65536 || (ps & (ps - 1))) return fail(MTPSD_EINVAL, "%s: page_size must be a power of two in 1..65536", who);
+  out->bt = pk->block_table;
+  out->stride = pk->bt_stride;
+  while ((1 << out->shift) < ps) ++out->shift;
+  return MTPSD_OK;
+}
+
 }  // namespace mtpsd
 
 using namespace mtpsd;
@@ -37,7 +50,7 @@ extern "C" {
 
 const char* mtpsd_last_error(void) { return g_err; }
 
-int32_t mtpsd_version(void) { return 101; }
+int32_t mtpsd_version(void) { return 102; }
 
 int mtpsd_merge_tokens(const int64_t* prompt_tokens, int64_t S, const uint32_t* prompt_offsets,
                        const int64_t* draft_tokens, int32_t B, int32_t K, int64_t* merged_tokens,
@@ -118,9 +131,12 @@ namespace mtpsd {
 // Checks the indexer arguments and launches the score kernels (plan + tensor-core GEMM, or the CUDA-core
 // kernel) into `*scores_out` (args->scores, else the head of the workspace).  need_scores: the call
 // requires a caller score buffer (mtpsd_indexer_scores).
-static int indexer_scores_checked(const mtpsd_indexer_args* a, bool need_scores, bool need_topk,
-                                  cudaStream_t st, float** scores_out, void** topk_ws, size_t* topk_ws_bytes) {
+static int indexer_scores_checked(const mtpsd_indexer_args* a, const mtpsd_paged_kv* paged, bool need_scores,
+                                  bool need_topk, cudaStream_t st, float** scores_out, void** topk_ws,
+                                  size_t* topk_ws_bytes) {
   if (!a) return fail(MTPSD_EINVAL, "indexer: null args");
+  Paging pg;
+  if (int rc = check_paged(paged, &pg, "indexer")) return rc;
   if (a->B < 1 || a->R < 0 || a->n_heads < 1)
     return fail(MTPSD_EINVAL, "indexer: need B >= 1, R >= 0, n_heads >= 1");
   if (a->max_visible < 0 || a->max_visible > 0x7fffffffLL)
@@ -137,7 +153,7 @@ static int indexer_scores_checked(const mtpsd_indexer_args* a, bool need_scores,
   if (need_topk && (a->topk < 1 || a->topk > 4096)) return fail(MTPSD_EINVAL, "indexer_topk: need 1 <= topk <= 4096");
   if (need_scores && !a->scores) return fail(MTPSD_EINVAL, "indexer_scores: args->scores is required");
   if (a->R == 0) return MTPSD_OK;
-  if (!a->q || !a->weights || !a->k_cache || !a->cache_start || !a->row_offsets || !a->row_pos ||
+  if (!a->q || !a->weights || !a->k_cache || (!pg.bt && !a->cache_start) || !a->row_offsets || !a->row_pos ||
       (need_topk && !a->topk_idx))
     return fail(MTPSD_EINVAL, "indexer: null pointer");
   // the workspace holds the scores (unless the caller gives a buffer), the work plan, and for the top-k
@@ -158,6 +174,7 @@ static int indexer_scores_checked(const mtpsd_indexer_args* a, bool need_scores,
   p.max_visible = a->max_visible; p.scores = scores; p.ld = ld;
   p.plan_ws = (char*)a->workspace + score_part;
   p.status = a->dev_status;
+  p.pg = pg;
   *scores_out = scores;
   *topk_ws = (char*)a->workspace + score_part + indexer_tc_plan_bytes(a->B, a->R);
   *topk_ws_bytes = topk_part;
@@ -167,25 +184,31 @@ static int indexer_scores_checked(const mtpsd_indexer_args* a, bool need_scores,
 
 extern "C" {
 
-int mtpsd_indexer_scores(const mtpsd_indexer_args* a, void* stream) {
+int mtpsd_indexer_scores_paged(const mtpsd_indexer_args* a, const mtpsd_paged_kv* paged, void* stream) {
   g_err[0] = 0;
   float* scores = nullptr;
   void* tws = nullptr;
   size_t twb = 0;
-  return indexer_scores_checked(a, true, false, (cudaStream_t)stream, &scores, &tws, &twb);
+  return indexer_scores_checked(a, paged, true, false, (cudaStream_t)stream, &scores, &tws, &twb);
+}
+
+int mtpsd_indexer_scores(const mtpsd_indexer_args* a, void* stream) {
+  return mtpsd_indexer_scores_paged(a, nullptr, stream);
 }
 
 int32_t mtpsd_indexer_scores_launch_count(int32_t n_heads, int32_t head_dim, int32_t dtype) {
   return indexer_launch_count(n_heads, head_dim, dtype) - 1;
 }
 
-int mtpsd_indexer_topk(const mtpsd_indexer_args* a, void* stream) {
+int mtpsd_indexer_topk(const mtpsd_indexer_args* a, void* stream) { return mtpsd_indexer_topk_paged(a, nullptr, stream); }
+
+int mtpsd_indexer_topk_paged(const mtpsd_indexer_args* a, const mtpsd_paged_kv* paged, void* stream) {
   g_err[0] = 0;
   cudaStream_t st = (cudaStream_t)stream;
   float* scores = nullptr;
   void* tws = nullptr;
   size_t twb = 0;
-  int rc = indexer_scores_checked(a, false, true, st, &scores, &tws, &twb);
+  int rc = indexer_scores_checked(a, paged, false, true, st, &scores, &tws, &twb);
   if (rc || a->R == 0) return rc;
   TopkPlan t;
   t.scores = scores; t.ld = mtpsd_scores_ld(a->max_visible); t.R = a->R; t.row_len = a->row_pos; t.len_add = 1;
@@ -240,9 +263,13 @@ int32_t mtpsd_sparse_mla_launch_count(int32_t R, int32_t n_heads, int32_t n_idx,
   return mla_launch_count(R, n_heads, n_idx, n_append, dtype);
 }
 
-int mtpsd_sparse_mla_decode(const mtpsd_mla_args* a, void* stream) {
+int mtpsd_sparse_mla_decode(const mtpsd_mla_args* a, void* stream) { return mtpsd_sparse_mla_decode_paged(a, nullptr, stream); }
+
+int mtpsd_sparse_mla_decode_paged(const mtpsd_mla_args* a, const mtpsd_paged_kv* paged, void* stream) {
   g_err[0] = 0;
   if (!a) return fail(MTPSD_EINVAL, "sparse_mla_decode: null args");
+  Paging pg;
+  if (int rc = check_paged(paged, &pg, "sparse_mla_decode")) return rc;
   if (a->B < 1 || a->R < 0 || a->n_heads < 1 || a->n_idx < 0 || a->n_append < 0)
     return fail(MTPSD_EINVAL, "sparse_mla_decode: need B >= 1, R >= 0, n_heads >= 1, n_idx >= 0, n_append >= 0");
   if (a->d_latent != 576 || a->d_v != 512)
@@ -255,7 +282,7 @@ int mtpsd_sparse_mla_decode(const mtpsd_mla_args* a, void* stream) {
   }
   if (a->n_append > 0 && !a->append_base) return fail(MTPSD_EINVAL, "sparse_mla_decode: n_append > 0 needs append_base");
   if (a->R == 0) return MTPSD_OK;
-  if (!a->q || !a->latent || !a->cache_start || !a->row_offsets || !a->row_pos || !a->out || (a->n_idx > 0 && !a->idx))
+  if (!a->q || !a->latent || (!pg.bt && !a->cache_start) || !a->row_offsets || !a->row_pos || !a->out || (a->n_idx > 0 && !a->idx))
     return fail(MTPSD_EINVAL, "sparse_mla_decode: null pointer");
   if (a->dtype != MTPSD_F32 && (!aligned(a->q, 16) || !aligned(a->latent, 16) || !aligned(a->out, 4)))
     return fail(MTPSD_EINVAL, "sparse_mla_decode: q and latent must be 16-byte aligned");
@@ -265,6 +292,7 @@ int mtpsd_sparse_mla_decode(const mtpsd_mla_args* a, void* stream) {
   p.q = a->q; p.latent = a->latent; p.pool = a->pool_tokens; p.cache_start = a->cache_start;
   p.row_offsets = a->row_offsets; p.row_pos = a->row_pos; p.idx = a->idx; p.append_base = a->append_base;
   p.out = a->out; p.lse = a->lse; p.ws = a->workspace; p.ws_bytes = a->workspace_bytes; p.status = a->dev_status;
+  p.pg = pg;
   return launch_sparse_mla(p, (cudaStream_t)stream);
 }
 
@@ -311,6 +339,63 @@ int mtpsd_kv_writeback(const void* src_latent, const uint8_t* src_idxk, const fl
     return fail(MTPSD_EINVAL, "kv_writeback: latent and key buffers must be 16-byte aligned");
   return launch_kv_writeback(src_latent, src_idxk, src_idxs, B, W, lat_bytes, idx_dim, num_accepted, dst_latent,
                              dst_idxk, dst_idxs, cache_start, dst_pos, pool_tokens, next_pos, dev_status, (cudaStream_t)stream);
+}
+
+int mtpsd_kv_writeback_slots(const void* src_latent, const uint8_t* src_idxk, const float* src_idxs, int32_t B, int32_t W,
+                             int32_t latent_dtype, int32_t idx_dim, const int32_t* num_accepted, void* dst_latent,
+                             uint8_t* dst_idxk, float* dst_idxs, const int64_t* dst_slots, int64_t pool_tokens,
+                             const int64_t* dst_pos, int64_t* next_pos, int32_t* dev_status, void* stream) {
+  g_err[0] = 0;
+  if (B < 0 || W < 1 || pool_tokens < 0 || B > 65535) return fail(MTPSD_EINVAL, "kv_writeback_slots: need 0 <= B <= 65535, W >= 1");
+  int lat_bytes;
+  if (latent_dtype == MTPSD_BF16) lat_bytes = 576 * 2;
+  else if (latent_dtype == MTPSD_F32) lat_bytes = 576 * 4;
+  else if (latent_dtype == MTPSD_FP8_DS_MLA) lat_bytes = 656;
+  else return fail(MTPSD_EUNSUPPORTED, "kv_writeback_slots: latent dtype must be MTPSD_BF16, MTPSD_F32 or MTPSD_FP8_DS_MLA");
+  if (idx_dim != 0 && idx_dim % 16) return fail(MTPSD_EUNSUPPORTED, "kv_writeback_slots: idx_dim must be a multiple of 16");
+  if (B == 0) return MTPSD_OK;
+  if (!src_latent || !dst_latent || !num_accepted || !dst_slots) return fail(MTPSD_EINVAL, "kv_writeback_slots: null pointer");
+  if ((dst_pos == nullptr) != (next_pos == nullptr)) return fail(MTPSD_EINVAL, "kv_writeback_slots: give dst_pos and next_pos together or neither");
+  if (idx_dim && (!src_idxk || !dst_idxk)) return fail(MTPSD_EINVAL, "kv_writeback_slots: null indexer key pointer");
+  if ((src_idxs == nullptr) != (dst_idxs == nullptr)) return fail(MTPSD_EINVAL, "kv_writeback_slots: give both key scale pointers or neither");
+  if (!aligned(src_latent, 16) || !aligned(dst_latent, 16) || (idx_dim && (!aligned(src_idxk, 16) || !aligned(dst_idxk, 16))))
+    return fail(MTPSD_EINVAL, "kv_writeback_slots: latent and key buffers must be 16-byte aligned");
+  return launch_kv_writeback(src_latent, src_idxk, src_idxs, B, W, lat_bytes, idx_dim, num_accepted, dst_latent,
+                             dst_idxk, dst_idxs, nullptr, dst_pos, pool_tokens, next_pos, dev_status, (cudaStream_t)stream,
+                             dst_slots);
+}
+
+int mtpsd_assign_cache_locs(const mtpsd_paged_kv* paged, int32_t B, const int64_t* start_pos, int32_t W,
+                            int64_t* out_cache_loc, int32_t* dev_status, void* stream) {
+  g_err[0] = 0;
+  if (!paged) return fail(MTPSD_EINVAL, "assign_cache_locs: paged descriptor required");
+  Paging pg;
+  if (int rc = check_paged(paged, &pg, "assign_cache_locs")) return rc;
+  if (B < 0 || W < 1) return fail(MTPSD_EINVAL, "assign_cache_locs: need B >= 0, W >= 1");
+  if ((int64_t)B * W > 0x7fffffffLL) return fail(MTPSD_EINVAL, "assign_cache_locs: B*W too large");
+  if (B == 0) return MTPSD_OK;
+  if (!start_pos || !out_cache_loc) return fail(MTPSD_EINVAL, "assign_cache_locs: null pointer");
+  return launch_assign_cache_locs(pg, B, start_pos, W, out_cache_loc, dev_status, (cudaStream_t)stream);
+}
+
+int mtpsd_kv_move_accepted(void* latent, int32_t latent_dtype, uint8_t* idxk, int32_t idx_dim, float* idxs,
+                           int64_t pool_tokens, const int64_t* out_cache_loc, const int32_t* accept_index,
+                           const int32_t* num_accepted, int32_t B, int32_t W, int32_t* dev_status, void* stream) {
+  g_err[0] = 0;
+  if (B < 0 || W < 1 || W > 16 || pool_tokens < 0) return fail(MTPSD_EINVAL, "kv_move_accepted: need B >= 0, 1 <= W <= 16");
+  int lat_bytes;
+  if (latent_dtype == MTPSD_BF16) lat_bytes = 576 * 2;
+  else if (latent_dtype == MTPSD_F32) lat_bytes = 576 * 4;
+  else if (latent_dtype == MTPSD_FP8_DS_MLA) lat_bytes = 656;
+  else return fail(MTPSD_EUNSUPPORTED, "kv_move_accepted: latent dtype must be MTPSD_BF16, MTPSD_F32 or MTPSD_FP8_DS_MLA");
+  if (idx_dim < 0 || idx_dim > 512 || idx_dim % 16) return fail(MTPSD_EUNSUPPORTED, "kv_move_accepted: idx_dim must be a multiple of 16 up to 512");
+  if (B == 0) return MTPSD_OK;
+  if (!latent || !out_cache_loc || !accept_index || !num_accepted || (idx_dim && !idxk))
+    return fail(MTPSD_EINVAL, "kv_move_accepted: null pointer");
+  if (!aligned(latent, 16) || (idx_dim && !aligned(idxk, 16)))
+    return fail(MTPSD_EINVAL, "kv_move_accepted: latent and key buffers must be 16-byte aligned");
+  return launch_kv_move(latent, lat_bytes, idxk, idx_dim, idxs, pool_tokens, out_cache_loc, accept_index, num_accepted, B, W,
+                        dev_status, (cudaStream_t)stream);
 }
 
 int mtpsd_topk_share_gather(const int32_t* step0_topk, const uint32_t* row_offsets, const int32_t* num_accepted,

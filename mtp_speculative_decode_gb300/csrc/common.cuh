@@ -57,6 +57,17 @@ __device__ __forceinline__ int request_of_row_warp(const uint32_t* row_offsets, 
   return lo;
 }
 
+// Pool slot of position s of request b in a paged cache (block table bt [B, stride], pages of
+// 2^shift tokens), or -1 when s is negative, lies past the table's width or its page entry is negative.
+__device__ __forceinline__ int64_t paged_slot(const int32_t* bt, int32_t stride, int32_t shift, int b, int64_t s) {
+  if (s < 0) return -1;
+  const int64_t pg = s >> shift;
+  if (pg >= stride) return -1;
+  const int32_t e = __ldg(bt + (int64_t)b * stride + pg);
+  if (e < 0) return -1;
+  return ((int64_t)e << shift) | (s & ((1LL << shift) - 1));
+}
+
 MTPSD_HD int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Programmatic dependent launch.  Every kernel of the library is launched with launch_k(), which lets

@@ -7,6 +7,14 @@
 
 namespace mtpsd {
 
+// Block-table indirection of a paged cache (bt == nullptr: contiguous, pool row cache_start[b] + s).
+// Position s of request b lives in slot bt[b * stride + (s >> shift)] << shift | (s & (2^shift - 1)).
+struct Paging {
+  const int32_t* bt = nullptr;
+  int32_t stride = 0;
+  int32_t shift = 0;
+};
+
 // 2D tensor map with the 128-byte swizzle (map: a 64-byte aligned CUtensorMap).
 // dtype_u8_or_bf16: 0 = uint8 elements, 1 = bf16 elements.
 bool tma_available();
@@ -25,7 +33,12 @@ int launch_accept_greedy(const int64_t* draft, const int64_t* tgt, int B, int K,
 int launch_kv_writeback(const void* src_l, const uint8_t* src_k, const float* src_s, int B, int W,
                         int lat_bytes, int idx_bytes, const int32_t* n_acc, void* dst_l, uint8_t* dst_k,
                         float* dst_s, const int64_t* cache_start, const int64_t* dst_pos, int64_t pool, int64_t* next_pos,
-                        int32_t* status, cudaStream_t st);
+                        int32_t* status, cudaStream_t st, const int64_t* dst_slots = nullptr);
+int launch_assign_cache_locs(const Paging& pg, int B, const int64_t* start_pos, int W, int64_t* out, int32_t* status,
+                             cudaStream_t st);
+int launch_kv_move(void* lat, int lat_bytes, uint8_t* idxk, int idx_bytes, float* idxs, int64_t pool,
+                   const int64_t* loc, const int32_t* acc_idx, const int32_t* n_acc, int B, int W, int32_t* status,
+                   cudaStream_t st);
 int launch_accept_stochastic(const int64_t* draft, const float* q, const float* p, const float* ua, const float* us,
                              int B, int K, int64_t V, int32_t* n_acc, int64_t* next, int32_t* status, cudaStream_t st);
 int launch_bounded_wait_check(int64_t limit_ns, int32_t* status, int64_t* out, cudaStream_t st);
@@ -41,6 +54,7 @@ struct IndexerPlan {
   int64_t max_visible; float* scores; int64_t ld;
   void* plan_ws;           // workspace for the tensor-core kernel's work plan (indexer_tc_plan_bytes)
   int32_t* status;
+  Paging pg;
 };
 int launch_indexer_scores(const IndexerPlan& p, cudaStream_t st);
 size_t indexer_tc_plan_bytes(int B, int R);
@@ -68,6 +82,7 @@ struct MlaPlan {
   void* out; float* lse;
   void* ws; size_t ws_bytes;
   int32_t* status;
+  Paging pg;
 };
 size_t mla_workspace_bytes(int R, int H, int n_idx, int n_append, int dtype);
 bool mla_tc_supported(const MlaPlan& p);

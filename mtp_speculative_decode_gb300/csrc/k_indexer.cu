@@ -35,15 +35,26 @@ __global__ void __launch_bounds__(256) indexer_scores_kernel(IndexerPlan p) {
   vmax = min(vmax, p.max_visible);
   const int64_t s0 = (int64_t)tile * IDX_TILE;
   if (s0 >= vmax) return;
-  const int64_t base = p.cache_start[b];
+  // pool row of each position of the tile (-1: not visible, or no row)
+  __shared__ int64_t rows_s[IDX_TILE];
+  if (threadIdx.x < IDX_TILE) {
+    const int64_t s = s0 + threadIdx.x;
+    int64_t row = -1;
+    if (s < vmax) {
+      row = p.pg.bt ? paged_slot(p.pg.bt, p.pg.stride, p.pg.shift, b, s) : p.cache_start[b] + s;
+      if (row >= p.pool) row = -1;
+      if (row < 0 && p.pg.bt) flag_status(p.status, MTPSD_STATUS_ROW_RANGE);
+    }
+    rows_s[threadIdx.x] = row;
+  }
+  __syncthreads();
 
   // key tile -> shared (dequantized to float)
   for (int e = threadIdx.x; e < IDX_TILE * D; e += blockDim.x) {
     int i = e / D, d = e % D;
-    int64_t s = s0 + i;
-    int64_t row = base + s;
+    int64_t row = rows_s[i];
     float v = 0.f;
-    if (s < vmax && row >= 0 && row < p.pool) {
+    if (row >= 0) {
       if (FP8) {
         __nv_fp8_e4m3 c;
         c.__x = ((const uint8_t*)p.k)[row * D + d];

@@ -43,6 +43,8 @@
 // MTPSD_STATUS_WAIT_TIMEOUT, drains its own copies in flight, frees TMEM and
 // returns.
 #include <cuda.h>
+
+#include <algorithm>
 #include <stdlib.h>
 #include <string.h>
 
@@ -103,6 +105,10 @@ struct Params {
   const int* g_tile0;      // [n_groups + 1]
   const int* n_groups;
   int32_t* status;
+  const float* k_scale;    // key scales (PAGED kernels copy them box by box)
+  const int32_t* bt;       // block table of a paged cache (PAGED kernels only)
+  int32_t bt_stride;
+  int32_t pg_shift;        // log2(page size), >= 3
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -124,6 +130,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   return mbar::wait<false>(bar, parity, abort_flag, status, WAIT_LIMIT_NS);
 }
 
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"((uint64_t)src), "r"(bytes), "r"(saddr(bar))
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
@@ -289,7 +300,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const uint32_t* __restrict__
   }
 }
 
-template <int H>
+// PAGED: the cache is paged (pages of 2^pg_shift >= 8 tokens).  A key tile of 128 positions is then
+// loaded as 128 / SUB boxes of SUB = min(page, 128) rows, each from the slot its page entry gives (1024-byte
+// aligned destinations keep the 128-byte swizzle), and the key scales of each box as one bulk copy; lane k of
+// the producer handles box k.  A box without a page (or outside the pool) loads zeros: its keys through an
+// out-of-range TMA row, its scales written as zeros by the lane itself.
+template <int H, bool PAGED>
 __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                 const __grid_constant__ CUtensorMap tmap_q,
                                                                 const __grid_constant__ CUtensorMap tmap_ks,
@@ -363,17 +379,34 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
 
   if (warp == PRODUCER_WARP) {
     int n_load = 0, gq = 0, cur_g = -1;
-    int64_t cstart = 0;
+    int64_t cstart = 0, cur_vmax = 0;
     bool ok = true;
     Cursor c;
     c.start(p, n_groups, it0);
+    // PAGED: this lane's box of a (group, tile): its page entry, loaded one tile ahead of its use
+    const int sub = PAGED ? min(TILE_M, 1 << p.pg_shift) : TILE_M;
+    const int n_sub = TILE_M / sub;
+    auto page_of = [&](int g, int tile) -> int32_t {
+      if (lane >= n_sub) return -1;
+      const int64_t pg = ((int64_t)tile * TILE_M + lane * sub) >> p.pg_shift;
+      if (pg >= p.bt_stride) return -1;
+      return __ldg(p.bt + (int64_t)p.g_b[g] * p.bt_stride + pg);
+    };
+    int32_t pe_cur = PAGED ? page_of(c.g, c.tile) : 0;
     for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups)) {
       const int g = c.g;
+      int32_t pe_next = -1;
+      if (PAGED && it + 1 < it1) {
+        Cursor cn = c;
+        cn.next(p, n_groups);
+        pe_next = page_of(cn.g, cn.tile);
+      }
       if (g != cur_g) {
         if (gq > 0) ok = __all_sync(0xffffffffu, mbar_wait(q_empty, (gq - 1) & 1, abort_flag, p.status));
         if (!ok) break;
         const int nrows = p.g_nrows[g], row0 = p.g_row0[g];
-        cstart = p.cache_start[p.g_b[g]];
+        if (PAGED) cur_vmax = p.g_vmax[g];
+        else cstart = p.cache_start[p.g_b[g]];
         if (elect_one()) {
           mbar_expect_tx(q_full, (uint32_t)(nrows * H * KB));
           for (int i = 0; i < nrows; ++i)
@@ -389,14 +422,39 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
       if (ok && kround > 0)
         ok = __all_sync(0xffffffffu, mbar_wait(&ks_empty[kslot], (kround - 1) & 1, abort_flag, p.status));
       if (!ok) break;
-      const int64_t y = cstart + (int64_t)c.tile * TILE_M;
-      if (elect_one()) {
-        mbar_expect_tx(&k_full[stage], TILE_M * KB);
-        tma_load_2d(saddr(sm + OFF_K + stage * TILE_M * KB), &tmap_k, 0, (int)y, &k_full[stage]);
-        // key scales of the tile from a 4-aligned start (16-byte aligned copy); elements past the pool
-        // read as zero
-        mbar_expect_tx(&ks_full[kslot], KS_BOX * 4);
-        tma_load_2d(saddr(sm + OFF_KS + kslot * KS_STRIDE), &tmap_ks, (int)(y & ~(int64_t)3), 0, &ks_full[kslot]);
+      if (PAGED) {
+        const int64_t s = (int64_t)c.tile * TILE_M + lane * sub;
+        int64_t slot = (lane < n_sub && pe_cur >= 0)
+                           ? (((int64_t)pe_cur << p.pg_shift) | (s & ((1LL << p.pg_shift) - 1))) : -1;
+        if (slot + sub > p.pool) slot = -1;
+        if (lane < n_sub && slot < 0 && s < cur_vmax) flag_status(p.status, MTPSD_STATUS_ROW_RANGE);
+        float* ks_dst = (float*)(sm + OFF_KS + kslot * KS_STRIDE) + lane * sub;
+        if (lane < n_sub && slot < 0)
+          for (int i = 0; i < sub; ++i) ks_dst[i] = 0.f;   // generic-proxy zeros, ordered by the arrive below
+        const uint32_t ks_bytes = (uint32_t)sub * 4u *
+                                  (uint32_t)__popc(__ballot_sync(0xffffffffu, lane < n_sub && slot >= 0));
+        __syncwarp();
+        if (elect_one()) {
+          mbar_expect_tx(&k_full[stage], TILE_M * KB);
+          mbar_expect_tx(&ks_full[kslot], ks_bytes);
+        }
+        __syncwarp();
+        if (lane < n_sub) {
+          tma_load_2d(saddr(sm + OFF_K + stage * TILE_M * KB + lane * sub * KB), &tmap_k, 0,
+                      slot >= 0 ? (int)slot : (int)p.pool, &k_full[stage]);
+          if (slot >= 0) bulk_load(saddr(ks_dst), p.k_scale + slot, (uint32_t)sub * 4u, &ks_full[kslot]);
+        }
+        pe_cur = pe_next;
+      } else {
+        const int64_t y = cstart + (int64_t)c.tile * TILE_M;
+        if (elect_one()) {
+          mbar_expect_tx(&k_full[stage], TILE_M * KB);
+          tma_load_2d(saddr(sm + OFF_K + stage * TILE_M * KB), &tmap_k, 0, (int)y, &k_full[stage]);
+          // key scales of the tile from a 4-aligned start (16-byte aligned copy); elements past the pool
+          // read as zero
+          mbar_expect_tx(&ks_full[kslot], KS_BOX * 4);
+          tma_load_2d(saddr(sm + OFF_KS + kslot * KS_STRIDE), &tmap_ks, (int)(y & ~(int64_t)3), 0, &ks_full[kslot]);
+        }
       }
       __syncwarp();
       ++n_load;
@@ -492,8 +550,8 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
         nrows = p.g_nrows[g];
         row0 = p.g_row0[g];
         vmax = p.g_vmax[g];
-        cstart = p.cache_start[p.g_b[g]];
-        ks_off = (int)(cstart & 3);
+        cstart = PAGED ? 0 : p.cache_start[p.g_b[g]];
+        ks_off = (int)(cstart & 3);   // paged: the scale slot holds the tile's 128 scales from its start
         units = (nrows * H + SLOT_COLS - 1) / SLOT_COLS;
         {   // all of the group's (row, head) weights in flight at once
           float wv[Q_ROWS / 32], qv[Q_ROWS / 32];
@@ -615,6 +673,9 @@ bool indexer_tc_supported(const IndexerPlan& p) {
   if (p.pool < 1 || p.pool > 0x7fffffffLL || (int64_t)p.R * p.H > 0x7fffffffLL) return false;
   if (p.max_visible > 0x7fffffffLL - itc::TILE_M) return false;
   if (!p.plan_ws) return false;
+  // paged caches: pages of at least 8 tokens (1024-byte aligned swizzled key boxes, 32-byte scale copies)
+  // that tile the pool
+  if (p.pg.bt && (p.pg.shift < 3 || (p.pool & ((1LL << p.pg.shift) - 1)) != 0)) return false;
   return tc_device_ok() && tma_available();
 }
 
@@ -628,7 +689,9 @@ int indexer_launch_count(int H, int D, int dtype) {
 int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {
   using namespace itc;
   CUtensorMap mk, mq, mks;
-  if (!make_map_rows128(&mk, p.k, p.pool, TILE_M) || !make_map_rows128(&mq, p.q, (int64_t)p.R * p.H, (uint32_t)p.H) ||
+  const bool paged = p.pg.bt != nullptr;
+  const uint32_t key_box = paged ? (uint32_t)std::min<int64_t>(TILE_M, 1LL << p.pg.shift) : (uint32_t)TILE_M;
+  if (!make_map_rows128(&mk, p.k, p.pool, key_box) || !make_map_rows128(&mq, p.q, (int64_t)p.R * p.H, (uint32_t)p.H) ||
       !make_tma_1d_f32(&mks, p.k_scale, (uint64_t)p.pool, KS_BOX)) {
     set_error("indexer: cuTensorMapEncodeTiled failed");
     return MTPSD_ECUDA;
@@ -652,16 +715,15 @@ int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {
   kp.row_pos = p.row_pos; kp.pool = p.pool; kp.max_visible = p.max_visible; kp.scores = p.scores; kp.ld = p.ld;
   kp.H = p.H; kp.g_b = g_b; kp.g_row0 = g_row0; kp.g_nrows = g_nrows; kp.g_vmax = g_vmax; kp.g_tile0 = g_tile0;
   kp.n_groups = n_groups; kp.status = p.status;
-  static std::atomic<uint64_t> attr64{0}, attr32{0};
-  if (!(p.H == 64 ? set_smem_limit_once(indexer_tc_kernel<64>, SMEM_BYTES, attr64)
-                  : set_smem_limit_once(indexer_tc_kernel<32>, SMEM_BYTES, attr32))) {
+  kp.k_scale = p.k_scale; kp.bt = p.pg.bt; kp.bt_stride = p.pg.stride; kp.pg_shift = p.pg.shift;
+  static std::atomic<uint64_t> attr[4];
+  auto kern = p.H == 64 ? (paged ? indexer_tc_kernel<64, true> : indexer_tc_kernel<64, false>)
+                        : (paged ? indexer_tc_kernel<32, true> : indexer_tc_kernel<32, false>);
+  if (!set_smem_limit_once(kern, SMEM_BYTES, attr[(p.H == 64 ? 0 : 2) + (paged ? 1 : 0)])) {
     set_error("indexer_tc: cudaFuncSetAttribute failed");
     return MTPSD_ECUDA;
   }
-  if (p.H == 64)
-    launch_k(indexer_tc_kernel<64>, num_sms(), THREADS, SMEM_BYTES, st, mk, mq, mks, kp);
-  else
-    launch_k(indexer_tc_kernel<32>, num_sms(), THREADS, SMEM_BYTES, st, mk, mq, mks, kp);
+  launch_k(kern, num_sms(), THREADS, SMEM_BYTES, st, mk, mq, mks, kp);
   return check_launch("indexer_tc");
 }
 

@@ -47,7 +47,7 @@ __device__ __forceinline__ int64_t mla_pool_row(const MlaPlan& p, int r, int b, 
     flag_status(p.status, MTPSD_STATUS_INDEX_RANGE);
     return -1;
   }
-  int64_t row = p.cache_start[b] + s;
+  int64_t row = p.pg.bt ? paged_slot(p.pg.bt, p.pg.stride, p.pg.shift, b, s) : p.cache_start[b] + s;
   if (row < 0 || row >= p.pool) {
     flag_status(p.status, MTPSD_STATUS_ROW_RANGE);
     return -1;

@@ -118,6 +118,9 @@ struct Params {
   const __nv_bfloat16* latent;
   int64_t pool;
   const int64_t* cache_start;
+  const int32_t* bt;          // block table of a paged cache, or null (contiguous)
+  int32_t bt_stride;
+  int32_t pg_shift;           // log2(page size)
   const uint32_t* row_offsets;
   const int64_t* row_pos;
   const int32_t* idx;
@@ -295,14 +298,28 @@ __device__ __forceinline__ float2 f16x2_to_f32(uint32_t u) {
   return __half22float2(h);
 }
 
-// Pool row of an entry, or -1 (padding, past the split, or out of range: flagged).
-__device__ __forceinline__ int64_t entry_row(const Params& p, int64_t s, int64_t base, int64_t limit) {
+// Position of an entry, or -1 (padding, past the split, or out of range: flagged).
+__device__ __forceinline__ int64_t entry_pos(const Params& p, int64_t s, int64_t limit) {
   if (s == -1 || s == -2) return -1;
   if (s < 0 || s > limit) {
     flag_status(p.status, MTPSD_STATUS_INDEX_RANGE);
     return -1;
   }
-  const int64_t row = base + s;
+  return s;
+}
+// Block-table entry of position s of request b (paged caches), or -1 when s has no page: the load is
+// issued a tile before its value is used (entry_row), so its latency hides behind that tile.
+__device__ __forceinline__ int32_t page_entry(const Params& p, int b, int64_t s) {
+  if (!p.bt || s < 0 || (s >> p.pg_shift) >= p.bt_stride) return -1;
+  return __ldg(p.bt + (int64_t)b * p.bt_stride + (s >> p.pg_shift));
+}
+// Pool row of position s (-1: padding / flagged), from the request's first row (contiguous) or its
+// page entry (paged); a row outside the pool, or a position without a page, is flagged.
+template <bool PAGED>
+__device__ __forceinline__ int64_t entry_row(const Params& p, int64_t s, int64_t base, int32_t page) {
+  if (s < 0) return -1;
+  const int64_t row = PAGED ? (page < 0 ? -1 : (((int64_t)page << p.pg_shift) | (s & ((1LL << p.pg_shift) - 1))))
+                            : base + s;
   if (row < 0 || row >= p.pool) {
     flag_status(p.status, MTPSD_STATUS_ROW_RANGE);
     return -1;
@@ -363,6 +380,8 @@ __device__ __noinline__ void merge_splits(const Params& p, int r, int h0, int hl
   }
 }
 
+// PAGED: positions resolve to pool rows through the block table (the producers look a tile ahead).
+template <bool PAGED>
 __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                                                                    const __grid_constant__ CUtensorMap tm_q,
                                                                    const __grid_constant__ CUtensorMap tm_st, Params p) {
@@ -757,18 +776,43 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     for (int i = 0; i < PF; ++i) rq[i] = i < n_tiles ? raw(j0 + (int64_t)i * NT + my_pos) : 0;
     const int64_t limit = p.row_pos[r] + p.row_pos_add;
     const int64_t abase = p.n_append > 0 ? p.append_base[r] + 1 : 0;   // first appended position
-    const int64_t base = p.cache_start[request_of_row_warp(p.row_offsets, p.B, (uint32_t)r)];
+    const int breq = request_of_row_warp(p.row_offsets, p.B, (uint32_t)r);
+    const int64_t base = PAGED ? 0 : p.cache_start[breq];
+    // checked position of this lane's entry in tile t, from its raw selected entry
+    auto tile_pos = [&](int t, int32_t rv) -> int64_t {
+      const int64_t j = j0 + (int64_t)t * NT + my_pos;
+      return entry_pos(p, j >= j1 ? -2 : (j < p.n_idx ? (int64_t)rv : abase + (j - p.n_idx)), limit);
+    };
+    // PAGED: tile t's position and page entry are taken one iteration ahead (the page load in flight)
+    int64_t s_next = 0;
+    int32_t pg_next = -1;
+    if (PAGED) {
+      s_next = n_tiles > 0 ? tile_pos(0, rq[0]) : -1;
+      pg_next = page_entry(p, breq, s_next);
+    }
     int issued = 0;
     for (int t = 0; t < n_tiles; ++t) {
-      const int32_t craw = rq[0];
+      int64_t s_cur;
+      int32_t pg_cur = -1;
+      if (PAGED) {
 #pragma unroll
-      for (int i = 0; i + 1 < PF; ++i) rq[i] = rq[i + 1];
-      rq[PF - 1] = t + PF < n_tiles ? raw(j0 + (int64_t)(t + PF) * NT + my_pos) : 0;
+        for (int i = 0; i + 1 < PF; ++i) rq[i] = rq[i + 1];
+        rq[PF - 1] = t + PF < n_tiles ? raw(j0 + (int64_t)(t + PF) * NT + my_pos) : 0;
+        s_cur = s_next;
+        pg_cur = pg_next;
+        s_next = t + 1 < n_tiles ? tile_pos(t + 1, rq[0]) : -1;
+        pg_next = page_entry(p, breq, s_next);
+      } else {
+        const int32_t craw = rq[0];
+#pragma unroll
+        for (int i = 0; i + 1 < PF; ++i) rq[i] = rq[i + 1];
+        rq[PF - 1] = t + PF < n_tiles ? raw(j0 + (int64_t)(t + PF) * NT + my_pos) : 0;
+        s_cur = craw;   // resolved after the wait below, as its position
+      }
       const int st = t % NSTAGE, P = t >> 1, q = P % NPAIR, R = P / NPAIR;
       if (R > 0 && !__all_sync(0xffffffffu, mbar_wait(&c_empty[q], (R - 1) & 1, abort_flag, p.status))) break;
-      const int64_t j = j0 + (int64_t)t * NT + my_pos;
-      const int64_t e = j >= j1 ? -2 : (j < p.n_idx ? (int64_t)craw : abase + (j - p.n_idx));
-      const int64_t row = entry_row(p, e, base, limit);
+      if (!PAGED) s_cur = tile_pos(t, (int32_t)s_cur);
+      const int64_t row = entry_row<PAGED>(p, s_cur, base, pg_cur);
       const bool valid = row >= 0 && lane < 8;
       const uint32_t bits = __reduce_or_sync(0xffffffffu, valid ? (1u << my_pos) : 0u);
       if (lane == 0) mask_s[st * 4 + pw] = bits;
@@ -917,7 +961,9 @@ cudaLaunchConfig_t mla_tc_config(dim3 grid, int cluster_z, cudaStream_t st, cuda
 }
 bool mla_tc_prepare() {
   static std::atomic<uint64_t> attr{0};
-  return set_smem_limit_once(mtc::sparse_mla_tc_kernel, mtc::SMEM_BYTES, attr);
+  static std::atomic<uint64_t> attr_paged{0};
+  return set_smem_limit_once(mtc::sparse_mla_tc_kernel<false>, mtc::SMEM_BYTES, attr) &&
+         set_smem_limit_once(mtc::sparse_mla_tc_kernel<true>, mtc::SMEM_BYTES, attr_paged);
 }
 // CTAs of this kernel that run at once with clusters of 2 x cluster_z CTAs (cached per device; -1 in
 // the cache stands for "none fit").
@@ -933,7 +979,7 @@ int mla_tc_resident_ctas(int cluster_z) {
   cudaLaunchAttribute attrs[1];
   cudaLaunchConfig_t cfg = mla_tc_config(dim3(1, 2, cluster_z), cluster_z, 0, attrs);
   if (mla_tc_prepare() &&
-      cudaOccupancyMaxActiveClusters(&clusters, (void*)mtc::sparse_mla_tc_kernel, &cfg) == cudaSuccess &&
+      cudaOccupancyMaxActiveClusters(&clusters, (void*)mtc::sparse_mla_tc_kernel<false>, &cfg) == cudaSuccess &&
       clusters > 0)
     n = 2 * cluster_z * clusters;
   else
@@ -981,7 +1027,8 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
   k.B = p.B; k.R = p.R; k.H = p.H; k.n_idx = p.n_idx; k.n_append = p.n_append;
   k.sl2 = p.scale * LOG2E; k.row_pos_add = p.row_pos_add;
   k.q = (const __nv_bfloat16*)p.q; k.latent = (const __nv_bfloat16*)p.latent; k.pool = p.pool;
-  k.cache_start = p.cache_start; k.row_offsets = p.row_offsets; k.row_pos = p.row_pos; k.idx = p.idx;
+  k.cache_start = p.cache_start; k.bt = p.pg.bt; k.bt_stride = p.pg.stride; k.pg_shift = p.pg.shift;
+  k.row_offsets = p.row_offsets; k.row_pos = p.row_pos; k.idx = p.idx;
   k.append_base = p.append_base; k.out = (__nv_bfloat16*)p.out; k.lse = p.lse; k.part_o = part_o; k.part_ml = part_ml;
   k.n_splits = n_splits; k.per_split = per_split; k.status = p.status;
   k.fused_combine = mla_tc_fuse(n_splits) ? 1 : 0;
@@ -1011,7 +1058,8 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see launch_k()
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel, tm_lat, tm_q, tm_st, k);
+  cudaError_t e = p.pg.bt ? cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<true>, tm_lat, tm_q, tm_st, k)
+                           : cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<false>, tm_lat, tm_q, tm_st, k);
   if (e != cudaSuccess) {
     set_error("sparse_mla_tc: launch failed: %s", cudaGetErrorString(e));
     return MTPSD_ECUDA;

@@ -178,7 +178,8 @@ __global__ void kv_writeback_kernel(const uint4* __restrict__ src_l, const uint4
                                     uint4* __restrict__ dst_k, float* __restrict__ dst_s,
                                     const int64_t* __restrict__ cache_start, const int64_t* __restrict__ dst_pos,
                                     int64_t pool,
-                                    int64_t* __restrict__ next_pos, int32_t* __restrict__ status) {
+                                    int64_t* __restrict__ next_pos, int32_t* __restrict__ status,
+                                    const int64_t* __restrict__ dst_slots) {
   griddep_wait();                // the previous kernel's writes are visible from here on
   griddep_launch_dependents();
   int b = blockIdx.y;
@@ -188,7 +189,8 @@ __global__ void kv_writeback_kernel(const uint4* __restrict__ src_l, const uint4
   if (n > W) n = W;
   if (i == 0 && threadIdx.x == 0 && next_pos) next_pos[b] = dst_pos[b] + n;
   if (i >= n) return;
-  int64_t t = cache_start[b] + dst_pos[b] + i;
+  // destination: the planned window slot (paged caches) or the row after the request's committed ones
+  int64_t t = dst_slots ? dst_slots[(int64_t)b * W + i] : cache_start[b] + dst_pos[b] + i;
   if (t < 0 || t >= pool) {
     if (threadIdx.x == 0) flag_status(status, MTPSD_STATUS_WRITE_RANGE);
     return;
@@ -203,11 +205,11 @@ int launch_kv_writeback(const void* src_l, const uint8_t* src_k, const float* sr
                         int lat_bytes, int idx_bytes, const int32_t* n_acc, void* dst_l, uint8_t* dst_k,
                         float* dst_s, const int64_t* cache_start, const int64_t* dst_pos, int64_t pool,
                         int64_t* next_pos,
-                        int32_t* status, cudaStream_t st) {
+                        int32_t* status, cudaStream_t st, const int64_t* dst_slots) {
   dim3 grid(W, B);
   launch_k(kv_writeback_kernel, grid, 64, 0, st, (const uint4*)src_l, (const uint4*)src_k, src_s, W, lat_bytes / 16,
                                            idx_bytes / 16, n_acc, (uint4*)dst_l, (uint4*)dst_k, dst_s,
-                                           cache_start, dst_pos, pool, next_pos, status);
+                                           cache_start, dst_pos, pool, next_pos, status, dst_slots);
   return check_launch("kv_writeback");
 }
 

@@ -52,9 +52,11 @@ class DecodeStep:
     step of the next round (seed_dsa_topk_from_draft_extend)."""
 
     def __init__(self, w: W.Workload, device="cuda", draft: Optional[Dict[str, torch.Tensor]] = None,
-                 seeded: bool = False, latent_fp8: bool = False):
+                 seeded: bool = False, latent_fp8: bool = False, page_size: Optional[int] = None):
         self.w = w
         self.seeded = seeded
+        self.page_size = page_size     # paged caches: every pool reached through one shared block table
+        self.paged = None
         self.latent_fp8 = latent_fp8   # latent caches as 656-byte FP8 rows ([P2] "草稿层 KV 的账")
         spec = w.spec
         self.spec = spec
@@ -164,6 +166,62 @@ class DecodeStep:
             self.ws_dmla = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
             if seeded:
                 self._init_extend(d, device)
+        if page_size:
+            if seeded:
+                raise ValueError("paged caches are built for the shared-index draft loop, not the seeded one")
+            self._init_paged(page_size, device)
+
+    def _init_paged(self, ps: int, device, seed: int = 1234):
+        """Moves every cache into a paged pool ([P2] "输入准备:prepare_for_draft": token slots reached through a
+        per-request table; page_size > 1 groups them into pages).  Request b's positions 0..cap_b-1 (its region of
+        the contiguous layout) take ceil(cap_b / ps) pages drawn at random from a pool with one spare page; the
+        target and draft layers share the table (each keeps its own pools).  Set-up only: the step then reads
+        and writes the caches through the table."""
+        w = self.w
+        B = self.B
+        T = int(self.latent.shape[0])
+        cs = np.asarray(w.cache_start, dtype=np.int64)
+        caps = np.diff(np.concatenate([cs, [T]]))
+        need = -(-caps // ps)
+        n_pages = int(need.sum()) + 1
+        perm = np.random.default_rng(seed).permutation(n_pages).astype(np.int32)
+        bt = np.full((B, int(need.max())), -1, dtype=np.int32)
+        src, dst = [], []
+        o = 0
+        for b in range(B):
+            bt[b, :need[b]] = perm[o:o + need[b]]
+            o += int(need[b])
+            s = np.arange(caps[b], dtype=np.int64)
+            src.append(cs[b] + s)
+            dst.append(bt[b, s // ps].astype(np.int64) * ps + s % ps)
+        src_t = torch.from_numpy(np.concatenate(src)).to(device)
+        dst_t = torch.from_numpy(np.concatenate(dst)).to(device)
+        rows = n_pages * ps
+
+        def to_pages(x):
+            y = torch.zeros((rows,) + tuple(x.shape[1:]), dtype=x.dtype, device=device)
+            y[dst_t] = x[src_t]
+            return y
+
+        self.latent = to_pages(self.latent)
+        self.k_cache = to_pages(self.k_cache)
+        if self.k_scale is not None:
+            self.k_scale = to_pages(self.k_scale)
+        if self.has_draft:
+            self.d_latent = to_pages(self.d_latent)
+            self.d_k_cache = to_pages(self.d_k_cache)
+            if self.d_k_scale is not None:
+                self.d_k_scale = to_pages(self.d_k_scale)
+        del src_t, dst_t
+        self.block_table_host = bt
+        self.block_table = _dev(bt, device, torch.int32)
+        self.paged = (self.block_table, ps)
+        self.cache_start = None       # positions resolve through the table
+        Wn = self.K + 1
+        self.win_start = _dev(w.L, device, torch.int64)          # the window follows the committed length
+        self.out_cache_loc = torch.empty(B, Wn, dtype=torch.int64, device=device)
+        # a chain of drafts accepts a prefix of the window: row i comes from window column i
+        self.accept_index = _dev(np.tile(np.arange(Wn, dtype=np.int32), (B, 1)), device, torch.int32)
 
     def _latent(self, x):
         """A latent pool as the step stores it: as generated, or packed into FP8 rows."""
@@ -211,7 +269,7 @@ class DecodeStep:
             api.quantize_fp8_block128(self.q_idx_raw, self.q_idx, self.q_scale, stream=stream)
         api.indexer_scores(self.q_idx, self.q_scale, self.w_idx, self.k_cache, self.k_scale, self.cache_start,
                            self.row_offsets, self.row_pos, self.max_visible, scores=self.scores,
-                           workspace=self.ws_plan, dev_status=self.status, stream=stream)
+                           workspace=self.ws_plan, dev_status=self.status, stream=stream, paged=self.paged)
 
     def verify_topk(self, stream=None):
         api.topk(self.scores, self.row_pos, self.max_visible, self.spec.topk, out_idx=self.topk_idx,
@@ -224,13 +282,31 @@ class DecodeStep:
     def verify_mla(self, stream=None):
         api.sparse_mla_decode(self.q_mla, self.latent, self.cache_start, self.row_offsets, self.row_pos,
                               self.topk_idx, W.SOFTMAX_SCALE, out=self.out, lse=self.lse, workspace=self.ws_mla,
-                              dev_status=self.status, stream=stream)
+                              dev_status=self.status, stream=stream, paged=self.paged)
 
     def accept(self, stream=None):
         api.accept_greedy(self.draft_tokens, self.target_argmax, 42, self.num_accepted, self.next_tokens,
                           stream=stream)
 
+    def plan(self, stream=None):
+        """Paged caches: the slots of the window positions L .. L + K (assign_cache_locs), shared by the
+        layers."""
+        api.assign_cache_locs(self.block_table, self.page_size, self.win_start, self.K + 1, self.out_cache_loc,
+                              dev_status=self.status, stream=stream)
+
+    def move(self, stream=None):
+        """Paged caches: the target layer's accepted KV moves to the window's front slots (a chain of drafts
+        accepts the window's prefix, which is already in place)."""
+        api.kv_move_accepted(self.latent, self.k_cache.view(torch.uint8), self.k_scale,
+                             self.out_cache_loc, self.accept_index, self.num_accepted, dev_status=self.status,
+                             stream=stream)
+
     def writeback(self, stream=None):
+        if self.page_size:
+            api.kv_writeback_slots(self.src_latent, self.src_idxk, self.src_idxs, self.num_accepted, self.d_latent,
+                                   self.d_k_cache.view(torch.uint8), self.d_k_scale, self.out_cache_loc,
+                                   self.dst_pos, self.next_pos, dev_status=self.status, stream=stream)
+            return
         api.kv_writeback(self.src_latent, self.src_idxk, self.src_idxs, self.num_accepted, self.d_latent,
                          self.d_k_cache.view(torch.uint8), self.d_k_scale, self.cache_start, self.dst_pos,
                          next_pos=self.next_pos, dev_status=self.status, stream=stream)
@@ -242,7 +318,8 @@ class DecodeStep:
             api.quantize_fp8_block128(self.d_q_idx_raw, self.d_q_idx, self.d_q_scale, stream=stream)
         api.indexer_scores(self.d_q_idx, self.d_q_scale, self.d_w_idx, self.d_k_cache, self.d_k_scale,
                            self.cache_start, self.d_row_offsets, self.next_pos, self.d_max_visible,
-                           scores=self.d_scores, workspace=self.ws_dplan, dev_status=self.status, stream=stream)
+                           scores=self.d_scores, workspace=self.ws_dplan, dev_status=self.status, stream=stream,
+                           paged=self.paged)
 
     def draft_topk(self, stream=None):
         """Draft step 0 selection, then the share gather that steps 1.. reuse."""
@@ -259,7 +336,8 @@ class DecodeStep:
         api.sparse_mla_decode(self.d_q_mla[j], self.d_latent, self.cache_start, self.d_row_offsets, self.next_pos,
                               self.shared_idx, W.SOFTMAX_SCALE, n_append=j,
                               append_base=self.next_pos if j else None, row_pos_add=j, out=self.d_out[j],
-                              lse=self.d_lse[j], workspace=self.ws_dmla, dev_status=self.status, stream=stream)
+                              lse=self.d_lse[j], workspace=self.ws_dmla, dev_status=self.status, stream=stream,
+                              paged=self.paged)
 
     def extend_scores(self, stream=None):
         """draft_extend: FP8 quantization of the window rows' draft indexer queries, then the score GEMM over
@@ -294,9 +372,16 @@ class DecodeStep:
         """The step as an ordered list of (name, callable(stream)): what step() runs."""
         ph = []
         if self.spec.verify:
-            ph += [("merge", self.merge), ("verify_scores", self.verify_scores), ("verify_topk", self.verify_topk),
+            ph.append(("merge", self.merge))
+            if self.page_size:
+                ph.append(("plan", self.plan))
+            ph += [("verify_scores", self.verify_scores), ("verify_topk", self.verify_topk),
                    ("verify_mla", self.verify_mla)]
+        elif self.page_size:
+            ph.append(("plan", self.plan))
         ph.append(("accept", self.accept))
+        if self.page_size:
+            ph.append(("move", self.move))
         if self.has_draft and self.seeded:
             ph += [("writeback", self.writeback), ("extend_scores", self.extend_scores),
                    ("extend_topk", self.extend_topk), ("extend_mla", self.extend_mla)]
@@ -324,6 +409,8 @@ class DecodeStep:
         if self.spec.verify:
             n += 1 + quant + scores + api.topk_launch_count(self.max_visible, k) + self._mla_launches(k, 0, self.R)
         n += 1
+        if self.page_size:
+            n += 2    # the window's slot plan and the accepted-KV move
         if self.has_draft and self.seeded:
             Rx = self.B * (self.K + 1)
             n += 1 + quant + scores + api.topk_launch_count(self.x_max_visible, k) + 1 + self._mla_launches(k, 0, Rx)

@@ -55,7 +55,8 @@ def _c_offsets(struct, fields):
     return [int(x) for x in out]
 
 
-@pytest.mark.parametrize("cname,pyname", [("mtpsd_indexer_args", "IndexerArgs"), ("mtpsd_mla_args", "MlaArgs")])
+@pytest.mark.parametrize("cname,pyname", [("mtpsd_indexer_args", "IndexerArgs"), ("mtpsd_mla_args", "MlaArgs"),
+                                          ("mtpsd_paged_kv", "PagedKV")])
 def test_struct_layout_matches_header(native, cname, pyname):
     st = getattr(native, pyname)
     fields = [f for f, _ in st._fields_]
@@ -88,6 +89,28 @@ def test_host_checks_reject_before_launch(native):
     assert lib.mtpsd_check_bounded_wait(0, 8, 8, None) == native.MTPSD_EINVAL
     assert lib.mtpsd_check_bounded_wait(2_000_000_000, 8, 8, None) == native.MTPSD_EINVAL
     assert lib.mtpsd_check_bounded_wait(1000, None, 8, None) == native.MTPSD_EINVAL
+
+
+def test_paged_checks_reject_before_launch(native):
+    lib = native.lib()
+    m = native.MlaArgs(B=1, R=1, n_heads=16, d_latent=576, d_v=512, n_idx=16, dtype=native.MTPSD_BF16)
+    for ps, bt, stride in ((3, 8, 4), (0, 8, 4), (1 << 17, 8, 4), (64, None, 4), (64, 8, 0)):
+        pk = native.PagedKV(block_table=bt, bt_stride=stride, page_size=ps)
+        assert lib.mtpsd_sparse_mla_decode_paged(C.byref(m), C.byref(pk), None) == native.MTPSD_EINVAL
+        assert b"page" in lib.mtpsd_last_error() or b"block_table" in lib.mtpsd_last_error()
+        assert lib.mtpsd_assign_cache_locs(C.byref(pk), 1, 8, 4, 8, None, None) == native.MTPSD_EINVAL
+    a = native.IndexerArgs(B=1, R=1, n_heads=64, head_dim=128, topk=16, dtype=native.MTPSD_FP8_E4M3)
+    pk = native.PagedKV(block_table=8, bt_stride=4, page_size=48)
+    assert lib.mtpsd_indexer_topk_paged(C.byref(a), C.byref(pk), None) == native.MTPSD_EINVAL
+    assert lib.mtpsd_assign_cache_locs(None, 1, 8, 4, 8, None, None) == native.MTPSD_EINVAL
+    # window wider than the move's shared staging, and an unknown latent type
+    assert lib.mtpsd_kv_move_accepted(8, native.MTPSD_BF16, None, 0, None, 10, 8, 8, 8, 1, 17, None,
+                                      None) == native.MTPSD_EINVAL
+    assert lib.mtpsd_kv_move_accepted(8, 7, None, 0, None, 10, 8, 8, 8, 1, 4, None, None) == native.MTPSD_EUNSUPPORTED
+    assert lib.mtpsd_kv_writeback_slots(None, None, None, 1, 6, native.MTPSD_BF16, 128, None, None, None, None, None,
+                                        10, None, None, None, None) == native.MTPSD_EINVAL
+    assert lib.mtpsd_kv_writeback_slots(16, 16, None, 1, 6, native.MTPSD_BF16, 128, 8, 16, 16, None, 8,
+                                        10, 8, None, None, None) == native.MTPSD_EINVAL   # dst_pos without next_pos
 
 
 def test_host_merged_offsets_mirror(native):

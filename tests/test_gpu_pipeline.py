@@ -25,11 +25,11 @@ def _sample(n, k, seed):
     return sorted(set([0, n - 1] + list(rng.choice(n, size=min(n, k), replace=False))))
 
 
-def run_case(mods, name, n_rows, n_reqs, heads=None, latent_fp8=False):
+def run_case(mods, name, n_rows, n_reqs, heads=None, latent_fp8=False, page_size=None):
     pipeline, W, OracleStep = mods
     w = W.build(name)
     d = W.draft_tensors(w) if w.spec.draft_steps else None
-    g = pipeline.DecodeStep(w, "cuda", d, latent_fp8=latent_fp8)
+    g = pipeline.DecodeStep(w, "cuda", d, latent_fp8=latent_fp8, page_size=page_size)
     g.step()
     torch.cuda.synchronize()
     assert g.status.item() == 0, f"device status {g.status.item()}"
@@ -88,6 +88,42 @@ def run_case(mods, name, n_rows, n_reqs, heads=None, latent_fp8=False):
 
 def test_tiny_all_rows(mods):
     run_case(mods, "tiny", n_rows=10 ** 6, n_reqs=10 ** 6)
+
+
+@pytest.mark.parametrize("ps", [4, 64])
+def test_tiny_paged(mods, ps):
+    """The step over paged caches (shuffled pages, one block table for both layers): the slot plan, the
+    accepted-KV move and the write-back by slot, and every read through the table, give the contiguous
+    step's results against the oracle.  The paged pools hold the workload's caches where the oracle's slot
+    map says, before and after the step."""
+    from oracle import paged as opaged
+    pipeline, W, _ = mods
+    rep = run_case(mods, "tiny", n_rows=10 ** 6, n_reqs=10 ** 6, page_size=ps)
+    w = W.build("tiny")
+    g = pipeline.DecodeStep(w, "cuda", W.draft_tensors(w), page_size=ps)
+    bt = g.block_table_host
+    lat = g.latent.cpu().numpy()
+    for b in range(w.B):
+        pos = range(int(w.L[b]) + w.r)
+        got = opaged.gather_positions(lat, bt, ps, b, pos)
+        want = np.asarray(w.tensors["latent"])[int(w.cache_start[b]) + np.arange(len(pos))]
+        assert np.array_equal(got, want)
+    g.step()
+    torch.cuda.synchronize()
+    assert g.status.item() == 0
+    want_loc = opaged.assign_cache_locs(bt, ps, w.L, w.spec.K + 1)
+    assert np.array_equal(g.out_cache_loc.cpu().numpy(), want_loc)
+    return rep
+
+
+@pytest.mark.slow
+def test_verify_paged_full_size(mods):
+    run_case(mods, "verify", n_rows=16, n_reqs=6, heads=range(0, 128, 16), page_size=64)
+
+
+@pytest.mark.slow
+def test_draft_loop_paged_full_size(mods):
+    run_case(mods, "draft", n_rows=0, n_reqs=6, heads=range(0, 128, 16), page_size=64)
 
 
 @pytest.mark.slow
