@@ -98,7 +98,7 @@ def test_tiny_paged(mods, ps):
     map says, before and after the step."""
     from oracle import paged as opaged
     pipeline, W, _ = mods
-    rep = run_case(mods, "tiny", n_rows=10 ** 6, n_reqs=10 ** 6, page_size=ps)
+    run_case(mods, "tiny", n_rows=10 ** 6, n_reqs=10 ** 6, page_size=ps)
     w = W.build("tiny")
     g = pipeline.DecodeStep(w, "cuda", W.draft_tensors(w), page_size=ps)
     bt = g.block_table_host
@@ -113,7 +113,6 @@ def test_tiny_paged(mods, ps):
     assert g.status.item() == 0
     want_loc = opaged.assign_cache_locs(bt, ps, w.L, w.spec.K + 1)
     assert np.array_equal(g.out_cache_loc.cpu().numpy(), want_loc)
-    return rep
 
 
 @pytest.mark.slow
