@@ -35,7 +35,9 @@ def nvcc() -> str:
 
 def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-c", src, "-o", obj]
+    # MTPSD_NVCC_DEFINES: extra -D tuning definitions (space separated), e.g. "MTPSD_IDX_CHUNK=4"
+    defs = [f"-D{d}" for d in os.environ.get("MTPSD_NVCC_DEFINES", "").split() if d]
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *defs, "-I", INCLUDE, "-c", src, "-o", obj]
     res = subprocess.run(cmd, capture_output=True, text=True)
     log = os.path.join(BUILD, os.path.basename(src) + ".log")
     with open(log, "w") as f:

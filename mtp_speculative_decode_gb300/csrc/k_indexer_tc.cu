@@ -71,6 +71,9 @@ constexpr int PRODUCER_WARP = EPI_WARPS;
 constexpr int MMA_WARP = EPI_WARPS + 1;
 constexpr int THREADS = 32 * (EPI_WARPS + 2);
 constexpr int MAX_GROUP_ROWS = Q_ROWS / 32;
+constexpr int SPLIT_STAGE_COLS = 256;                  // TMEM columns of one head half (8 rows x 32 heads)
+constexpr int SPLIT_HALF_BYTES = 8 * 32 * KB;          // query bytes of one head half (8 rows x 32 heads)
+static_assert(2 * SPLIT_HALF_BYTES == Q_ROWS * KB && 2 * SPLIT_STAGE_COLS == NSLOT * SLOT_COLS, "split layout");
 
 constexpr int OFF_K = 0;
 constexpr int OFF_Q = OFF_K + NSTAGE * TILE_M * KB;      // 98304
@@ -168,6 +171,8 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_byte_addr) {
 __device__ __forceinline__ uint32_t idesc(int c) {
   return (1u << 4) | ((uint32_t)(64 * c) >> 3 << 17) | ((128u >> 4) << 24);
 }
+// The same with N given in columns (a multiple of 16, at most 256).
+__device__ __forceinline__ uint32_t idesc_n(int n) { return (1u << 4) | ((uint32_t)n >> 3 << 17) | ((128u >> 4) << 24); }
 
 __device__ __forceinline__ void mma_fp8(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t id, uint32_t accumulate) {
   asm volatile(
@@ -305,7 +310,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const uint32_t* __restrict__
 // aligned destinations keep the 128-byte swizzle), and the key scales of each box as one bulk copy; lane k of
 // the producer handles box k.  A box without a page (or outside the pool) loads zeros: its keys through an
 // out-of-range TMA row, its scales written as zeros by the lane itself.
-template <int H, bool PAGED>
+// SPLIT (64 heads, groups of up to 8 rows): every key tile is scored in two halves, heads 0..31 then heads
+// 32..63 of all the group's rows, each half in its own 256-column TMEM stage (N = 32 x rows), so that the MMAs
+// of one half run while the epilogue drains the other.  A six-row tile has 384 accumulator columns, and
+// without the split the next tile's MMAs could only start after the epilogue had read most of this one:
+// every tile paid a full MMA -> epilogue -> MMA round trip.  The query block is held as [half][row][32 heads];
+// epilogue warpgroup w takes the row pairs (2j, 2j+1) with j = w and j = w + 3 in both halves and carries the
+// first half's partial head sums in registers to the second.
+template <int H, bool PAGED, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                                 const __grid_constant__ CUtensorMap tmap_q,
                                                                 const __grid_constant__ CUtensorMap tmap_ks,
@@ -341,7 +353,8 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int i = 0; i < NCH; ++i) mbar_init(&chunk_full[i], 1);
-    for (int i = 0; i < NSLOT; ++i) mbar_init(&slot_empty[i], 4);   // the four warps of the unit's warpgroup
+    // the four warps of the unit's warpgroup; SPLIT: every epilogue warp, once per half
+    for (int i = 0; i < NSLOT; ++i) mbar_init(&slot_empty[i], SPLIT ? EPI_WARPS : 4);
     for (int i = 0; i < NKS; ++i) {
       mbar_init(&ks_full[i], 1);
       mbar_init(&ks_empty[i], EPI_WARPS);    // every epilogue warp, once per tile
@@ -409,8 +422,15 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
         else cstart = p.cache_start[p.g_b[g]];
         if (elect_one()) {
           mbar_expect_tx(q_full, (uint32_t)(nrows * H * KB));
-          for (int i = 0; i < nrows; ++i)
-            tma_load_2d(saddr(sm + OFF_Q + i * H * KB), &tmap_q, 0, (row0 + i) * H, q_full);
+          if (SPLIT) {   // [half][row][32 heads]: two boxes of 32 head vectors per row
+            for (int i = 0; i < nrows; ++i)
+              for (int h = 0; h < 2; ++h)
+                tma_load_2d(saddr(sm + OFF_Q + h * SPLIT_HALF_BYTES + i * 32 * KB), &tmap_q, 0, (row0 + i) * H + h * 32,
+                            q_full);
+          } else {
+            for (int i = 0; i < nrows; ++i)
+              tma_load_2d(saddr(sm + OFF_Q + i * H * KB), &tmap_q, 0, (row0 + i) * H, q_full);
+          }
         }
         __syncwarp();
         ++gq;
@@ -471,6 +491,54 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
       }
       if (gq > 0) mbar_wait(q_full, (gq - 1) & 1, &dummy, p.status);
     }
+  } else if (warp == MMA_WARP && SPLIT) {
+    // per key tile: half h (heads 32h .. 32h+31 of every row) into TMEM stage h, N = 32 x rows
+    int n_cons = 0, gq = 0, cur_g = -1, nrows = 0;
+    bool ok = true;
+    Cursor c;
+    c.start(p, n_groups, it0);
+    for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups)) {
+      const int g = c.g;
+      if (g != cur_g) {
+        if (cur_g >= 0) {
+          if (elect_one()) mma_commit(q_empty);
+          __syncwarp();
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(q_full, gq & 1, abort_flag, p.status));
+        if (!ok) break;
+        ++gq;
+        cur_g = g;
+        nrows = p.g_nrows[g];
+      }
+      const int stage = n_cons % NSTAGE, round = n_cons / NSTAGE;
+      ok = __all_sync(0xffffffffu, mbar_wait(&k_full[stage], round & 1, abort_flag, p.status));
+      if (!ok) break;
+      const uint32_t a_base = saddr(sm + OFF_K + stage * TILE_M * KB);
+      const uint32_t id = idesc_n(32 * nrows);
+      for (int h = 0; h < 2 && ok; ++h) {
+        // stage h was last used by the previous tile's half h
+        if (n_cons > 0) ok = __all_sync(0xffffffffu, mbar_wait(&slot_empty[h], (n_cons - 1) & 1, abort_flag, p.status));
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t b_base = saddr(sm + OFF_Q + h * SPLIT_HALF_BYTES);
+          const uint32_t d = tmem_base + (uint32_t)(h * SPLIT_STAGE_COLS);
+#pragma unroll
+          for (int kk = 0; kk < KB / 32; ++kk)
+            mma_fp8(d, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), id, kk > 0 ? 1u : 0u);
+          mma_commit(&chunk_full[h]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (elect_one()) mma_commit(&k_empty[stage]);
+      __syncwarp();
+      ++n_cons;
+    }
+    if (elect_one()) mma_commit(drain);
+    __syncwarp();
+    volatile int dummy = 0;
+    mbar_wait(drain, 0, &dummy, p.status);
   } else if (warp == MMA_WARP) {
     int n_cons = 0, gq = 0, cur_g = -1, units = 0;
     int u = 0;        // running unit (slot use) index
@@ -532,6 +600,102 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
     __syncwarp();
     volatile int dummy = 0;
     mbar_wait(drain, 0, &dummy, p.status);
+  } else if (SPLIT) {
+    // ------------------------------------------------------------ epilogue of the head halves
+    const int wg = warp >> 2;
+    const int quarter = warp & 3;
+    const int pos_in_tile = quarter * 32 + lane;
+    int cur_g = -1, nrows = 0, row0 = 0, n_tile = 0, ks_off = 0;
+    int64_t vmax = 0, cstart = 0;
+    bool ok = true;
+    Cursor c;
+    c.start(p, n_groups, it0);
+    for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups), ++n_tile) {
+      const int g = c.g;
+      if (g != cur_g) {
+        __syncwarp();
+        nrows = p.g_nrows[g];
+        row0 = p.g_row0[g];
+        vmax = p.g_vmax[g];
+        cstart = PAGED ? 0 : p.cache_start[p.g_b[g]];
+        ks_off = (int)(cstart & 3);
+        {
+          float wv[Q_ROWS / 32], qv[Q_ROWS / 32];
+#pragma unroll
+          for (int k = 0; k < Q_ROWS / 32; ++k) {
+            const int e = lane + 32 * k;
+            const bool in = e < nrows * H;
+            wv[k] = in ? p.w[(int64_t)row0 * H + e] : 0.f;
+            qv[k] = in ? p.q_scale[(int64_t)row0 * H + e] : 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < Q_ROWS / 32; ++k)
+            if (lane + 32 * k < nrows * H) wq[lane + 32 * k] = 0.5f * (wv[k] * qv[k]);
+        }
+        for (int i = lane; i < nrows; i += 32) vis[i] = min(p.row_pos[row0 + i] + 1, p.max_visible);
+        __syncwarp();
+        cur_g = g;
+      }
+      const int kslot = n_tile % NKS, kround = n_tile / NKS;
+      ok = __all_sync(0xffffffffu, mbar_wait(&ks_full[kslot], kround & 1, abort_flag, p.status));
+      if (!ok) break;
+      const int64_t s = (int64_t)c.tile * TILE_M + pos_in_tile;
+      const float ks = (s < vmax) ? ((const float*)(sm + OFF_KS + kslot * KS_STRIDE))[ks_off + pos_in_tile] : 0.f;
+      // this warpgroup's row pairs: j = wg (k = 0) and j = wg + 3 (k = 1), rows 2j and 2j + 1
+      const int n_pairs = (nrows + 1) >> 1;
+      const int n_mine = (wg < n_pairs ? 1 : 0) + (wg + EPI_WG < n_pairs ? 1 : 0);
+      float part[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+      for (int h = 0; h < 2 && ok; ++h) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&chunk_full[h], n_tile & 1, abort_flag, p.status));
+        if (!ok) break;
+        tc_fence_after();
+        if (n_mine == 0) {   // nothing to read: release the stage at once
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&slot_empty[h]);
+          continue;
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int j = wg + EPI_WG * k;
+          if (k >= n_mine) break;
+          float x[64];   // x[0..31]: row 2j, x[32..63]: row 2j + 1 (heads 32h ..)
+          const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                 (uint32_t)(h * SPLIT_STAGE_COLS + j * 64);
+          tmem_ld32(taddr, x);
+          tmem_ld32(taddr + 32, x + 32);
+          tmem_ld_wait();
+          if (k == n_mine - 1) {   // the warp's last read of this stage
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&slot_empty[h]);
+          }
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int i = 2 * j + r;   // row within the group
+            if (i >= nrows) break;
+            const float4* wr = (const float4*)(wq + i * H + h * 32);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              const float4 ww = wr[m];
+              acc[0] = fmaf(ww.x, x[32 * r + 4 * m + 0] + fabsf(x[32 * r + 4 * m + 0]), acc[0]);
+              acc[1] = fmaf(ww.y, x[32 * r + 4 * m + 1] + fabsf(x[32 * r + 4 * m + 1]), acc[1]);
+              acc[2] = fmaf(ww.z, x[32 * r + 4 * m + 2] + fabsf(x[32 * r + 4 * m + 2]), acc[2]);
+              acc[3] = fmaf(ww.w, x[32 * r + 4 * m + 3] + fabsf(x[32 * r + 4 * m + 3]), acc[3]);
+            }
+            const float sc = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            if (h == 0) {
+              part[k][r] = sc;
+            } else if (s < vis[i]) {
+              p.scores[(int64_t)(row0 + i) * p.ld + s] = (part[k][r] + sc) * ks;
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ks_empty[kslot]);
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int wg = warp >> 2;              // this warpgroup takes units u with u % EPI_WG == wg
@@ -691,7 +855,11 @@ int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {
   CUtensorMap mk, mq, mks;
   const bool paged = p.pg.bt != nullptr;
   const uint32_t key_box = paged ? (uint32_t)std::min<int64_t>(TILE_M, 1LL << p.pg.shift) : (uint32_t)TILE_M;
-  if (!make_map_rows128(&mk, p.k, p.pool, key_box) || !make_map_rows128(&mq, p.q, (int64_t)p.R * p.H, (uint32_t)p.H) ||
+  // head halves: groups average five or more rows (64 heads), so a tile's accumulators would fill most of TMEM
+  const char* env_split = getenv("MTPSD_INDEXER_SPLIT");
+  const bool split = p.H == 64 && (env_split ? env_split[0] == '1' : (int64_t)p.R >= 5LL * p.B);
+  if (!make_map_rows128(&mk, p.k, p.pool, key_box) ||
+      !make_map_rows128(&mq, p.q, (int64_t)p.R * p.H, split ? 32u : (uint32_t)p.H) ||
       !make_tma_1d_f32(&mks, p.k_scale, (uint64_t)p.pool, KS_BOX)) {
     set_error("indexer: cuTensorMapEncodeTiled failed");
     return MTPSD_ECUDA;
@@ -716,10 +884,12 @@ int launch_indexer_scores_tc(const IndexerPlan& p, cudaStream_t st) {
   kp.H = p.H; kp.g_b = g_b; kp.g_row0 = g_row0; kp.g_nrows = g_nrows; kp.g_vmax = g_vmax; kp.g_tile0 = g_tile0;
   kp.n_groups = n_groups; kp.status = p.status;
   kp.k_scale = p.k_scale; kp.bt = p.pg.bt; kp.bt_stride = p.pg.stride; kp.pg_shift = p.pg.shift;
-  static std::atomic<uint64_t> attr[4];
-  auto kern = p.H == 64 ? (paged ? indexer_tc_kernel<64, true> : indexer_tc_kernel<64, false>)
-                        : (paged ? indexer_tc_kernel<32, true> : indexer_tc_kernel<32, false>);
-  if (!set_smem_limit_once(kern, SMEM_BYTES, attr[(p.H == 64 ? 0 : 2) + (paged ? 1 : 0)])) {
+  static std::atomic<uint64_t> attr[6];
+  auto kern = p.H == 64 ? (split ? (paged ? indexer_tc_kernel<64, true, true> : indexer_tc_kernel<64, false, true>)
+                                 : (paged ? indexer_tc_kernel<64, true, false> : indexer_tc_kernel<64, false, false>))
+                        : (paged ? indexer_tc_kernel<32, true, false> : indexer_tc_kernel<32, false, false>);
+  const int which = p.H == 64 ? (split ? 4 : 0) + (paged ? 1 : 0) : 2 + (paged ? 1 : 0);
+  if (!set_smem_limit_once(kern, SMEM_BYTES, attr[which])) {
     set_error("indexer_tc: cudaFuncSetAttribute failed");
     return MTPSD_ECUDA;
   }

@@ -237,13 +237,21 @@ def _indexer_case(H, D, lens, r_per, fp8, seed):
     return dict(q=q, k=k, w=w, cache_start=cache_start, row_req=row_req, row_pos=row_pos, ro=ro, T=T)
 
 
-@pytest.mark.parametrize("H,D,lens,r_per,k,fp8", [
-    (4, 64, [100, 300], 4, 32, False),                 # the tiny float32 shape
-    (64, 128, [300, 1000, 129, 5], 6, 256, True),       # several tiles + ragged tails, FP8
-    (64, 128, [4100, 200], 1, 2048, True),              # draft-step shape: one row per request
-    (32, 128, [777, 1500, 64], 3, 512, True),
+@pytest.mark.parametrize("H,D,lens,r_per,k,fp8,split", [
+    (4, 64, [100, 300], 4, 32, False, None),                 # the tiny float32 shape
+    (64, 128, [300, 1000, 129, 5], 6, 256, True, None),       # several tiles + ragged tails, FP8 (head halves)
+    (64, 128, [300, 1000, 129, 5], 6, 256, True, "0"),        # the same without the head halves
+    (64, 128, [4100, 200], 1, 2048, True, None),              # draft-step shape: one row per request
+    (64, 128, [4100, 200], 1, 2048, True, "1"),               # one row in head halves (N = 32)
+    (64, 128, [500, 1300, 129], 5, 512, True, None),          # odd rows: the last pair holds one row
+    (64, 128, [700, 64, 2000], 7, 512, True, None),
+    (64, 128, [900, 300], 8, 1024, True, None),               # a full pair for warpgroup 0's second unit
+    (64, 128, [900, 300, 50], 11, 256, True, None),           # requests cut into groups of 8 + 3 rows
+    (32, 128, [777, 1500, 64], 3, 512, True, None),
 ])
-def test_indexer_scores_and_topk(mt, H, D, lens, r_per, k, fp8):
+def test_indexer_scores_and_topk(mt, H, D, lens, r_per, k, fp8, split, monkeypatch):
+    if split is not None:
+        monkeypatch.setenv("MTPSD_INDEXER_SPLIT", split)
     c = _indexer_case(H, D, lens, r_per, fp8, seed=H + D + k)
     R = len(c["row_req"])
     maxv = int(max(c["row_pos"])) + 1
