@@ -478,6 +478,38 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p, SplitLevel sl
   const int eq_before = block_exclusive_scan(n_eq, warp_sums, &total_s);
   int take_eq = max(0, min(n_eq, need_eq - eq_before));
   int out_pos = gt_before + min(eq_before, need_eq);
+  if constexpr (MODE == 2) {
+    // merged lists carry their positions: eight of this thread's are loaded together before they are
+    // emitted, instead of one dependent load per emitted entry
+#pragma unroll
+    for (int c0 = 0; c0 < KPT; c0 += 8) {
+      int32_t pv[8];
+      if ((k & 3) == 0 && a + c0 + 8 <= lim) {
+        const int4 v0 = *(const int4*)(prow + a + c0), v1 = *(const int4*)(prow + a + c0 + 4);
+        pv[0] = v0.x; pv[1] = v0.y; pv[2] = v0.z; pv[3] = v0.w;
+        pv[4] = v1.x; pv[5] = v1.y; pv[6] = v1.z; pv[7] = v1.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pv[j] = a + c0 + j < lim ? prow[a + c0 + j] : -1;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = c0 + j;
+        bool take = key[i] > T;
+        if (key[i] == T && take_eq > 0) {
+          take = true;
+          --take_eq;
+        }
+        if (take && out_pos < k) {
+          opos[out_pos] = pv[j];
+          if (okey) okey[out_pos] = key[i];
+          else if (oscore) oscore[out_pos] = key_float(key[i]);
+          ++out_pos;
+        }
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < KPT; ++i) {
     bool take = key[i] > T;
