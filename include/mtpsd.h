@@ -216,8 +216,8 @@ int mtpsd_indexer_topk_noalloc(const mtpsd_indexer_args* args, void* stream);
  *   MTPSD_STATUS_INDEX_RANGE when a length exceeds it)
  *   -> out_idx [R, topk] (ascending positions, -1 padded), out_score nullable.
  * Rows of up to 40960 keys take one CTA each (16-byte aligned rows, ld % 4 == 0).
- * Longer rows are split: one CTA per 32768-key segment selects that segment's
- * exact top-k, and merge levels over groups of 32768/topk such lists follow
+ * Longer rows are split: one CTA per 16384-key segment selects that segment's
+ * exact top-k, and merge levels over groups of 16384/topk such lists follow
  * (one launch per level, mtpsd_topk_launch_count); their candidate lists live
  * in the workspace (mtpsd_topk_workspace_size, 256-byte aligned; 0 bytes when
  * max_len <= 40960).  Unaligned score rows take a one-CTA-per-row radix kernel.

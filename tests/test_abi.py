@@ -128,9 +128,10 @@ def test_workspace_queries(native):
     ws = lib.mtpsd_indexer_topk_workspace_size(32, 192, 8198, 2048)
     assert ws >= 192 * 8198 * 4
     assert lib.mtpsd_topk_workspace_size(192, 40960, 2048) == 0
-    # split path: two list buffers (level 1: 4 lists of 2048, level 2 is final) of 8-byte entries
-    assert lib.mtpsd_topk_workspace_size(10, 100000, 2048) == 10 * 4 * 2048 * 8
-    assert lib.mtpsd_topk_workspace_size(10, 600000, 2048) == 10 * 19 * 2048 * 8 + 10 * 2 * 2048 * 8
+    # split path: two list buffers of 8-byte entries (16384-key segments; 100000 keys: level 1 has 7 lists
+    # of 2048, level 2 is final; 600000 keys: 37 lists, then 5, then the final one)
+    assert lib.mtpsd_topk_workspace_size(10, 100000, 2048) == 10 * 7 * 2048 * 8
+    assert lib.mtpsd_topk_workspace_size(10, 600000, 2048) == 10 * 37 * 2048 * 8 + 10 * 5 * 2048 * 8
     plan = lib.mtpsd_indexer_topk_plan_bytes(32, 192)
     assert 0 < plan < 64 * 1024 and plan % 256 == 0
     # the workspace is the padded score matrix followed by the plan
@@ -148,12 +149,12 @@ def test_launch_count_queries(native):
     assert lib.mtpsd_indexer_topk_launch_count(64, 128, native.MTPSD_FP8_E4M3, 8198, 2048) in (2, 3)
     assert lib.mtpsd_indexer_topk_launch_count(64, 128, native.MTPSD_F32, 8198, 2048) == 2
     assert lib.mtpsd_indexer_topk_launch_count(48, 128, native.MTPSD_FP8_E4M3, 8198, 2048) == 2   # no tensor-core shape
-    # rows past 40960 keys: one launch per split level (32768-key segments, then merges of 16 lists)
+    # rows past 40960 keys: one launch per split level (16384-key segments, then merges of 8 lists of 2048)
     assert lib.mtpsd_topk_launch_count(40960, 2048) == 1
     assert lib.mtpsd_topk_launch_count(40961, 2048) == 2
-    assert lib.mtpsd_topk_launch_count(16 * 32768, 2048) == 2
-    assert lib.mtpsd_topk_launch_count(16 * 32768 + 1, 2048) == 3
-    assert lib.mtpsd_topk_launch_count(1 << 20, 4096) == 3            # 32 segments, merges of 8
+    assert lib.mtpsd_topk_launch_count(8 * 16384, 2048) == 2
+    assert lib.mtpsd_topk_launch_count(8 * 16384 + 1, 2048) == 3
+    assert lib.mtpsd_topk_launch_count(1 << 20, 4096) == 4            # 64 segments, merges of 4: 16, 4, 1
     assert lib.mtpsd_indexer_topk_launch_count(48, 128, native.MTPSD_F32, 100000, 2048) == 3
 
 

@@ -187,7 +187,7 @@ def test_share_gather(mt):
                                       (3000, 1, True), (4096, 4096, False), (9000, 4096, True),
                                       # one tail key per thread at 1024 threads, 32768+ equal keys in a row
                                       (33000, 2048, True), (37000, 2048, True), (33000, 2048, False),
-                                      # split rows: 32768-key segments, then merges of 32768/k lists
+                                      # split rows: 16384-key segments, then merges of 16384/k lists
                                       (262144, 2048, True), (1048576, 2048, True), (600000, 2048, False),
                                       (1048576, 4096, False), (100000, 7, True), (65536, 2048, True)])
 def test_topk_exact(mt, V, k, ties):
@@ -203,8 +203,8 @@ def test_topk_exact(mt, V, k, ties):
     lens[3] = min(V, k)
     lens[4] = 0
     if V > 40960:   # split rows whose last segment holds fewer than k keys
-        lens[5] = 32769
-        lens[6] = min(V, 2 * 32768 + k - 1)
+        lens[5] = 16385
+        lens[6] = min(V, 2 * 16384 + k - 1)
     ld = V + 4
     buf = np.zeros((R, ld), np.float32)
     buf[:, :V] = sc
