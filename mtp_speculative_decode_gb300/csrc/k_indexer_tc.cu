@@ -202,20 +202,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// (group, tile) cursor over the flattened work list
-struct Cursor {
-  int g, tile;
+// (group, tile) cursor over the flattened work list.  CACHE: the current group's tile count is kept in
+// a register, so advancing within a group touches no memory (one-row groups: a global load per tile in
+// every role's loop put its latency on each role's critical path); without it the count is reloaded
+// (the head-halves kernel, whose epilogue has no register to spare).
+template <bool CACHE>
+struct CursorT {
+  int g, tile, len;
   // called by all 32 lanes of a warp: the last g with g_tile0[g] <= it (which skips groups without
   // tiles), found with rounds of 32 parallel loads
   __device__ void start(const Params& p, int n_groups, int it) {
     g = request_of_row_warp((const uint32_t*)p.g_tile0, n_groups, (uint32_t)it);
     tile = it - p.g_tile0[g];
+    if (CACHE) len = p.g_tile0[g + 1] - p.g_tile0[g];
   }
   __device__ void next(const Params& p, int n_groups) {
     ++tile;
-    while (g + 1 <= n_groups - 1 && tile >= p.g_tile0[g + 1] - p.g_tile0[g]) {
-      tile -= p.g_tile0[g + 1] - p.g_tile0[g];
-      ++g;
+    if (CACHE) {
+      while (g + 1 <= n_groups - 1 && tile >= len) {
+        tile -= len;
+        ++g;
+        len = p.g_tile0[g + 1] - p.g_tile0[g];
+      }
+    } else {
+      while (g + 1 <= n_groups - 1 && tile >= p.g_tile0[g + 1] - p.g_tile0[g]) {
+        tile -= p.g_tile0[g + 1] - p.g_tile0[g];
+        ++g;
+      }
     }
   }
 };
@@ -394,7 +407,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
     int n_load = 0, gq = 0, cur_g = -1;
     int64_t cstart = 0, cur_vmax = 0;
     bool ok = true;
-    Cursor c;
+    CursorT<!SPLIT> c;
     c.start(p, n_groups, it0);
     // PAGED: this lane's box of a (group, tile): its page entry, loaded one tile ahead of its use
     const int sub = PAGED ? min(TILE_M, 1 << p.pg_shift) : TILE_M;
@@ -410,7 +423,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
       const int g = c.g;
       int32_t pe_next = -1;
       if (PAGED && it + 1 < it1) {
-        Cursor cn = c;
+        CursorT<!SPLIT> cn = c;
         cn.next(p, n_groups);
         pe_next = page_of(cn.g, cn.tile);
       }
@@ -495,7 +508,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
     // per key tile: half h (heads 32h .. 32h+31 of every row) into TMEM stage h, N = 32 x rows
     int n_cons = 0, gq = 0, cur_g = -1, nrows = 0;
     bool ok = true;
-    Cursor c;
+    CursorT<!SPLIT> c;
     c.start(p, n_groups, it0);
     for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups)) {
       const int g = c.g;
@@ -544,7 +557,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
     int u = 0;        // running unit (slot use) index
     int nchunk = 0;   // running MMA chunk index
     bool ok = true;
-    Cursor c;
+    CursorT<!SPLIT> c;
     c.start(p, n_groups, it0);
     for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups)) {
       const int g = c.g;
@@ -608,7 +621,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
     int cur_g = -1, nrows = 0, row0 = 0, n_tile = 0, ks_off = 0;
     int64_t vmax = 0, cstart = 0;
     bool ok = true;
-    Cursor c;
+    CursorT<!SPLIT> c;
     c.start(p, n_groups, it0);
     for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups), ++n_tile) {
       const int g = c.g;
@@ -705,7 +718,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_tc_kernel(const __grid_con
     int u = 0, nchunk = 0;   // running unit and MMA chunk indices (the MMA warp's chunking, replayed)
     int64_t vmax = 0, cstart = 0;
     bool ok = true;
-    Cursor c;
+    CursorT<!SPLIT> c;
     c.start(p, n_groups, it0);
     for (int it = it0; it < it1 && ok; ++it, c.next(p, n_groups), ++n_tile) {
       const int g = c.g;
