@@ -23,6 +23,7 @@ bool make_tma_store_map(void* map, bool f32, const void* base, int rank, const u
 bool make_tma_2d(void* map, int dtype_u8_or_bf16, const void* base, uint64_t inner_elems, uint64_t rows,
                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, bool l2_256);
 bool make_tma_1d_f32(void* map, const void* base, uint64_t n_elems, uint32_t box_elems);
+bool make_tma_2d_plain_u8(void* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes);
 
 int launch_merge_tokens(const int64_t* prompt, int64_t S, const uint32_t* po, const int64_t* draft,
                         int B, int K, int64_t* out, uint32_t* mo, cudaStream_t st);

@@ -548,40 +548,55 @@ static bool use_tc(int H, int dtype) {
   return mla_tc_supported(q);
 }
 
-// splits of the selected list for the kernel that will run
-static MlaSplit plan_split(int R, int H, int n_idx, int n_append, int dtype) {
-  if (use_tc(H, dtype)) {
-    int64_t total = (int64_t)n_idx + n_append;
-    MlaSplit sp;
-    sp.per_split = mla_tc_per_split(R, H, total);
-    sp.n_splits = total > 0 ? (int)ceil_div(total, sp.per_split) : 1;
-    return sp;
-  }
-  return choose_split(R, H, n_idx, n_append, dtype);
+// splits of the selected list for the tensor-core kernel
+static MlaSplit plan_split_tc(int R, int H, int n_idx, int n_append) {
+  int64_t total = (int64_t)n_idx + n_append;
+  MlaSplit sp;
+  sp.per_split = mla_tc_per_split(R, H, total);
+  sp.n_splits = total > 0 ? (int)ceil_div(total, sp.per_split) : 1;
+  return sp;
+}
+
+// splits of the selected list for the kernel that will run: the tensor-core kernel's own plan, or the
+// portable kernels' (at most MLA_MAX_SPLIT positions per split)
+static MlaSplit plan_split(int R, int H, int n_idx, int n_append, int dtype, bool tc) {
+  return tc ? plan_split_tc(R, H, n_idx, n_append) : choose_split(R, H, n_idx, n_append, dtype);
 }
 
 int mla_launch_count(int R, int H, int n_idx, int n_append, int dtype) {
   if (R <= 0) return 0;
-  MlaSplit sp = plan_split(R, H, n_idx, n_append, dtype);
+  const bool tc = use_tc(H, dtype);
+  MlaSplit sp = plan_split(R, H, n_idx, n_append, dtype, tc);
   if (sp.n_splits <= 1) return 1;
-  if (dtype == MTPSD_BF16 && use_tc(H, dtype) && mla_tc_fuse(sp.n_splits)) return 1;
+  if (tc && mla_tc_fuse(sp.n_splits)) return 1;
   return 2;
 }
 
-size_t mla_workspace_bytes(int R, int H, int n_idx, int n_append, int dtype) {
-  MlaSplit sp = plan_split(R, H, n_idx, n_append, dtype);
+static size_t split_bytes(int R, int H, const MlaSplit& sp) {
   if (sp.n_splits == 1) return 0;
   size_t rh = (size_t)R * H * sp.n_splits;
   return rh * MLA_DV * sizeof(float) + rh * 4 * sizeof(float) + 256;   // up to two (max, sum) pairs per split
 }
 
+// Covers both kernels: a call whose buffers miss the tensor-core kernel's alignment runs the portable one.
+size_t mla_workspace_bytes(int R, int H, int n_idx, int n_append, int dtype) {
+  size_t n = split_bytes(R, H, plan_split(R, H, n_idx, n_append, dtype, false));
+  if (use_tc(H, dtype)) {
+    const size_t t = split_bytes(R, H, plan_split(R, H, n_idx, n_append, dtype, true));
+    if (t > n) n = t;
+  }
+  return n;
+}
+
 int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
   if (p.R == 0) return MTPSD_OK;
-  MlaSplit sp = plan_split(p.R, p.H, p.n_idx, p.n_append, p.dtype);
+  // the kernel is decided once, and the split plan is that kernel's
+  const bool tc = mla_tc_supported(p);
+  MlaSplit sp = plan_split(p.R, p.H, p.n_idx, p.n_append, p.dtype, tc);
   float* part_o = nullptr;
   float* part_ml = nullptr;
   if (sp.n_splits > 1) {
-    size_t need = mla_workspace_bytes(p.R, p.H, p.n_idx, p.n_append, p.dtype);
+    size_t need = split_bytes(p.R, p.H, sp);
     if (!p.ws || p.ws_bytes < need) {
       set_error("sparse_mla_decode: workspace of %zu bytes needed, %zu given", need, p.ws_bytes);
       return MTPSD_EWORKSPACE;
@@ -589,7 +604,7 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
     part_o = (float*)p.ws;
     part_ml = part_o + (size_t)p.R * p.H * sp.n_splits * MLA_DV;
   }
-  if (p.dtype == MTPSD_BF16 && mla_tc_supported(p)) {
+  if (tc) {   // bf16 or the FP8 latent rows (dequantized by the producers)
     bool combined = false;
     int rc = launch_sparse_mla_tc(p, sp.n_splits, (int)sp.per_split, part_o, part_ml, st, &combined);
     if (rc) return rc;

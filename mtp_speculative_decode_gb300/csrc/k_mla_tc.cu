@@ -69,6 +69,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -108,6 +109,20 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr unsigned long long WAIT_LIMIT_NS = mbar::DEFAULT_LIMIT_NS;
 constexpr int MAX_FUSED_SPLITS_K = 4;     // splits of a row that share one cluster and merge in the kernel
+// FP8 latent rows (656 bytes: 512 E4M3 codes, 4 float32 block scales, 64 bf16 rope values).  The ring
+// then has three pair buffers, and the fourth pair's space holds each producer warp's staging ring of
+// FD tiles: per tile its 8 rows' codes for this CTA's 256 dims ([group][half][4 rows][128 B]), their
+// 16-byte scale records ([group][4 rows][16 B], each group at a 128-byte boundary) and, on rank 0,
+// their rope bytes ([group][4 rows][128 B]).
+constexpr int FP8_ROW = 656;
+constexpr int FD = 3;
+constexpr int F_CODES = 2 * 2 * 512;
+constexpr int F_SCL = 2 * 128;
+constexpr int F_ROPE = 2 * 512;
+constexpr int F_TILE = F_CODES + F_SCL + F_ROPE;
+constexpr int OFF_F = OFF_C + 3 * PAIR_STRIDE;           // the fourth pair buffer
+static_assert(4 * FD * F_TILE + 4 * FD * 8 <= PAIR_STRIDE && (F_TILE % 128) == 0 && (OFF_F % 1024) == 0,
+              "FP8 staging fits the fourth pair buffer");
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct Params {
@@ -381,16 +396,22 @@ __device__ __noinline__ void merge_splits(const Params& p, int r, int h0, int hl
 }
 
 // PAGED: positions resolve to pool rows through the block table (the producers look a tile ahead).
-template <bool PAGED>
+// FP8KV: the latent pool holds 656-byte FP8 rows; tm_lat is a uint8 map of them with 128-byte boxes and
+// tm_sc one with 16-byte boxes (the scale records); the producers dequantize into the pair buffers.
+template <bool PAGED, bool FP8KV>
 __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                                                                    const __grid_constant__ CUtensorMap tm_q,
-                                                                   const __grid_constant__ CUtensorMap tm_st, Params p) {
+                                                                   const __grid_constant__ CUtensorMap tm_st,
+                                                                   const __grid_constant__ CUtensorMap tm_sc, Params p) {
+  constexpr int NPAIR_K = FP8KV ? 3 : NPAIR;   // pair buffers of the ring
+  constexpr int NSTAGE_K = 2 * NPAIR_K;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + OFF_BAR);
   uint64_t* c_full = bars;                 // per tile stage: the producers' bytes landed
-  uint64_t* c_empty = bars + NSTAGE;       // per pair buffer: its PV completed
+  uint64_t* c_empty = bars + NSTAGE;       // per pair buffer: its PV completed (NPAIR_K used)
   uint64_t* s_full = c_empty + NPAIR;      // partial scores of the pair in score buffer s are in TMEM
+  uint64_t* f_full = (uint64_t*)(sm + OFF_F + 4 * FD * F_TILE);   // FP8KV: [producer][FD] staging tiles landed
   uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;
   uint64_t* x_full = pv_done + 2;          // [slot][half]: half of receive slot s holds the other CTA's scores
@@ -422,6 +443,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSTAGE; ++i) mbar_init(&c_full[i], N_PROD);
     for (int i = 0; i < NPAIR; ++i) mbar_init(&c_empty[i], 1);
+    if (FP8KV)
+      for (int i = 0; i < 4 * FD; ++i) mbar_init(&f_full[i], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
@@ -491,8 +514,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     for (int P = 0; P < n_pairs && ok; ++P) {
       const int s = P & 1;
       const uint32_t par = (P >> 1) & 1;
-      const int st0 = 2 * (P % NPAIR);
-      const uint32_t cpar = (P / NPAIR) & 1;
+      const int st0 = 2 * (P % NPAIR_K);
+      const uint32_t cpar = (P / NPAIR_K) & 1;
       if (h == 0) {
         mbar_arrive_expect_tx(&x_full[2 * s], XHALF_BYTES);
         mbar_arrive_expect_tx(&x_full[2 * s + 1], XHALF_BYTES);
@@ -790,6 +813,102 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       s_next = n_tiles > 0 ? tile_pos(0, rq[0]) : -1;
       pg_next = page_entry(p, breq, s_next);
     }
+    if constexpr (FP8KV) {
+      // ---- FP8 rows: gather this warp's 8 rows of tile ti into staging slot ti % FD (FD tiles ahead of
+      // the dequantization), then per tile t: dequantize them into the pair buffer, publish the validity
+      // bits and arrive on the tile's c_full (one arrival per producer warp).
+      uint8_t* fstg = sm + OFF_F + pw * FD * F_TILE;
+      uint64_t* ffull = f_full + pw * FD;
+      uint32_t mq[FD];
+      int ti = 0, done = 0;
+      bool ok = true;
+      auto issue_tile = [&](int tt) {
+        const int32_t craw = rq[0];
+#pragma unroll
+        for (int i = 0; i + 1 < PF; ++i) rq[i] = rq[i + 1];
+        rq[PF - 1] = tt + PF < n_tiles ? raw(j0 + (int64_t)(tt + PF) * NT + my_pos) : 0;
+        const int64_t sp = tile_pos(tt, craw);
+        const int64_t row = entry_row<PAGED>(p, sp, base, PAGED ? page_entry(p, breq, sp) : -1);
+        const bool valid = row >= 0 && lane < 8;
+        mq[tt % FD] = __reduce_or_sync(0xffffffffu, valid ? (1u << my_pos) : 0u);
+        const int yv = row >= 0 ? (int)row : oob;
+        int y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = __shfl_sync(0xffffffffu, yv, i);
+        const int k = tt % FD;
+        const uint32_t sb = saddr(fstg + k * F_TILE);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&ffull[k], (uint32_t)(F_CODES + 2 * 64 + (rank == 0 ? F_ROPE : 0)));
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi) {
+            const int* yg = y + 4 * gi;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+              tma_gather4(sb + (gi * 2 + hf) * 512, &tm_lat, (int)rank * 256 + hf * 128, yg[0], yg[1], yg[2], yg[3],
+                          &ffull[k]);
+            tma_gather4(sb + F_CODES + gi * 128, &tm_sc, 512, yg[0], yg[1], yg[2], yg[3], &ffull[k]);
+            if (rank == 0)
+              tma_gather4(sb + F_CODES + F_SCL + gi * 512, &tm_lat, 528, yg[0], yg[1], yg[2], yg[3], &ffull[k]);
+          }
+        }
+        __syncwarp();
+      };
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        while (ti < n_tiles && ti < t + FD) issue_tile(ti++);
+        const int k = t % FD;
+        ok = __all_sync(0xffffffffu, mbar_wait(&ffull[k], (t / FD) & 1, abort_flag, p.status));
+        const int st = t % NSTAGE_K, P = t >> 1, q = P % NPAIR_K, R = P / NPAIR_K;
+        if (ok && R > 0) ok = __all_sync(0xffffffffu, mbar_wait(&c_empty[q], (R - 1) & 1, abort_flag, p.status));
+        if (!ok) break;
+        const uint8_t* sb = fstg + k * F_TILE;
+        uint8_t* pair = sm + OFF_C + q * PAIR_STRIDE;
+        // One row half (128 codes, contiguous in staging) per step: lane l takes codes 4l .. 4l+3, so the
+        // staging reads are conflict-free; they land as 8 bytes of bf16 in chunk (2 half + l / 16), 16-byte
+        // slot (l % 16) / 2, at the 128-byte swizzle the MMAs read.
+#pragma unroll 4
+        for (int it = 0; it < 16; ++it) {
+          const int row8 = it >> 1, hf = it & 1, gi = row8 >> 2, rig = row8 & 3;
+          const int pos = (t & 1) * NT + 4 * (pw + 4 * gi) + rig;   // position within the pair
+          const uint32_t w4 = *(const uint32_t*)(sb + (gi * 2 + hf) * 512 + rig * 128 + lane * 4);
+          const float sc = *(const float*)(sb + F_CODES + gi * 128 + rig * 16 + ((int)rank * 2 + hf) * 4);
+          uint32_t ow[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w4 >> (16 * e)) & 0xffffu);
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);   // exact
+            const float2 f = __half22float2(*(const __half2*)&hr);
+            const __nv_bfloat162 bv = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+            ow[e] = *(const uint32_t*)&bv;
+          }
+          const int cc = hf * 2 + (lane >> 4), kk = (lane & 15) >> 1;
+          *(uint2*)(pair + cc * CHUNK_BYTES + pos * 128 + ((kk ^ (pos & 7)) << 4) + (lane & 1) * 8) = make_uint2(ow[0], ow[1]);
+        }
+        if (rank == 0) {   // rope bytes (bf16 already) into chunk 4, swizzled
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int id = lane * 2 + e, row8 = id >> 3, kk = id & 7, gi = row8 >> 2, rig = row8 & 3;
+            const int pos = (t & 1) * NT + 4 * (pw + 4 * gi) + rig;
+            *(uint4*)(pair + 4 * CHUNK_BYTES + pos * 128 + ((kk ^ (pos & 7)) << 4)) =
+                *(const uint4*)(sb + F_CODES + F_SCL + gi * 512 + rig * 128 + kk * 16);
+          }
+        }
+        // the MMAs (async proxy) read what these generic stores wrote, and the next gathers into this
+        // staging slot come after its reads
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mask_s[st * 4 + pw] = mq[k];
+          mbar_arrive(&c_full[st]);
+        }
+        __syncwarp();
+        done = t + 1;
+      }
+      if (*abort_flag && lane == 0) {   // wait (bounded) for this warp's staging copies still in flight
+        volatile int dummy = 0;
+        for (int tt = done; tt < ti; ++tt) mbar_wait(&ffull[tt % FD], (tt / FD) & 1, &dummy, p.status);
+        if (rank == 0 && pw == 0) mbar_wait(q_ready, 0, &dummy, p.status);
+      }
+    } else {
     int issued = 0;
     for (int t = 0; t < n_tiles; ++t) {
       int64_t s_cur;
@@ -809,7 +928,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
         rq[PF - 1] = t + PF < n_tiles ? raw(j0 + (int64_t)(t + PF) * NT + my_pos) : 0;
         s_cur = craw;   // resolved after the wait below, as its position
       }
-      const int st = t % NSTAGE, P = t >> 1, q = P % NPAIR, R = P / NPAIR;
+      const int st = t % NSTAGE_K, P = t >> 1, q = P % NPAIR_K, R = P / NPAIR_K;
       if (R > 0 && !__all_sync(0xffffffffu, mbar_wait(&c_empty[q], (R - 1) & 1, abort_flag, p.status))) break;
       if (!PAGED) s_cur = tile_pos(t, (int32_t)s_cur);
       const int64_t row = entry_row<PAGED>(p, s_cur, base, pg_cur);
@@ -838,12 +957,13 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     }
     if (*abort_flag && lane == 0) {   // wait (bounded) for this CTA's copies still in flight
       volatile int dummy = 0;
-      for (int st = 0; st < NSTAGE; ++st) {
-        const int n = issued / NSTAGE + (st < issued % NSTAGE ? 1 : 0);
+      for (int st = 0; st < NSTAGE_K; ++st) {
+        const int n = issued / NSTAGE_K + (st < issued % NSTAGE_K ? 1 : 0);
         if (n > 0) mbar_wait(&c_full[st], (n - 1) & 1, &dummy, p.status);
       }
       if (rank == 0 && pw == 0) mbar_wait(q_ready, 0, &dummy, p.status);
     }
+    }   // bf16 rows
   } else {
     // ------------------------------------------------ MMA issue (warp 12; one elected lane issues)
     bool ok = __all_sync(0xffffffffu, mbar_wait(q_ready, 0, abort_flag, p.status));
@@ -857,8 +977,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     // published P.  The waits suspend the warp (try_wait) instead of polling, so the softmax warp that
     // shares this scheduler keeps its issue slots.
     auto issue_qk = [&](int nq) -> bool {
-      const int bq = nq % NPAIR;
-      const uint32_t par = (nq / NPAIR) & 1;
+      const int bq = nq % NPAIR_K;
+      const uint32_t par = (nq / NPAIR_K) & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&c_full[2 * bq], par, abort_flag, p.status) &&
                                        mbar_wait(&c_full[2 * bq + 1], par, abort_flag, p.status)))
         return false;
@@ -889,7 +1009,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       const int sp = np & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&p_full[sp], (np >> 1) & 1, abort_flag, p.status))) break;
       fence_after();
-      const int bp = np % NPAIR;
+      const int bp = np % NPAIR_K;
       const uint64_t vd = v_desc0 + (uint64_t)((bp * PAIR_STRIDE) >> 4);
       if (elect_one()) {
 #pragma unroll
@@ -929,7 +1049,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
 }  // namespace mtc
 
 bool mla_tc_supported(const MlaPlan& p) {
-  if (p.dtype != MTPSD_BF16 || p.d_latent != 576 || p.d_v != 512) return false;
+  if ((p.dtype != MTPSD_BF16 && p.dtype != MTPSD_FP8_DS_MLA) || p.d_latent != 576 || p.d_v != 512) return false;
   if (p.H % mtc::HG != 0) return false;
   if (cc_major() != 10) return false;
   const char* env = getenv("MTPSD_MLA");
@@ -960,10 +1080,11 @@ cudaLaunchConfig_t mla_tc_config(dim3 grid, int cluster_z, cudaStream_t st, cuda
   return cfg;
 }
 bool mla_tc_prepare() {
-  static std::atomic<uint64_t> attr{0};
-  static std::atomic<uint64_t> attr_paged{0};
-  return set_smem_limit_once(mtc::sparse_mla_tc_kernel<false>, mtc::SMEM_BYTES, attr) &&
-         set_smem_limit_once(mtc::sparse_mla_tc_kernel<true>, mtc::SMEM_BYTES, attr_paged);
+  static std::atomic<uint64_t> attr[4];
+  return set_smem_limit_once(mtc::sparse_mla_tc_kernel<false, false>, mtc::SMEM_BYTES, attr[0]) &&
+         set_smem_limit_once(mtc::sparse_mla_tc_kernel<true, false>, mtc::SMEM_BYTES, attr[1]) &&
+         set_smem_limit_once(mtc::sparse_mla_tc_kernel<false, true>, mtc::SMEM_BYTES, attr[2]) &&
+         set_smem_limit_once(mtc::sparse_mla_tc_kernel<true, true>, mtc::SMEM_BYTES, attr[3]);
 }
 // CTAs of this kernel that run at once with clusters of 2 x cluster_z CTAs (cached per device; -1 in
 // the cache stands for "none fit").
@@ -979,7 +1100,7 @@ int mla_tc_resident_ctas(int cluster_z) {
   cudaLaunchAttribute attrs[1];
   cudaLaunchConfig_t cfg = mla_tc_config(dim3(1, 2, cluster_z), cluster_z, 0, attrs);
   if (mla_tc_prepare() &&
-      cudaOccupancyMaxActiveClusters(&clusters, (void*)mtc::sparse_mla_tc_kernel<false>, &cfg) == cudaSuccess &&
+      cudaOccupancyMaxActiveClusters(&clusters, (void*)mtc::sparse_mla_tc_kernel<false, false>, &cfg) == cudaSuccess &&
       clusters > 0)
     n = 2 * cluster_z * clusters;
   else
@@ -1033,7 +1154,8 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
   k.n_splits = n_splits; k.per_split = per_split; k.status = p.status;
   k.fused_combine = mla_tc_fuse(n_splits) ? 1 : 0;
   if (combined) *combined = k.fused_combine != 0;
-  alignas(64) CUtensorMap tm_lat, tm_q, tm_st;
+  alignas(64) CUtensorMap tm_lat, tm_q, tm_st, tm_sc;
+  const bool fp8 = p.dtype == MTPSD_FP8_DS_MLA;
   // epilogue stores: boxes of 32 heads x 128 bytes, into out [R*H, 512] bf16 or into the split
   // partials [R*H, splits, 512] float32
   const uint64_t rh = (uint64_t)p.R * p.H;
@@ -1044,8 +1166,13 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
   const uint32_t po_box[3] = {32, 1, 32};
   const bool st_ok = n_splits == 1 ? make_tma_store_map(&tm_st, false, p.out, 2, out_dims, out_strides, out_box)
                                    : make_tma_store_map(&tm_st, true, part_o, 3, po_dims, po_strides, po_box);
-  if (!st_ok || !make_tma_2d(&tm_lat, 1, p.latent, DL, (uint64_t)p.pool, DL * 2, 64, 1, false) ||
-      !make_tma_2d(&tm_q, 1, p.q, DL, (uint64_t)p.R * p.H, DL * 2, 64, HG, true)) {
+  // latent gathers: bf16 rows in 64-value (128-byte) boxes, swizzled for the MMAs; FP8 rows as bytes
+  // without swizzle, in 128-byte boxes (codes, rope) and 16-byte boxes (the scale records)
+  const bool lat_ok = fp8 ? (make_tma_2d_plain_u8(&tm_lat, p.latent, FP8_ROW, (uint64_t)p.pool, 128) &&
+                             make_tma_2d_plain_u8(&tm_sc, p.latent, FP8_ROW, (uint64_t)p.pool, 16))
+                          : make_tma_2d(&tm_lat, 1, p.latent, DL, (uint64_t)p.pool, DL * 2, 64, 1, false);
+  if (!fp8) tm_sc = tm_lat;   // unused
+  if (!st_ok || !lat_ok || !make_tma_2d(&tm_q, 1, p.q, DL, (uint64_t)p.R * p.H, DL * 2, 64, HG, true)) {
     set_error("sparse_mla: cuTensorMapEncodeTiled failed");
     return MTPSD_ECUDA;
   }
@@ -1058,8 +1185,13 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see launch_k()
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 2;
-  cudaError_t e = p.pg.bt ? cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<true>, tm_lat, tm_q, tm_st, k)
-                           : cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<false>, tm_lat, tm_q, tm_st, k);
+  cudaError_t e;
+  if (fp8)
+    e = p.pg.bt ? cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<true, true>, tm_lat, tm_q, tm_st, tm_sc, k)
+                : cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<false, true>, tm_lat, tm_q, tm_st, tm_sc, k);
+  else
+    e = p.pg.bt ? cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<true, false>, tm_lat, tm_q, tm_st, tm_sc, k)
+                : cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<false, false>, tm_lat, tm_q, tm_st, tm_sc, k);
   if (e != cudaSuccess) {
     set_error("sparse_mla_tc: launch failed: %s", cudaGetErrorString(e));
     return MTPSD_ECUDA;

@@ -39,6 +39,21 @@ bool make_tma_2d(void* map, int dtype_u8_or_bf16, const void* base, uint64_t inn
   return r == CUDA_SUCCESS;
 }
 
+// Rows of row_bytes uint8 values as a [rows, row_bytes] tensor map without swizzle, for one-row boxes of
+// box_bytes bytes (tile::gather4 loads; box_bytes and row_bytes multiples of 16).
+bool make_tma_2d_plain_u8(void* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {box_bytes, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn((CUtensorMap*)map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Float32 vector as a [1, n_elems] tensor map without swizzle (rank 2 with a single row, so the
 // encoding has a stride to check; box of box_elems x 1, box_elems * 4 a multiple of 16 bytes; a copy's
 // start coordinate must be a multiple of 4 elements).  Elements past n_elems read as 0.
