@@ -581,10 +581,15 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       }
       if (!ok) break;
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      if (mt > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mt > -INFINITY)) {
-        // new reference max for this head; rescale what O already holds
-        if (m_ref > -INFINITY) {
-          const float alpha = ex2(m_ref - mt);
+      // A head whose max grew past the reference takes a new one.  The decision is made per warp: the
+      // TMEM loads and stores below are warp-collective, so every thread of a warp in which any head
+      // moves runs them (the others keep their reference and scale O by 1).
+      const bool grow = mt > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mt > -INFINITY);
+      if (__any_sync(0xffffffffu, grow)) {
+        const float m_new = grow ? mt : m_ref;
+        const bool scale_o = grow && m_ref > -INFINITY;   // O already holds this head's earlier pairs
+        if (__any_sync(0xffffffffu, scale_o)) {
+          const float alpha = scale_o ? ex2(m_ref - m_new) : 1.f;
           // O must not be touched while the previous PV is still accumulating
           mbar_wait(&pv_done[(P - 1) & 1], ((P - 1) >> 1) & 1, abort_flag, p.status);
           fence_after();
@@ -600,16 +605,17 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
           }
           tm_wait_st();
         }
-        m_ref = mt;
-        // this pair's exponentials again, against the new reference
+        m_ref = m_new;
+        // this pair's exponentials again, against the (possibly) new reference
+        const float mo1 = m_ref == -INFINITY ? 0.f : m_ref;
 #pragma unroll
         for (int i = 0; i < 4; ++i) psum[i] = 0.f;
         if (full) {
-          half_pass(0, false, m_ref);
-          half_pass(1, false, m_ref);
+          half_pass(0, false, mo1);
+          half_pass(1, false, mo1);
         } else {
-          half_pass(0, true, m_ref);
-          half_pass(1, true, m_ref);
+          half_pass(0, true, mo1);
+          half_pass(1, true, mo1);
         }
       }
       // slot s may be written again (pair P+2) once all four warps have consumed it
