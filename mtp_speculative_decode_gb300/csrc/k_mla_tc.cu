@@ -5,6 +5,12 @@
 // head h, softmax attention over the selected latent rows c[s_j, 0:576] with
 // values c[s_j, 0:512].
 //
+// The latent rows are bf16 (1152 bytes), or the 656-byte FP8 rows of [P2]
+// "草稿层 KV 的账" (512 E4M3 codes in four blocks of 128 with float32 scales,
+// then the 64 rope values as bf16): the FP8 instantiation stages each
+// producer warp's rows in shared memory and dequantizes them into the same
+// bf16 operand layout (below, at the producers).
+//
 // A cluster of two CTAs owns (row, 128-head group, split of the selected
 // list); the 128 heads are the MMA's M.  The two CTAs split the 576 latent
 // dims instead of duplicating them, so every selected row is gathered once:
