@@ -408,7 +408,11 @@ int mtpsd_kv_writeback_slots(const void* src_latent, const uint8_t* src_idxk, co
  * position without a slot reads as zero keys (score 0 x its scale: 0) in the
  * indexer and is skipped in the attention, both flagged
  * MTPSD_STATUS_ROW_RANGE.  Everything else is as the contiguous calls,
- * including workspaces and launch counts.  paged NULL = the contiguous call. */
+ * including workspaces and launch counts.  The tensor-core indexer reads
+ * pages of at least 8 tokens (a 128-position key tile as page-sized TMA
+ * boxes) when the pool is a whole number of pages; smaller pages take the
+ * CUDA-core score kernel, one launch fewer than
+ * mtpsd_indexer_topk_launch_count.  paged NULL = the contiguous call. */
 int mtpsd_indexer_topk_paged(const mtpsd_indexer_args* args, const mtpsd_paged_kv* paged, void* stream);
 int mtpsd_indexer_scores_paged(const mtpsd_indexer_args* args, const mtpsd_paged_kv* paged, void* stream);
 int mtpsd_sparse_mla_decode_paged(const mtpsd_mla_args* args, const mtpsd_paged_kv* paged, void* stream);
