@@ -274,9 +274,13 @@ size_t mtpsd_sparse_mla_workspace_size(int32_t R, int32_t n_heads, int32_t n_idx
                                        int32_t dtype);
 /* Kernel launches one mtpsd_sparse_mla_decode call with these sizes makes on the current device: 1, or 2
  * when the selected list is split and the split partials are merged by a second kernel (they are merged
- * inside the first when the splits of a row fit one thread-block cluster).  The count assumes the
- * tensor-core kernel, which needs q, latent, out and workspace 16-byte aligned (TMA loads and stores);
- * other calls run the portable kernel.  0 for sizes that launch nothing. */
+ * inside the first when the splits of a row fit one thread-block cluster).  With many rows of bf16
+ * latent (where a measured cost model favours it; environment MTPSD_MLA_PERSIST=0 turns it off, =1
+ * forces it) the tensor-core kernel runs persistently, one cluster per pair of SMs, each taking an equal
+ * run of 64-position pairs across rows; a row cut between two clusters leaves float32 pieces in the
+ * workspace that a second kernel merges.  The count assumes the tensor-core kernel, which needs q,
+ * latent, out and workspace 16-byte aligned (TMA loads and stores); other calls run the portable
+ * kernel.  0 for sizes that launch nothing.  The workspace size covers every plan. */
 int32_t mtpsd_sparse_mla_launch_count(int32_t R, int32_t n_heads, int32_t n_idx, int32_t n_append, int32_t dtype);
 int mtpsd_sparse_mla_decode(const mtpsd_mla_args* args, void* stream);
 

@@ -91,9 +91,21 @@ int mla_tc_per_split(int R, int H, int64_t total);
 int mla_tc_ml_halves();
 bool mla_tc_fuse(int n_splits);
 int mla_launch_count(int R, int H, int n_idx, int n_append, int dtype);
-// Launches the tensor-core kernel; *combined tells whether it also merged the split partials.
+// Persistent launch of the tensor-core kernel over bf16 rows: `clusters` clusters of two CTAs each take
+// pq consecutive pairs of the flattened (row, head group, pair) list (ppr pairs per row and head group,
+// hgn head groups, tp pairs in total); `cut`: some row is split between clusters, which leaves float32
+// pieces in the workspace and adds the piece merge launch.
+struct MlaPersist {
+  int clusters, pq, ppr, hgn;
+  int64_t tp;
+  bool cut;
+};
+bool mla_tc_persist_plan(int R, int H, int64_t total, int dtype, MlaPersist* pl);
+size_t mla_tc_persist_bytes(const MlaPersist& pl);
+// Launches the tensor-core kernel; *combined tells whether it also merged the split partials.  With
+// pl: the persistent launch (and the piece merge), the pieces in part_o / part_ml.
 int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* part_o, float* part_ml,
-                         cudaStream_t st, bool* combined);
+                         cudaStream_t st, bool* combined, const MlaPersist* pl = nullptr);
 int launch_sparse_mla(const MlaPlan& p, cudaStream_t st);
 
 }  // namespace mtpsd

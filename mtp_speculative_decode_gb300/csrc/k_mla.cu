@@ -566,6 +566,8 @@ static MlaSplit plan_split(int R, int H, int n_idx, int n_append, int dtype, boo
 int mla_launch_count(int R, int H, int n_idx, int n_append, int dtype) {
   if (R <= 0) return 0;
   const bool tc = use_tc(H, dtype);
+  MlaPersist pl;
+  if (tc && mla_tc_persist_plan(R, H, (int64_t)n_idx + n_append, dtype, &pl)) return pl.cut ? 2 : 1;
   MlaSplit sp = plan_split(R, H, n_idx, n_append, dtype, tc);
   if (sp.n_splits <= 1) return 1;
   if (tc && mla_tc_fuse(sp.n_splits)) return 1;
@@ -584,6 +586,9 @@ size_t mla_workspace_bytes(int R, int H, int n_idx, int n_append, int dtype) {
   if (use_tc(H, dtype)) {
     const size_t t = split_bytes(R, H, plan_split(R, H, n_idx, n_append, dtype, true));
     if (t > n) n = t;
+    MlaPersist pl;
+    if (mla_tc_persist_plan(R, H, (int64_t)n_idx + n_append, dtype, &pl) && mla_tc_persist_bytes(pl) > n)
+      n = mla_tc_persist_bytes(pl);
   }
   return n;
 }
@@ -592,6 +597,15 @@ int launch_sparse_mla(const MlaPlan& p, cudaStream_t st) {
   if (p.R == 0) return MTPSD_OK;
   // the kernel is decided once, and the split plan is that kernel's
   const bool tc = mla_tc_supported(p);
+  MlaPersist pl;
+  if (tc && mla_tc_persist_plan(p.R, p.H, (int64_t)p.n_idx + p.n_append, p.dtype, &pl)) {
+    const size_t need = mla_tc_persist_bytes(pl);
+    if (need && (!p.ws || p.ws_bytes < need)) {
+      set_error("sparse_mla_decode: workspace of %zu bytes needed, %zu given", need, p.ws_bytes);
+      return MTPSD_EWORKSPACE;
+    }
+    return launch_sparse_mla_tc(p, 1, 0, nullptr, nullptr, st, nullptr, &pl);
+  }
   MlaSplit sp = plan_split(p.R, p.H, p.n_idx, p.n_append, p.dtype, tc);
   float* part_o = nullptr;
   float* part_ml = nullptr;

@@ -153,8 +153,58 @@ struct Params {
   int n_splits;
   int per_split;              // positions per split (multiple of NP)
   int fused_combine;          // the splits of a row share one cluster and merge their partials in-kernel
+  // Persistent launch: cluster c takes the pairs [c pq, min(tp, (c + 1) pq)) of the flattened list of
+  // (row, head group, pair) units, row by row; a row cut between clusters leaves one float32 piece per
+  // cluster (slot 0: the cluster's first unit, slot 1: its last) for the piece merge.
+  int pq;                     // pairs per cluster
+  int ppr;                    // pairs per (row, head group)
+  int hgn;                    // head groups, H / 128
+  int64_t tp;                 // pairs in total
   int32_t* status;
 };
+
+// One (row, head group) range of pairs that a cluster processes.
+struct Item {
+  int r, h0;                  // query row and first head
+  int64_t j0, j1;             // positions [j0, j1) of the row's list (selected, then appended)
+  int n_pairs;
+  int g0;                     // the CTA's running pair index of the first pair (ring and barrier phases)
+  int slot;                   // -1: the whole row (normalised output); else the piece slot of a cut row
+};
+
+template <bool PERSIST>
+__device__ __forceinline__ int n_items_of(const Params& p) {
+  if (!PERSIST) return 1;
+  const int64_t a0 = (int64_t)blockIdx.x * p.pq, a1 = min(p.tp, a0 + (int64_t)p.pq);
+  return a1 > a0 ? (int)((a1 - 1) / p.ppr - a0 / p.ppr + 1) : 0;
+}
+template <bool PERSIST>
+__device__ __forceinline__ Item item_of(const Params& p, int i) {
+  Item I;
+  const int64_t total = (int64_t)p.n_idx + p.n_append;
+  if (!PERSIST) {   // one (row, head group, split) per cluster
+    I.r = blockIdx.x;
+    I.h0 = (int)(blockIdx.y >> 1) * HG;
+    I.j0 = (int64_t)blockIdx.z * p.per_split;
+    I.j1 = min(total, I.j0 + (int64_t)p.per_split);
+    I.n_pairs = I.j1 > I.j0 ? (int)((I.j1 - I.j0 + NP - 1) / NP) : 0;   // a last half pair: zero rows
+    I.g0 = 0;
+    I.slot = -1;
+    return I;
+  }
+  const int64_t a0 = (int64_t)blockIdx.x * p.pq, a1 = min(p.tp, a0 + (int64_t)p.pq);
+  const int64_t u = a0 / p.ppr + i;
+  const int64_t ua = u * p.ppr, ub = ua + p.ppr;
+  const int64_t pa = max(a0, ua), pb = min(a1, ub);
+  I.r = (int)(u / p.hgn);
+  I.h0 = (int)(u % p.hgn) * HG;
+  I.j0 = (pa - ua) * NP;
+  I.j1 = min(total, (pb - ua) * NP);
+  I.n_pairs = (int)(pb - pa);
+  I.g0 = (int)(pa - a0);
+  I.slot = (pa == ua && pb == ub) ? -1 : (i == 0 ? 0 : 1);
+  return I;
+}
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(b)),
@@ -401,14 +451,57 @@ __device__ __noinline__ void merge_splits(const Params& p, int r, int h0, int hl
   }
 }
 
+// This CTA's 256 query dims of head h0 + h (thread = head = TMEM lane) -> TMEM columns [0,128) as bf16
+// pairs, then the thread's arrival on q_ready.  Two rounds of 16 loads of 16 bytes, each round's loads
+// in flight together.
+__device__ __forceinline__ void load_q_tmem(const Params& p, uint32_t taddr, int r, int h0, int h, uint32_t rank,
+                                            uint64_t* q_ready) {
+  const bool head_ok = (h0 + h) < p.H;
+  const uint4* src = (const uint4*)(p.q + ((int64_t)r * p.H + h0 + h) * DL + rank * QTM);
+#pragma unroll
+  for (int c2 = 0; c2 < QTM / 128; ++c2) {
+    uint4 x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = head_ok ? src[c2 * 16 + i] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t v[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 y = x[cc * 8 + i];
+        v[4 * i] = y.x; v[4 * i + 1] = y.y; v[4 * i + 2] = y.z; v[4 * i + 3] = y.w;
+      }
+      tm_st32(taddr + TM_Q + (2 * c2 + cc) * 32, v);
+    }
+  }
+  tm_wait_st();
+  fence_before();
+  mbar_arrive(q_ready);
+}
+// The lines of those query dims (and on rank 0 of the rope dims) into L2, ahead of load_q_tmem and the
+// rope copy.
+__device__ __forceinline__ void prefetch_q_l2(const Params& p, int r, int h0, int h, uint32_t rank) {
+  if (h0 + h >= p.H) return;
+  const char* row = (const char*)(p.q + ((int64_t)r * p.H + h0 + h) * DL);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + rank * QTM * 2 + k * 128));
+  if (rank == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 2 * QTM * 2));
+}
+
 // PAGED: positions resolve to pool rows through the block table (the producers look a tile ahead).
 // FP8KV: the latent pool holds 656-byte FP8 rows; tm_lat is a uint8 map of them with 128-byte boxes and
 // tm_sc one with 16-byte boxes (the scale records); the producers dequantize into the pair buffers.
-template <bool PAGED, bool FP8KV>
+// PERSIST: one cluster per pair of SMs, each working through its range of pairs item by item (Params):
+// every role keeps its running pair index across the items, so every ring slot and barrier phase
+// advances as within one row; the sender warps load the next item's queries once the last QK of the
+// previous item has completed, and the softmax warps write each item's O from registers (the gather
+// ring is busy with the next item's rows).
+template <bool PAGED, bool FP8KV, bool PERSIST>
 __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                                                                    const __grid_constant__ CUtensorMap tm_q,
                                                                    const __grid_constant__ CUtensorMap tm_st,
                                                                    const __grid_constant__ CUtensorMap tm_sc, Params p) {
+  static_assert(!(FP8KV && PERSIST), "the persistent launch takes bf16 rows");
   constexpr int NPAIR_K = FP8KV ? 3 : NPAIR;   // pair buffers of the ring
   constexpr int NSTAGE_K = 2 * NPAIR_K;
   extern __shared__ uint8_t smem_raw[];
@@ -436,15 +529,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   const uint32_t rank = crank & 1u;        // = the value half this CTA owns
   const uint32_t peer = crank ^ 1u;
   const int nch = rank == 0 ? 5 : 4;       // 64-dim chunks this CTA gathers
-  const int r = blockIdx.x;
-  const int hg = blockIdx.y >> 1;
   const int split = blockIdx.z;
-  const int h0 = hg * HG;
-  const int64_t total = (int64_t)p.n_idx + p.n_append;
-  const int64_t j0 = (int64_t)split * p.per_split;
-  const int64_t j1 = min(total, j0 + (int64_t)p.per_split);
-  const int n_pairs = j1 > j0 ? (int)((j1 - j0 + NP - 1) / NP) : 0;
-  const int n_tiles = 2 * n_pairs;        // a last half pair is filled with zero rows
+  const int n_items = n_items_of<PERSIST>(p);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSTAGE; ++i) mbar_init(&c_full[i], N_PROD);
@@ -485,28 +571,14 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   griddep_wait();
   griddep_launch_dependents();
   const uint32_t tmem = *tmem_slot;
-  const __nv_bfloat16* qrow = p.q + ((int64_t)r * p.H + h0) * DL;
 
   if (warp < 4) {
     // ------------------------------------------------ softmax / epilogue: thread = head
     const int h = threadIdx.x;                 // 0..127 = TMEM lane
-    const bool head_ok = (h0 + h) < p.H;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    {   // this CTA's 256 query dims -> TMEM columns [0,128) as bf16 pairs
-      const uint4* src = (const uint4*)(qrow + (int64_t)h * DL + rank * QTM);
-#pragma unroll
-      for (int c = 0; c < QTM / 64; ++c) {
-        uint32_t v[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint4 x = head_ok ? src[c * 8 + i] : make_uint4(0, 0, 0, 0);
-          v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
-        }
-        tm_st32(tmem + lane_off + TM_Q + c * 32, v);
-      }
-      tm_wait_st();
-      fence_before();
-      mbar_arrive(q_ready);
+    if (!PERSIST) {   // the queries of the one item (the persistent launch: the sender warps, per item)
+      const Item I0 = item_of<PERSIST>(p, 0);
+      load_q_tmem(p, tmem + lane_off, I0.r, I0.h0, h, rank, q_ready);
     }
     // receive slot layout: two halves (positions 0..31, 32..63) that arrive separately; head h's 32
     // fp16 scores of a half are 4 pieces of 16 bytes at h*64, piece c at (c ^ ((h >> 1) & 3)), so that
@@ -515,208 +587,257 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     const uint32_t xfree_peer = map_rank(saddr(x_free), peer);
     const uint32_t stgfree_peer = map_rank(saddr(stg_free), peer);
     const uint32_t swz = (uint32_t)((h >> 1) & 3);
-    float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int P = 0; P < n_pairs && ok; ++P) {
-      const int s = P & 1;
-      const uint32_t par = (P >> 1) & 1;
-      const int st0 = 2 * (P % NPAIR_K);
-      const uint32_t cpar = (P / NPAIR_K) & 1;
-      if (h == 0) {
-        mbar_arrive_expect_tx(&x_full[2 * s], XHALF_BYTES);
-        mbar_arrive_expect_tx(&x_full[2 * s + 1], XHALF_BYTES);
-      }
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s], par, abort_flag, p.status));
-      // the validity bits were written by the producers before they released the two tiles
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[st0], cpar, abort_flag, p.status));
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[st0 + 1], cpar, abort_flag, p.status));
-      if (!ok) break;
-      fence_after();
-      const uint32_t* m0 = mask_s + st0 * 4;
-      const uint32_t* m1 = mask_s + (st0 + 1) * 4;
-      const uint64_t mask = (uint64_t)(m0[0] | m0[1] | m0[2] | m0[3]) | ((uint64_t)(m1[0] | m1[1] | m1[2] | m1[3]) << 32);
-      // S = this CTA's partial (fp32, TMEM) + the other's (fp16, receive slot), in log2 units, and in the
-      // same pass p = 2^(S - m_ref) against the current reference max (lazy max: the reference moves only
-      // when a head's max grows by more than 2^RESCALE_LOG2, and then the pass runs again from TMEM and
-      // the slot, which stay intact until P is published and the slot released).  The two halves of the
-      // pair (positions 0..31, 32..63) are processed as they land.  The mask is the same for the whole
-      // CTA, so the branch is uniform; a pair without padding skips the per-position select.  Masked
-      // positions (-inf) give exact zeros.  The sum is taken over the fp32 values (their bf16 rounding
-      // in P is unbiased and below the output tolerance).
-      const bool full = mask == ~0ull;
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      float psum[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
-      auto half_pass = [&](const int half, const bool masked, const float mo) {
-        uint32_t sr[32];
-        tm_ld32(tmem + lane_off + TM_S0 + s * 64 + half * 32, sr);
-        tm_wait_ld();
-        const uint32_t xo = x_own + (uint32_t)s * XSLOT_BYTES + (uint32_t)half * XHALF_BYTES;
+    for (int it = 0; it < n_items && ok; ++it) {
+      const Item I = item_of<PERSIST>(p, it);
+      const int r = I.r, h0 = I.h0, n_pairs = I.n_pairs;
+      const bool head_ok = (h0 + h) < p.H;
+      float m_ref = -INFINITY, l = 0.f;
+      // P: the CTA's running pair index (ring slots and barrier phases)
+      for (int P = I.g0; P < I.g0 + n_pairs && ok; ++P) {
+        const int s = P & 1;
+        const uint32_t par = (P >> 1) & 1;
+        const int st0 = 2 * (P % NPAIR_K);
+        const uint32_t cpar = (P / NPAIR_K) & 1;
+        if (h == 0) {
+          mbar_arrive_expect_tx(&x_full[2 * s], XHALF_BYTES);
+          mbar_arrive_expect_tx(&x_full[2 * s + 1], XHALF_BYTES);
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s], par, abort_flag, p.status));
+        // the validity bits were written by the producers before they released the two tiles
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[st0], cpar, abort_flag, p.status));
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(&c_full[st0 + 1], cpar, abort_flag, p.status));
+        if (!ok) break;
+        fence_after();
+        const uint32_t* m0 = mask_s + st0 * 4;
+        const uint32_t* m1 = mask_s + (st0 + 1) * 4;
+        const uint64_t mask =
+            (uint64_t)(m0[0] | m0[1] | m0[2] | m0[3]) | ((uint64_t)(m1[0] | m1[1] | m1[2] | m1[3]) << 32);
+        // S = this CTA's partial (fp32, TMEM) + the other's (fp16, receive slot), in log2 units, and in the
+        // same pass p = 2^(S - m_ref) against the current reference max (lazy max: the reference moves only
+        // when a head's max grows by more than 2^RESCALE_LOG2, and then the pass runs again from TMEM and
+        // the slot, which stay intact until P is published and the slot released).  The two halves of the
+        // pair (positions 0..31, 32..63) are processed as they land.  The mask is the same for the whole
+        // CTA, so the branch is uniform; a pair without padding skips the per-position select.  Masked
+        // positions (-inf) give exact zeros.  The sum is taken over the fp32 values (their bf16 rounding
+        // in P is unbiased and below the output tolerance).
+        const bool full = mask == ~0ull;
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float psum[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[32];
+        auto half_pass = [&](const int half, const bool masked, const float mo) {
+          uint32_t sr[32];
+          tm_ld32(tmem + lane_off + TM_S0 + s * 64 + half * 32, sr);
+          tm_wait_ld();
+          const uint32_t xo = x_own + (uint32_t)s * XSLOT_BYTES + (uint32_t)half * XHALF_BYTES;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t px[4];
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(px[0]), "=r"(px[1]), "=r"(px[2]), "=r"(px[3])
-                       : "r"(xo + ((c ^ swz) << 4))
-                       : "memory");
+          for (int c = 0; c < 4; ++c) {
+            uint32_t px[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(px[0]), "=r"(px[1]), "=r"(px[2]), "=r"(px[3])
+                         : "r"(xo + ((c ^ swz) << 4))
+                         : "memory");
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j = 8 * c + 2 * i;   // within the half
-            const float2 o = f16x2_to_f32(px[i]);
-            float v0 = fmaf(__uint_as_float(sr[j]), p.sl2, o.x);
-            float v1 = fmaf(__uint_as_float(sr[j + 1]), p.sl2, o.y);
-            if (masked) {
-              v0 = ((mask >> (32 * half + j)) & 1ull) ? v0 : -INFINITY;
-              v1 = ((mask >> (32 * half + j + 1)) & 1ull) ? v1 : -INFINITY;
+            for (int i = 0; i < 4; ++i) {
+              const int j = 8 * c + 2 * i;   // within the half
+              const float2 o = f16x2_to_f32(px[i]);
+              float v0 = fmaf(__uint_as_float(sr[j]), p.sl2, o.x);
+              float v1 = fmaf(__uint_as_float(sr[j + 1]), p.sl2, o.y);
+              if (masked) {
+                v0 = ((mask >> (32 * half + j)) & 1ull) ? v0 : -INFINITY;
+                v1 = ((mask >> (32 * half + j + 1)) & 1ull) ? v1 : -INFINITY;
+              }
+              mx[i] = fmaxf(mx[i], fmaxf(v0, v1));
+              const float e0 = ex2(v0 - mo), e1 = ex2(v1 - mo);
+              pk[16 * half + (j >> 1)] = pack_bf16(e0, e1);
+              psum[i] += e0 + e1;
             }
-            mx[i] = fmaxf(mx[i], fmaxf(v0, v1));
-            const float e0 = ex2(v0 - mo), e1 = ex2(v1 - mo);
-            pk[16 * half + (j >> 1)] = pack_bf16(e0, e1);
-            psum[i] += e0 + e1;
+          }
+        };
+        const float mo0 = m_ref == -INFINITY ? 0.f : m_ref;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_full[2 * s + half], par, abort_flag, p.status));
+          if (!ok) break;
+          if (half == 1 && h == 0) mbar_arrive_remote(stgfree_peer);   // the other CTA may restage
+          if (full) half_pass(half, false, mo0);
+          else half_pass(half, true, mo0);
+        }
+        if (!ok) break;
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        // A head whose max grew past the reference takes a new one.  The decision is made per warp: the
+        // TMEM loads and stores below are warp-collective, so every thread of a warp in which any head
+        // moves runs them (the others keep their reference and scale O by 1).
+        const bool grow = mt > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mt > -INFINITY);
+        if (__any_sync(0xffffffffu, grow)) {
+          const float m_new = grow ? mt : m_ref;
+          const bool scale_o = grow && m_ref > -INFINITY;   // O already holds this head's earlier pairs
+          if (__any_sync(0xffffffffu, scale_o)) {
+            const float alpha = scale_o ? ex2(m_ref - m_new) : 1.f;
+            // O must not be touched while the previous PV is still accumulating
+            mbar_wait(&pv_done[(P - 1) & 1], ((P - 1) >> 1) & 1, abort_flag, p.status);
+            fence_after();
+            l *= alpha;
+#pragma unroll 1
+            for (int c = 0; c < DVH / 32; ++c) {
+              uint32_t o[32];
+              tm_ld32(tmem + lane_off + TM_O + c * 32, o);
+              tm_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tm_st32(tmem + lane_off + TM_O + c * 32, o);
+            }
+            tm_wait_st();
+          }
+          m_ref = m_new;
+          // this pair's exponentials again, against the (possibly) new reference
+          const float mo1 = m_ref == -INFINITY ? 0.f : m_ref;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) psum[i] = 0.f;
+          if (full) {
+            half_pass(0, false, mo1);
+            half_pass(1, false, mo1);
+          } else {
+            half_pass(0, true, mo1);
+            half_pass(1, true, mo1);
           }
         }
-      };
-      const float mo0 = m_ref == -INFINITY ? 0.f : m_ref;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_full[2 * s + half], par, abort_flag, p.status));
+        // slot s may be written again (pair P+2) once all four warps have consumed it
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(xfree_peer + (uint32_t)s * 8u);
+        l += (psum[0] + psum[1]) + (psum[2] + psum[3]);
+        // P overwrites the scores: the senders must have read them
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_read[s], par, abort_flag, p.status));
         if (!ok) break;
-        if (half == 1 && h == 0) mbar_arrive_remote(stgfree_peer);   // the other CTA may restage
-        if (full) half_pass(half, false, mo0);
-        else half_pass(half, true, mo0);
+        tm_st32(tmem + lane_off + TM_S0 + s * 64, pk);
+        tm_wait_st();
+        fence_before();
+        mbar_arrive(&p_full[s]);
       }
-      if (!ok) break;
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      // A head whose max grew past the reference takes a new one.  The decision is made per warp: the
-      // TMEM loads and stores below are warp-collective, so every thread of a warp in which any head
-      // moves runs them (the others keep their reference and scale O by 1).
-      const bool grow = mt > m_ref + RESCALE_LOG2 || (m_ref == -INFINITY && mt > -INFINITY);
-      if (__any_sync(0xffffffffu, grow)) {
-        const float m_new = grow ? mt : m_ref;
-        const bool scale_o = grow && m_ref > -INFINITY;   // O already holds this head's earlier pairs
-        if (__any_sync(0xffffffffu, scale_o)) {
-          const float alpha = scale_o ? ex2(m_ref - m_new) : 1.f;
-          // O must not be touched while the previous PV is still accumulating
-          mbar_wait(&pv_done[(P - 1) & 1], ((P - 1) >> 1) & 1, abort_flag, p.status);
-          fence_after();
-          l *= alpha;
+      // ------------------------------------------------ epilogue
+      if (ok && n_pairs > 0) {
+        const int last = I.g0 + n_pairs - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[last & 1], (last >> 1) & 1, abort_flag, p.status));
+      }
+      if (ok) fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if constexpr (PERSIST) {
+        // O leaves from registers (the gather ring already holds the next item's rows): each thread
+        // writes its head's 256 value dims, 512 contiguous bytes of bf16, or 1 KB of float32 for a piece
+        // of a cut row with the piece's (max, sum)
+        if (!ok) break;
+        const int64_t rh = (int64_t)r * p.H + h0 + h;
+        if (I.slot < 0) {
+          uint4* dst = (uint4*)(p.out + rh * DV + rank * DVH);
+#pragma unroll 1
+          for (int c = 0; c < DVH / 32; ++c) {
+            uint32_t o[32];
+            tm_ld32(tmem + lane_off + TM_O + c * 32, o);
+            tm_wait_ld();
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+            if (head_ok) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[c * 4 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            }
+          }
+          if (head_ok && rank == 0 && p.lse) p.lse[rh] = l > 0.f ? (m_ref + log2f(l)) / LOG2E : -INFINITY;
+        } else {
+          const int64_t pc = ((int64_t)blockIdx.x * 2 + I.slot) * HG + h;   // piece row of this head
+          uint4* dst = (uint4*)(p.part_o + pc * DV + rank * DVH);
 #pragma unroll 1
           for (int c = 0; c < DVH / 32; ++c) {
             uint32_t o[32];
             tm_ld32(tmem + lane_off + TM_O + c * 32, o);
             tm_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tm_st32(tmem + lane_off + TM_O + c * 32, o);
+            for (int q = 0; q < 8; ++q) dst[c * 8 + q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
           }
-          tm_wait_st();
+          float* ml = p.part_ml + (pc * 2 + rank) * 2;
+          ml[0] = l > 0.f ? m_ref : -INFINITY;
+          ml[1] = l;
         }
-        m_ref = m_new;
-        // this pair's exponentials again, against the (possibly) new reference
-        const float mo1 = m_ref == -INFINITY ? 0.f : m_ref;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) psum[i] = 0.f;
-        if (full) {
-          half_pass(0, false, mo1);
-          half_pass(1, false, mo1);
-        } else {
-          half_pass(0, true, mo1);
-          half_pass(1, true, mo1);
-        }
-      }
-      // slot s may be written again (pair P+2) once all four warps have consumed it
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(xfree_peer + (uint32_t)s * 8u);
-      l += (psum[0] + psum[1]) + (psum[2] + psum[3]);
-      // P overwrites the scores: the senders must have read them
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_read[s], par, abort_flag, p.status));
-      if (!ok) break;
-      tm_st32(tmem + lane_off + TM_S0 + s * 64, pk);
-      tm_wait_st();
-      fence_before();
-      mbar_arrive(&p_full[s]);
-    }
-    // ------------------------------------------------ epilogue
-    if (ok && n_pairs > 0) {
-      const int last = n_pairs - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[last & 1], (last >> 1) & 1, abort_flag, p.status));
-    }
-    if (ok) fence_after();
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    // O leaves through shared memory (the drained gather ring): each warp writes its 32 heads as
-    // boxes of 32 rows x 128 bytes with the 128-byte swizzle (16-byte piece c of row i at c ^ (i & 7),
-    // so the eight rows of a quarter warp hit all banks), then one lane stores them with TMA.
-    const bool have_o = n_pairs > 0 && ok;
-    const uint32_t row_off = (uint32_t)lane * 128u;
-    const uint32_t sw = (uint32_t)(lane & 7);
-    if (p.n_splits == 1) {
-      const uint32_t stg = saddr(sm + OFF_C) + (uint32_t)warp * 16384u;   // 4 boxes of 64 bf16 columns
+      } else {
+        // O leaves through shared memory (the drained gather ring): each warp writes its 32 heads as
+        // boxes of 32 rows x 128 bytes with the 128-byte swizzle (16-byte piece c of row i at c ^ (i & 7),
+        // so the eight rows of a quarter warp hit all banks), then one lane stores them with TMA.
+        const bool have_o = n_pairs > 0 && ok;
+        const uint32_t row_off = (uint32_t)lane * 128u;
+        const uint32_t sw = (uint32_t)(lane & 7);
+        if (p.n_splits == 1) {
+          const uint32_t stg = saddr(sm + OFF_C) + (uint32_t)warp * 16384u;   // 4 boxes of 64 bf16 columns
 #pragma unroll 1
-      for (int c = 0; c < DVH / 32; ++c) {
-        uint32_t o[32];
-        if (have_o) {
-          tm_ld32(tmem + lane_off + TM_O + c * 32, o);
-          tm_wait_ld();
+          for (int c = 0; c < DVH / 32; ++c) {
+            uint32_t o[32];
+            if (have_o) {
+              tm_ld32(tmem + lane_off + TM_O + c * 32, o);
+              tm_wait_ld();
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+            const uint32_t box = stg + (uint32_t)(c >> 1) * 4096u + row_off;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(box + ((((uint32_t)(c & 1) * 4u + q) ^ sw) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2],
+                           w[4 * q + 3]);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the TMA store
+          __syncwarp();
+          if (ok && lane == 0) {
+#pragma unroll
+            for (int bx = 0; bx < DVH / 64; ++bx)
+              tma_store_2d(&tm_st, stg + (uint32_t)bx * 4096u, (int)rank * DVH + bx * 64, r * p.H + h0 + warp * 32);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // the staging is read before exit
+          }
+          __syncwarp();
+          if (head_ok && rank == 0 && p.lse)
+            p.lse[(int64_t)r * p.H + h0 + h] = l > 0.f ? (m_ref + log2f(l)) / LOG2E : -INFINITY;
         } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
-        }
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-        const uint32_t box = stg + (uint32_t)(c >> 1) * 4096u + row_off;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          st_shared_v4(box + ((((uint32_t)(c & 1) * 4u + q) ^ sw) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2],
-                       w[4 * q + 3]);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the TMA store
-      __syncwarp();
-      if (ok && lane == 0) {
-#pragma unroll
-        for (int bx = 0; bx < DVH / 64; ++bx)
-          tma_store_2d(&tm_st, stg + (uint32_t)bx * 4096u, (int)rank * DVH + bx * 64, r * p.H + h0 + warp * 32);
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // the staging is read before exit
-      }
-      __syncwarp();
-      if (head_ok && rank == 0 && p.lse)
-        p.lse[(int64_t)r * p.H + h0 + h] = l > 0.f ? (m_ref + log2f(l)) / LOG2E : -INFINITY;
-    } else {
-      const uint32_t stg = saddr(sm + OFF_C) + (uint32_t)warp * 32768u;   // 8 boxes of 32 float columns
+          const uint32_t stg = saddr(sm + OFF_C) + (uint32_t)warp * 32768u;   // 8 boxes of 32 float columns
 #pragma unroll 1
-      for (int c = 0; c < DVH / 32; ++c) {
-        uint32_t o[32];
-        if (have_o) {
-          tm_ld32(tmem + lane_off + TM_O + c * 32, o);
-          tm_wait_ld();
-        } else {
+          for (int c = 0; c < DVH / 32; ++c) {
+            uint32_t o[32];
+            if (have_o) {
+              tm_ld32(tmem + lane_off + TM_O + c * 32, o);
+              tm_wait_ld();
+            } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
+              for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
+            const uint32_t box = stg + (uint32_t)c * 4096u + row_off;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st_shared_v4(box + (((uint32_t)q ^ sw) << 4), o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (ok && lane == 0) {
+#pragma unroll
+            for (int c = 0; c < DVH / 32; ++c)
+              tma_store_3d(&tm_st, stg + (uint32_t)c * 4096u, (int)rank * DVH + c * 32, split,
+                           r * p.H + h0 + warp * 32);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            // the partials are complete in global memory, and ordered before this thread's later
+            // generic accesses (the cluster barrier that releases them to the merging CTAs)
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
+          __syncwarp();
+          if (head_ok) {   // each value half carries its own (max, sum)
+            float* ml = p.part_ml + ((((int64_t)r * p.H + h0 + h) * p.n_splits + split) * 2 + rank) * 2;
+            ml[0] = l > 0.f ? m_ref : -INFINITY;
+            ml[1] = l;
+          }
         }
-        const uint32_t box = stg + (uint32_t)c * 4096u + row_off;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st_shared_v4(box + (((uint32_t)q ^ sw) << 4), o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (ok && lane == 0) {
-#pragma unroll
-        for (int c = 0; c < DVH / 32; ++c)
-          tma_store_3d(&tm_st, stg + (uint32_t)c * 4096u, (int)rank * DVH + c * 32, split, r * p.H + h0 + warp * 32);
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        // the partials are complete in global memory, and ordered before this thread's later
-        // generic accesses (the cluster barrier that releases them to the merging CTAs)
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-      }
-      __syncwarp();
-      if (head_ok) {   // each value half carries its own (max, sum)
-        float* ml = p.part_ml + ((((int64_t)r * p.H + h0 + h) * p.n_splits + split) * 2 + rank) * 2;
-        ml[0] = l > 0.f ? m_ref : -INFINITY;
-        ml[1] = l;
       }
     }
   } else if (warp < SEND_WARP + 4) {
@@ -737,51 +858,77 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     const uint32_t swz = (uint32_t)((h >> 1) & 3);
     const uint32_t off = (uint32_t)(warp & 3) * 32u * 64u;   // this warp's rows within a half
     bool ok = true;
-    for (int P = 0; P < n_pairs && ok; ++P) {
-      const int s = P & 1;
-      const uint32_t par = (P >> 1) & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s], par, abort_flag, p.status));
-      if (!ok) break;
-      fence_after();
-      uint32_t sr[64];
-      tm_ld32(tmem + lane_off + TM_S0 + s * 64, sr);
-      tm_ld32(tmem + lane_off + TM_S0 + s * 64 + 32, sr + 32);
-      tm_wait_ld();
-      fence_before();
-      mbar_arrive(&s_read[s]);
-      // the other CTA received pair P-1 (so its copies have read the staging slot)
-      if (P >= 1) ok = __all_sync(0xffffffffu, mbar_wait_cl(stg_free, (P - 1) & 1, abort_flag, p.status));
-      if (!ok) break;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t hx[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          hx[j] = pack_f16_sat(__uint_as_float(sr[32 * half + 2 * j]) * p.sl2,
-                               __uint_as_float(sr[32 * half + 2 * j + 1]) * p.sl2);
-        const uint32_t row = stg_row + (uint32_t)half * XHALF_BYTES;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c ^ swz) << 4)),
-                       "r"(hx[4 * c]), "r"(hx[4 * c + 1]), "r"(hx[4 * c + 2]), "r"(hx[4 * c + 3])
-                       : "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the bulk copy
-        // the other CTA has consumed what was sent into its slot s two pairs ago
-        if (half == 0 && P >= 2)
-          ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_free[s], ((P - 2) >> 1) & 1, abort_flag, p.status));
-        else
+    int q_issued = 0;   // rope query loads issued by this warp (rank 0, first sender warp)
+    for (int it = 0; it < n_items && ok; ++it) {
+      const Item I = item_of<PERSIST>(p, it);
+      if (PERSIST) {
+        // The item's queries.  TMEM columns [0,128) and the rope dims in shared memory are free: this warp
+        // waited for the previous item's last QK to complete (its s_full) in its last pair.
+        if (rank == 0 && warp == SEND_WARP) {
+          if (elect_one()) {
+            mbar_arrive_expect_tx(q_ready, HG * 128);
+            tma_load_2d(saddr(sm + OFF_QR), &tm_q, 512, I.r * p.H + I.h0, q_ready);
+          }
           __syncwarp();
-        if (!ok) break;
-        if (lane == 0) {
-          const uint32_t ho = (uint32_t)s * XSLOT_BYTES + (uint32_t)half * XHALF_BYTES + off;
-          asm volatile(
-              "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-              ::"r"(x_peer0 + ho), "r"(stg0 + (uint32_t)half * XHALF_BYTES + off), "r"(32 * 64),
-              "r"(xfull_peer + (uint32_t)(2 * s + half) * 8u)
-              : "memory");
+          ++q_issued;
         }
-        __syncwarp();
+        load_q_tmem(p, tmem + lane_off, I.r, I.h0, h, rank, q_ready);
+        if (it + 1 < n_items) {   // the next item's queries into L2 while this one runs
+          const Item In = item_of<PERSIST>(p, it + 1);
+          prefetch_q_l2(p, In.r, In.h0, h, rank);
+        }
       }
+      // P: the CTA's running pair index
+      for (int P = I.g0; P < I.g0 + I.n_pairs && ok; ++P) {
+        const int s = P & 1;
+        const uint32_t par = (P >> 1) & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s], par, abort_flag, p.status));
+        if (!ok) break;
+        fence_after();
+        uint32_t sr[64];
+        tm_ld32(tmem + lane_off + TM_S0 + s * 64, sr);
+        tm_ld32(tmem + lane_off + TM_S0 + s * 64 + 32, sr + 32);
+        tm_wait_ld();
+        fence_before();
+        mbar_arrive(&s_read[s]);
+        // the other CTA received pair P-1 (so its copies have read the staging slot)
+        if (P >= 1) ok = __all_sync(0xffffffffu, mbar_wait_cl(stg_free, (P - 1) & 1, abort_flag, p.status));
+        if (!ok) break;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t hx[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            hx[j] = pack_f16_sat(__uint_as_float(sr[32 * half + 2 * j]) * p.sl2,
+                                 __uint_as_float(sr[32 * half + 2 * j + 1]) * p.sl2);
+          const uint32_t row = stg_row + (uint32_t)half * XHALF_BYTES;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c ^ swz) << 4)),
+                         "r"(hx[4 * c]), "r"(hx[4 * c + 1]), "r"(hx[4 * c + 2]), "r"(hx[4 * c + 3])
+                         : "memory");
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the bulk copy
+          // the other CTA has consumed what was sent into its slot s two pairs ago
+          if (half == 0 && P >= 2)
+            ok = __all_sync(0xffffffffu, mbar_wait_cl(&x_free[s], ((P - 2) >> 1) & 1, abort_flag, p.status));
+          else
+            __syncwarp();
+          if (!ok) break;
+          if (lane == 0) {
+            const uint32_t ho = (uint32_t)s * XSLOT_BYTES + (uint32_t)half * XHALF_BYTES + off;
+            asm volatile(
+                "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                ::"r"(x_peer0 + ho), "r"(stg0 + (uint32_t)half * XHALF_BYTES + off), "r"(32 * 64),
+                "r"(xfull_peer + (uint32_t)(2 * s + half) * 8u)
+                : "memory");
+          }
+          __syncwarp();
+        }
+      }
+    }
+    if (PERSIST && q_issued > 0 && *abort_flag && lane == 0) {   // the last rope load lands before exit
+      volatile int dummy = 0;
+      mbar_wait(q_ready, (q_issued - 1) & 1, &dummy, p.status);
     }
   } else if (warp < PROD_WARP + N_PROD) {
     // ------------------------------------------------ producers
@@ -796,190 +943,205 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
     const int32_t oob = (int32_t)p.pool;   // a row outside the tensor map: TMA reads zeros
     // first latent column of local chunk c
     auto chunk_x = [&](int c) -> int { return rank == 0 ? (c < 4 ? c * 64 : 512) : 256 + c * 64; };
-    if (rank == 0 && pw == 0 && elect_one()) {   // rope query dims of the 128 heads: one box of 64 dims x 128 rows
+    if (!PERSIST && rank == 0 && pw == 0 && elect_one()) {
+      // rope query dims of the 128 heads: one box of 64 dims x 128 rows (the persistent launch: the
+      // sender warps, per item)
+      const Item I0 = item_of<PERSIST>(p, 0);
       mbar_arrive_expect_tx(q_ready, HG * 128);
-      tma_load_2d(saddr(sm + OFF_QR), &tm_q, 512, r * p.H + h0, q_ready);
+      tma_load_2d(saddr(sm + OFF_QR), &tm_q, 512, I0.r * p.H + I0.h0, q_ready);
     }
     __syncwarp();
-    const int32_t* idx_row = p.idx + (int64_t)r * p.n_idx;
-    // raw selected entry of position j (or a clamped dummy when j is an appended / past-the-split position)
-    auto raw = [&](int64_t j) -> int32_t { return p.n_idx > 0 ? idx_row[min(j, (int64_t)p.n_idx - 1)] : 0; };
-    // the first entries and the row's visible limit are loaded while the warp looks up the request
-    constexpr int PF = 4;
-    int32_t rq[PF];
+    bool pok = true;   // no abort seen
+    int issued = 0;    // bf16 rows: the CTA's running index of the next tile to issue
+    for (int it = 0; it < n_items && pok; ++it) {
+      const Item I = item_of<PERSIST>(p, it);
+      const int r = I.r;
+      const int64_t j0 = I.j0, j1 = I.j1;
+      const int n_tiles = 2 * I.n_pairs;   // a last half pair is filled with zero rows
+      const int T0 = 2 * I.g0;             // the CTA's running index of the item's first tile
+      const int32_t* idx_row = p.idx + (int64_t)r * p.n_idx;
+      // raw selected entry of position j (or a clamped dummy when j is an appended / past-the-split position)
+      auto raw = [&](int64_t j) -> int32_t { return p.n_idx > 0 ? idx_row[min(j, (int64_t)p.n_idx - 1)] : 0; };
+      // the first entries and the row's visible limit are loaded while the warp looks up the request
+      constexpr int PF = 4;
+      int32_t rq[PF];
 #pragma unroll
-    for (int i = 0; i < PF; ++i) rq[i] = i < n_tiles ? raw(j0 + (int64_t)i * NT + my_pos) : 0;
-    const int64_t limit = p.row_pos[r] + p.row_pos_add;
-    const int64_t abase = p.n_append > 0 ? p.append_base[r] + 1 : 0;   // first appended position
-    const int breq = request_of_row_warp(p.row_offsets, p.B, (uint32_t)r);
-    const int64_t base = PAGED ? 0 : p.cache_start[breq];
-    // checked position of this lane's entry in tile t, from its raw selected entry
-    auto tile_pos = [&](int t, int32_t rv) -> int64_t {
-      const int64_t j = j0 + (int64_t)t * NT + my_pos;
-      return entry_pos(p, j >= j1 ? -2 : (j < p.n_idx ? (int64_t)rv : abase + (j - p.n_idx)), limit);
-    };
-    // PAGED: tile t's position and page entry are taken one iteration ahead (the page load in flight)
-    int64_t s_next = 0;
-    int32_t pg_next = -1;
-    if (PAGED) {
-      s_next = n_tiles > 0 ? tile_pos(0, rq[0]) : -1;
-      pg_next = page_entry(p, breq, s_next);
-    }
-    if constexpr (FP8KV) {
-      // ---- FP8 rows: gather this warp's 8 rows of tile ti into staging slot ti % FD (FD tiles ahead of
-      // the dequantization), then per tile t: dequantize them into the pair buffer, publish the validity
-      // bits and arrive on the tile's c_full (one arrival per producer warp).
-      uint8_t* fstg = sm + OFF_F + pw * FD * F_TILE;
-      uint64_t* ffull = f_full + pw * FD;
-      uint32_t mq[FD];
-      int ti = 0, done = 0;
-      bool ok = true;
-      auto issue_tile = [&](int tt) {
-        const int32_t craw = rq[0];
-#pragma unroll
-        for (int i = 0; i + 1 < PF; ++i) rq[i] = rq[i + 1];
-        rq[PF - 1] = tt + PF < n_tiles ? raw(j0 + (int64_t)(tt + PF) * NT + my_pos) : 0;
-        const int64_t sp = tile_pos(tt, craw);
-        const int64_t row = entry_row<PAGED>(p, sp, base, PAGED ? page_entry(p, breq, sp) : -1);
-        const bool valid = row >= 0 && lane < 8;
-        mq[tt % FD] = __reduce_or_sync(0xffffffffu, valid ? (1u << my_pos) : 0u);
-        const int yv = row >= 0 ? (int)row : oob;
-        int y[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = __shfl_sync(0xffffffffu, yv, i);
-        const int k = tt % FD;
-        const uint32_t sb = saddr(fstg + k * F_TILE);
-        if (elect_one()) {
-          mbar_arrive_expect_tx(&ffull[k], (uint32_t)(F_CODES + 2 * 64 + (rank == 0 ? F_ROPE : 0)));
-#pragma unroll
-          for (int gi = 0; gi < 2; ++gi) {
-            const int* yg = y + 4 * gi;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
-              tma_gather4(sb + (gi * 2 + hf) * 512, &tm_lat, (int)rank * 256 + hf * 128, yg[0], yg[1], yg[2], yg[3],
-                          &ffull[k]);
-            tma_gather4(sb + F_CODES + gi * 128, &tm_sc, 512, yg[0], yg[1], yg[2], yg[3], &ffull[k]);
-            if (rank == 0)
-              tma_gather4(sb + F_CODES + F_SCL + gi * 512, &tm_lat, 528, yg[0], yg[1], yg[2], yg[3], &ffull[k]);
-          }
-        }
-        __syncwarp();
+      for (int i = 0; i < PF; ++i) rq[i] = i < n_tiles ? raw(j0 + (int64_t)i * NT + my_pos) : 0;
+      const int64_t limit = p.row_pos[r] + p.row_pos_add;
+      const int64_t abase = p.n_append > 0 ? p.append_base[r] + 1 : 0;   // first appended position
+      const int breq = request_of_row_warp(p.row_offsets, p.B, (uint32_t)r);
+      const int64_t base = PAGED ? 0 : p.cache_start[breq];
+      // checked position of this lane's entry in tile t, from its raw selected entry
+      auto tile_pos = [&](int t, int32_t rv) -> int64_t {
+        const int64_t j = j0 + (int64_t)t * NT + my_pos;
+        return entry_pos(p, j >= j1 ? -2 : (j < p.n_idx ? (int64_t)rv : abase + (j - p.n_idx)), limit);
       };
-      for (int t = 0; t < n_tiles && ok; ++t) {
-        while (ti < n_tiles && ti < t + FD) issue_tile(ti++);
-        const int k = t % FD;
-        ok = __all_sync(0xffffffffu, mbar_wait(&ffull[k], (t / FD) & 1, abort_flag, p.status));
-        const int st = t % NSTAGE_K, P = t >> 1, q = P % NPAIR_K, R = P / NPAIR_K;
-        if (ok && R > 0) ok = __all_sync(0xffffffffu, mbar_wait(&c_empty[q], (R - 1) & 1, abort_flag, p.status));
-        if (!ok) break;
-        const uint8_t* sb = fstg + k * F_TILE;
-        uint8_t* pair = sm + OFF_C + q * PAIR_STRIDE;
-        // One row half (128 codes, contiguous in staging) per step: lane l takes codes 4l .. 4l+3, so the
-        // staging reads are conflict-free; they land as 8 bytes of bf16 in chunk (2 half + l / 16), 16-byte
-        // slot (l % 16) / 2, at the 128-byte swizzle the MMAs read.
-#pragma unroll 4
-        for (int it = 0; it < 16; ++it) {
-          const int row8 = it >> 1, hf = it & 1, gi = row8 >> 2, rig = row8 & 3;
-          const int pos = (t & 1) * NT + 4 * (pw + 4 * gi) + rig;   // position within the pair
-          const uint32_t w4 = *(const uint32_t*)(sb + (gi * 2 + hf) * 512 + rig * 128 + lane * 4);
-          const float sc = *(const float*)(sb + F_CODES + gi * 128 + rig * 16 + ((int)rank * 2 + hf) * 4);
-          uint32_t ow[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w4 >> (16 * e)) & 0xffffu);
-            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);   // exact
-            const float2 f = __half22float2(*(const __half2*)&hr);
-            const __nv_bfloat162 bv = __floats2bfloat162_rn(f.x * sc, f.y * sc);
-            ow[e] = *(const uint32_t*)&bv;
-          }
-          const int cc = hf * 2 + (lane >> 4), kk = (lane & 15) >> 1;
-          *(uint2*)(pair + cc * CHUNK_BYTES + pos * 128 + ((kk ^ (pos & 7)) << 4) + (lane & 1) * 8) = make_uint2(ow[0], ow[1]);
-        }
-        if (rank == 0) {   // rope bytes (bf16 already) into chunk 4, swizzled
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int id = lane * 2 + e, row8 = id >> 3, kk = id & 7, gi = row8 >> 2, rig = row8 & 3;
-            const int pos = (t & 1) * NT + 4 * (pw + 4 * gi) + rig;
-            *(uint4*)(pair + 4 * CHUNK_BYTES + pos * 128 + ((kk ^ (pos & 7)) << 4)) =
-                *(const uint4*)(sb + F_CODES + F_SCL + gi * 512 + rig * 128 + kk * 16);
-          }
-        }
-        // the MMAs (async proxy) read what these generic stores wrote, and the next gathers into this
-        // staging slot come after its reads
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          mask_s[st * 4 + pw] = mq[k];
-          mbar_arrive(&c_full[st]);
-        }
-        __syncwarp();
-        done = t + 1;
-      }
-      if (*abort_flag && lane == 0) {   // wait (bounded) for this warp's staging copies still in flight
-        volatile int dummy = 0;
-        for (int tt = done; tt < ti; ++tt) mbar_wait(&ffull[tt % FD], (tt / FD) & 1, &dummy, p.status);
-        if (rank == 0 && pw == 0) mbar_wait(q_ready, 0, &dummy, p.status);
-      }
-    } else {
-    int issued = 0;
-    for (int t = 0; t < n_tiles; ++t) {
-      int64_t s_cur;
-      int32_t pg_cur = -1;
+      // PAGED: tile t's position and page entry are taken one iteration ahead (the page load in flight)
+      int64_t s_next = 0;
+      int32_t pg_next = -1;
       if (PAGED) {
-#pragma unroll
-        for (int i = 0; i + 1 < PF; ++i) rq[i] = rq[i + 1];
-        rq[PF - 1] = t + PF < n_tiles ? raw(j0 + (int64_t)(t + PF) * NT + my_pos) : 0;
-        s_cur = s_next;
-        pg_cur = pg_next;
-        s_next = t + 1 < n_tiles ? tile_pos(t + 1, rq[0]) : -1;
+        s_next = n_tiles > 0 ? tile_pos(0, rq[0]) : -1;
         pg_next = page_entry(p, breq, s_next);
-      } else {
-        const int32_t craw = rq[0];
-#pragma unroll
-        for (int i = 0; i + 1 < PF; ++i) rq[i] = rq[i + 1];
-        rq[PF - 1] = t + PF < n_tiles ? raw(j0 + (int64_t)(t + PF) * NT + my_pos) : 0;
-        s_cur = craw;   // resolved after the wait below, as its position
       }
-      const int st = t % NSTAGE_K, P = t >> 1, q = P % NPAIR_K, R = P / NPAIR_K;
-      if (R > 0 && !__all_sync(0xffffffffu, mbar_wait(&c_empty[q], (R - 1) & 1, abort_flag, p.status))) break;
-      if (!PAGED) s_cur = tile_pos(t, (int32_t)s_cur);
-      const int64_t row = entry_row<PAGED>(p, s_cur, base, pg_cur);
-      const bool valid = row >= 0 && lane < 8;
-      const uint32_t bits = __reduce_or_sync(0xffffffffu, valid ? (1u << my_pos) : 0u);
-      if (lane == 0) mask_s[st * 4 + pw] = bits;
-      const int yv = row >= 0 ? (int)row : oob;
-      int y[8];
+      if constexpr (FP8KV) {
+        // ---- FP8 rows: gather this warp's 8 rows of tile ti into staging slot ti % FD (FD tiles ahead of
+        // the dequantization), then per tile t: dequantize them into the pair buffer, publish the validity
+        // bits and arrive on the tile's c_full (one arrival per producer warp).
+        uint8_t* fstg = sm + OFF_F + pw * FD * F_TILE;
+        uint64_t* ffull = f_full + pw * FD;
+        uint32_t mq[FD];
+        int ti = 0, done = 0;
+        bool ok = true;
+        auto issue_tile = [&](int tt) {
+          const int32_t craw = rq[0];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = __shfl_sync(0xffffffffu, yv, i);
-      const uint32_t dst = saddr(sm + OFF_C + q * PAIR_STRIDE + (t & 1) * (NT * 128));
-      if (elect_one()) {
-        mbar_arrive_expect_tx(&c_full[st], (uint32_t)nch * 1024u);
+          for (int i = 0; i + 1 < PF; ++i) rq[i] = rq[i + 1];
+          rq[PF - 1] = tt + PF < n_tiles ? raw(j0 + (int64_t)(tt + PF) * NT + my_pos) : 0;
+          const int64_t sp = tile_pos(tt, craw);
+          const int64_t row = entry_row<PAGED>(p, sp, base, PAGED ? page_entry(p, breq, sp) : -1);
+          const bool valid = row >= 0 && lane < 8;
+          mq[tt % FD] = __reduce_or_sync(0xffffffffu, valid ? (1u << my_pos) : 0u);
+          const int yv = row >= 0 ? (int)row : oob;
+          int y[8];
 #pragma unroll
-        for (int gi = 0; gi < 2; ++gi) {
-          const int g = pw + 4 * gi;
+          for (int i = 0; i < 8; ++i) y[i] = __shfl_sync(0xffffffffu, yv, i);
+          const int k = tt % FD;
+          const uint32_t sb = saddr(fstg + k * F_TILE);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&ffull[k], (uint32_t)(F_CODES + 2 * 64 + (rank == 0 ? F_ROPE : 0)));
 #pragma unroll
-          for (int c = 0; c < NCH_MAX; ++c)
-            if (c < nch)
-              tma_gather4(dst + c * CHUNK_BYTES + g * 512, &tm_lat, chunk_x(c), y[4 * gi], y[4 * gi + 1],
-                          y[4 * gi + 2], y[4 * gi + 3], &c_full[st]);
+            for (int gi = 0; gi < 2; ++gi) {
+              const int* yg = y + 4 * gi;
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf)
+                tma_gather4(sb + (gi * 2 + hf) * 512, &tm_lat, (int)rank * 256 + hf * 128, yg[0], yg[1], yg[2], yg[3],
+                            &ffull[k]);
+              tma_gather4(sb + F_CODES + gi * 128, &tm_sc, 512, yg[0], yg[1], yg[2], yg[3], &ffull[k]);
+              if (rank == 0)
+                tma_gather4(sb + F_CODES + F_SCL + gi * 512, &tm_lat, 528, yg[0], yg[1], yg[2], yg[3], &ffull[k]);
+            }
+          }
+          __syncwarp();
+        };
+        for (int t = 0; t < n_tiles && ok; ++t) {
+          while (ti < n_tiles && ti < t + FD) issue_tile(ti++);
+          const int k = t % FD;
+          ok = __all_sync(0xffffffffu, mbar_wait(&ffull[k], (t / FD) & 1, abort_flag, p.status));
+          const int st = t % NSTAGE_K, P = t >> 1, q = P % NPAIR_K, R = P / NPAIR_K;
+          if (ok && R > 0) ok = __all_sync(0xffffffffu, mbar_wait(&c_empty[q], (R - 1) & 1, abort_flag, p.status));
+          if (!ok) break;
+          const uint8_t* sb = fstg + k * F_TILE;
+          uint8_t* pair = sm + OFF_C + q * PAIR_STRIDE;
+          // One row half (128 codes, contiguous in staging) per step: lane l takes codes 4l .. 4l+3, so the
+          // staging reads are conflict-free; they land as 8 bytes of bf16 in chunk (2 half + l / 16), 16-byte
+          // slot (l % 16) / 2, at the 128-byte swizzle the MMAs read.
+#pragma unroll 4
+          for (int it = 0; it < 16; ++it) {
+            const int row8 = it >> 1, hf = it & 1, gi = row8 >> 2, rig = row8 & 3;
+            const int pos = (t & 1) * NT + 4 * (pw + 4 * gi) + rig;   // position within the pair
+            const uint32_t w4 = *(const uint32_t*)(sb + (gi * 2 + hf) * 512 + rig * 128 + lane * 4);
+            const float sc = *(const float*)(sb + F_CODES + gi * 128 + rig * 16 + ((int)rank * 2 + hf) * 4);
+            uint32_t ow[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w4 >> (16 * e)) & 0xffffu);
+              const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);   // exact
+              const float2 f = __half22float2(*(const __half2*)&hr);
+              const __nv_bfloat162 bv = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+              ow[e] = *(const uint32_t*)&bv;
+            }
+            const int cc = hf * 2 + (lane >> 4), kk = (lane & 15) >> 1;
+            *(uint2*)(pair + cc * CHUNK_BYTES + pos * 128 + ((kk ^ (pos & 7)) << 4) + (lane & 1) * 8) =
+                make_uint2(ow[0], ow[1]);
+          }
+          if (rank == 0) {   // rope bytes (bf16 already) into chunk 4, swizzled
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int id = lane * 2 + e, row8 = id >> 3, kk = id & 7, gi = row8 >> 2, rig = row8 & 3;
+              const int pos = (t & 1) * NT + 4 * (pw + 4 * gi) + rig;
+              *(uint4*)(pair + 4 * CHUNK_BYTES + pos * 128 + ((kk ^ (pos & 7)) << 4)) =
+                  *(const uint4*)(sb + F_CODES + F_SCL + gi * 512 + rig * 128 + kk * 16);
+            }
+          }
+          // the MMAs (async proxy) read what these generic stores wrote, and the next gathers into this
+          // staging slot come after its reads
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            mask_s[st * 4 + pw] = mq[k];
+            mbar_arrive(&c_full[st]);
+          }
+          __syncwarp();
+          done = t + 1;
+        }
+        pok = ok;
+        if (*abort_flag && lane == 0) {   // wait (bounded) for this warp's staging copies still in flight
+          volatile int dummy = 0;
+          for (int tt = done; tt < ti; ++tt) mbar_wait(&ffull[tt % FD], (tt / FD) & 1, &dummy, p.status);
+          if (rank == 0 && pw == 0) mbar_wait(q_ready, 0, &dummy, p.status);
+        }
+      } else {
+        for (int t = 0; t < n_tiles; ++t) {
+          int64_t s_cur;
+          int32_t pg_cur = -1;
+          if (PAGED) {
+#pragma unroll
+            for (int i = 0; i + 1 < PF; ++i) rq[i] = rq[i + 1];
+            rq[PF - 1] = t + PF < n_tiles ? raw(j0 + (int64_t)(t + PF) * NT + my_pos) : 0;
+            s_cur = s_next;
+            pg_cur = pg_next;
+            s_next = t + 1 < n_tiles ? tile_pos(t + 1, rq[0]) : -1;
+            pg_next = page_entry(p, breq, s_next);
+          } else {
+            const int32_t craw = rq[0];
+#pragma unroll
+            for (int i = 0; i + 1 < PF; ++i) rq[i] = rq[i + 1];
+            rq[PF - 1] = t + PF < n_tiles ? raw(j0 + (int64_t)(t + PF) * NT + my_pos) : 0;
+            s_cur = craw;   // resolved after the wait below, as its position
+          }
+          const int tg = T0 + t;   // running tile index: ring stage and pair buffer
+          const int st = tg % NSTAGE_K, P = tg >> 1, q = P % NPAIR_K, R = P / NPAIR_K;
+          if (R > 0 && !__all_sync(0xffffffffu, mbar_wait(&c_empty[q], (R - 1) & 1, abort_flag, p.status))) {
+            pok = false;
+            break;
+          }
+          if (!PAGED) s_cur = tile_pos(t, (int32_t)s_cur);
+          const int64_t row = entry_row<PAGED>(p, s_cur, base, pg_cur);
+          const bool valid = row >= 0 && lane < 8;
+          const uint32_t bits = __reduce_or_sync(0xffffffffu, valid ? (1u << my_pos) : 0u);
+          if (lane == 0) mask_s[st * 4 + pw] = bits;
+          const int yv = row >= 0 ? (int)row : oob;
+          int y[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) y[i] = __shfl_sync(0xffffffffu, yv, i);
+          const uint32_t dst = saddr(sm + OFF_C + q * PAIR_STRIDE + (t & 1) * (NT * 128));
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&c_full[st], (uint32_t)nch * 1024u);
+#pragma unroll
+            for (int gi = 0; gi < 2; ++gi) {
+              const int g = pw + 4 * gi;
+#pragma unroll
+              for (int c = 0; c < NCH_MAX; ++c)
+                if (c < nch)
+                  tma_gather4(dst + c * CHUNK_BYTES + g * 512, &tm_lat, chunk_x(c), y[4 * gi], y[4 * gi + 1],
+                              y[4 * gi + 2], y[4 * gi + 3], &c_full[st]);
+            }
+          }
+          __syncwarp();
+          issued = tg + 1;
         }
       }
-      __syncwarp();
-      issued = t + 1;
     }
-    if (*abort_flag && lane == 0) {   // wait (bounded) for this CTA's copies still in flight
+    if (!FP8KV && *abort_flag && lane == 0) {   // wait (bounded) for this CTA's copies still in flight
       volatile int dummy = 0;
       for (int st = 0; st < NSTAGE_K; ++st) {
         const int n = issued / NSTAGE_K + (st < issued % NSTAGE_K ? 1 : 0);
         if (n > 0) mbar_wait(&c_full[st], (n - 1) & 1, &dummy, p.status);
       }
-      if (rank == 0 && pw == 0) mbar_wait(q_ready, 0, &dummy, p.status);
+      if (!PERSIST && rank == 0 && pw == 0) mbar_wait(q_ready, 0, &dummy, p.status);
     }
-    }   // bf16 rows
   } else {
     // ------------------------------------------------ MMA issue (warp 12; one elected lane issues)
-    bool ok = __all_sync(0xffffffffu, mbar_wait(q_ready, 0, abort_flag, p.status));
-    if (ok) fence_after();
     const uint64_t qr_desc = desc_sw128(saddr(sm + OFF_QR), 16, 1024);
     const uint64_t c_desc0 = desc_sw128(saddr(sm + OFF_C), 16, 1024);
     const uint64_t v_desc0 = desc_sw128(saddr(sm + OFF_C), CHUNK_BYTES, 1024);
@@ -1014,12 +1176,45 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
       __syncwarp();
       return true;
     };
-    if (ok && n_pairs > 0) ok = issue_qk(0);
-    for (int np = 0; np < n_pairs && ok; ++np) {
-      if (np + 1 < n_pairs && !issue_qk(np + 1)) break;
+    // The pairs of all items run in one sequence (np: the CTA's running pair index), in the order above
+    // except at an item boundary: the first QK of an item waits for its queries (q_ready), which the
+    // sender warps load once the previous item's last QK completed, so the previous item's last PV is
+    // issued before it (its epilogue does not wait for the new queries; measured faster than the other
+    // order).  The first PV of an item overwrites O.
+    const int n_total = PERSIST ? (int)(min(p.tp, (int64_t)(blockIdx.x + 1) * p.pq) - (int64_t)blockIdx.x * p.pq)
+                                : item_of<PERSIST>(p, 0).n_pairs;
+    int q_item = 0, q_start = 0;   // the next item whose queries the QKs wait for, and its first pair
+    auto qk = [&](int g) -> bool {
+      if (g == q_start) {
+        if (!__all_sync(0xffffffffu, mbar_wait(q_ready, q_item & 1, abort_flag, p.status))) return false;
+        fence_after();
+        ++q_item;
+        q_start = q_item < n_items ? item_of<PERSIST>(p, q_item).g0 : INT_MAX;
+      }
+      return issue_qk(g);
+    };
+    bool ok = true;
+    if (n_total == 0 && n_items > 0)   // nothing to compute: the query copies still land before exit
+      ok = __all_sync(0xffffffffu, mbar_wait(q_ready, 0, abort_flag, p.status));
+    if (ok && n_total > 0) ok = qk(0);
+    int p_item = 0, p_start = 0;   // the item of the next PV and its first pair
+    for (int np = 0; np < n_total && ok; ++np) {
+      const bool boundary = np + 1 == q_start;   // np + 1 is the first pair of the next item
+      if (np + 1 < n_total && !boundary && !qk(np + 1)) {
+        ok = false;
+        break;
+      }
+      const bool first = np == p_start;
+      if (first) {
+        ++p_item;
+        p_start = p_item < n_items ? item_of<PERSIST>(p, p_item).g0 : INT_MAX;
+      }
       // O += P(np) V(np): A = P from TMEM, B = chunks 0..3 of the pair buffer as MN-major (N = 256 dims)
       const int sp = np & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&p_full[sp], (np >> 1) & 1, abort_flag, p.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&p_full[sp], (np >> 1) & 1, abort_flag, p.status))) {
+        ok = false;
+        break;
+      }
       fence_after();
       const int bp = np % NPAIR_K;
       const uint64_t vd = v_desc0 + (uint64_t)((bp * PAIR_STRIDE) >> 4);
@@ -1027,11 +1222,12 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
 #pragma unroll
         for (int k = 0; k < NP / 16; ++k)
           mma_ts(tmem + TM_O, tmem + TM_S0 + sp * 64 + k * 8, vd + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV,
-                 (np > 0 || k > 0) ? 1u : 0u);
+                 (!first || k > 0) ? 1u : 0u);
         commit(&pv_done[sp]);
         commit(&c_empty[bp]);
       }
       __syncwarp();
+      if (np + 1 < n_total && boundary && !qk(np + 1)) ok = false;
     }
     if (elect_one()) commit(drain);
     __syncwarp();
@@ -1048,14 +1244,69 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const __grid_
   // the other CTA no longer writes into this CTA's shared memory; with a fused combine, every split of
   // this row has also written its partials (the barrier releases and acquires at cluster scope)
   cluster_sync();
-  if (p.fused_combine) {
+  if (!PERSIST && p.fused_combine) {
+    const Item I0 = item_of<PERSIST>(p, 0);
     const int hlo = split * HG / p.n_splits, hhi = (split + 1) * HG / p.n_splits;
     switch (p.n_splits) {
-      case 2: merge_splits<2>(p, r, h0, hlo, hhi, rank); break;
-      case 3: merge_splits<3>(p, r, h0, hlo, hhi, rank); break;
-      default: merge_splits<4>(p, r, h0, hlo, hhi, rank); break;
+      case 2: merge_splits<2>(p, I0.r, I0.h0, hlo, hhi, rank); break;
+      case 3: merge_splits<3>(p, I0.r, I0.h0, hlo, hhi, rank); break;
+      default: merge_splits<4>(p, I0.r, I0.h0, hlo, hhi, rank); break;
     }
   }
+}
+
+// Merge of the pieces of the rows cut between clusters of the persistent launch.  CTA (c, y) takes heads
+// 4y .. 4y + 3 of the row (unit) cut at pair (c + 1) pq when that is the first cut inside it; the unit's
+// pieces are those of the clusters whose ranges overlap it (slot 0 when the unit is the cluster's first,
+// else slot 1).  Per head and value half, o = sum_k 2^(m_k - m) o_k / sum_k 2^(m_k - m) l_k; thread =
+// (head, 8 value dims).  Every piece is read without a condition (a piece without mass holds zeros and
+// weighs 0), so the loads of all pieces are in flight together.
+constexpr int MERGE_HEADS = 4;
+struct PieceMerge {
+  __nv_bfloat16* out;
+  float* lse;
+  const float* part_o;
+  const float* part_ml;
+  int H, pq, ppr, hgn;
+  int64_t tp;
+};
+__global__ void __launch_bounds__(64 * MERGE_HEADS) mla_piece_merge_kernel(PieceMerge a) {
+  griddep_wait();                // the persistent kernel's pieces are visible from here on
+  griddep_launch_dependents();
+  const int64_t cut = (int64_t)(blockIdx.x + 1) * a.pq;
+  if (cut >= a.tp || cut % a.ppr == 0) return;
+  const int64_t u = cut / a.ppr, ua = u * a.ppr, ub = ua + a.ppr;
+  if (ua / a.pq != (int64_t)blockIdx.x) return;   // an earlier cut of this unit merges it
+  const int c_first = (int)(ua / a.pq), c_last = (int)((ub - 1) / a.pq);
+  const int r = (int)(u / a.hgn), h0 = (int)(u % a.hgn) * HG;
+  const int hh = blockIdx.y * MERGE_HEADS + (threadIdx.x >> 6);
+  const int d8 = threadIdx.x & 63, half = d8 >> 5;   // value dims 8 d8 .. 8 d8 + 7
+  auto piece = [&](int c) -> int64_t {   // piece row of head hh from cluster c
+    return ((int64_t)c * 2 + ((int64_t)c * a.pq / a.ppr == u ? 0 : 1)) * HG + hh;
+  };
+  float m = -INFINITY;
+#pragma unroll 4
+  for (int c = c_first; c <= c_last; ++c) m = fmaxf(m, a.part_ml[(piece(c) * 2 + half) * 2]);
+  float l = 0.f;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int c = c_first; c <= c_last; ++c) {
+    const int64_t pc = piece(c);
+    const float2 ml = *(const float2*)(a.part_ml + (pc * 2 + half) * 2);   // (max, sum) of the piece
+    const float4* src = (const float4*)(a.part_o + pc * DV) + 2 * d8;
+    const float4 x = src[0], y = src[1];
+    const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - m);
+    l += w * ml.y;
+    acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+    acc[4] += w * y.x; acc[5] += w * y.y; acc[6] += w * y.z; acc[7] += w * y.w;
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const int64_t rh = (int64_t)r * a.H + h0 + hh;
+  uint32_t w4[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) w4[k] = pack_bf16(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+  *((uint4*)(a.out + rh * DV) + d8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  if (d8 == 0 && a.lse) a.lse[rh] = l > 0.f ? (m + log2f(l)) / LOG2E : -INFINITY;
 }
 
 }  // namespace mtc
@@ -1092,11 +1343,13 @@ cudaLaunchConfig_t mla_tc_config(dim3 grid, int cluster_z, cudaStream_t st, cuda
   return cfg;
 }
 bool mla_tc_prepare() {
-  static std::atomic<uint64_t> attr[4];
-  return set_smem_limit_once(mtc::sparse_mla_tc_kernel<false, false>, mtc::SMEM_BYTES, attr[0]) &&
-         set_smem_limit_once(mtc::sparse_mla_tc_kernel<true, false>, mtc::SMEM_BYTES, attr[1]) &&
-         set_smem_limit_once(mtc::sparse_mla_tc_kernel<false, true>, mtc::SMEM_BYTES, attr[2]) &&
-         set_smem_limit_once(mtc::sparse_mla_tc_kernel<true, true>, mtc::SMEM_BYTES, attr[3]);
+  static std::atomic<uint64_t> attr[6];
+  return set_smem_limit_once(mtc::sparse_mla_tc_kernel<false, false, false>, mtc::SMEM_BYTES, attr[0]) &&
+         set_smem_limit_once(mtc::sparse_mla_tc_kernel<true, false, false>, mtc::SMEM_BYTES, attr[1]) &&
+         set_smem_limit_once(mtc::sparse_mla_tc_kernel<false, true, false>, mtc::SMEM_BYTES, attr[2]) &&
+         set_smem_limit_once(mtc::sparse_mla_tc_kernel<true, true, false>, mtc::SMEM_BYTES, attr[3]) &&
+         set_smem_limit_once(mtc::sparse_mla_tc_kernel<false, false, true>, mtc::SMEM_BYTES, attr[4]) &&
+         set_smem_limit_once(mtc::sparse_mla_tc_kernel<true, false, true>, mtc::SMEM_BYTES, attr[5]);
 }
 // CTAs of this kernel that run at once with clusters of 2 x cluster_z CTAs (cached per device; -1 in
 // the cache stands for "none fit").
@@ -1112,7 +1365,7 @@ int mla_tc_resident_ctas(int cluster_z) {
   cudaLaunchAttribute attrs[1];
   cudaLaunchConfig_t cfg = mla_tc_config(dim3(1, 2, cluster_z), cluster_z, 0, attrs);
   if (mla_tc_prepare() &&
-      cudaOccupancyMaxActiveClusters(&clusters, (void*)mtc::sparse_mla_tc_kernel<false, false>, &cfg) == cudaSuccess &&
+      cudaOccupancyMaxActiveClusters(&clusters, (void*)mtc::sparse_mla_tc_kernel<false, false, false>, &cfg) == cudaSuccess &&
       clusters > 0)
     n = 2 * cluster_z * clusters;
   else
@@ -1129,9 +1382,58 @@ bool mla_tc_fuse(int n_splits) {
   return n_splits >= 2 && n_splits <= MAX_FUSED_SPLITS && mla_tc_resident_ctas(n_splits) > 0;
 }
 
+static int64_t split_plan(int R, int H, int64_t total, double* cost_out);
+
+// The persistent launch for bf16 rows, where it is modelled faster than the split launch
+// (MTPSD_MLA_PERSIST=0 turns it off, =1 takes it whenever it applies): every resident cluster gets the
+// same number of consecutive pairs, so no wave is partly empty.  Measured on GB300, an item costs as
+// much beyond its pairs as a row of the split launch does (four whole rows per cluster ran exactly as
+// long as four waves), about PERSIST_ITEM_PAIRS pairs, and the piece merge about PERSIST_MERGE_PAIRS;
+// the gain is the last wave's idle clusters, so large row counts (the 768-row verify, the 384-row
+// draft_extend) take it and a few waves of rows do not.
+constexpr double PERSIST_ITEM_PAIRS = 4.5;
+constexpr double PERSIST_MERGE_PAIRS = 10.0;
+bool mla_tc_persist_plan(int R, int H, int64_t total, int dtype, MlaPersist* pl) {
+  if (dtype != MTPSD_BF16 || total <= 0 || R <= 0 || H % mtc::HG != 0) return false;
+  const char* env = getenv("MTPSD_MLA_PERSIST");
+  if (env && env[0] == '0') return false;
+  const int slots = mla_tc_resident_ctas(1) / 2;
+  if (slots < 1) return false;
+  const int hgn = H / mtc::HG;
+  const int64_t ppr = (total + mtc::NP - 1) / mtc::NP;
+  const int64_t units = (int64_t)R * hgn;
+  const int64_t tp = units * ppr;
+  if (tp > 0x3fffffffLL) return false;   // the running pair index is an int
+  const int64_t pq = (tp + slots - 1) / slots;
+  pl->clusters = (int)((tp + pq - 1) / pq);
+  pl->pq = (int)pq;
+  pl->ppr = (int)ppr;
+  pl->hgn = hgn;
+  pl->tp = tp;
+  pl->cut = false;
+  for (int c = 0; c + 1 < pl->clusters; ++c)
+    if (((int64_t)(c + 1) * pq) % ppr != 0) pl->cut = true;
+  if (env && env[0] == '1') return true;
+  double split_cost = 0.0;
+  split_plan(R, H, total, &split_cost);
+  const double items = (double)((pq + ppr - 1) / ppr + 1);
+  const double cost = (double)pq + 4.0 + items * PERSIST_ITEM_PAIRS + (pl->cut ? PERSIST_MERGE_PAIRS : 0.0);
+  return cost < split_cost;
+}
+
+// Pieces of the persistent launch: two per cluster (its first and its last unit), each 128 heads x 512
+// float32 values, then per piece, head and value half a (max, sum) pair.
+size_t mla_tc_persist_bytes(const MlaPersist& pl) {
+  if (!pl.cut) return 0;
+  const size_t rows = (size_t)pl.clusters * 2 * mtc::HG;
+  return (rows * mtc::DV * sizeof(float) + 255) / 256 * 256 + rows * 4 * sizeof(float);
+}
+
 // Splits of the selected list that balance whole waves of resident clusters.
 // Returns the positions per split (a multiple of NP).
-int mla_tc_per_split(int R, int H, int64_t total) {
+// The split count s with the least modelled time, in units of one pair's time: waves of resident CTAs,
+// each taking its split's pairs plus about four pairs of start-up.
+static int64_t split_plan(int R, int H, int64_t total, double* cost_out) {
   const int64_t tiles = (total + mtc::NP - 1) / mtc::NP;
   const int64_t units = (int64_t)R * (H / mtc::HG) * 2;
   int64_t best = 1;
@@ -1146,6 +1448,12 @@ int mla_tc_per_split(int R, int H, int64_t total) {
       best = s;
     }
   }
+  if (cost_out) *cost_out = best_cost;
+  return best;
+}
+int mla_tc_per_split(int R, int H, int64_t total) {
+  const int64_t tiles = (total + mtc::NP - 1) / mtc::NP;
+  const int64_t best = split_plan(R, H, total, nullptr);
   const int64_t per = ((tiles + best - 1) / best) * mtc::NP;
   return (int)(per > 0 ? per : mtc::NP);
 }
@@ -1154,8 +1462,15 @@ int mla_tc_per_split(int R, int H, int64_t total) {
 int mla_tc_ml_halves() { return 2; }
 
 int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* part_o, float* part_ml,
-                         cudaStream_t st, bool* combined) {
+                         cudaStream_t st, bool* combined, const MlaPersist* pl) {
   using namespace mtc;
+  if (pl) {   // one item list per cluster; pieces of cut rows in the workspace
+    n_splits = 1;
+    per_split = 0;
+    part_o = pl->cut ? (float*)p.ws : nullptr;
+    part_ml = pl->cut ? (float*)((char*)p.ws + ((size_t)pl->clusters * 2 * HG * DV * sizeof(float) + 255) / 256 * 256)
+                      : nullptr;
+  }
   Params k;
   k.B = p.B; k.R = p.R; k.H = p.H; k.n_idx = p.n_idx; k.n_append = p.n_append;
   k.sl2 = p.scale * LOG2E; k.row_pos_add = p.row_pos_add;
@@ -1164,8 +1479,12 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
   k.row_offsets = p.row_offsets; k.row_pos = p.row_pos; k.idx = p.idx;
   k.append_base = p.append_base; k.out = (__nv_bfloat16*)p.out; k.lse = p.lse; k.part_o = part_o; k.part_ml = part_ml;
   k.n_splits = n_splits; k.per_split = per_split; k.status = p.status;
-  k.fused_combine = mla_tc_fuse(n_splits) ? 1 : 0;
+  k.fused_combine = !pl && mla_tc_fuse(n_splits) ? 1 : 0;
   if (combined) *combined = k.fused_combine != 0;
+  k.pq = pl ? pl->pq : 0;
+  k.ppr = pl ? pl->ppr : 0;
+  k.hgn = pl ? pl->hgn : 0;
+  k.tp = pl ? pl->tp : 0;
   alignas(64) CUtensorMap tm_lat, tm_q, tm_st, tm_sc;
   const bool fp8 = p.dtype == MTPSD_FP8_DS_MLA;
   // epilogue stores: boxes of 32 heads x 128 bytes, into out [R*H, 512] bf16 or into the split
@@ -1193,22 +1512,39 @@ int launch_sparse_mla_tc(const MlaPlan& p, int n_splits, int per_split, float* p
     return MTPSD_ECUDA;
   }
   cudaLaunchAttribute attrs[2];
-  cudaLaunchConfig_t cfg = mla_tc_config(dim3(p.R, (p.H / HG) * 2, n_splits), k.fused_combine ? n_splits : 1, st, attrs);
+  const dim3 grid = pl ? dim3(pl->clusters, 2, 1) : dim3(p.R, (p.H / HG) * 2, n_splits);
+  cudaLaunchConfig_t cfg = mla_tc_config(grid, k.fused_combine ? n_splits : 1, st, attrs);
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see launch_k()
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 2;
   cudaError_t e;
-  if (fp8)
-    e = p.pg.bt ? cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<true, true>, tm_lat, tm_q, tm_st, tm_sc, k)
-                : cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<false, true>, tm_lat, tm_q, tm_st, tm_sc, k);
+  if (pl)
+    e = p.pg.bt ? cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<true, false, true>, tm_lat, tm_q, tm_st, tm_sc, k)
+                : cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<false, false, true>, tm_lat, tm_q, tm_st, tm_sc, k);
+  else if (fp8)
+    e = p.pg.bt ? cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<true, true, false>, tm_lat, tm_q, tm_st, tm_sc, k)
+                : cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<false, true, false>, tm_lat, tm_q, tm_st, tm_sc, k);
   else
-    e = p.pg.bt ? cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<true, false>, tm_lat, tm_q, tm_st, tm_sc, k)
-                : cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<false, false>, tm_lat, tm_q, tm_st, tm_sc, k);
+    e = p.pg.bt ? cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<true, false, false>, tm_lat, tm_q, tm_st, tm_sc, k)
+                : cudaLaunchKernelEx(&cfg, sparse_mla_tc_kernel<false, false, false>, tm_lat, tm_q, tm_st, tm_sc, k);
   if (e != cudaSuccess) {
     set_error("sparse_mla_tc: launch failed: %s", cudaGetErrorString(e));
     return MTPSD_ECUDA;
   }
-  return check_launch("sparse_mla_tc");
+  int rc = check_launch("sparse_mla_tc");
+  if (rc || !pl || !pl->cut) return rc;
+  PieceMerge a;
+  a.out = (__nv_bfloat16*)p.out;
+  a.lse = p.lse;
+  a.part_o = part_o;
+  a.part_ml = part_ml;
+  a.H = p.H;
+  a.pq = pl->pq;
+  a.ppr = pl->ppr;
+  a.hgn = pl->hgn;
+  a.tp = pl->tp;
+  launch_k(mla_piece_merge_kernel, dim3((unsigned)(pl->clusters - 1), HG / MERGE_HEADS), 64 * MERGE_HEADS, 0, st, a);
+  return check_launch("sparse_mla_piece_merge");
 }
 
 }  // namespace mtpsd

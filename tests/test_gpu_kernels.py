@@ -342,6 +342,51 @@ def test_sparse_mla(mt, H, lens, n_idx, dtype):
     print(f"worst relative L2 error {worst:.2e}")
 
 
+@pytest.mark.parametrize("H,lens,n_idx,n_rows,n_append,force", [
+    (128, [300, 2100, 50], 512, 3, 0, True),      # one pair per cluster: every row in 8 pieces, masked pieces
+    (128, [9000], 2048, 3, 0, True),              # 16 pieces per row
+    (256, [700, 40], 256, 2, 0, True),            # two head groups per row
+    (128, [5000, 64], 2048, 2, 1, True),          # an appended position: a last pair of one position
+    (128, [3000] * 30, 256, 3, 0, False),         # 90 rows: the default choice, whole rows and cut ones
+    (128, [1200] * 40, 128, 2, 2, False),         # 80 rows, two pairs each with appended positions
+])
+def test_sparse_mla_persistent(mt, H, lens, n_idx, n_rows, n_append, force, monkeypatch):
+    """The persistent launch: clusters take equal runs of pairs across rows, and rows cut between
+    clusters are merged from their pieces."""
+    if force:
+        monkeypatch.setenv("MTPSD_MLA_PERSIST", "1")
+    c = _mla_case(H, lens, n_idx, torch.bfloat16, seed=H + n_idx + n_rows, n_rows=n_rows)
+    R = len(c["row_req"])
+    scale = 1.0 / math.sqrt(576.0)
+    base = c["row_pos"].astype(np.int64) - n_append
+    idx = c["idx"].copy()
+    idx[idx > base[:, None]] = -1
+    lse = torch.empty(R, H, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = mt.sparse_mla_decode(dev(c["q"]), dev(c["latent"]), dev(c["cache_start"]), u32(c["ro"]),
+                               dev(base, torch.int64), dev(idx), scale, n_append=n_append,
+                               append_base=dev(base, torch.int64) if n_append else None, row_pos_add=n_append,
+                               lse=lse, dev_status=status)
+    assert status.item() == 0
+    ref = omla.sparse_mla(c["q"], c["latent"], c["cache_start"], c["row_req"], idx, scale, n_append=n_append,
+                          append_base=base if n_append else None)
+    o = out.float().cpu().numpy()
+    ls = lse.cpu().numpy()
+    worst = 0.0
+    for r in range(R):
+        worst = max(worst, parity.check_attention_row(o[r], ref[r][0], parity.ATT_TOL_BF16))
+        assert np.max(np.abs(ls[r] - ref[r][1])) <= 2e-3 * max(1.0, np.max(np.abs(ref[r][1])))
+    # the same call on the split launch gives the same rows within the tolerance
+    monkeypatch.setenv("MTPSD_MLA_PERSIST", "0")
+    out0 = mt.sparse_mla_decode(dev(c["q"]), dev(c["latent"]), dev(c["cache_start"]), u32(c["ro"]),
+                                dev(base, torch.int64), dev(idx), scale, n_append=n_append,
+                                append_base=dev(base, torch.int64) if n_append else None, row_pos_add=n_append)
+    o0 = out0.float().cpu().numpy()
+    for r in range(R):
+        parity.check_attention_row(o[r], o0[r].astype(np.float64), parity.ATT_TOL_BF16)
+    print(f"worst relative L2 error {worst:.2e}")
+
+
 # ----------------------------------------------------------------------------- FP8 latent cache
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])

@@ -297,8 +297,12 @@ def test_indexer_paged_missing_page(mt, ps):
     (16, [700, 40], 256, "bf16", 8, 0),                   # mma.sync kernel
     (8, [100, 300], 32, "f32", 4, 0),
     (128, [3000, 64], 1024, "fp8", 32, 1),                # the 656-byte FP8 latent rows
+    (128, [2500, 700], 1024, "persist", 64, 0),           # the persistent launch (rows cut between clusters)
+    (128, [5000, 64], 2048, "persist", 8, 2),
 ])
-def test_sparse_mla_paged(mt, H, lens, n_idx, kind, ps, n_append):
+def test_sparse_mla_paged(mt, H, lens, n_idx, kind, ps, n_append, monkeypatch):
+    if kind == "persist":
+        monkeypatch.setenv("MTPSD_MLA_PERSIST", "1")
     rng = np.random.default_rng(H + n_idx + ps)
     B, n_rows = len(lens), 3
     caps = np.asarray(lens) + n_rows + n_append + 1
