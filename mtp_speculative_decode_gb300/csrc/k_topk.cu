@@ -373,30 +373,39 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p, SplitLevel sl
   const uint32_t diff = kand ^ kor;
   const int b0 = diff ? 31 - __clz(diff) : -1;   // highest bit where visible keys differ
   uint32_t T = b0 >= 31 ? 0u : (b0 < 0 ? kand : (kand & (~0u << (b0 + 1))));
-  // Eleven bits at a time while at least eleven are left: a 2048-bin histogram of bits b-10..b of the
-  // keys that share T's bits above b (keys above that prefix are only counted), then the bin where the
-  // count from the top reaches k.  Thread t owns bins BPT*t .. BPT*t+BPT-1.
+  // Eleven bits at a time, the last level taking what is left (1 to 11 bits): a 2048-bin histogram of
+  // the level's bits of the keys that share T's bits above it (keys above that prefix are only
+  // counted), then the bin where the count from the top reaches k; after the last level T is the k-th
+  // largest key.  Thread t owns bins BPT*t .. BPT*t+BPT-1.  The keys past the row's end are 0, below
+  // every key of a finite score, and there are more than k valid keys, so counting them (in the lowest
+  // bin, when the prefix is 0) never moves the k-th largest: no validity test per key.  The increment is
+  // a predicated shared-memory reduction, so that the per-key work has no branch.
   constexpr int BPT = 2048 / NTH;
   __shared__ int hist[2048];
   __shared__ int dsel;
+  const uint32_t hist_s = (uint32_t)__cvta_generic_to_shared(hist);
   int bl = b0;
 #pragma unroll 1
-  while (bl >= 10) {
-    const int sh = bl - 10;
+  while (bl >= 0) {
+    const int nb = bl >= 10 ? 11 : bl + 1;   // bits of this level: bl - nb + 1 .. bl
+    const int sh = bl + 1 - nb;
+    const uint32_t bmask = (1u << nb) - 1u;
+    const uint32_t sh1 = (uint32_t)(bl + 1);   // the prefix above the level (32: none)
 #pragma unroll
     for (int e = 0; e < BPT; ++e) hist[threadIdx.x * BPT + e] = 0;
     __syncthreads();
-    const uint32_t preT = bl >= 31 ? 0u : (T >> (bl + 1));
+    const uint32_t preT = __funnelshift_rc(T, 0u, sh1);
     int above = 0;
-    auto put = [&](uint32_t kv, bool valid) {
-      if (!valid) return;
-      const uint32_t pre = bl >= 31 ? 0u : (kv >> (bl + 1));
-      if (pre > preT) ++above;
-      else if (pre == preT) atomicAdd(&hist[(kv >> sh) & 2047u], 1);
+    auto put = [&](uint32_t kv) {
+      const uint32_t pre = __funnelshift_rc(kv, 0u, sh1);
+      above += pre > preT ? 1 : 0;
+      const uint32_t addr = hist_s + (((kv >> sh) & bmask) << 2);
+      asm volatile("{\n .reg .pred q;\n setp.eq.u32 q, %1, %2;\n @q red.shared.add.u32 [%0], 1;\n}\n"
+                   ::"r"(addr), "r"(pre), "r"(preT) : "memory");
     };
 #pragma unroll
-    for (int i = 0; i < KPT; ++i) put(key[i], a + i < V);
-    if constexpr (XT) put(xkey, xv);
+    for (int i = 0; i < KPT; ++i) put(key[i]);
+    if constexpr (XT) put(xkey);
     __syncthreads();
     int hv[BPT], lsum = 0;
 #pragma unroll
@@ -404,8 +413,8 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p, SplitLevel sl
       hv[e] = hist[threadIdx.x * BPT + e];
       lsum += hv[e];
     }
-    // both fields stay below 65536 (at most 40960 keys): one unsigned scan carries the bin counts in
-    // the low half and the keys above the prefix in the high half
+    // both fields stay below 65536 (at most 41984 keys, padding included): one unsigned scan carries
+    // the bin counts in the low half and the keys above the prefix in the high half
     const uint32_t pk = block_exclusive_scan<uint32_t>((uint32_t)lsum | ((uint32_t)above << 16), uwarp_sums, &utotal_s);
     const int tot = (int)(utotal_s & 0xffffu), A = (int)(utotal_s >> 16);
     const int U = A + tot - (int)(pk & 0xffffu) - lsum;   // keys in the bins above this thread's, and above the prefix
@@ -423,20 +432,7 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p, SplitLevel sl
     }
     __syncthreads();
     T |= (uint32_t)dsel << sh;
-    bl -= 11;
-  }
-#pragma unroll 1
-  for (int b = bl; b >= 0; --b) {
-    const uint32_t cand = T | (1u << b);
-    unsigned c = 0;
-#pragma unroll
-    for (int i = 0; i < KPT; ++i) c += key[i] >= cand ? 1u : 0u;
-    if constexpr (XT) c += xkey >= cand ? 1u : 0u;
-    c = __reduce_add_sync(0xffffffffu, c);
-    if (lane == 0) wsum[b & 1][wid] = (int)c;
-    __syncthreads();   // the other buffer is rewritten only after the next barrier
-    const unsigned tot = __reduce_add_sync(0xffffffffu, lane < NW ? (unsigned)wsum[b & 1][lane] : 0u);
-    if (tot >= (unsigned)k) T = cand;
+    bl -= nb;
   }
   int n_gt = 0, n_eq = 0;
 #pragma unroll
