@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(TOPK_THREADS, 1) topk_kernel(TopkPlan p, int64
 // the tail keys, whose positions follow every regular one, are compacted after
 // them.
 //
-// Longer rows are split (MODE 1 and 2, one launch per level).  Level 1 cuts a
+// Longer rows are split (MODE 1, then 2 or 3, one launch per level).  Level 1 cuts a
 // row into segments of SPLIT_SEG keys, one CTA each, and every CTA selects its
 // segment's exact top-k under the same order (larger key first, ties to the
 // lower position) as a list of k (key, position) entries in position order; a
@@ -191,7 +191,8 @@ __global__ void __launch_bounds__(TOPK_THREADS, 1) topk_kernel(TopkPlan p, int64
 // of its group) under that order, so every level is exact; the lists of a row
 // stay in position order (segment u's positions precede segment u+1's), so the
 // compaction, which writes in list order, keeps the output ascending.  The level
-// at which a row has one list left writes the row's final output.
+// at which a row has one list left writes the row's final output.  MODE 3 is MODE 2
+// held to 64 registers, so that two CTAs share an SM when there are more rows than SMs.
 // 16384-key segments on 512 threads (32 keys each): two CTAs fit one SM, so one CTA's loads and barriers
 // overlap the other's counting (one 1024-thread CTA per SM over 32768-key segments was 18 % slower on
 // 768 rows of up to 118 K keys, and 256-thread CTAs over 8192-key segments 15 % slower).
@@ -232,7 +233,7 @@ __host__ __device__ __forceinline__ void split_shape(int64_t V, int k, int G, in
 }
 
 template <int KPT, int NTH, bool XT, int MODE>
-__global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p, SplitLevel sl) {
+__global__ void __launch_bounds__(NTH, MODE == 3 ? 2 : 0) topk_reg_kernel(TopkPlan p, SplitLevel sl) {
   griddep_wait();                // the previous kernel's writes are visible from here on
   griddep_launch_dependents();
   static_assert(MODE == 0 || !XT, "tail keys only for whole rows");
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p, SplitLevel sl
   }
   if (Vrow < 0) Vrow = 0;
   const int k = p.k;
-  // this CTA's keys: V of them, from a score row (MODE 0, 1) or a list of (key, position) (MODE 2)
+  // this CTA's keys: V of them, from a score row (MODE 0, 1) or a list of (key, position) (MODE 2, 3)
   const float* row = nullptr;
   const uint32_t* krow = nullptr;
   const int32_t* prow = nullptr;
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p, SplitLevel sl
     int n, lv, np, plv;
     split_shape(Vrow, k, sl.G, sl.level, n, lv, np, plv);
     const int u = blockIdx.y;
-    if (MODE == 2 && np <= 1) return;   // the row was finished at an earlier level
+    if (MODE >= 2 && np <= 1) return;   // the row was finished at an earlier level
     if (u >= n) return;
     fin = n == 1;
     if constexpr (MODE == 1) {
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p, SplitLevel sl
     }
   }
   auto pos_of = [&](int i) -> int32_t {
-    if constexpr (MODE == 2) return prow[i];
+    if constexpr (MODE >= 2) return prow[i];
     else return (int32_t)(pos_base + i);
   };
   auto emit = [&](int slot, int i, uint32_t kv) {
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p, SplitLevel sl
     for (int i = threadIdx.x; i < k; i += blockDim.x) {
       if (i < V) {
         uint32_t kv;
-        if constexpr (MODE == 2) kv = krow[i];
+        if constexpr (MODE >= 2) kv = krow[i];
         else kv = float_key(row[i]);
         emit(i, i, kv);
       } else {
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p, SplitLevel sl
   // keys of this thread's entries; 0 (below every finite key) past the end
   const int a = threadIdx.x * KPT;
   uint32_t key[KPT];
-  if constexpr (MODE == 2) {
+  if constexpr (MODE >= 2) {
     if ((k & 3) == 0) {   // 16-byte aligned lists (k and the row stride are multiples of 4)
 #pragma unroll
       for (int i = 0; i < KPT; i += 4) {
@@ -478,7 +479,7 @@ __global__ void __launch_bounds__(NTH) topk_reg_kernel(TopkPlan p, SplitLevel sl
   const int eq_before = block_exclusive_scan(n_eq, warp_sums, &total_s);
   int take_eq = max(0, min(n_eq, need_eq - eq_before));
   int out_pos = gt_before + min(eq_before, need_eq);
-  if constexpr (MODE == 2) {
+  if constexpr (MODE >= 2) {
     // merged lists carry their positions: eight of this thread's are loaded together before they are
     // emitted, instead of one dependent load per emitted entry
 #pragma unroll
@@ -608,6 +609,8 @@ static int launch_topk_split(const TopkPlan& p, cudaStream_t st) {
     const dim3 grid(p.R, n_at[l - 1]);
     if (l == 1)
       launch_k(topk_reg_kernel<SPLIT_KPT, SPLIT_NTH, false, 1>, grid, SPLIT_NTH, 0, st, p, sl);
+    else if (p.R > num_sms())   // more rows than SMs: two CTAs per SM (64 registers) outrun one faster CTA
+      launch_k(topk_reg_kernel<SPLIT_KPT, SPLIT_NTH, false, 3>, grid, SPLIT_NTH, 0, st, p, sl);
     else
       launch_k(topk_reg_kernel<SPLIT_KPT, SPLIT_NTH, false, 2>, grid, SPLIT_NTH, 0, st, p, sl);
     const int rc = check_launch("topk_split");

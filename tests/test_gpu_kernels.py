@@ -218,6 +218,23 @@ def test_topk_exact(mt, V, k, ties):
         assert np.array_equal(gs[r, :n], sc[r, got[r, :n]])
 
 
+def test_topk_split_many_rows(mt):
+    """More rows than SMs on the split path (the merge level then runs two CTAs per SM), ragged lengths."""
+    rng = np.random.default_rng(11)
+    R, V, k = 200, 50000, 2048
+    sc = rng.normal(size=(R, V)).astype(np.float32)
+    sc[::7] = np.round(sc[::7] * 4)                       # rows with heavy ties
+    lens = rng.integers(1, V + 1, R).astype(np.int64)
+    lens[0], lens[1], lens[2], lens[3] = V, 40961, k, 16385
+    ld = V + 4
+    buf = np.zeros((R, ld), np.float32)
+    buf[:, :V] = sc
+    got = mt.topk(dev(buf), dev(lens), V, k).cpu().numpy()
+    for r in range(R):
+        want = otopk.topk_select(sc[r, :lens[r]].astype(np.float64), k)
+        assert np.array_equal(got[r], want.astype(np.int32)), f"row {r}"
+
+
 # ----------------------------------------------------------------------------- indexer
 
 def _indexer_case(H, D, lens, r_per, fp8, seed):
