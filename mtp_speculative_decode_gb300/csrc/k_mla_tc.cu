@@ -1389,10 +1389,14 @@ static int64_t split_plan(int R, int H, int64_t total, double* cost_out);
 // same number of consecutive pairs, so no wave is partly empty.  Measured on GB300, an item costs as
 // much beyond its pairs as a row of the split launch does (four whole rows per cluster ran exactly as
 // long as four waves), about PERSIST_ITEM_PAIRS pairs, and the piece merge about PERSIST_MERGE_PAIRS;
-// the gain is the last wave's idle clusters, so large row counts (the 768-row verify, the 384-row
-// draft_extend) take it and a few waves of rows do not.
+// the gain is the last wave's idle clusters.  The model counts every pair alike; ragged rows (short
+// contexts leave masked pairs) are balanced by the split launch's dynamic CTA scheduling and not by the
+// equal runs, so the persistent launch needs a PERSIST_MARGIN lead: the 384 uniform draft_extend rows
+// take it (measured 311 -> 283 us), the 768 ragged verify rows of the decode workload do not (measured
+// neutral to 10 us slower).
 constexpr double PERSIST_ITEM_PAIRS = 4.5;
 constexpr double PERSIST_MERGE_PAIRS = 10.0;
+constexpr double PERSIST_MARGIN = 0.97;
 bool mla_tc_persist_plan(int R, int H, int64_t total, int dtype, MlaPersist* pl) {
   if (dtype != MTPSD_BF16 || total <= 0 || R <= 0 || H % mtc::HG != 0) return false;
   const char* env = getenv("MTPSD_MLA_PERSIST");
@@ -1418,7 +1422,7 @@ bool mla_tc_persist_plan(int R, int H, int64_t total, int dtype, MlaPersist* pl)
   split_plan(R, H, total, &split_cost);
   const double items = (double)((pq + ppr - 1) / ppr + 1);
   const double cost = (double)pq + 4.0 + items * PERSIST_ITEM_PAIRS + (pl->cut ? PERSIST_MERGE_PAIRS : 0.0);
-  return cost < split_cost;
+  return cost < PERSIST_MARGIN * split_cost;
 }
 
 // Pieces of the persistent launch: two per cluster (its first and its last unit), each 128 heads x 512
